@@ -1,0 +1,133 @@
+"""Torch-facing entry points of libsaf (device memory and streams only).
+
+These wrappers allocate outputs and the workspace with torch, pass raw
+device addresses and the current CUDA stream to the C ABI, and raise on any
+non-OK status.  All arithmetic runs in libsaf's kernels.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import _binding as B
+
+__all__ = ["HybridAttention", "Calibration", "num_select", "SafError"]
+
+SafError = B.SafError
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device=None):
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _check(st, where):
+    if st != B.SAF_OK:
+        raise B.SafError(st, where)
+
+
+class HybridAttention:
+    """One hybrid causal attention layer of shape (B, H, T, d_h).
+
+    ``head_is_static`` marks the frozen heads (host booleans, length H).
+    ``dtype`` is torch.bfloat16 or torch.float32 (fp32 I/O is computed in
+    bf16 inside the library).
+    """
+
+    def __init__(self, B_: int, H: int, T: int, d_h: int, head_is_static,
+                 dtype=torch.bfloat16, device="cuda", want_param_grads=False):
+        self.shape = (B_, H, T, d_h)
+        self.dtype = dtype
+        self.device = torch.device(device)
+        code = B.SAF_BF16 if dtype == torch.bfloat16 else B.SAF_F32
+        self.dims = B._dims(B_, H, T, d_h, code)
+        self.head_is_static = bytes(np.asarray(head_is_static, dtype=np.uint8).tolist())
+        assert len(self.head_is_static) == H
+        self.ws_bytes = B.saf_hybrid_attn_workspace_size(self.dims, int(want_param_grads))
+        if self.ws_bytes == 0:
+            raise B.SafError(B.SAF_ERR_UNSUPPORTED, "saf_hybrid_attn_workspace_size")
+        self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
+
+    def forward(self, q, k, v, alpha, rho, out=None, lse=None):
+        B_, H, T, d = self.shape
+        if out is None:
+            out = torch.empty((B_, H, T, d), dtype=self.dtype, device=self.device)
+        if lse is None:
+            lse = torch.empty((B_, H, T), dtype=torch.float32, device=self.device)
+        st = B.saf_hybrid_attn_fwd(self.dims, _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(rho),
+                                   self.head_is_static, _ptr(out), _ptr(lse),
+                                   _ptr(self.workspace), self.ws_bytes, _stream(self.device))
+        _check(st, "saf_hybrid_attn_fwd")
+        return out, lse
+
+    def backward(self, q, k, v, out, lse, dout, alpha, rho, want_param_grads=False,
+                 grads=None):
+        B_, H, T, d = self.shape
+        if grads is None:
+            mk = lambda: torch.empty((B_, H, T, d), dtype=self.dtype, device=self.device)
+            dq, dk, dv = mk(), mk(), mk()
+            da = dr = None
+            if want_param_grads:
+                da = torch.empty((H, T), dtype=torch.float32, device=self.device)
+                dr = torch.empty((H, T), dtype=torch.float32, device=self.device)
+        else:
+            dq, dk, dv, da, dr = grads
+        st = B.saf_hybrid_attn_bwd(self.dims, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                   _ptr(dout), _ptr(alpha), _ptr(rho), self.head_is_static,
+                                   _ptr(dq), _ptr(dk), _ptr(dv), _ptr(da), _ptr(dr),
+                                   _ptr(self.workspace), self.ws_bytes, _stream(self.device))
+        _check(st, "saf_hybrid_attn_bwd")
+        return dq, dk, dv, da, dr
+
+    def device_status(self):
+        return B.saf_get_device_status(_ptr(self.workspace), 0, _stream(self.device))
+
+
+class Calibration:
+    """Streaming calibration state for ``num_heads`` heads of length T."""
+
+    def __init__(self, num_heads: int, T: int, device="cuda"):
+        self.device = torch.device(device)
+        with torch.cuda.device(self.device):
+            st, self.handle = B.saf_calib_create(num_heads, T)
+        _check(st, "saf_calib_create")
+        self.num_heads, self.T = num_heads, T
+
+    def accumulate(self, A, head_begin=0):
+        n, hc = A.shape[0], A.shape[1]
+        st = B.saf_calib_accumulate(self.handle, _ptr(A), n, head_begin, hc, _stream(self.device))
+        _check(st, "saf_calib_accumulate")
+
+    def finalize(self, k, want_mean=True):
+        A_hat = None
+        if want_mean:
+            A_hat = torch.empty((self.num_heads, self.T, self.T), dtype=torch.float32,
+                                device=self.device)
+        s_var = torch.empty(self.num_heads, dtype=torch.float32, device=self.device)
+        sel = torch.empty(max(k, 1), dtype=torch.int32, device=self.device)
+        st = B.saf_calib_finalize(self.handle, k, _ptr(A_hat), _ptr(s_var), _ptr(sel),
+                                  _stream(self.device))
+        _check(st, "saf_calib_finalize")
+        return A_hat, s_var, sel[:k]
+
+    def reset(self):
+        _check(B.saf_calib_reset(self.handle), "saf_calib_reset")
+
+    def close(self):
+        if self.handle is not None:
+            B.saf_calib_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def num_select(r: float, num_heads: int) -> int:
+    return B.saf_calib_num_select(r, num_heads)

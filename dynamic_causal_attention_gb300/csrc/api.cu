@@ -1,0 +1,556 @@
+// api.cu — host side of the libsaf C ABI: argument checks, workspace carving,
+// TMA descriptor encoding, head lists and the launch sequence of each call.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+#include <vector>
+
+#include "../../include/saf.h"
+#include "attn_kernels.h"
+#include "internal.h"
+
+namespace saf {
+
+static thread_local int g_launches = 0;
+void note_launch() { ++g_launches; }
+
+namespace {
+
+constexpr int kMaxT = 16384;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+int sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// dependency on libcuda).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D view [rows, d] of a bf16 tensor, box of 128 rows x one swizzle chunk.
+bool encode_rows(CUtensorMap* m, const void* base, uint64_t rows, int d) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const int swz = d >= 64 ? 128 : 64;
+  const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)(swz / 2), 128u};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swz == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------ workspace
+struct WsLayout {
+  size_t status, a_tab, r_tab, row_tab, logZ, mode;
+  size_t q16, k16, v16, o16, do16, dq16, dk16, dv16;
+  size_t Dvec, lse2, Dsum, dq_acc;
+  size_t total;
+};
+
+WsLayout ws_layout(const saf_attn_dims& d) {
+  WsLayout L;
+  const size_t B = d.B, H = d.H, T = d.T, D = d.d_h;
+  const size_t elems = B * H * T * D;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align256(off + bytes);
+    return o;
+  };
+  L.status = take(256);
+  L.a_tab = take(H * T * 4);
+  L.r_tab = take(H * (T + 128) * 4);
+  L.row_tab = take(H * T * 4);
+  L.logZ = take(H * T * 4);
+  L.mode = take(H * 4);
+  const bool f32 = d.dtype == SAF_F32;
+  const size_t stage = f32 ? elems * 2 : 0;
+  L.q16 = take(stage);
+  L.k16 = take(stage);
+  L.v16 = take(stage);
+  L.o16 = take(stage);
+  L.do16 = take(stage);
+  L.dq16 = take(stage);
+  L.dk16 = take(stage);
+  L.dv16 = take(stage);
+  L.Dvec = take(B * H * T * 4);
+  L.lse2 = take(B * H * T * 4);
+  L.Dsum = take(H * T * 4);
+  L.dq_acc = take(elems * 4);
+  L.total = off;
+  return L;
+}
+
+saf_status check_dims(const saf_attn_dims* d) {
+  if (!d) return SAF_ERR_INVALID_ARG;
+  if (d->B < 1 || d->H < 1 || d->T < 1 || d->d_h < 1) return SAF_ERR_INVALID_ARG;
+  if (d->dtype != SAF_BF16 && d->dtype != SAF_F32) return SAF_ERR_INVALID_ARG;
+  if (d->H > kMaxHeads) return SAF_ERR_UNSUPPORTED;
+  if (d->T % 128 != 0 || d->T > kMaxT) return SAF_ERR_UNSUPPORTED;
+  if (d->d_h != 32 && d->d_h != 64 && d->d_h != 128) return SAF_ERR_UNSUPPORTED;
+  if ((uint64_t)d->B * d->H * d->T >= (1ull << 31)) return SAF_ERR_UNSUPPORTED;
+  return SAF_OK;
+}
+
+struct HeadSplit {
+  int n_static = 0, n_dynamic = 0;
+  uint8_t st[kMaxHeads], dy[kMaxHeads], is_static[kMaxHeads];
+};
+
+HeadSplit split_heads(const uint8_t* head_is_static, int H) {
+  HeadSplit s;
+  memset(s.is_static, 0, sizeof(s.is_static));
+  for (int h = 0; h < H; ++h) {
+    if (head_is_static[h]) {
+      s.st[s.n_static++] = (uint8_t)h;
+      s.is_static[h] = 1;
+    } else {
+      s.dy[s.n_dynamic++] = (uint8_t)h;
+    }
+  }
+  return s;
+}
+
+saf_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SAF_OK : SAF_ERR_CUDA; }
+
+#define SAF_TRY(expr)                           \
+  do {                                          \
+    cudaError_t e_ = (expr);                    \
+    if (e_ != cudaSuccess) return SAF_ERR_CUDA; \
+  } while (0)
+
+StaticPrep make_prep(const saf_attn_dims& d, const HeadSplit& hs, const float* alpha,
+                     const float* rho, uint8_t* ws, const WsLayout& L) {
+  StaticPrep sp;
+  memset(&sp, 0, sizeof(sp));
+  sp.T = d.T;
+  sp.n_static = hs.n_static;
+  memcpy(sp.heads, hs.st, sizeof(sp.heads));
+  sp.alpha = alpha;
+  sp.rho = rho;
+  sp.a_tab = reinterpret_cast<float*>(ws + L.a_tab);
+  sp.r_tab = reinterpret_cast<float*>(ws + L.r_tab);
+  sp.row_tab = reinterpret_cast<float*>(ws + L.row_tab);
+  sp.logZ = reinterpret_cast<float*>(ws + L.logZ);
+  sp.mode = reinterpret_cast<int*>(ws + L.mode);
+  return sp;
+}
+
+void fill_fwd_params(FwdParams& p, const saf_attn_dims& d, const HeadSplit& hs, uint8_t* ws,
+                     const WsLayout& L, bool transposed) {
+  memset(&p, 0, sizeof(p));
+  p.B = d.B;
+  p.H = d.H;
+  p.T = d.T;
+  p.nI = d.T / 128;
+  p.n_static = hs.n_static;
+  p.n_dynamic = transposed ? 0 : hs.n_dynamic;
+  p.group = 256 / d.d_h < d.B ? 256 / d.d_h : d.B;
+  p.n_groups = (d.B + p.group - 1) / p.group;
+  p.n_items = p.nI * (p.n_static * p.n_groups + (transposed ? 0 : d.B * hs.n_dynamic));
+  p.scale_log2 = 1.4426950408889634f / sqrtf((float)d.d_h);
+  memcpy(p.static_heads, hs.st, sizeof(p.static_heads));
+  memcpy(p.dynamic_heads, hs.dy, sizeof(p.dynamic_heads));
+  p.a_tab = reinterpret_cast<const float*>(ws + L.a_tab);
+  p.r_tab = reinterpret_cast<const float*>(ws + L.r_tab);
+  p.row_tab = reinterpret_cast<const float*>(ws + L.row_tab);
+  p.logZ = reinterpret_cast<const float*>(ws + L.logZ);
+  p.mode = reinterpret_cast<const int*>(ws + L.mode);
+  p.status = reinterpret_cast<int*>(ws + L.status);
+}
+
+}  // namespace
+}  // namespace saf
+
+using namespace saf;
+
+extern "C" {
+
+const char* saf_status_string(saf_status s) {
+  switch (s) {
+    case SAF_OK: return "SAF_OK";
+    case SAF_ERR_INVALID_ARG: return "SAF_ERR_INVALID_ARG";
+    case SAF_ERR_UNSUPPORTED: return "SAF_ERR_UNSUPPORTED";
+    case SAF_ERR_CUDA: return "SAF_ERR_CUDA";
+    case SAF_ERR_STATE: return "SAF_ERR_STATE";
+    case SAF_ERR_TIMEOUT: return "SAF_ERR_TIMEOUT";
+  }
+  return "SAF_ERR_UNKNOWN";
+}
+
+int saf_last_launch_count(void) { return g_launches; }
+
+size_t saf_hybrid_attn_workspace_size(const saf_attn_dims* dims, int want_param_grads) {
+  (void)want_param_grads;  // the parameter-gradient pass needs no extra scratch
+  if (check_dims(dims) != SAF_OK) return 0;
+  return ws_layout(*dims).total;
+}
+
+saf_status saf_hybrid_attn_fwd(const saf_attn_dims* dims, const void* Q, const void* K,
+                               const void* V, const float* alpha, const float* rho,
+                               const uint8_t* head_is_static, void* out, float* lse,
+                               void* workspace, size_t ws_bytes, void* stream) {
+  g_launches = 0;
+  const saf_status ds = check_dims(dims);
+  if (ds != SAF_OK) return ds;
+  const saf_attn_dims d = *dims;
+  if (!head_is_static || !V || !out || !workspace) return SAF_ERR_INVALID_ARG;
+  const HeadSplit hs = split_heads(head_is_static, d.H);
+  if (hs.n_dynamic > 0 && (!Q || !K)) return SAF_ERR_INVALID_ARG;
+  if (hs.n_static > 0 && (!alpha || !rho)) return SAF_ERR_INVALID_ARG;
+  if ((Q && !aligned16(Q)) || (K && !aligned16(K)) || !aligned16(V) || !aligned16(out) ||
+      (lse && !aligned16(lse)) || (alpha && !aligned16(alpha)) || (rho && !aligned16(rho)))
+    return SAF_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SAF_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(d);
+  if (ws_bytes < L.total) return SAF_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t elems = (size_t)d.B * d.H * d.T * d.d_h;
+  SAF_TRY(cudaMemsetAsync(ws + L.status, 0, sizeof(int), s));
+
+  const void *q16 = Q, *k16 = K, *v16 = V;
+  void* o16 = out;
+  if (d.dtype == SAF_F32) {
+    if (hs.n_dynamic > 0) {
+      SAF_TRY(launch_f32_to_bf16(static_cast<const float*>(Q), ws + L.q16, elems, s));
+      SAF_TRY(launch_f32_to_bf16(static_cast<const float*>(K), ws + L.k16, elems, s));
+    }
+    SAF_TRY(launch_f32_to_bf16(static_cast<const float*>(V), ws + L.v16, elems, s));
+    q16 = ws + L.q16;
+    k16 = ws + L.k16;
+    v16 = ws + L.v16;
+    o16 = ws + L.o16;
+  }
+  if (hs.n_static > 0) SAF_TRY(launch_static_prep(make_prep(d, hs, alpha, rho, ws, L), s));
+
+  FwdLaunch fl;
+  memset(&fl, 0, sizeof(fl));
+  fill_fwd_params(fl.p, d, hs, ws, L, false);
+  fl.p.out = static_cast<__nv_bfloat16*>(o16);
+  fl.p.lse = lse;
+  const uint64_t rows = (uint64_t)d.B * d.H * d.T;
+  // Q/K maps must be valid descriptors even when only static heads exist.
+  const void* qb = q16 ? q16 : v16;
+  const void* kb = k16 ? k16 : v16;
+  if (!encode_rows(&fl.tm_q, qb, rows, d.d_h) || !encode_rows(&fl.tm_k, kb, rows, d.d_h) ||
+      !encode_rows(&fl.tm_v, v16, rows, d.d_h))
+    return SAF_ERR_CUDA;
+  fl.d_h = d.d_h;
+  fl.transposed = false;
+  fl.num_sms = sm_count();
+  SAF_TRY(launch_hybrid_fwd(fl, s));
+  if (d.dtype == SAF_F32) SAF_TRY(launch_bf16_to_f32(o16, static_cast<float*>(out), elems, s));
+  return SAF_OK;
+}
+
+saf_status saf_hybrid_attn_bwd(const saf_attn_dims* dims, const void* Q, const void* K,
+                               const void* V, const void* out, const float* lse,
+                               const void* dout, const float* alpha, const float* rho,
+                               const uint8_t* head_is_static, void* dQ, void* dK, void* dV,
+                               float* dalpha, float* drho, void* workspace, size_t ws_bytes,
+                               void* stream) {
+  g_launches = 0;
+  const saf_status ds = check_dims(dims);
+  if (ds != SAF_OK) return ds;
+  const saf_attn_dims d = *dims;
+  if (!head_is_static || !V || !out || !lse || !dout || !dQ || !dK || !dV || !workspace)
+    return SAF_ERR_INVALID_ARG;
+  if ((dalpha == nullptr) != (drho == nullptr)) return SAF_ERR_INVALID_ARG;
+  const HeadSplit hs = split_heads(head_is_static, d.H);
+  if (hs.n_dynamic > 0 && (!Q || !K)) return SAF_ERR_INVALID_ARG;
+  if (hs.n_static > 0 && (!alpha || !rho)) return SAF_ERR_INVALID_ARG;
+  const void* ptrs[] = {V, out, lse, dout, dQ, dK, dV};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return SAF_ERR_INVALID_ARG;
+  if ((Q && !aligned16(Q)) || (K && !aligned16(K)) || (alpha && !aligned16(alpha)) ||
+      (rho && !aligned16(rho)) || (dalpha && !aligned16(dalpha)) || (drho && !aligned16(drho)))
+    return SAF_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SAF_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(d);
+  if (ws_bytes < L.total) return SAF_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t elems = (size_t)d.B * d.H * d.T * d.d_h;
+  const uint64_t rows = (uint64_t)d.B * d.H * d.T;
+  SAF_TRY(cudaMemsetAsync(ws + L.status, 0, sizeof(int), s));
+
+  const void *q16 = Q, *k16 = K, *v16 = V, *o16 = out, *do16 = dout;
+  void *dq16 = dQ, *dk16 = dK, *dv16 = dV;
+  if (d.dtype == SAF_F32) {
+    if (hs.n_dynamic > 0) {
+      SAF_TRY(launch_f32_to_bf16(static_cast<const float*>(Q), ws + L.q16, elems, s));
+      SAF_TRY(launch_f32_to_bf16(static_cast<const float*>(K), ws + L.k16, elems, s));
+    }
+    SAF_TRY(launch_f32_to_bf16(static_cast<const float*>(V), ws + L.v16, elems, s));
+    SAF_TRY(launch_f32_to_bf16(static_cast<const float*>(out), ws + L.o16, elems, s));
+    SAF_TRY(launch_f32_to_bf16(static_cast<const float*>(dout), ws + L.do16, elems, s));
+    q16 = ws + L.q16;
+    k16 = ws + L.k16;
+    v16 = ws + L.v16;
+    o16 = ws + L.o16;
+    do16 = ws + L.do16;
+    dq16 = ws + L.dq16;
+    dk16 = ws + L.dk16;
+    dv16 = ws + L.dv16;
+  }
+  if (hs.n_static > 0) SAF_TRY(launch_static_prep(make_prep(d, hs, alpha, rho, ws, L), s));
+
+  // pre-pass: D, lse2, per-head batch sums of D for static heads
+  BwdPre pre;
+  memset(&pre, 0, sizeof(pre));
+  pre.B = d.B; pre.H = d.H; pre.T = d.T; pre.d_h = d.d_h;
+  pre.out = static_cast<const __nv_bfloat16*>(o16);
+  pre.dout = static_cast<const __nv_bfloat16*>(do16);
+  pre.lse = lse;
+  pre.Dvec = reinterpret_cast<float*>(ws + L.Dvec);
+  pre.lse2 = reinterpret_cast<float*>(ws + L.lse2);
+  pre.Dsum = dalpha ? reinterpret_cast<float*>(ws + L.Dsum) : nullptr;
+  pre.n_static = hs.n_static;
+  memcpy(pre.static_heads, hs.st, sizeof(pre.static_heads));
+  SAF_TRY(launch_bwd_pre(pre, s));
+
+  float* dq_acc = reinterpret_cast<float*>(ws + L.dq_acc);
+  if (hs.n_dynamic > 0) {
+    SAF_TRY(launch_zero_u32(dq_acc, elems, s));
+    BwdLaunch bl;
+    memset(&bl, 0, sizeof(bl));
+    BwdParams& p = bl.p;
+    p.B = d.B; p.H = d.H; p.T = d.T; p.nI = d.T / 128;
+    p.n_dynamic = hs.n_dynamic;
+    p.n_items = p.nI * d.B * hs.n_dynamic;
+    p.scale = 1.0f / sqrtf((float)d.d_h);
+    p.scale_log2 = 1.4426950408889634f * p.scale;
+    memcpy(p.dynamic_heads, hs.dy, sizeof(p.dynamic_heads));
+    p.lse2 = pre.lse2;
+    p.Dvec = pre.Dvec;
+    p.dq_acc = dq_acc;
+    p.dK = static_cast<__nv_bfloat16*>(dk16);
+    p.dV = static_cast<__nv_bfloat16*>(dv16);
+    p.status = reinterpret_cast<int*>(ws + L.status);
+    if (!encode_rows(&bl.tm_q, q16, rows, d.d_h) || !encode_rows(&bl.tm_k, k16, rows, d.d_h) ||
+        !encode_rows(&bl.tm_v, v16, rows, d.d_h) || !encode_rows(&bl.tm_do, do16, rows, d.d_h))
+      return SAF_ERR_CUDA;
+    bl.d_h = d.d_h;
+    bl.num_sms = sm_count();
+    SAF_TRY(launch_bwd_dynamic(bl, s));
+  }
+  if (hs.n_static > 0) {
+    // dV = P^T dO for the frozen heads: the forward's static engine, transposed.
+    FwdLaunch fl;
+    memset(&fl, 0, sizeof(fl));
+    fill_fwd_params(fl.p, d, hs, ws, L, true);
+    fl.p.out = static_cast<__nv_bfloat16*>(dv16);
+    fl.p.lse = nullptr;
+    if (!encode_rows(&fl.tm_q, do16, rows, d.d_h) || !encode_rows(&fl.tm_k, do16, rows, d.d_h) ||
+        !encode_rows(&fl.tm_v, do16, rows, d.d_h))
+      return SAF_ERR_CUDA;
+    fl.d_h = d.d_h;
+    fl.transposed = true;
+    fl.num_sms = sm_count();
+    SAF_TRY(launch_hybrid_fwd(fl, s));
+  }
+  if (dalpha) {
+    SAF_TRY(launch_zero_u32(dalpha, (size_t)d.H * d.T, s));
+    SAF_TRY(launch_zero_u32(drho, (size_t)d.H * d.T, s));
+    if (hs.n_static > 0) {
+      ParamGradLaunch gl;
+      memset(&gl, 0, sizeof(gl));
+      ParamGradParams& p = gl.p;
+      p.B = d.B; p.H = d.H; p.T = d.T; p.nI = d.T / 128;
+      p.n_static = hs.n_static;
+      p.n_items = hs.n_static * p.nI;
+      memcpy(p.static_heads, hs.st, sizeof(p.static_heads));
+      p.a_tab = reinterpret_cast<const float*>(ws + L.a_tab);
+      p.r_tab = reinterpret_cast<const float*>(ws + L.r_tab);
+      p.row_tab = reinterpret_cast<const float*>(ws + L.row_tab);
+      p.mode = reinterpret_cast<const int*>(ws + L.mode);
+      p.Dsum = pre.Dsum;
+      p.dalpha = dalpha;
+      p.drho = drho;
+      p.status = reinterpret_cast<int*>(ws + L.status);
+      if (!encode_rows(&gl.tm_v, v16, rows, d.d_h) || !encode_rows(&gl.tm_do, do16, rows, d.d_h))
+        return SAF_ERR_CUDA;
+      gl.d_h = d.d_h;
+      gl.num_sms = sm_count();
+      SAF_TRY(launch_param_grads(gl, s));
+    }
+  }
+  BwdPost post;
+  memset(&post, 0, sizeof(post));
+  post.B = d.B; post.H = d.H; post.T = d.T; post.d_h = d.d_h;
+  post.dq_acc = dq_acc;
+  post.dQ = static_cast<__nv_bfloat16*>(dq16);
+  post.dK = static_cast<__nv_bfloat16*>(dk16);
+  memcpy(post.is_static, hs.is_static, sizeof(post.is_static));
+  SAF_TRY(launch_bwd_post(post, s));
+  if (d.dtype == SAF_F32) {
+    SAF_TRY(launch_bf16_to_f32(dq16, static_cast<float*>(dQ), elems, s));
+    SAF_TRY(launch_bf16_to_f32(dk16, static_cast<float*>(dK), elems, s));
+    SAF_TRY(launch_bf16_to_f32(dv16, static_cast<float*>(dV), elems, s));
+  }
+  return SAF_OK;
+}
+
+// ------------------------------------------------------------ calibration
+namespace {
+struct CalibHandle {
+  int num_heads = 0, T = 0;
+  float* mean = nullptr;
+  float* m2 = nullptr;
+  double* partials = nullptr;
+  int* status = nullptr;
+  std::vector<int> counts;
+};
+}  // namespace
+
+saf_status saf_calib_create(void** handle, int num_heads, int T) {
+  g_launches = 0;
+  if (!handle) return SAF_ERR_INVALID_ARG;
+  *handle = nullptr;
+  if (num_heads < 1 || T < 4 || T % 4 != 0) return SAF_ERR_INVALID_ARG;
+  if (T > kMaxT || num_heads > 8192) return SAF_ERR_UNSUPPORTED;
+  CalibHandle* h = new CalibHandle();
+  h->num_heads = num_heads;
+  h->T = T;
+  h->counts.assign(num_heads, 0);
+  const size_t n = (size_t)num_heads * T * T;
+  if (cudaMalloc(&h->mean, n * 4) != cudaSuccess || cudaMalloc(&h->m2, n * 4) != cudaSuccess ||
+      cudaMalloc(&h->partials, (size_t)num_heads * T * 8) != cudaSuccess ||
+      cudaMalloc(&h->status, 256) != cudaSuccess || cudaMemset(h->status, 0, 256) != cudaSuccess) {
+    cudaFree(h->mean);
+    cudaFree(h->m2);
+    cudaFree(h->partials);
+    cudaFree(h->status);
+    delete h;
+    return SAF_ERR_CUDA;
+  }
+  *handle = h;
+  return SAF_OK;
+}
+
+saf_status saf_calib_accumulate(void* handle, const float* A, int n, int head_begin,
+                                int head_count, void* stream) {
+  g_launches = 0;
+  CalibHandle* h = static_cast<CalibHandle*>(handle);
+  if (!h || !A || !aligned16(A) || n < 1 || head_count < 1 || head_begin < 0 ||
+      head_begin + head_count > h->num_heads)
+    return SAF_ERR_INVALID_ARG;
+  const int c0 = h->counts[head_begin];
+  for (int i = head_begin; i < head_begin + head_count; ++i)
+    if (h->counts[i] != c0) return SAF_ERR_STATE;
+  CalibLaunch p;
+  p.A = A;
+  p.n = n;
+  p.head_begin = head_begin;
+  p.head_count = head_count;
+  p.T = h->T;
+  p.count0 = c0;
+  p.mean = h->mean;
+  p.m2 = h->m2;
+  const cudaError_t e = launch_calib_accumulate(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return SAF_ERR_CUDA;
+  for (int i = head_begin; i < head_begin + head_count; ++i) h->counts[i] += n;
+  return SAF_OK;
+}
+
+int saf_calib_num_select(double r, int num_heads) {
+  const double x = r * (double)num_heads;
+  return (int)nearbyint(x);  // default rounding mode: ties to even
+}
+
+saf_status saf_calib_finalize(void* handle, int k, float* A_hat, float* s_var, int32_t* selected,
+                              void* stream) {
+  g_launches = 0;
+  CalibHandle* h = static_cast<CalibHandle*>(handle);
+  if (!h || !s_var || !aligned16(s_var) || (A_hat && !aligned16(A_hat))) return SAF_ERR_INVALID_ARG;
+  if (k < 0 || k > h->num_heads || (k > 0 && !selected)) return SAF_ERR_INVALID_ARG;
+  const int N = h->counts[0];
+  for (int c : h->counts)
+    if (c != N) return SAF_ERR_STATE;
+  if (N < 2) return SAF_ERR_STATE;
+  CalibFinalize p;
+  p.num_heads = h->num_heads;
+  p.T = h->T;
+  p.N = N;
+  p.k = k;
+  p.mean = h->mean;
+  p.m2 = h->m2;
+  p.row_partials = h->partials;
+  p.A_hat = A_hat;
+  p.s_var = s_var;
+  p.selected = selected;
+  return cuda_status(launch_calib_finalize(p, static_cast<cudaStream_t>(stream)));
+}
+
+saf_status saf_calib_reset(void* handle) {
+  CalibHandle* h = static_cast<CalibHandle*>(handle);
+  if (!h) return SAF_ERR_INVALID_ARG;
+  for (int& c : h->counts) c = 0;
+  return SAF_OK;
+}
+
+saf_status saf_calib_destroy(void* handle) {
+  CalibHandle* h = static_cast<CalibHandle*>(handle);
+  if (!h) return SAF_OK;
+  cudaDeviceSynchronize();
+  cudaFree(h->mean);
+  cudaFree(h->m2);
+  cudaFree(h->partials);
+  cudaFree(h->status);
+  delete h;
+  return SAF_OK;
+}
+
+saf_status saf_get_device_status(void* workspace_or_handle, int is_calib_handle, int* site,
+                                 void* stream) {
+  if (site) *site = 0;
+  if (!workspace_or_handle) return SAF_ERR_INVALID_ARG;
+  int* word = is_calib_handle ? static_cast<CalibHandle*>(workspace_or_handle)->status
+                              : static_cast<int*>(workspace_or_handle);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int v = 0;
+  if (cudaMemcpyAsync(&v, word, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemsetAsync(word, 0, sizeof(int), s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return SAF_ERR_CUDA;
+  if (site) *site = v;
+  return v == 0 ? SAF_OK : SAF_ERR_TIMEOUT;
+}
+
+}  // extern "C"

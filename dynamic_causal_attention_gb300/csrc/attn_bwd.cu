@@ -1,0 +1,604 @@
+// attn_bwd.cu — backward of the SAF hybrid layer: dynamic heads, and the
+// alpha/rho gradients of frozen heads.
+//
+// ("When Can Attention Heads Be Statically Defined?", close-reading notes:
+// dynamic heads keep the ordinary attention backward; a frozen head's
+// attention backward is only dV = P^T dZ, §3.3 / App. D.2 — that part reuses
+// the forward's static engine, transposed.  The alpha/rho gradients are an
+// extension: the chain rule through Eq. (3).)
+//
+// bwd_dynamic_kernel (K4): one persistent launch over items (b, h, J), J a
+// 128-row key tile, longest first.  Per item K_J and V_J stay in shared
+// memory and dK_J, dV_J accumulate in TMEM while the query tiles I = J..nI-1
+// stream through:
+//     S^T  = K_J Q_I^T,  dP^T = V_J dO_I^T           (tcgen05, fp32 in TMEM)
+//     P^T  = exp2(S^T * log2e/sqrt(d) - lse2(i)),   dS^T = P^T * (dP^T - D(i))
+//                                                   (compute warps, 1 row/thread)
+//     dV_J += P^T dO_I,  dK_J += dS^T Q_I,  dQ_I = dS K_J   (tcgen05)
+// dQ_I is read from TMEM by a second warpgroup and added into an fp32
+// accumulator with vector atomics; a post-pass scales it by 1/sqrt(d) and
+// converts it.
+//
+// param_grad_kernel (K5): items (h_static, J).  For I = J..nI-1 the batch-
+// summed dP^T(j, i) = sum_b V_b(j) . dO_b(i) is one MMA chain with K = B*d;
+// the compute warps form dl = P(i,j) (dP - sum_b D_b(i)) with P(i,j) rebuilt
+// from the static tables, keep the column sums (alpha) per thread, and
+// accumulate the diagonal sums (rho) in shared memory, flushed to global with
+// atomics once per tile.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "attn_common.cuh"
+#include "attn_kernels.h"
+#include "internal.h"
+
+namespace saf {
+namespace {
+
+constexpr uint32_t kTmemCols = 512;
+
+template <int D>
+struct BwdSmem {
+  using G = TileGeom<D>;
+  static constexpr int QST = (D == 128) ? 1 : 2;
+  static constexpr int STAGE = 2 * G::TILE_BYTES + 1024;  // Q_I, dO_I, lse2[128], D[128]
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + G::TILE_BYTES;
+  static constexpr int OFF_Q = OFF_V + G::TILE_BYTES;
+  static constexpr int OFF_PT = OFF_Q + QST * STAGE;
+  static constexpr int OFF_DST = OFF_PT + SqTile::BYTES;
+  static constexpr int OFF_BAR = OFF_DST + SqTile::BYTES;
+  static constexpr int NBAR = 2 + 2 * QST + 8;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int ALLOC = OFF_MISC + 16 + 1024;
+  static_assert(ALLOC <= 232448, "shared memory budget exceeded");
+  // TMEM columns
+  static constexpr uint32_t T_S = 0, T_DP = 128, T_DV = 256, T_DK = 256 + D;
+  static constexpr bool DQ_ALIAS = (256 + 3 * D > 512);
+  static constexpr uint32_t T_DQ = DQ_ALIAS ? 0 : 256 + 2 * D;
+};
+
+enum : int {
+  kSiteBProdKV = 101, kSiteBProdQ, kSiteBMmaKV, kSiteBMmaQ, kSiteBMmaS, kSiteBMmaP, kSiteBMmaKD,
+  kSiteBMmaDQ, kSiteBCmpQ, kSiteBCmpS, kSiteBCmpP, kSiteBCmpKD, kSiteBDq
+};
+
+struct BItem {
+  int b, h, J, nsteps;
+};
+
+__device__ __forceinline__ BItem decode_bwd(const BwdParams& p, int it) {
+  BItem r;
+  const int per = p.B * p.n_dynamic;
+  r.J = it / per;
+  const int rem = it - r.J * per;
+  r.b = rem / p.n_dynamic;
+  r.h = p.dynamic_heads[rem - r.b * p.n_dynamic];
+  r.nsteps = p.nI - r.J;
+  return r;
+}
+
+template <int D>
+__global__ void __launch_bounds__(384, 1)
+    bwd_dynamic_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+  using G = TileGeom<D>;
+  using L = BwdSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~(uintptr_t)1023);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
+  uint64_t* kv_full = bars + 0;
+  uint64_t* kv_empty = bars + 1;
+  uint64_t* q_full = bars + 2;
+  uint64_t* q_empty = q_full + L::QST;
+  uint64_t* s_full = q_empty + L::QST;
+  uint64_t* s_free = s_full + 1;
+  uint64_t* p_full = s_free + 1;
+  uint64_t* p_empty = p_full + 1;
+  uint64_t* dq_full = p_empty + 1;
+  uint64_t* dq_empty = dq_full + 1;
+  uint64_t* kd_full = dq_empty + 1;
+  uint64_t* kd_empty = kd_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
+  const WaitCtl wc{abort_flag, p.status};
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    mbar_init(kv_empty, 1);
+    for (int s = 0; s < L::QST; ++s) { mbar_init(q_full + s, 1); mbar_init(q_empty + s, 1); }
+    mbar_init(s_full, 1);
+    mbar_init(s_free, 128);
+    mbar_init(p_full, 128);
+    mbar_init(p_empty, 1);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_empty, 128);
+    mbar_init(kd_full, 1);
+    mbar_init(kd_empty, 128);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t sK = smem_u32(smem + L::OFF_K);
+  const uint32_t sV = smem_u32(smem + L::OFF_V);
+  const uint32_t sPT = smem_u32(smem + L::OFF_PT);
+  const uint32_t sDST = smem_u32(smem + L::OFF_DST);
+  const int H = p.H, T = p.T;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- producer
+    if (lane == 0) {
+      uint32_t kvc = 0, qc = 0;
+      for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+        const BItem w = decode_bwd(p, it);
+        const int row0 = (w.b * H + w.h) * T;
+        mbar_wait(kv_empty, (kvc & 1) ^ 1, wc, kSiteBProdKV);
+        ++kvc;
+        mbar_arrive_expect_tx(kv_full, 2 * G::TILE_BYTES);
+        for (int c = 0; c < G::NCHUNK; ++c) {
+          tma_load_2d(smem + L::OFF_K + c * G::CHUNK_BYTES, &tm_k, kv_full, c * G::CHUNK,
+                      row0 + w.J * 128);
+          tma_load_2d(smem + L::OFF_V + c * G::CHUNK_BYTES, &tm_v, kv_full, c * G::CHUNK,
+                      row0 + w.J * 128);
+        }
+        for (int t = 0; t < w.nsteps; ++t) {
+          const int I = w.J + t;
+          const int qs = qc % L::QST;
+          mbar_wait(q_empty + qs, ((qc / L::QST) & 1) ^ 1, wc, kSiteBProdQ);
+          ++qc;
+          uint8_t* st = smem + L::OFF_Q + qs * L::STAGE;
+          mbar_arrive_expect_tx(q_full + qs, 2 * G::TILE_BYTES + 1024);
+          for (int c = 0; c < G::NCHUNK; ++c) {
+            tma_load_2d(st + c * G::CHUNK_BYTES, &tm_q, q_full + qs, c * G::CHUNK, row0 + I * 128);
+            tma_load_2d(st + G::TILE_BYTES + c * G::CHUNK_BYTES, &tm_do, q_full + qs, c * G::CHUNK,
+                        row0 + I * 128);
+          }
+          bulk_load(st + 2 * G::TILE_BYTES, p.lse2 + row0 + I * 128, 512, q_full + qs);
+          bulk_load(st + 2 * G::TILE_BYTES + 512, p.Dvec + row0 + I * 128, 512, q_full + qs);
+        }
+      }
+      if (kvc > 0) mbar_drain(kv_full, (kvc - 1) & 1);
+      for (int s = 0; s < L::QST; ++s)
+        if (qc > (uint32_t)s) mbar_drain(q_full + s, ((qc - 1 - s) / L::QST) & 1);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t id_acc = idesc_bf16(128, D, false, true);
+      constexpr uint32_t id_dq = idesc_bf16(128, D, true, true);
+      uint32_t kvc = 0, qc = 0, sc = 0, pc = 0, dqc = 0, kdc = 0;
+      for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+        const BItem w = decode_bwd(p, it);
+        mbar_wait(kv_full, kvc & 1, wc, kSiteBMmaKV);
+        ++kvc;
+        for (int t = 0; t < w.nsteps; ++t) {
+          const int qs = qc % L::QST;
+          mbar_wait(q_full + qs, (qc / L::QST) & 1, wc, kSiteBMmaQ);
+          mbar_wait(s_free, (sc & 1) ^ 1, wc, kSiteBMmaS);
+          if (L::DQ_ALIAS) mbar_wait(dq_empty, (dqc & 1) ^ 1, wc, kSiteBMmaDQ);
+          tc_fence_after();
+          const uint32_t sQ = smem_u32(smem + L::OFF_Q + qs * L::STAGE);
+          const uint32_t sDO = sQ + G::TILE_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < G::KSTEPS; ++kk)
+            mma_bf16_ss(tmem + L::T_S, G::kmajor_desc(sK, kk), G::kmajor_desc(sQ, kk), id_s,
+                        kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < G::KSTEPS; ++kk)
+            mma_bf16_ss(tmem + L::T_DP, G::kmajor_desc(sV, kk), G::kmajor_desc(sDO, kk), id_s,
+                        kk > 0);
+          mma_commit(s_full);
+          ++sc;
+          mbar_wait(p_full, pc & 1, wc, kSiteBMmaP);
+          if (t == 0) mbar_wait(kd_empty, (kdc & 1) ^ 1, wc, kSiteBMmaKD);
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tmem + L::T_DV, SqTile::kmajor_desc(sPT, kk), G::mnmajor_desc(sDO, kk),
+                        id_acc, (t > 0 || kk > 0));
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tmem + L::T_DK, SqTile::kmajor_desc(sDST, kk), G::mnmajor_desc(sQ, kk),
+                        id_acc, (t > 0 || kk > 0));
+          if (!L::DQ_ALIAS) mbar_wait(dq_empty, (dqc & 1) ^ 1, wc, kSiteBMmaDQ);
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tmem + L::T_DQ, SqTile::mnmajor_desc(sDST, kk), G::mnmajor_desc(sK, kk),
+                        id_dq, kk > 0);
+          mma_commit(q_empty + qs);
+          mma_commit(p_empty);
+          mma_commit(dq_full);
+          ++qc;
+          ++pc;
+          ++dqc;
+        }
+        mma_commit(kd_full);
+        mma_commit(kv_empty);
+        ++kdc;
+      }
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ---------------------------------------------------------- compute WG
+    const int r = threadIdx.x - 128;  // key row j within the tile == TMEM lane
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    uint32_t qc = 0, sc = 0, pc = 0, kdc = 0;
+    for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+      const BItem w = decode_bwd(p, it);
+      for (int t = 0; t < w.nsteps; ++t) {
+        const int qs = qc % L::QST;
+        mbar_wait(q_full + qs, (qc / L::QST) & 1, wc, kSiteBCmpQ);
+        const float* lse_s = reinterpret_cast<const float*>(smem + L::OFF_Q + qs * L::STAGE +
+                                                            2 * G::TILE_BYTES);
+        const float* d_s = lse_s + 128;
+        mbar_wait(s_full, sc & 1, wc, kSiteBCmpS);
+        mbar_wait(p_empty, (pc & 1) ^ 1, wc, kSiteBCmpP);
+        tc_fence_after();
+        const bool diag = (t == 0);
+#pragma unroll 1
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t sv[32], dv[32];
+          tmem_ld_x32(tmem + lane_base + L::T_S + c0, sv);
+          tmem_ld_x32(tmem + lane_base + L::T_DP + c0, dv);
+          tmem_wait_ld(sv);
+          tmem_wait_ld(dv);
+          uint32_t pk[16], dk[16];
+#pragma unroll
+          for (int k = 0; k < 32; k += 2) {
+            const int c = c0 + k;
+            float p0 = fast_exp2(fmaf(__uint_as_float(sv[k]), p.scale_log2, -lse_s[c]));
+            float p1 = fast_exp2(fmaf(__uint_as_float(sv[k + 1]), p.scale_log2, -lse_s[c + 1]));
+            if (diag && c < r) p0 = 0.f;
+            if (diag && c + 1 < r) p1 = 0.f;
+            const float g0 = p0 * (__uint_as_float(dv[k]) - d_s[c]);
+            const float g1 = p1 * (__uint_as_float(dv[k + 1]) - d_s[c + 1]);
+            pk[k >> 1] = pack_bf16x2(p0, p1);
+            dk[k >> 1] = pack_bf16x2(g0, g1);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t unit = (uint32_t)(c0 >> 3) + u;
+            st_shared_v4(SqTile::unit_addr(sPT, r, unit), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2],
+                         pk[4 * u + 3]);
+            st_shared_v4(SqTile::unit_addr(sDST, r, unit), dk[4 * u], dk[4 * u + 1],
+                         dk[4 * u + 2], dk[4 * u + 3]);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(s_free);
+        fence_proxy_async_smem();
+        mbar_arrive(p_full);
+        ++qc;
+        ++sc;
+        ++pc;
+      }
+      // epilogue: dV_J, dK_J (scaled) -> global
+      mbar_wait(kd_full, kdc & 1, wc, kSiteBCmpKD);
+      tc_fence_after();
+      const size_t orow = (size_t)(w.b * H + w.h) * T + (size_t)w.J * 128 + r;
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {
+        __nv_bfloat16* dst = (which == 0 ? p.dV : p.dK) + orow * D;
+        const float sc_out = which == 0 ? 1.0f : p.scale;
+        const uint32_t col = which == 0 ? L::T_DV : L::T_DK;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 16) {
+          uint32_t o[16];
+          tmem_ld_x16(tmem + lane_base + col + c0, o);
+          tmem_wait_ld(o);
+          uint4 v0, v1;
+          v0.x = pack_bf16x2(__uint_as_float(o[0]) * sc_out, __uint_as_float(o[1]) * sc_out);
+          v0.y = pack_bf16x2(__uint_as_float(o[2]) * sc_out, __uint_as_float(o[3]) * sc_out);
+          v0.z = pack_bf16x2(__uint_as_float(o[4]) * sc_out, __uint_as_float(o[5]) * sc_out);
+          v0.w = pack_bf16x2(__uint_as_float(o[6]) * sc_out, __uint_as_float(o[7]) * sc_out);
+          v1.x = pack_bf16x2(__uint_as_float(o[8]) * sc_out, __uint_as_float(o[9]) * sc_out);
+          v1.y = pack_bf16x2(__uint_as_float(o[10]) * sc_out, __uint_as_float(o[11]) * sc_out);
+          v1.z = pack_bf16x2(__uint_as_float(o[12]) * sc_out, __uint_as_float(o[13]) * sc_out);
+          v1.w = pack_bf16x2(__uint_as_float(o[14]) * sc_out, __uint_as_float(o[15]) * sc_out);
+          *reinterpret_cast<uint4*>(dst + c0) = v0;
+          *reinterpret_cast<uint4*>(dst + c0 + 8) = v1;
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(kd_empty);
+      ++kdc;
+    }
+  } else if (warp >= 8) {
+    // ---------------------------------------------------------- dQ warps
+    const int r = threadIdx.x - 256;  // query row i within the tile == TMEM lane
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    uint32_t dqc = 0;
+    for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+      const BItem w = decode_bwd(p, it);
+      for (int t = 0; t < w.nsteps; ++t) {
+        const int I = w.J + t;
+        mbar_wait(dq_full, dqc & 1, wc, kSiteBDq);
+        tc_fence_after();
+        float* dst = p.dq_acc + ((size_t)(w.b * H + w.h) * T + (size_t)I * 128 + r) * D;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 16) {
+          uint32_t o[16];
+          tmem_ld_x16(tmem + lane_base + L::T_DQ + c0, o);
+          tmem_wait_ld(o);
+#pragma unroll
+          for (int e = 0; e < 16; e += 4)
+            atomicAdd(reinterpret_cast<float4*>(dst + c0 + e),
+                      make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]),
+                                  __uint_as_float(o[e + 2]), __uint_as_float(o[e + 3])));
+        }
+        tc_fence_before();
+        mbar_arrive(dq_empty);
+        ++dqc;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ============================================================ K5: dalpha/drho
+template <int D>
+struct PgSmem {
+  using G = TileGeom<D>;
+  static constexpr int ST = (D == 128) ? 3 : 4;        // (V_b[J], dO_b[I]) pairs
+  static constexpr int STAGE = 2 * G::TILE_BYTES;
+  static constexpr int AUX = 2048;                     // col values, D sums, window
+  static constexpr int OFF_ST = 0;
+  static constexpr int OFF_AUX = OFF_ST + ST * STAGE;
+  static constexpr int OFF_WIN = OFF_AUX + 2 * AUX;    // 256 floats of diagonal sums
+  static constexpr int OFF_BAR = OFF_WIN + 1024;
+  static constexpr int NBAR = 2 * ST + 4 + 4;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int ALLOC = OFF_MISC + 16 + 1024;
+  static_assert(ALLOC <= 232448, "shared memory budget exceeded");
+};
+
+enum : int { kSitePgProd = 201, kSitePgProdAux, kSitePgMma, kSitePgMmaAcc, kSitePgAux, kSitePgAcc };
+
+template <int D>
+__global__ void __launch_bounds__(256, 1)
+    param_grad_kernel(const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_do, const ParamGradParams p) {
+  using G = TileGeom<D>;
+  using L = PgSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~(uintptr_t)1023);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
+  uint64_t* st_full = bars;
+  uint64_t* st_empty = st_full + L::ST;
+  uint64_t* aux_full = st_empty + L::ST;
+  uint64_t* aux_empty = aux_full + 2;
+  uint64_t* acc_full = aux_empty + 2;
+  uint64_t* acc_empty = acc_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
+  const WaitCtl wc{abort_flag, p.status};
+  float* win = reinterpret_cast<float*>(smem + L::OFF_WIN);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < L::ST; ++s) { mbar_init(st_full + s, 1); mbar_init(st_empty + s, 1); }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(aux_full + s, 1);
+      mbar_init(aux_empty + s, 1);
+      mbar_init(acc_full + s, 1);
+      mbar_init(acc_empty + s, 128);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int H = p.H, T = p.T, B = p.B;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t sc = 0, ac = 0;
+      for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+        const int J = it / p.n_static, hs = it - J * p.n_static, h = p.static_heads[hs];
+        for (int I = J; I < p.nI; ++I) {
+          const int as = ac & 1;
+          mbar_wait(aux_empty + as, ((ac >> 1) & 1) ^ 1, wc, kSitePgProdAux);
+          ++ac;
+          uint8_t* aux = smem + L::OFF_AUX + as * L::AUX;
+          mbar_arrive_expect_tx(aux_full + as, 2048);
+          bulk_load(aux, p.row_tab + (size_t)hs * T + I * 128, 512, aux_full + as);
+          bulk_load(aux + 512, p.Dsum + (size_t)hs * T + I * 128, 512, aux_full + as);
+          bulk_load(aux + 1024, p.r_tab + (size_t)hs * (T + 128) + (I - J) * 128, 1024,
+                    aux_full + as);
+          for (int b = 0; b < B; ++b) {
+            const int s = sc % L::ST;
+            mbar_wait(st_empty + s, ((sc / L::ST) & 1) ^ 1, wc, kSitePgProd);
+            ++sc;
+            uint8_t* st = smem + L::OFF_ST + s * L::STAGE;
+            const int row0 = (b * H + h) * T;
+            mbar_arrive_expect_tx(st_full + s, 2 * G::TILE_BYTES);
+            for (int c = 0; c < G::NCHUNK; ++c) {
+              tma_load_2d(st + c * G::CHUNK_BYTES, &tm_v, st_full + s, c * G::CHUNK,
+                          row0 + J * 128);
+              tma_load_2d(st + G::TILE_BYTES + c * G::CHUNK_BYTES, &tm_do, st_full + s,
+                          c * G::CHUNK, row0 + I * 128);
+            }
+          }
+        }
+      }
+      for (int s = 0; s < L::ST; ++s)
+        if (sc > (uint32_t)s) mbar_drain(st_full + s, ((sc - 1 - s) / L::ST) & 1);
+      for (int s = 0; s < 2; ++s)
+        if (ac > (uint32_t)s) mbar_drain(aux_full + s, ((ac - 1 - s) >> 1) & 1);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t id = idesc_bf16(128, 128, false, false);
+      uint32_t sc = 0, cc = 0;
+      for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+        const int J = it / p.n_static;
+        for (int I = J; I < p.nI; ++I) {
+          const int ab = cc & 1;
+          mbar_wait(acc_empty + ab, ((cc >> 1) & 1) ^ 1, wc, kSitePgMmaAcc);
+          tc_fence_after();
+          for (int b = 0; b < B; ++b) {
+            const int s = sc % L::ST;
+            mbar_wait(st_full + s, (sc / L::ST) & 1, wc, kSitePgMma);
+            tc_fence_after();
+            const uint32_t sv = smem_u32(smem + L::OFF_ST + s * L::STAGE);
+#pragma unroll
+            for (int kk = 0; kk < G::KSTEPS; ++kk)
+              mma_bf16_ss(tmem + ab * 128, G::kmajor_desc(sv, kk),
+                          G::kmajor_desc(sv + G::TILE_BYTES, kk), id, (b > 0 || kk > 0));
+            mma_commit(st_empty + s);
+            ++sc;
+          }
+          mma_commit(acc_full + ab);
+          ++cc;
+        }
+      }
+    }
+  } else if (warp >= 4) {
+    const int r = threadIdx.x - 128;  // key row j within tile J
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    uint32_t ac = 0, cc = 0;
+    for (int t = r; t < 256; t += 128) win[t] = 0.f;
+    named_bar_sync(1, 128);
+    for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+      const int J = it / p.n_static, hs = it - J * p.n_static, h = p.static_heads[hs];
+      const bool exact = p.mode[hs] != 0;
+      const float rowv = p.a_tab[(size_t)hs * T + J * 128 + r];
+      float dalpha = 0.f;
+      for (int I = J; I < p.nI; ++I) {
+        const int as = ac & 1;
+        mbar_wait(aux_full + as, (ac >> 1) & 1, wc, kSitePgAux);
+        const float* aux = reinterpret_cast<const float*>(smem + L::OFF_AUX + as * L::AUX);
+        const float* colv = aux;          // 1/Z'(i) or -log2 Z(i)
+        const float* dsum = aux + 128;    // sum_b D_b(i)
+        const float* rwin = aux + 256;    // r(i - j), centre 127
+        const int ab = cc & 1;
+        mbar_wait(acc_full + ab, (cc >> 1) & 1, wc, kSitePgAcc);
+        tc_fence_after();
+#pragma unroll 1
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld_x32(tmem + lane_base + ab * 128 + c0, v);
+          tmem_wait_ld(v);
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const int c = c0 + k;
+            const float wv = rwin[127 + c - r];
+            const float pij = exact ? fast_exp2(rowv + wv + colv[c]) : rowv * wv * colv[c];
+            const float dl = pij * (__uint_as_float(v[k]) - dsum[c]);
+            dalpha += dl;
+            atomicAdd(&win[127 + c - r], dl);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(acc_empty + ab);
+        ++cc;
+        named_bar_sync(1, 128);
+        if (r == 0) mbar_arrive(aux_empty + as);
+        ++ac;
+        // flush the diagonal sums of this tile: distance (I-J)*128 - 127 + t
+        for (int t = r; t < 256; t += 128) {
+          const int delta = (I - J) * 128 - 127 + t;
+          const float vsum = win[t];
+          win[t] = 0.f;
+          if (delta >= 0 && delta < T && vsum != 0.f) atomicAdd(&p.drho[(size_t)h * T + delta], vsum);
+        }
+        named_bar_sync(1, 128);
+      }
+      p.dalpha[(size_t)h * T + J * 128 + r] = dalpha;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+template <typename K>
+cudaError_t set_smem(K kern, int bytes, bool& done) {
+  if (done) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done = true;
+  return e;
+}
+
+template <int D>
+cudaError_t launch_dyn(const BwdLaunch& L, cudaStream_t s) {
+  static bool done = false;
+  cudaError_t e = set_smem(bwd_dynamic_kernel<D>, BwdSmem<D>::ALLOC, done);
+  if (e != cudaSuccess) return e;
+  if (L.p.n_items == 0) return cudaSuccess;
+  const int grid = L.p.n_items < L.num_sms ? L.p.n_items : L.num_sms;
+  bwd_dynamic_kernel<D><<<grid, 384, BwdSmem<D>::ALLOC, s>>>(L.tm_q, L.tm_k, L.tm_v, L.tm_do, L.p);
+  note_launch();
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_pg(const ParamGradLaunch& L, cudaStream_t s) {
+  static bool done = false;
+  cudaError_t e = set_smem(param_grad_kernel<D>, PgSmem<D>::ALLOC, done);
+  if (e != cudaSuccess) return e;
+  if (L.p.n_items == 0) return cudaSuccess;
+  const int grid = L.p.n_items < L.num_sms ? L.p.n_items : L.num_sms;
+  param_grad_kernel<D><<<grid, 256, PgSmem<D>::ALLOC, s>>>(L.tm_v, L.tm_do, L.p);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_dynamic(const BwdLaunch& L, cudaStream_t s) {
+  switch (L.d_h) {
+    case 32: return launch_dyn<32>(L, s);
+    case 64: return launch_dyn<64>(L, s);
+    case 128: return launch_dyn<128>(L, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_param_grads(const ParamGradLaunch& L, cudaStream_t s) {
+  switch (L.d_h) {
+    case 32: return launch_pg<32>(L, s);
+    case 64: return launch_pg<64>(L, s);
+    case 128: return launch_pg<128>(L, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace saf

@@ -1,0 +1,121 @@
+// attn_bwd_aux.cu — the small bandwidth-bound passes around the backward
+// kernels of the hybrid layer:
+//   bwd_pre   D(b,h,i) = sum_d dO(b,h,i,d) * out(b,h,i,d) (the softmax
+//             backward's row term), lse2 = lse * log2(e), and for frozen heads
+//             the batch sums of D that the alpha/rho gradients need;
+//   bwd_post  dQ = (1/sqrt(d_h)) * fp32 accumulator -> bf16, and zeros for the
+//             dQ/dK rows of frozen heads (they have no query/key path).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "attn_kernels.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace saf {
+namespace {
+
+// One group of D/8 lanes per row; each lane reads 8 bf16 of dO and of out.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(BwdPre p) {
+  constexpr int LPR = D / 8;  // lanes per row
+  const size_t rows = (size_t)p.B * p.H * p.T;
+  const int lane = threadIdx.x & 31;
+  const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t row = tid / LPR;
+  const int sub = (int)(tid % LPR);
+  float acc = 0.f;
+  if (row < rows) {
+    const uint4 a = *reinterpret_cast<const uint4*>(p.out + row * D + sub * 8);
+    const uint4 b = *reinterpret_cast<const uint4*>(p.dout + row * D + sub * 8);
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 x = __bfloat1622float2(a2[k]), y = __bfloat1622float2(b2[k]);
+      acc = fmaf(x.x, y.x, acc);
+      acc = fmaf(x.y, y.y, acc);
+    }
+  }
+#pragma unroll
+  for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  (void)lane;
+  if (row < rows && sub == 0) {
+    p.Dvec[row] = acc;
+    p.lse2[row] = p.lse[row] * 1.4426950408889634f;
+  }
+}
+
+__global__ void dsum_kernel(BwdPre p) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x, hs = blockIdx.y;
+  if (i >= p.T) return;
+  const int h = p.static_heads[hs];
+  float s = 0.f;
+  for (int b = 0; b < p.B; ++b) s += p.Dvec[((size_t)b * p.H + h) * p.T + i];
+  p.Dsum[(size_t)hs * p.T + i] = s;
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) bwd_post_kernel(BwdPost p, float scale) {
+  const size_t n8 = (size_t)p.B * p.H * p.T * D / 8;
+  for (size_t t = (size_t)blockIdx.x * blockDim.x + threadIdx.x; t < n8;
+       t += (size_t)gridDim.x * blockDim.x) {
+    const size_t e = t * 8;
+    const int h = (int)((e / ((size_t)p.T * D)) % p.H);
+    uint4 q;
+    if (p.is_static[h]) {
+      q = make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(p.dK + e) = q;
+    } else {
+      const float4 a = *reinterpret_cast<const float4*>(p.dq_acc + e);
+      const float4 b = *reinterpret_cast<const float4*>(p.dq_acc + e + 4);
+      q.x = pack_bf16x2(a.x * scale, a.y * scale);
+      q.y = pack_bf16x2(a.z * scale, a.w * scale);
+      q.z = pack_bf16x2(b.x * scale, b.y * scale);
+      q.w = pack_bf16x2(b.z * scale, b.w * scale);
+    }
+    *reinterpret_cast<uint4*>(p.dQ + e) = q;
+  }
+}
+
+int grid_for(size_t threads) {
+  size_t b = (threads + 255) / 256;
+  if (b < 1) b = 1;
+  if (b > 8192) b = 8192;
+  return (int)b;
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_pre(const BwdPre& p, cudaStream_t s) {
+  const size_t threads = (size_t)p.B * p.H * p.T * (p.d_h / 8);
+  const int blocks = (int)((threads + 255) / 256);
+  switch (p.d_h) {
+    case 32: bwd_pre_kernel<32><<<blocks, 256, 0, s>>>(p); break;
+    case 64: bwd_pre_kernel<64><<<blocks, 256, 0, s>>>(p); break;
+    case 128: bwd_pre_kernel<128><<<blocks, 256, 0, s>>>(p); break;
+    default: return cudaErrorInvalidValue;
+  }
+  note_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || p.Dsum == nullptr || p.n_static == 0) return e;
+  dsum_kernel<<<dim3((p.T + 255) / 256, p.n_static), 256, 0, s>>>(p);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_post(const BwdPost& p, cudaStream_t s) {
+  const float scale = 1.0f / sqrtf((float)p.d_h);
+  const int blocks = grid_for((size_t)p.B * p.H * p.T * p.d_h / 8);
+  switch (p.d_h) {
+    case 32: bwd_post_kernel<32><<<blocks, 256, 0, s>>>(p, scale); break;
+    case 64: bwd_post_kernel<64><<<blocks, 256, 0, s>>>(p, scale); break;
+    case 128: bwd_post_kernel<128><<<blocks, 256, 0, s>>>(p, scale); break;
+    default: return cudaErrorInvalidValue;
+  }
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace saf

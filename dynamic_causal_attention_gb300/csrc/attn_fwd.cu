@@ -1,0 +1,725 @@
+// attn_fwd.cu — forward of the SAF hybrid causal attention layer, and the
+// static-head engine that the backward reuses for dV.
+//
+// Method ("When Can Attention Heads Be Statically Defined?", close-reading
+// notes): a dynamic head computes softmax_causal(Q K^T / sqrt(d_h)) V (§1); a
+// frozen head mixes V with P(i,j) = exp(alpha(j) + rho(i-j)) / Z(i), j <= i
+// (Eq. (3)), which the fused kernel rebuilds tile by tile from alpha, rho and
+// Z and multiplies by V, without any Q/K work (§3.3, App. D.2, Fig. 2).
+//
+// Kernels
+//   static_prep_kernel  (K1) per static head: the generator tables and
+//                       log Z(i).  Because alpha/rho are shared by the batch,
+//                       this runs once per head, not once per sequence.
+//   hybrid_fwd_kernel   (K2) one persistent launch, one CTA per SM, over a
+//                       longest-first list of work items:
+//     dynamic item (b, h, I): Q tile I against key tiles J = 0..I; S = Q K^T
+//       and O += P V run on tcgen05 with fp32 accumulators in TMEM; online
+//       softmax in registers, one query row per thread.
+//     static item (h, I, batch group): for J = 0..I a generated tile G[I,J]
+//       (bf16, in shared memory) feeds one MMA per sequence of the group, so
+//       one generated tile serves the whole batch.
+//
+// Factored static generator.  With a(j) = exp(alpha(j) - max alpha) and
+// r(d) = exp(rho(d) - max rho), P(i,j) = a(j) r(i-j) / Z'(i) where
+// Z'(i) = sum_{k<=i} a(k) r(i-k): the shift cancels between numerator and
+// Z.  A tile element is then two multiplies, no exponential.  When
+// range(alpha) + range(rho) > 80 the products could underflow in fp32, and
+// the head falls back to the exact form exp2(alpha2(j) + rho2(i-j) - log2 Z(i)).
+//
+// Warp roles in K2 (256 threads): warp 0 issues TMA copies, warp 1 issues
+// tcgen05 MMAs (one elected lane), warp 2 owns the TMEM allocation, warps
+// 4..7 are the compute warpgroup (softmax / tile generation / epilogue), one
+// tile row per thread, matching TMEM lanes 0..127.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "attn_common.cuh"
+#include "attn_kernels.h"
+#include "internal.h"
+
+namespace saf {
+
+// ============================================================ K1: static prep
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kMaxFactoredRange = 80.0f;
+
+__device__ __forceinline__ void block_minmax(float& mx, float& mn, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+  }
+  __syncthreads();
+  if (lane == 0) {
+    red[warp] = mx;
+    red[32 + warp] = mn;
+  }
+  __syncthreads();
+  mx = red[0];
+  mn = red[32];
+  for (int w = 1; w < nw; ++w) {
+    mx = fmaxf(mx, red[w]);
+    mn = fminf(mn, red[32 + w]);
+  }
+}
+
+// grid (ceil(T / 256), n_static), 256 threads, dynamic smem 2*T floats.
+__global__ void __launch_bounds__(256) static_prep_kernel(StaticPrep p) {
+  extern __shared__ float sh[];
+  __shared__ float red[64];
+  const int T = p.T, hs = blockIdx.y, h = p.heads[hs];
+  float* sa = sh;
+  float* sr = sh + T;
+  const float* alpha = p.alpha + (size_t)h * T;
+  const float* rho = p.rho + (size_t)h * T;
+  // finite max/min of alpha and rho
+  float amax = -INFINITY, amin = INFINITY, rmax = -INFINITY, rmin = INFINITY;
+  for (int t = threadIdx.x; t < T; t += blockDim.x) {
+    const float a = alpha[t], r = rho[t];
+    sa[t] = a;
+    sr[t] = r;
+    if (isfinite(a)) { amax = fmaxf(amax, a); amin = fminf(amin, a); }
+    if (isfinite(r)) { rmax = fmaxf(rmax, r); rmin = fminf(rmin, r); }
+  }
+  block_minmax(amax, amin, red);
+  block_minmax(rmax, rmin, red);
+  const bool all_masked = !(amax > -INFINITY) || !(rmax > -INFINITY);
+  const bool exact = !all_masked && ((amax - amin) + (rmax - rmin) > kMaxFactoredRange);
+  float* a_tab = p.a_tab + (size_t)hs * T;
+  float* r_tab = p.r_tab + (size_t)hs * (T + 128);
+  float* row_tab = p.row_tab + (size_t)hs * T;
+  float* logZ = p.logZ + (size_t)hs * T;
+  if (blockIdx.x == 0 && threadIdx.x == 0) p.mode[hs] = exact ? 1 : 0;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+
+  if (!exact) {
+    // transform in place to a = exp(alpha - max), r = exp(rho - max)
+    __syncthreads();
+    for (int t = threadIdx.x; t < T; t += blockDim.x) {
+      sa[t] = all_masked ? 0.f : expf(sa[t] - amax);
+      sr[t] = all_masked ? 0.f : expf(sr[t] - rmax);
+    }
+    __syncthreads();
+    if (i < T) {
+      float z = 0.f;
+      for (int k = 0; k <= i; ++k) z = fmaf(sa[k], sr[i - k], z);
+      row_tab[i] = z > 0.f ? 1.0f / z : 0.f;
+      logZ[i] = z > 0.f ? logf(z) + amax + rmax : -INFINITY;
+      a_tab[i] = sa[i];
+      r_tab[127 + i] = sr[i];
+    }
+    if (blockIdx.x == 0 && threadIdx.x < 127) r_tab[threadIdx.x] = 0.f;
+    if (blockIdx.x == 0 && threadIdx.x == 127) r_tab[T + 127] = 0.f;
+  } else {
+    if (i < T) {
+      float m = -INFINITY, s = 0.f;
+      for (int k = 0; k <= i; ++k) {
+        const float t = sa[k] + sr[i - k];
+        if (t > m) {
+          s = s * expf(m - t) + 1.f;
+          m = t;
+        } else if (t > -INFINITY) {
+          s += expf(t - m);
+        }
+      }
+      const float lz = (m > -INFINITY) ? m + logf(s) : -INFINITY;
+      logZ[i] = lz;
+      row_tab[i] = (m > -INFINITY) ? -lz * kLog2e : -INFINITY;
+      a_tab[i] = sa[i] * kLog2e;
+      r_tab[127 + i] = sr[i] * kLog2e;
+    }
+    if (blockIdx.x == 0 && threadIdx.x < 127) r_tab[threadIdx.x] = -INFINITY;
+    if (blockIdx.x == 0 && threadIdx.x == 127) r_tab[T + 127] = -INFINITY;
+  }
+}
+
+__global__ void f32_to_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst,
+                                   size_t n) {
+  for (size_t i = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 4; i < n;
+       i += (size_t)gridDim.x * blockDim.x * 4) {
+    const float4 v = *reinterpret_cast<const float4*>(src + i);
+    uint2 o;
+    o.x = pack_bf16x2(v.x, v.y);
+    o.y = pack_bf16x2(v.z, v.w);
+    *reinterpret_cast<uint2*>(dst + i) = o;
+  }
+}
+
+__global__ void bf16_to_f32_kernel(const __nv_bfloat16* __restrict__ src, float* __restrict__ dst,
+                                   size_t n) {
+  for (size_t i = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 4; i < n;
+       i += (size_t)gridDim.x * blockDim.x * 4) {
+    const uint2 v = *reinterpret_cast<const uint2*>(src + i);
+    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&v.x);
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&v.y);
+    *reinterpret_cast<float4*>(dst + i) =
+        make_float4(__low2float(a), __high2float(a), __low2float(b), __high2float(b));
+  }
+}
+
+__global__ void zero_u32_kernel(uint32_t* dst, size_t n) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x)
+    dst[i] = 0u;
+}
+
+int elementwise_blocks(size_t n) {
+  size_t b = (n + 1023) / 1024;
+  if (b < 1) b = 1;
+  if (b > 4096) b = 4096;
+  return (int)b;
+}
+
+}  // namespace
+
+cudaError_t launch_static_prep(const StaticPrep& p, cudaStream_t s) {
+  if (p.n_static == 0) return cudaSuccess;
+  const size_t smem = 2 * (size_t)p.T * sizeof(float);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(static_prep_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  static_prep_kernel<<<dim3((p.T + 255) / 256, p.n_static), 256, smem, s>>>(p);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_f32_to_bf16(const float* src, void* dst, size_t n, cudaStream_t s) {
+  f32_to_bf16_kernel<<<elementwise_blocks(n / 4), 256, 0, s>>>(
+      src, static_cast<__nv_bfloat16*>(dst), n);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bf16_to_f32(const void* src, float* dst, size_t n, cudaStream_t s) {
+  bf16_to_f32_kernel<<<elementwise_blocks(n / 4), 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(src), dst, n);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_zero_u32(void* dst, size_t n_words, cudaStream_t s) {
+  zero_u32_kernel<<<elementwise_blocks(n_words / 4), 256, 0, s>>>(static_cast<uint32_t*>(dst),
+                                                                  n_words);
+  note_launch();
+  return cudaGetLastError();
+}
+
+// ============================================================ K2: fused kernel
+namespace {
+
+template <int D>
+struct FwdSmem {
+  using G = TileGeom<D>;
+  static constexpr int KST = (D == 128) ? 2 : 3;  // K ring (also holds static aux)
+  static constexpr int VST = (D == 128) ? 2 : 3;  // V ring
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + G::TILE_BYTES;
+  static constexpr int OFF_V = OFF_K + KST * G::TILE_BYTES;
+  static constexpr int OFF_P = OFF_V + VST * G::TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_P + 2 * SqTile::BYTES;
+  static constexpr int NBAR = 2 + 2 * KST + 2 * VST + 4 + 4 + 2;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int BYTES = OFF_MISC + 16;
+  static constexpr int ALLOC = BYTES + 1024;  // slack to align the base to 1024 B
+  static_assert(ALLOC <= 232448, "shared memory budget exceeded");
+  // aux block (static items) inside a K-ring slot: 128 column values then a
+  // 256-entry distance window.
+  static constexpr int AUX_COL = 0;
+  static constexpr int AUX_WIN = 512;
+  static constexpr int AUX_BYTES = 512 + 1024;
+};
+
+// TMEM columns: S double buffer at 0 and 128, O accumulator at 256 (up to 256
+// columns: d_h for a dynamic item, group * d_h for a static item).
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemS = 0;
+constexpr uint32_t kTmemO = 256;
+
+enum : int {
+  kSiteProdQ = 1, kSiteProdK, kSiteProdV, kSiteMmaQ, kSiteMmaK, kSiteMmaS, kSiteMmaV,
+  kSiteMmaP, kSiteMmaO, kSiteCmpS, kSiteCmpP, kSiteCmpPV, kSiteCmpO, kSiteCmpAux
+};
+
+struct Item {
+  bool is_static;
+  int b;       // dynamic: sequence; static: first sequence of the group
+  int nb;      // static: sequences in the group
+  int h;       // head id
+  int hs;      // static: index into the static tables
+  int X;       // output tile index (I forward, J transposed)
+  int nsteps;  // inner tiles
+};
+
+// Longest first: forward items in descending query tile; for each tile the
+// static items (each worth a group of sequences) come before the dynamic ones.
+// Transposed (static dV) items in ascending key tile.
+template <bool TRANSPOSED>
+__device__ __forceinline__ Item decode_item(const FwdParams& p, int it) {
+  Item r;
+  const int n_st_items = p.n_static * p.n_groups;
+  const int per_x = n_st_items + (TRANSPOSED ? 0 : p.B * p.n_dynamic);
+  const int q = it / per_x, rem = it - q * per_x;
+  r.X = TRANSPOSED ? q : (p.nI - 1 - q);
+  r.nsteps = TRANSPOSED ? (p.nI - r.X) : (r.X + 1);
+  if (rem < n_st_items) {
+    r.is_static = true;
+    r.hs = rem / p.n_groups;
+    const int g = rem - r.hs * p.n_groups;
+    r.h = p.static_heads[r.hs];
+    r.b = g * p.group;
+    r.nb = min(p.group, p.B - r.b);
+  } else {
+    const int d = rem - n_st_items;
+    r.is_static = false;
+    r.b = d / p.n_dynamic;
+    r.h = p.dynamic_heads[d - r.b * p.n_dynamic];
+    r.hs = -1;
+    r.nb = 1;
+  }
+  return r;
+}
+
+template <int D, bool TRANSPOSED>
+__global__ void __launch_bounds__(256, 1)
+    hybrid_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  using G = TileGeom<D>;
+  using L = FwdSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~(uintptr_t)1023);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
+  uint64_t* q_full = bars + 0;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* k_full = bars + 2;
+  uint64_t* k_empty = k_full + L::KST;
+  uint64_t* v_full = k_empty + L::KST;
+  uint64_t* v_empty = v_full + L::VST;
+  uint64_t* s_full = v_empty + L::VST;
+  uint64_t* s_empty = s_full + 2;
+  uint64_t* p_full = s_empty + 2;
+  uint64_t* p_empty = p_full + 2;
+  uint64_t* o_full = p_empty + 2;
+  uint64_t* o_empty = o_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
+  const WaitCtl wc{abort_flag, p.status};
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int s = 0; s < L::KST; ++s) { mbar_init(k_full + s, 1); mbar_init(k_empty + s, 1); }
+    for (int s = 0; s < L::VST; ++s) { mbar_init(v_full + s, 1); mbar_init(v_empty + s, 1); }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(s_full + s, 1);
+      mbar_init(s_empty + s, 128);
+      mbar_init(p_full + s, 128);
+      mbar_init(p_empty + s, 1);
+    }
+    mbar_init(o_full, 1);
+    mbar_init(o_empty, 128);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t sQ = smem_u32(smem + L::OFF_Q);
+  const uint32_t sK = smem_u32(smem + L::OFF_K);
+  const uint32_t sV = smem_u32(smem + L::OFF_V);
+  const uint32_t sP = smem_u32(smem + L::OFF_P);
+  const int H = p.H, T = p.T;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- producer
+    if (lane == 0) {
+      uint32_t qc = 0, kc = 0, vc = 0;
+      for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+        const Item w = decode_item<TRANSPOSED>(p, it);
+        if (!w.is_static) {
+          const int row0 = (w.b * H + w.h) * T;
+          mbar_wait(q_empty, (qc & 1) ^ 1, wc, kSiteProdQ);
+          ++qc;
+          mbar_arrive_expect_tx(q_full, G::TILE_BYTES);
+          for (int c = 0; c < G::NCHUNK; ++c)
+            tma_load_2d(smem + L::OFF_Q + c * G::CHUNK_BYTES, &tm_q, q_full, c * G::CHUNK,
+                        row0 + w.X * 128);
+          for (int j = 0; j < w.nsteps; ++j) {
+            const int ks = kc % L::KST;
+            mbar_wait(k_empty + ks, ((kc / L::KST) & 1) ^ 1, wc, kSiteProdK);
+            ++kc;
+            mbar_arrive_expect_tx(k_full + ks, G::TILE_BYTES);
+            for (int c = 0; c < G::NCHUNK; ++c)
+              tma_load_2d(smem + L::OFF_K + ks * G::TILE_BYTES + c * G::CHUNK_BYTES, &tm_k,
+                          k_full + ks, c * G::CHUNK, row0 + j * 128);
+            const int vs = vc % L::VST;
+            mbar_wait(v_empty + vs, ((vc / L::VST) & 1) ^ 1, wc, kSiteProdV);
+            ++vc;
+            mbar_arrive_expect_tx(v_full + vs, G::TILE_BYTES);
+            for (int c = 0; c < G::NCHUNK; ++c)
+              tma_load_2d(smem + L::OFF_V + vs * G::TILE_BYTES + c * G::CHUNK_BYTES, &tm_v,
+                          v_full + vs, c * G::CHUNK, row0 + j * 128);
+          }
+        } else {
+          for (int step = 0; step < w.nsteps; ++step) {
+            // inner tile Y: J (forward) or I (transposed)
+            const int Y = TRANSPOSED ? (w.X + step) : step;
+            const int dist0 = TRANSPOSED ? (Y - w.X) : (w.X - Y);  // (I - J) in tiles
+            const int ks = kc % L::KST;
+            mbar_wait(k_empty + ks, ((kc / L::KST) & 1) ^ 1, wc, kSiteProdK);
+            ++kc;
+            mbar_arrive_expect_tx(k_full + ks, L::AUX_BYTES);
+            uint8_t* aux = smem + L::OFF_K + ks * G::TILE_BYTES;
+            // column values: a(j) for j in tile J (forward) or row values of
+            // tile I (transposed)
+            const float* col_src = TRANSPOSED ? (p.row_tab + (size_t)w.hs * T + Y * 128)
+                                              : (p.a_tab + (size_t)w.hs * T + Y * 128);
+            bulk_load(aux + L::AUX_COL, col_src, 512, k_full + ks);
+            bulk_load(aux + L::AUX_WIN, p.r_tab + (size_t)w.hs * (T + 128) + dist0 * 128, 1024,
+                      k_full + ks);
+            for (int bb = 0; bb < w.nb; ++bb) {
+              const int vs = vc % L::VST;
+              mbar_wait(v_empty + vs, ((vc / L::VST) & 1) ^ 1, wc, kSiteProdV);
+              ++vc;
+              mbar_arrive_expect_tx(v_full + vs, G::TILE_BYTES);
+              const int row0 = ((w.b + bb) * H + w.h) * T;
+              for (int c = 0; c < G::NCHUNK; ++c)
+                tma_load_2d(smem + L::OFF_V + vs * G::TILE_BYTES + c * G::CHUNK_BYTES, &tm_v,
+                            v_full + vs, c * G::CHUNK, row0 + Y * 128);
+            }
+          }
+        }
+      }
+      // Drain: every copy issued must have landed before the CTA exits.
+      if (qc > 0) mbar_drain(q_full, (qc - 1) & 1);
+      for (int s = 0; s < L::KST; ++s)
+        if (kc > (uint32_t)s) mbar_drain(k_full + s, ((kc - 1 - s) / L::KST) & 1);
+      for (int s = 0; s < L::VST; ++s)
+        if (vc > (uint32_t)s) mbar_drain(v_full + s, ((vc - 1 - s) / L::VST) & 1);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16(128, D, false, true);
+      uint32_t qc = 0, kc = 0, vc = 0, sc = 0, pc = 0, oc = 0;
+      for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+        const Item w = decode_item<TRANSPOSED>(p, it);
+        if (!w.is_static) {
+          mbar_wait(q_full, qc & 1, wc, kSiteMmaQ);
+          ++qc;
+          for (int j = 0; j <= w.nsteps; ++j) {
+            if (j < w.nsteps) {
+              const int ks = kc % L::KST;
+              mbar_wait(k_full + ks, (kc / L::KST) & 1, wc, kSiteMmaK);
+              const int sb = sc & 1;
+              mbar_wait(s_empty + sb, ((sc >> 1) & 1) ^ 1, wc, kSiteMmaS);
+              tc_fence_after();
+              const uint32_t kt = sK + ks * G::TILE_BYTES;
+#pragma unroll
+              for (int kk = 0; kk < G::KSTEPS; ++kk)
+                mma_bf16_ss(tmem + kTmemS + sb * 128, G::kmajor_desc(sQ, kk),
+                            G::kmajor_desc(kt, kk), idesc_s, kk > 0);
+              mma_commit(k_empty + ks);
+              mma_commit(s_full + sb);
+              if (j == w.nsteps - 1) mma_commit(q_empty);
+              ++kc;
+              ++sc;
+            }
+            if (j >= 1) {
+              const int vs = vc % L::VST;
+              mbar_wait(v_full + vs, (vc / L::VST) & 1, wc, kSiteMmaV);
+              const int pb = pc & 1;
+              mbar_wait(p_full + pb, (pc >> 1) & 1, wc, kSiteMmaP);
+              if (j == 1) mbar_wait(o_empty, (oc & 1) ^ 1, wc, kSiteMmaO);
+              tc_fence_after();
+              const uint32_t vt = sV + vs * G::TILE_BYTES;
+              const uint32_t pt = sP + pb * SqTile::BYTES;
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                mma_bf16_ss(tmem + kTmemO, SqTile::kmajor_desc(pt, kk), G::mnmajor_desc(vt, kk),
+                            idesc_pv, (j > 1 || kk > 0));
+              mma_commit(v_empty + vs);
+              mma_commit(p_empty + pb);
+              ++vc;
+              ++pc;
+            }
+          }
+          mma_commit(o_full);
+          ++oc;
+        } else {
+          for (int step = 0; step < w.nsteps; ++step) {
+            ++kc;  // the aux entry of this step is consumed by the compute warps
+            const int pb = pc & 1;
+            mbar_wait(p_full + pb, (pc >> 1) & 1, wc, kSiteMmaP);
+            if (step == 0) mbar_wait(o_empty, (oc & 1) ^ 1, wc, kSiteMmaO);
+            const uint32_t pt = sP + pb * SqTile::BYTES;
+            for (int bb = 0; bb < w.nb; ++bb) {
+              const int vs = vc % L::VST;
+              mbar_wait(v_full + vs, (vc / L::VST) & 1, wc, kSiteMmaV);
+              tc_fence_after();
+              const uint32_t vt = sV + vs * G::TILE_BYTES;
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                mma_bf16_ss(tmem + kTmemO + bb * D, SqTile::kmajor_desc(pt, kk),
+                            G::mnmajor_desc(vt, kk), idesc_pv, (step > 0 || kk > 0));
+              mma_commit(v_empty + vs);
+              ++vc;
+            }
+            mma_commit(p_empty + pb);
+            ++pc;
+          }
+          mma_commit(o_full);
+          ++oc;
+        }
+      }
+    }
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------- compute WG
+    const int r = threadIdx.x - 128;             // tile row == TMEM lane
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    uint32_t kc = 0, sc = 0, pc = 0, oc = 0;
+    for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+      const Item w = decode_item<TRANSPOSED>(p, it);
+      if (!w.is_static) {
+        kc += w.nsteps;
+        float m_run = -INFINITY, l_run = 0.f;
+        for (int j = 0; j < w.nsteps; ++j) {
+          const int sb = sc & 1;
+          mbar_wait(s_full + sb, (sc >> 1) & 1, wc, kSiteCmpS);
+          tc_fence_after();
+          uint32_t sr[128];
+          {
+            uint32_t (&a0)[32] = *reinterpret_cast<uint32_t(*)[32]>(sr);
+            uint32_t (&a1)[32] = *reinterpret_cast<uint32_t(*)[32]>(sr + 32);
+            uint32_t (&a2)[32] = *reinterpret_cast<uint32_t(*)[32]>(sr + 64);
+            uint32_t (&a3)[32] = *reinterpret_cast<uint32_t(*)[32]>(sr + 96);
+            const uint32_t ta = tmem + lane_base + kTmemS + sb * 128;
+            tmem_ld_x32(ta, a0);
+            tmem_ld_x32(ta + 32, a1);
+            tmem_ld_x32(ta + 64, a2);
+            tmem_ld_x32(ta + 96, a3);
+            tmem_wait_ld(a0);
+            tmem_wait_ld(a1);
+            tmem_wait_ld(a2);
+            tmem_wait_ld(a3);
+          }
+          tc_fence_before();
+          mbar_arrive(s_empty + sb);
+          ++sc;
+          const bool diag = (j == w.X);
+          float mt = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < 128; ++c) {
+            float v = __uint_as_float(sr[c]) * p.scale_log2;
+            if (diag && c > r) v = -INFINITY;
+            sr[c] = __float_as_uint(v);
+            mt = fmaxf(mt, v);
+          }
+          const float m_new = fmaxf(m_run, mt);
+          const bool need = m_new > m_run + 8.0f;
+          const float m_use = need ? m_new : m_run;
+          const float corr = need ? fast_exp2(m_run - m_new) : 1.0f;
+          // Rescale O (in TMEM) when some row of this warp moved its max.
+          if (j > 0 && __any_sync(0xffffffffu, need)) {
+            const uint32_t pprev = pc - 1;
+            mbar_wait(p_empty + (pprev & 1), (pprev >> 1) & 1, wc, kSiteCmpPV);
+            tc_fence_after();
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 16) {
+              uint32_t o[16];
+              const uint32_t ta = tmem + lane_base + kTmemO + c0;
+              tmem_ld_x16(ta, o);
+              tmem_wait_ld(o);
+#pragma unroll
+              for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+              tmem_st_x16(ta, o);
+            }
+            tmem_wait_st();
+          }
+          const int pb = pc & 1;
+          mbar_wait(p_empty + pb, ((pc >> 1) & 1) ^ 1, wc, kSiteCmpP);
+          const uint32_t pt = sP + pb * SqTile::BYTES;
+          float rs = 0.f;
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            float e[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              e[k] = fast_exp2(__uint_as_float(sr[u * 8 + k]) - m_use);
+              rs += e[k];
+            }
+            st_shared_v4(SqTile::unit_addr(pt, r, u), pack_bf16x2(e[0], e[1]),
+                         pack_bf16x2(e[2], e[3]), pack_bf16x2(e[4], e[5]),
+                         pack_bf16x2(e[6], e[7]));
+          }
+          l_run = l_run * corr + rs;
+          m_run = m_use;
+          fence_proxy_async_smem();
+          tc_fence_before();
+          mbar_arrive(p_full + pb);
+          ++pc;
+        }
+        // epilogue: O / l -> out, lse
+        mbar_wait(o_full, oc & 1, wc, kSiteCmpO);
+        tc_fence_after();
+        const float inv_l = 1.0f / l_run;
+        const size_t orow = ((size_t)(w.b * H + w.h) * T + (size_t)w.X * 128 + r);
+        __nv_bfloat16* dst = p.out + orow * D;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 16) {
+          uint32_t o[16];
+          tmem_ld_x16(tmem + lane_base + kTmemO + c0, o);
+          tmem_wait_ld(o);
+          uint4 v0, v1;
+          v0.x = pack_bf16x2(__uint_as_float(o[0]) * inv_l, __uint_as_float(o[1]) * inv_l);
+          v0.y = pack_bf16x2(__uint_as_float(o[2]) * inv_l, __uint_as_float(o[3]) * inv_l);
+          v0.z = pack_bf16x2(__uint_as_float(o[4]) * inv_l, __uint_as_float(o[5]) * inv_l);
+          v0.w = pack_bf16x2(__uint_as_float(o[6]) * inv_l, __uint_as_float(o[7]) * inv_l);
+          v1.x = pack_bf16x2(__uint_as_float(o[8]) * inv_l, __uint_as_float(o[9]) * inv_l);
+          v1.y = pack_bf16x2(__uint_as_float(o[10]) * inv_l, __uint_as_float(o[11]) * inv_l);
+          v1.z = pack_bf16x2(__uint_as_float(o[12]) * inv_l, __uint_as_float(o[13]) * inv_l);
+          v1.w = pack_bf16x2(__uint_as_float(o[14]) * inv_l, __uint_as_float(o[15]) * inv_l);
+          *reinterpret_cast<uint4*>(dst + c0) = v0;
+          *reinterpret_cast<uint4*>(dst + c0 + 8) = v1;
+        }
+        if (p.lse) p.lse[orow] = (m_run + log2f(l_run)) * kLn2;
+        tc_fence_before();
+        mbar_arrive(o_empty);
+        ++oc;
+      } else {
+        // static item: generate G (or G^T) tiles, then the epilogue
+        const bool exact = p.mode[w.hs] != 0;
+        // per-row value: forward 1/Z'(i) or -log2 Z(i); transposed a(j)
+        const float rowv = TRANSPOSED ? p.a_tab[(size_t)w.hs * T + w.X * 128 + r]
+                                      : p.row_tab[(size_t)w.hs * T + w.X * 128 + r];
+        for (int step = 0; step < w.nsteps; ++step) {
+          const int ks = kc % L::KST;
+          mbar_wait(k_full + ks, (kc / L::KST) & 1, wc, kSiteCmpAux);
+          const float* aux = reinterpret_cast<const float*>(smem + L::OFF_K + ks * G::TILE_BYTES);
+          const float* colv = aux;                 // 128 values
+          const float* win = aux + L::AUX_WIN / 4; // window, centre at 127
+          const int pb = pc & 1;
+          mbar_wait(p_empty + pb, ((pc >> 1) & 1) ^ 1, wc, kSiteCmpP);
+          const uint32_t pt = sP + pb * SqTile::BYTES;
+#pragma unroll 2
+          for (int u = 0; u < 16; ++u) {
+            float e[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const int c = u * 8 + k;
+              // forward: element (i = row, j = col), distance r - c
+              // transposed: element (j = row, i = col), distance c - r
+              const float wv = TRANSPOSED ? win[127 + c - r] : win[127 + r - c];
+              e[k] = exact ? fast_exp2(colv[c] + wv + rowv) : colv[c] * wv * rowv;
+            }
+            st_shared_v4(SqTile::unit_addr(pt, r, u), pack_bf16x2(e[0], e[1]),
+                         pack_bf16x2(e[2], e[3]), pack_bf16x2(e[4], e[5]),
+                         pack_bf16x2(e[6], e[7]));
+          }
+          fence_proxy_async_smem();
+          tc_fence_before();
+          mbar_arrive(p_full + pb);
+          ++pc;
+          // all 128 threads have read the aux slot: release it once
+          named_bar_sync(1, 128);
+          if (r == 0) mbar_arrive(k_empty + ks);
+          ++kc;
+        }
+        mbar_wait(o_full, oc & 1, wc, kSiteCmpO);
+        tc_fence_after();
+        const int trow = w.X * 128 + r;
+        for (int bb = 0; bb < w.nb; ++bb) {
+          const size_t orow = ((size_t)((w.b + bb) * H + w.h) * T + trow);
+          __nv_bfloat16* dst = p.out + orow * D;
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 16) {
+            uint32_t o[16];
+            tmem_ld_x16(tmem + lane_base + kTmemO + bb * D + c0, o);
+            tmem_wait_ld(o);
+            uint4 v0, v1;
+            v0.x = pack_bf16x2(__uint_as_float(o[0]), __uint_as_float(o[1]));
+            v0.y = pack_bf16x2(__uint_as_float(o[2]), __uint_as_float(o[3]));
+            v0.z = pack_bf16x2(__uint_as_float(o[4]), __uint_as_float(o[5]));
+            v0.w = pack_bf16x2(__uint_as_float(o[6]), __uint_as_float(o[7]));
+            v1.x = pack_bf16x2(__uint_as_float(o[8]), __uint_as_float(o[9]));
+            v1.y = pack_bf16x2(__uint_as_float(o[10]), __uint_as_float(o[11]));
+            v1.z = pack_bf16x2(__uint_as_float(o[12]), __uint_as_float(o[13]));
+            v1.w = pack_bf16x2(__uint_as_float(o[14]), __uint_as_float(o[15]));
+            *reinterpret_cast<uint4*>(dst + c0) = v0;
+            *reinterpret_cast<uint4*>(dst + c0 + 8) = v1;
+          }
+          if (!TRANSPOSED && p.lse) p.lse[orow] = p.logZ[(size_t)w.hs * T + trow];
+        }
+        (void)exact;
+        tc_fence_before();
+        mbar_arrive(o_empty);
+        ++oc;
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D, bool TRANSPOSED>
+cudaError_t launch_fused(const FwdLaunch& L, cudaStream_t s) {
+  using S = FwdSmem<D>;
+  auto kern = hybrid_fwd_kernel<D, TRANSPOSED>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::ALLOC);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  if (L.p.n_items == 0) return cudaSuccess;
+  const int grid = L.p.n_items < L.num_sms ? L.p.n_items : L.num_sms;
+  kern<<<grid, 256, S::ALLOC, s>>>(L.tm_q, L.tm_k, L.tm_v, L.p);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_hybrid_fwd(const FwdLaunch& L, cudaStream_t s) {
+  switch (L.d_h) {
+    case 32: return L.transposed ? launch_fused<32, true>(L, s) : launch_fused<32, false>(L, s);
+    case 64: return L.transposed ? launch_fused<64, true>(L, s) : launch_fused<64, false>(L, s);
+    case 128:
+      return L.transposed ? launch_fused<128, true>(L, s) : launch_fused<128, false>(L, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace saf

@@ -1,0 +1,111 @@
+// attn_kernels.h — launch descriptors of the attention kernels (internal).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "internal.h"
+
+namespace saf {
+
+// Parameters of the fused forward kernel (and of its transposed static-only
+// form, which computes dV = P^T dO for the frozen heads).
+struct FwdParams {
+  int B, H, T, nI;            // nI = T / 128
+  int n_static, n_dynamic;    // head counts
+  int group, n_groups;        // sequences per static item, groups per head
+  int n_items;
+  float scale_log2;           // log2(e) / sqrt(d_h)
+  uint8_t static_heads[kMaxHeads];
+  uint8_t dynamic_heads[kMaxHeads];
+  const float* a_tab;         // [n_static, T]
+  const float* r_tab;         // [n_static, T + 128]
+  const float* row_tab;       // [n_static, T]
+  const float* logZ;          // [n_static, T]
+  const int* mode;            // [n_static]
+  __nv_bfloat16* out;         // forward: out; transposed: dV
+  float* lse;                 // forward only (nullable)
+  int* status;                // device status word
+};
+
+struct FwdLaunch {
+  CUtensorMap tm_q, tm_k, tm_v;  // [B*H*T, d_h] bf16 views; tm_v = dO when transposed
+  FwdParams p;
+  int d_h;
+  bool transposed;
+  int num_sms;
+};
+cudaError_t launch_hybrid_fwd(const FwdLaunch& L, cudaStream_t s);
+
+// Backward pre-pass: D(b,h,i) = sum_d dO * O for every row, the log2-scaled
+// lse copy for dynamic heads, and the batch sums of D for static heads.
+struct BwdPre {
+  int B, H, T, d_h;
+  const __nv_bfloat16* out;
+  const __nv_bfloat16* dout;
+  const float* lse;
+  float* Dvec;        // [B, H, T]
+  float* lse2;        // [B, H, T]  lse * log2(e)
+  float* Dsum;        // [n_static, T] (nullable)
+  int n_static;
+  uint8_t static_heads[kMaxHeads];
+};
+cudaError_t launch_bwd_pre(const BwdPre& p, cudaStream_t s);
+
+// Dynamic-head backward (KV-tile parallel).
+struct BwdParams {
+  int B, H, T, nI;
+  int n_dynamic, n_items;
+  float scale_log2;           // log2(e) / sqrt(d_h)
+  float scale;                // 1 / sqrt(d_h)
+  uint8_t dynamic_heads[kMaxHeads];
+  const float* lse2;          // [B, H, T]
+  const float* Dvec;          // [B, H, T]
+  float* dq_acc;              // [B, H, T, d_h] fp32, zeroed
+  __nv_bfloat16* dK;
+  __nv_bfloat16* dV;
+  int* status;
+};
+struct BwdLaunch {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;
+  BwdParams p;
+  int d_h;
+  int num_sms;
+};
+cudaError_t launch_bwd_dynamic(const BwdLaunch& L, cudaStream_t s);
+
+// Static-head alpha/rho gradients.
+struct ParamGradParams {
+  int B, H, T, nI;
+  int n_static, n_items;
+  uint8_t static_heads[kMaxHeads];
+  const float* a_tab;
+  const float* r_tab;
+  const float* row_tab;
+  const int* mode;
+  const float* Dsum;          // [n_static, T]
+  float* dalpha;              // [H, T]
+  float* drho;                // [H, T]
+  int* status;
+};
+struct ParamGradLaunch {
+  CUtensorMap tm_v, tm_do;
+  ParamGradParams p;
+  int d_h;
+  int num_sms;
+};
+cudaError_t launch_param_grads(const ParamGradLaunch& L, cudaStream_t s);
+
+// dQ: fp32 accumulator -> output dtype (scaled); zero dQ/dK rows of static heads.
+struct BwdPost {
+  int B, H, T, d_h;
+  const float* dq_acc;
+  __nv_bfloat16* dQ;
+  __nv_bfloat16* dK;
+  uint8_t is_static[kMaxHeads];
+};
+cudaError_t launch_bwd_post(const BwdPost& p, cudaStream_t s);
+
+}  // namespace saf

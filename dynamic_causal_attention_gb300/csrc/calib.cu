@@ -1,0 +1,192 @@
+// calib.cu — the calibration reduction of SAF ("When Can Attention Heads Be
+// Statically Defined?", §3.1): per-head mean pattern A_hat over N sequences,
+// the variance score s_var of Eq. (1), and the global ascending top-k with
+// k = round(r L H).
+//
+// The work is a streaming reduction over the n axis of A [n, heads, T, T]:
+// HBM-bound, so the kernels read each lower-triangle float4 of A exactly once
+// with streaming (evict-first) 16-byte loads, keep eight samples per element
+// in flight, and touch the upper triangle never.
+//
+// Per element the state holds mean and M2 (sum of squared deviations) in
+// fp32.  Each batch of up to 8 samples is reduced two-pass in registers and
+// merged into the state with the pairwise update of Chan, Golub and LeVeque
+// (1979):  n = na + nb,  delta = mean_b - mean_a,
+//          mean = mean_a + delta * nb / n,
+//          M2   = M2_a + M2_b + delta^2 * na * nb / n.
+// s_var sums M2 over the triangle in fp64 with a fixed reduction order, so
+// results are deterministic run to run.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "internal.h"
+
+namespace saf {
+namespace {
+
+constexpr int kBatch = 8;
+
+// Lower-triangle float4 units of a T x T matrix (T % 4 == 0): rows 4q..4q+3
+// each have q + 1 units; the group of rows 4q..4q+3 starts at unit 2 q (q+1).
+__device__ __forceinline__ void unit_to_row_col(uint32_t u, int& row, int& c4) {
+  int q = (int)((sqrtf(1.0f + 2.0f * (float)u) - 1.0f) * 0.5f);
+  while (2u * (uint32_t)q * (uint32_t)(q + 1) > u) --q;
+  while (2u * (uint32_t)(q + 1) * (uint32_t)(q + 2) <= u) ++q;
+  const uint32_t rel = u - 2u * (uint32_t)q * (uint32_t)(q + 1);
+  row = 4 * q + (int)(rel / (uint32_t)(q + 1));
+  c4 = (int)(rel % (uint32_t)(q + 1));
+}
+
+__device__ __forceinline__ float4 masked(float4 v, int row, int col0) {
+  // Entries above the diagonal (col > row) are treated as zero.
+  if (col0 + 0 > row) v.x = 0.f;
+  if (col0 + 1 > row) v.y = 0.f;
+  if (col0 + 2 > row) v.z = 0.f;
+  if (col0 + 3 > row) v.w = 0.f;
+  return v;
+}
+
+__global__ void __launch_bounds__(256) calib_accumulate_kernel(CalibLaunch p) {
+  const int T = p.T;
+  const uint32_t units_per_head = 2u * (uint32_t)(T / 4) * (uint32_t)(T / 4 + 1);
+  const uint64_t total = (uint64_t)units_per_head * (uint64_t)p.head_count;
+  const size_t sample_stride = (size_t)p.head_count * (size_t)T * (size_t)T;
+  for (uint64_t g = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total;
+       g += (uint64_t)gridDim.x * blockDim.x) {
+    const int hl = (int)(g / units_per_head);
+    int row, c4;
+    unit_to_row_col((uint32_t)(g - (uint64_t)hl * units_per_head), row, c4);
+    const int col0 = c4 * 4;
+    const size_t in_off = ((size_t)hl * T + row) * (size_t)T + col0;
+    const size_t st_off = ((size_t)(p.head_begin + hl) * T + row) * (size_t)T + col0;
+
+    float4 mean = make_float4(0.f, 0.f, 0.f, 0.f), m2 = mean;
+    if (p.count0 > 0) {
+      mean = *reinterpret_cast<const float4*>(p.mean + st_off);
+      m2 = *reinterpret_cast<const float4*>(p.m2 + st_off);
+    }
+    int cnt = p.count0;
+    const float* src = p.A + in_off;
+    for (int s = 0; s < p.n; s += kBatch) {
+      const int m = min(kBatch, p.n - s);
+      float4 x[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k)
+        if (k < m) x[k] = __ldcs(reinterpret_cast<const float4*>(src + (size_t)(s + k) * sample_stride));
+      const float inv_m = 1.0f / (float)m;
+      float4 mb = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k)
+        if (k < m) {
+          x[k] = masked(x[k], row, col0);
+          mb.x += x[k].x; mb.y += x[k].y; mb.z += x[k].z; mb.w += x[k].w;
+        }
+      mb.x *= inv_m; mb.y *= inv_m; mb.z *= inv_m; mb.w *= inv_m;
+      float4 qb = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k)
+        if (k < m) {
+          const float dx = x[k].x - mb.x, dy = x[k].y - mb.y, dz = x[k].z - mb.z,
+                      dw = x[k].w - mb.w;
+          qb.x += dx * dx; qb.y += dy * dy; qb.z += dz * dz; qb.w += dw * dw;
+        }
+      if (cnt == 0) {
+        mean = mb;
+        m2 = qb;
+      } else {
+        const float n_tot = (float)(cnt + m);
+        const float wb = (float)m / n_tot;
+        const float wab = (float)cnt * (float)m / n_tot;
+        const float dx = mb.x - mean.x, dy = mb.y - mean.y, dz = mb.z - mean.z, dw = mb.w - mean.w;
+        mean.x += dx * wb; mean.y += dy * wb; mean.z += dz * wb; mean.w += dw * wb;
+        m2.x += qb.x + dx * dx * wab; m2.y += qb.y + dy * dy * wab;
+        m2.z += qb.z + dz * dz * wab; m2.w += qb.w + dw * dw * wab;
+      }
+      cnt += m;
+    }
+    *reinterpret_cast<float4*>(p.mean + st_off) = mean;
+    *reinterpret_cast<float4*>(p.m2 + st_off) = m2;
+  }
+}
+
+// One block per (row, head): writes the full row of A_hat (zeros above the
+// diagonal) and the row's sum of M2 over its lower part, in fp64.
+__global__ void __launch_bounds__(128) calib_rows_kernel(CalibFinalize p) {
+  const int row = blockIdx.x, h = blockIdx.y, T = p.T;
+  const size_t base = ((size_t)h * T + row) * (size_t)T;
+  double acc = 0.0;
+  for (int c4 = threadIdx.x; c4 < T / 4; c4 += blockDim.x) {
+    const int col0 = c4 * 4;
+    float4 mu = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (col0 <= row) {
+      mu = masked(*reinterpret_cast<const float4*>(p.mean + base + col0), row, col0);
+      const float4 q = masked(*reinterpret_cast<const float4*>(p.m2 + base + col0), row, col0);
+      acc += (double)((q.x + q.y) + (q.z + q.w));
+    }
+    if (p.A_hat) __stcs(reinterpret_cast<float4*>(p.A_hat + base + col0), mu);
+  }
+  // fixed-order block reduction
+  __shared__ double red[128];
+  red[threadIdx.x] = acc;
+  __syncthreads();
+  for (int s = 64; s > 0; s >>= 1) {
+    if (threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) p.row_partials[(size_t)h * T + row] = red[0];
+}
+
+// One block: s_var per head (one warp per head, fixed-order sums) and the
+// exact top-k by rank over the unique 64-bit keys (bits(s_var) << 32 | index).
+constexpr int kMaxCalibHeads = 8192;
+
+__global__ void __launch_bounds__(1024) calib_select_kernel(CalibFinalize p) {
+  __shared__ float sv[kMaxCalibHeads];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  const double denom = (double)(p.N - 1) * (double)p.T * (double)p.T;
+  for (int h = warp; h < p.num_heads; h += nwarps) {
+    double acc = 0.0;
+    for (int r = lane; r < p.T; r += 32) acc += p.row_partials[(size_t)h * p.T + r];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) {
+      const float v = (float)(acc / denom);
+      sv[h] = v;
+      p.s_var[h] = v;
+    }
+  }
+  __syncthreads();
+  for (int h = threadIdx.x; h < p.num_heads; h += blockDim.x) {
+    const uint64_t kh = ((uint64_t)__float_as_uint(sv[h]) << 32) | (uint32_t)h;
+    int rank = 0;
+    for (int g = 0; g < p.num_heads; ++g) {
+      const uint64_t kg = ((uint64_t)__float_as_uint(sv[g]) << 32) | (uint32_t)g;
+      rank += (kg < kh) ? 1 : 0;
+    }
+    if (rank < p.k) p.selected[rank] = h;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_calib_accumulate(const CalibLaunch& p, cudaStream_t s) {
+  const uint64_t units = 2ull * (uint64_t)(p.T / 4) * (uint64_t)(p.T / 4 + 1) * (uint64_t)p.head_count;
+  const uint64_t want = (units + 255) / 256;
+  const int blocks = (int)(want < (1u << 30) ? want : (1u << 30));
+  calib_accumulate_kernel<<<blocks, 256, 0, s>>>(p);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_calib_finalize(const CalibFinalize& p, cudaStream_t s) {
+  if (p.num_heads > kMaxCalibHeads) return cudaErrorInvalidValue;
+  calib_rows_kernel<<<dim3(p.T, p.num_heads), 128, 0, s>>>(p);
+  note_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  calib_select_kernel<<<1, 1024, 0, s>>>(p);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace saf

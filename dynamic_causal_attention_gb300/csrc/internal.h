@@ -1,0 +1,67 @@
+// internal.h — declarations shared by the host API (api.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/saf.h"
+
+namespace saf {
+
+// Counts kernel launches made by the current API call (per host thread).
+void note_launch();
+
+// ------------------------------------------------------------ calibration
+struct CalibLaunch {
+  const float* A;     // [n, head_count, T, T]
+  int n;
+  int head_begin;
+  int head_count;
+  int T;
+  int count0;         // samples already merged into these heads
+  float* mean;        // [num_heads, T, T]
+  float* m2;          // [num_heads, T, T]
+};
+cudaError_t launch_calib_accumulate(const CalibLaunch& p, cudaStream_t s);
+
+struct CalibFinalize {
+  int num_heads;
+  int T;
+  int N;
+  int k;
+  const float* mean;
+  const float* m2;
+  double* row_partials;  // [num_heads, T]
+  float* A_hat;          // nullable
+  float* s_var;
+  int32_t* selected;     // nullable when k == 0
+};
+cudaError_t launch_calib_finalize(const CalibFinalize& p, cudaStream_t s);
+
+// ------------------------------------------------------------ attention
+constexpr int kMaxHeads = 256;
+
+// Static-head pre-pass (alpha/rho -> generator tables and log Z).
+struct StaticPrep {
+  int T;
+  int n_static;
+  const uint8_t* heads_dev;  // unused (heads passed by value below)
+  uint8_t heads[kMaxHeads];  // static head ids
+  const float* alpha;        // [H, T]
+  const float* rho;          // [H, T]
+  float* a_tab;              // [n_static, T]
+  float* r_tab;              // [n_static, T + 128] (127 leading pads)
+  float* row_tab;            // [n_static, T] : 1/Z' (factored) or log2 Z (exact)
+  float* logZ;               // [n_static, T] natural log
+  int* mode;                 // [n_static] 0 factored, 1 exact
+};
+cudaError_t launch_static_prep(const StaticPrep& p, cudaStream_t s);
+
+// Elementwise helpers.
+cudaError_t launch_f32_to_bf16(const float* src, void* dst, size_t n, cudaStream_t s);
+cudaError_t launch_bf16_to_f32(const void* src, float* dst, size_t n, cudaStream_t s);
+cudaError_t launch_zero_u32(void* dst, size_t n_words, cudaStream_t s);
+
+}  // namespace saf

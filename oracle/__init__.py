@@ -35,6 +35,8 @@ from .attention import (
     static_head_bwd,
     hybrid_attn_fwd,
     hybrid_attn_bwd,
+    dynamic_head_fwd_rows,
+    static_head_fwd_rows,
 )
 from .calibration import (
     calib_mean,
@@ -55,6 +57,8 @@ __all__ = [
     "static_head_bwd",
     "hybrid_attn_fwd",
     "hybrid_attn_bwd",
+    "dynamic_head_fwd_rows",
+    "static_head_fwd_rows",
     "calib_mean",
     "calib_svar",
     "calib_mean_svar",

@@ -23,6 +23,8 @@ __all__ = [
     "static_head_bwd",
     "hybrid_attn_fwd",
     "hybrid_attn_bwd",
+    "dynamic_head_fwd_rows",
+    "static_head_fwd_rows",
 ]
 
 
@@ -210,3 +212,34 @@ def hybrid_attn_bwd(Q, K, V, alpha, rho, head_is_static, dout,
                                               dout[b, h])
                 dQ[b, h], dK[b, h], dV[b, h] = dq, dk, dv
     return dQ, dK, dV, dalpha, drho
+
+
+# --------------------------------------------------------------------------
+# Row-restricted forms (the same definitions evaluated on a subset of query
+# rows), for spot checks of full-size outputs.
+# --------------------------------------------------------------------------
+
+def dynamic_head_fwd_rows(q, k, v, rows):
+    """Rows ``rows`` of (out, lse) of one dynamic head.  Row i of causal
+    attention depends only on q_i and keys/values 0..i."""
+    q, k, v = _as64(q), _as64(k), _as64(v)
+    T, d = k.shape
+    rows = np.asarray(rows)
+    S = (q[rows] @ k.T) / np.sqrt(d)
+    S = np.where(np.arange(T)[None, :] <= rows[:, None], S, -np.inf)
+    A, lse = _causal_row_softmax(S)
+    return A @ v, lse
+
+
+def static_head_fwd_rows(alpha, rho, v, rows):
+    """Rows ``rows`` of (out, log Z) of one frozen head."""
+    alpha, rho, v = _as64(alpha), _as64(rho), _as64(v)
+    T = alpha.shape[0]
+    rows = np.asarray(rows)
+    j = np.arange(T)[None, :]
+    dist = rows[:, None] - j
+    L = np.full((len(rows), T), -np.inf)
+    m = dist >= 0
+    L[m] = (alpha[None, :] + rho[np.clip(dist, 0, T - 1)])[m]
+    P, lse = _causal_row_softmax(L)
+    return P @ v, lse

@@ -62,3 +62,7 @@ def load_golden(name: str) -> dict:
 @pytest.fixture
 def golden():
     return load_golden
+
+TESTS = os.path.join(ROOT, "tests")
+if TESTS not in sys.path:
+    sys.path.insert(0, TESTS)

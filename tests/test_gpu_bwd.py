@@ -1,0 +1,131 @@
+"""Parity of the hybrid layer's backward (libsaf, sm_103a) with the float64
+oracle: dQ, dK, dV for dynamic heads, dV (and optionally dalpha, drho) for
+frozen heads, zero dQ/dK on frozen heads.  Same inputs and tolerance rules as
+the forward tests; the backward is fed the GPU's own forward output and lse
+(as in training), while the oracle recomputes everything from the inputs.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import assert_close, bf16_round, to_dev, to_np
+from dynamic_causal_attention_gb300.synthetic import ATTN_CONFIGS, AttnConfig, attn_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def api():
+    from dynamic_causal_attention_gb300 import api as _api
+    return _api
+
+
+def gpu_fwd_bwd(api, inp, mask, grads, dtype=torch.bfloat16):
+    B, H, T, d = inp["V"].shape
+    layer = api.HybridAttention(B, H, T, d, mask, dtype=dtype, want_param_grads=grads)
+    q, k, v, do = (to_dev(inp[n], dtype) for n in ("Q", "K", "V", "dO"))
+    alpha = to_dev(inp["alpha"], torch.float32)
+    rho = to_dev(inp["rho"], torch.float32)
+    out, lse = layer.forward(q, k, v, alpha, rho)
+    res = layer.backward(q, k, v, out, lse, do, alpha, rho, want_param_grads=grads)
+    torch.cuda.synchronize()
+    st, site = layer.device_status()
+    assert st == 0, f"device wait timed out at site {site}"
+    return [None if x is None else to_np(x) for x in res]
+
+
+def oracle_bwd(inp, mask, grads):
+    Q, K, V, dO = (bf16_round(inp[n]) for n in ("Q", "K", "V", "dO"))
+    return oracle.hybrid_attn_bwd(Q, K, V, inp["alpha"], inp["rho"], mask, dO, grads)
+
+
+def compare(got, ref, mask, tag, grads):
+    st = np.asarray(mask, bool)
+    dq, dk, dv, da, dr = got
+    rq, rk, rv, ra, rr = ref
+    if (~st).any():
+        assert_close(dq[:, ~st], rq[:, ~st], f"{tag} dQ")
+        assert_close(dk[:, ~st], rk[:, ~st], f"{tag} dK")
+        assert_close(dv[:, ~st], rv[:, ~st], f"{tag} dV[dynamic]")
+    if st.any():
+        assert np.all(dq[:, st] == 0) and np.all(dk[:, st] == 0)
+        assert_close(dv[:, st], rv[:, st], f"{tag} dV[static]")
+        if grads:
+            assert_close(da[st], ra[st], f"{tag} dalpha")
+            assert_close(dr[st], rr[st], f"{tag} drho")
+    if grads:
+        assert np.all(da[~st] == 0) and np.all(dr[~st] == 0)
+
+
+def test_tiny_config_fp32_with_param_grads(api):
+    cfg = ATTN_CONFIGS["tiny"]
+    inp = attn_inputs(cfg)
+    got = gpu_fwd_bwd(api, inp, cfg.head_is_static, True, dtype=torch.float32)
+    compare(got, oracle_bwd(inp, cfg.head_is_static, True), cfg.head_is_static, "tiny", True)
+
+
+@pytest.mark.parametrize("d_h", [32, 64, 128])
+@pytest.mark.parametrize("B,H,T,static,grads", [(2, 3, 384, (1,), True), (1, 2, 256, (), False),
+                                                (3, 2, 256, (0, 1), True),
+                                                (2, 4, 640, (0, 3), False)])
+def test_hybrid_bwd_matches_oracle(api, d_h, B, H, T, static, grads):
+    cfg = AttnConfig("t", B=B, H=H, T=T, d_h=d_h, dtype="bf16", static_heads=static)
+    inp = attn_inputs(cfg, seed=21 + d_h)
+    got = gpu_fwd_bwd(api, inp, cfg.head_is_static, grads)
+    compare(got, oracle_bwd(inp, cfg.head_is_static, grads), cfg.head_is_static, f"d{d_h}", grads)
+
+
+def test_identity_pattern_backward(api):
+    B, H, T, d = 2, 1, 256, 64
+    cfg = AttnConfig("id", B=B, H=H, T=T, d_h=d, dtype="bf16", static_heads=(0,))
+    inp = attn_inputs(cfg, seed=6)
+    inp["rho"][:] = -np.inf
+    inp["rho"][:, 0] = 0.0
+    dq, dk, dv, da, dr = gpu_fwd_bwd(api, inp, cfg.head_is_static, True)
+    np.testing.assert_array_equal(dv, bf16_round(inp["dO"]))
+    # the identity pattern has no free logits: every gradient of alpha/rho is 0
+    assert np.abs(da).max() < 1e-4 and np.abs(dr).max() < 1e-4
+
+
+def test_running_mean_backward_and_gauge(api):
+    B, H, T, d = 3, 1, 384, 32
+    cfg = AttnConfig("rm", B=B, H=H, T=T, d_h=d, dtype="bf16", static_heads=(0,))
+    inp = attn_inputs(cfg, seed=7)
+    inp["alpha"][:] = 0.0
+    inp["rho"][:] = 0.0
+    dq, dk, dv, da, dr = gpu_fwd_bwd(api, inp, cfg.head_is_static, True)
+    dO = bf16_round(inp["dO"])[:, 0]
+    want = np.cumsum((dO / np.arange(1, T + 1)[None, :, None])[:, ::-1], axis=1)[:, ::-1]
+    assert_close(dv[:, 0], want, "running-mean dV")
+    # gauge invariance: alpha + c and rho + c leave P unchanged
+    scale = np.abs(da).max() + np.abs(dr).max()
+    assert abs(da.sum()) <= 1e-3 * scale * np.sqrt(T)
+    assert abs(dr.sum()) <= 1e-3 * scale * np.sqrt(T)
+
+
+@pytest.mark.parametrize("name", ["124m", "1b"])
+def test_full_size_one_head_of_each_class(api, name):
+    cfg = ATTN_CONFIGS[name]
+    inp = attn_inputs(cfg)
+    grads = cfg.want_param_grads
+    dq, dk, dv, da, dr = gpu_fwd_bwd(api, inp, cfg.head_is_static, grads)
+    st = cfg.head_is_static
+    hd = [h for h in range(cfg.H) if not st[h]][0]
+    hs = cfg.static_heads[0]
+    b = cfg.B - 1
+    Q, K, V, dO = (bf16_round(inp[n][b, hd]) for n in ("Q", "K", "V", "dO"))
+    rq, rk, rv = oracle.dynamic_head_bwd(Q, K, V, dO)
+    assert_close(dq[b, hd], rq, f"{name} dQ")
+    assert_close(dk[b, hd], rk, f"{name} dK")
+    assert_close(dv[b, hd], rv, f"{name} dV[dynamic]")
+    vs = [bf16_round(inp["V"][bb, hs]) for bb in range(cfg.B)]
+    dos = [bf16_round(inp["dO"][bb, hs]) for bb in range(cfg.B)]
+    rvs, ra, rr = oracle.static_head_bwd(inp["alpha"][hs], inp["rho"][hs], vs, dos)
+    for bb in range(cfg.B):
+        assert_close(dv[bb, hs], rvs[bb], f"{name} dV[static] b{bb}")
+    assert np.all(dq[:, hs] == 0) and np.all(dk[:, hs] == 0)
+    if grads:
+        assert_close(da[hs], ra, f"{name} dalpha")
+        assert_close(dr[hs], rr, f"{name} drho")

@@ -1,0 +1,154 @@
+"""Parity of the calibration reduction (libsaf) with the float64 oracle.
+
+Tolerances: s_var within 1e-5 relative per head; A_hat within
+1e-5 * max|A_hat| per head (max-abs) and 1e-5 rel-L2; the selected head list
+bit-exact against a host sort of the GPU's own s_var (which checks the device
+top-k), and equal to the oracle's float64 ranking whenever the gap between the
+k-th and (k+1)-th scores exceeds the s_var tolerance.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dynamic_causal_attention_gb300.synthetic import CALIB_CONFIG, calib_probabilities
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def api():
+    from dynamic_causal_attention_gb300 import api as _api
+    return _api
+
+
+def host_topk(s_var32, k):
+    s = np.asarray(s_var32, dtype=np.float32)
+    return np.asarray(sorted(range(len(s)), key=lambda i: (s[i], i))[:k])
+
+
+def check_stats(A_hat, s_var, sel, ref_hat, ref_s, k, tag):
+    for h in range(len(ref_s)):
+        if A_hat is not None:
+            scale = np.abs(ref_hat[h]).max()
+            err = np.abs(A_hat[h] - ref_hat[h]).max()
+            assert err <= 1e-5 * scale, f"{tag} A_hat head {h}: {err:.3e}"
+            rel = np.linalg.norm(A_hat[h] - ref_hat[h]) / np.linalg.norm(ref_hat[h])
+            assert rel <= 1e-5, f"{tag} A_hat head {h} rel {rel:.3e}"
+        assert abs(s_var[h] - ref_s[h]) <= 1e-5 * abs(ref_s[h]), \
+            f"{tag} s_var head {h}: {s_var[h]} vs {ref_s[h]}"
+    np.testing.assert_array_equal(sel, host_topk(s_var, k))
+    order = np.sort(ref_s)
+    if k < len(ref_s) and k > 0:
+        gap = (order[k] - order[k - 1]) / max(abs(order[k]), 1e-30)
+        if gap > 2e-5:
+            np.testing.assert_array_equal(sel, oracle.select_heads(ref_s, k))
+
+
+def run(api, A, num_heads, T, k, chunks=None, head_chunks=None):
+    cal = api.Calibration(num_heads, T)
+    if chunks:
+        s = 0
+        for c in chunks:
+            cal.accumulate(A[s:s + c])
+            s += c
+    elif head_chunks:
+        h0 = 0
+        for c in head_chunks:
+            cal.accumulate(A[:, h0:h0 + c].contiguous(), head_begin=h0)
+            h0 += c
+    else:
+        cal.accumulate(A)
+    A_hat, s_var, sel = cal.finalize(k)
+    torch.cuda.synchronize()
+    out = (A_hat.cpu().numpy(), s_var.cpu().numpy(), sel.cpu().numpy())
+    cal.close()
+    return out
+
+
+@pytest.mark.parametrize("N,nh,T,k", [(10, 6, 64, 2), (17, 5, 128, 3), (2, 3, 8, 1)])
+def test_small_matches_oracle(api, N, nh, T, k):
+    A = calib_probabilities(N, nh, T, d_h=16, seed=N)
+    ref_hat, ref_s = oracle.calib_mean_svar(A.numpy())
+    got = run(api, A.cuda(), nh, T, k)
+    check_stats(*got, ref_hat, ref_s, k, f"N{N}")
+    assert np.all(got[0][:, np.triu_indices(T, 1)[0], np.triu_indices(T, 1)[1]] == 0)
+
+
+def test_upper_triangle_is_never_used(api):
+    N, nh, T = 9, 3, 64
+    A = calib_probabilities(N, nh, T, d_h=16, seed=2)
+    ref_hat, ref_s = oracle.calib_mean_svar(A.numpy())
+    A_bad = A.clone()
+    iu = torch.triu_indices(T, T, 1)
+    A_bad[:, :, iu[0], iu[1]] = float("nan")
+    got = run(api, A_bad.cuda(), nh, T, 1)
+    check_stats(*got, ref_hat, ref_s, 1, "nan-upper")
+
+
+def test_chunked_equals_one_shot(api):
+    N, nh, T = 24, 4, 64
+    A = calib_probabilities(N, nh, T, d_h=16, seed=3).cuda()
+    one = run(api, A, nh, T, 2)
+    aligned = run(api, A, nh, T, 2, chunks=[8, 16])
+    for x, y in zip(one, aligned):
+        np.testing.assert_array_equal(x, y)          # same batches: bitwise
+    heads = run(api, A, nh, T, 2, head_chunks=[1, 3])
+    for x, y in zip(one, heads):
+        np.testing.assert_array_equal(x, y)
+    ragged = run(api, A, nh, T, 2, chunks=[3, 5, 11, 5])
+    np.testing.assert_allclose(ragged[0], one[0], rtol=0, atol=1e-6)
+    np.testing.assert_allclose(ragged[1], one[1], rtol=1e-5)
+    np.testing.assert_array_equal(ragged[2], one[2])
+
+
+def test_identical_samples_give_zero_variance(api):
+    A = calib_probabilities(1, 3, 64, d_h=16, seed=4).repeat(12, 1, 1, 1)
+    _, s_var, _ = run(api, A.cuda(), 3, 64, 1)
+    assert np.all(s_var < 1e-12)
+
+
+def test_state_errors(api):
+    from dynamic_causal_attention_gb300 import _binding as B
+    cal = api.Calibration(4, 16)
+    A = calib_probabilities(1, 4, 16, d_h=8, seed=5).cuda()
+    cal.accumulate(A)
+    with pytest.raises(B.SafError) as e:
+        cal.finalize(1)                       # N = 1 < 2
+    assert e.value.status == B.SAF_ERR_STATE
+    cal.accumulate(A[:, :2].contiguous(), head_begin=0)   # uneven counts
+    with pytest.raises(B.SafError) as e:
+        cal.finalize(1)
+    assert e.value.status == B.SAF_ERR_STATE
+    cal.reset()
+    cal.accumulate(torch.cat([A, A]))
+    with pytest.raises(B.SafError) as e:
+        cal.finalize(5)                       # k > heads
+    assert e.value.status == B.SAF_ERR_INVALID_ARG
+    cal.close()
+
+
+def test_full_size_calibration(api):
+    c = CALIB_CONFIG
+    k = oracle.num_select(c.r, c.num_heads)
+    assert k == 36 and api.num_select(c.r, c.num_heads) == 36
+    A = calib_probabilities(c.N, c.num_heads, c.T, d_h=c.d_h, device="cuda")
+    cal = api.Calibration(c.num_heads, c.T)
+    for layer in range(c.L):  # one call per layer
+        cal.accumulate(A[:, layer * c.H:(layer + 1) * c.H].contiguous(), head_begin=layer * c.H)
+    A_hat, s_var, sel = cal.finalize(k)
+    torch.cuda.synchronize()
+    s_var = s_var.cpu().numpy()
+    sel = sel.cpu().numpy()
+    ref_s = np.zeros(c.num_heads)
+    sampled = {0, 77, 143}
+    for h in range(c.num_heads):
+        Ah = A[:, h].double().cpu().numpy()
+        ref_hat = oracle.calib_mean(Ah)
+        ref_s[h] = oracle.calib_svar(Ah, ref_hat)
+        if h in sampled:
+            got = A_hat[h].double().cpu().numpy()
+            assert np.abs(got - ref_hat).max() <= 1e-5 * np.abs(ref_hat).max()
+    check_stats(None, s_var, sel, None, ref_s, k, "full")
+    cal.close()

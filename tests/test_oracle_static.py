@@ -107,3 +107,18 @@ def test_hybrid_routes_heads_and_batches():
     Q2 = Q.copy(); Q2[:, 1] = np.nan
     out2, _ = oracle.hybrid_attn_fwd(Q2, K, V, alpha, rho, mask)
     np.testing.assert_array_equal(out2, out)
+
+
+def test_row_restricted_forms_match_full():
+    T, d = 50, 4
+    q, k, v = (RNG.normal(size=(T, d)) for _ in range(3))
+    alpha, rho = RNG.normal(size=T), RNG.normal(size=T)
+    rows = [0, 1, 17, 49]
+    o, l, _ = oracle.dynamic_head_fwd(q, k, v)
+    orow, lrow = oracle.dynamic_head_fwd_rows(q, k, v, rows)
+    np.testing.assert_allclose(orow, o[rows], atol=1e-14)
+    np.testing.assert_allclose(lrow, l[rows], atol=1e-14)
+    o, l = oracle.static_head_fwd(alpha, rho, v)
+    orow, lrow = oracle.static_head_fwd_rows(alpha, rho, v, rows)
+    np.testing.assert_allclose(orow, o[rows], atol=1e-14)
+    np.testing.assert_allclose(lrow, l[rows], atol=1e-14)
