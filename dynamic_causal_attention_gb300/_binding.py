@@ -38,6 +38,9 @@ EXPORTED = (
     "saf_get_device_status",
     "saf_status_string",
     "saf_last_launch_count",
+    "saf_trace_enable",
+    "saf_trace_count",
+    "saf_trace_get",
 )
 
 
@@ -92,6 +95,12 @@ _lib.saf_status_string.argtypes = [_i]
 _lib.saf_status_string.restype = ctypes.c_char_p
 _lib.saf_last_launch_count.argtypes = []
 _lib.saf_last_launch_count.restype = _i
+_lib.saf_trace_enable.argtypes = [_i]
+_lib.saf_trace_enable.restype = _i
+_lib.saf_trace_count.argtypes = []
+_lib.saf_trace_count.restype = _i
+_lib.saf_trace_get.argtypes = [_i, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float)]
+_lib.saf_trace_get.restype = _i
 
 
 def lib():
@@ -108,6 +117,21 @@ def saf_status_string(status: int) -> str:
 
 def saf_last_launch_count() -> int:
     return _lib.saf_last_launch_count()
+
+
+def saf_trace_enable(enable: int) -> int:
+    return _lib.saf_trace_enable(int(enable))
+
+
+def saf_trace_count() -> int:
+    return _lib.saf_trace_count()
+
+
+def saf_trace_get(index: int):
+    name = ctypes.c_char_p()
+    ms = ctypes.c_float()
+    st = _lib.saf_trace_get(int(index), ctypes.byref(name), ctypes.byref(ms))
+    return st, (name.value.decode() if name.value else None), ms.value
 
 
 def saf_hybrid_attn_workspace_size(dims: saf_attn_dims, want_param_grads: int) -> int:

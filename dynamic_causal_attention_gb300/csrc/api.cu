@@ -15,7 +15,46 @@
 namespace saf {
 
 static thread_local int g_launches = 0;
-void note_launch() { ++g_launches; }
+
+// Kernel trace: a per-thread list of (kernel, start event, end event).
+struct TraceRec {
+  const char* name;
+  cudaEvent_t ev[2];
+};
+struct TraceState {
+  bool on = false;
+  std::vector<TraceRec> recs;   // recorded this trace
+  std::vector<cudaEvent_t> pool;
+  size_t next_event = 0;
+  cudaEvent_t take() {
+    if (next_event == pool.size()) {
+      cudaEvent_t e = nullptr;
+      if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+      pool.push_back(e);
+    }
+    return pool[next_event++];
+  }
+};
+static thread_local TraceState g_trace;
+static thread_local cudaEvent_t g_pending = nullptr;
+constexpr size_t kMaxTraceRecords = 1u << 16;
+
+void trace_begin(cudaStream_t s) {
+  g_pending = nullptr;
+  if (!g_trace.on || g_trace.recs.size() >= kMaxTraceRecords) return;
+  g_pending = g_trace.take();
+  if (g_pending) cudaEventRecord(g_pending, s);
+}
+
+void trace_end(cudaStream_t s, const char* kernel) {
+  ++g_launches;
+  if (!g_pending) return;
+  cudaEvent_t e = g_trace.take();
+  if (!e) return;
+  cudaEventRecord(e, s);
+  g_trace.recs.push_back(TraceRec{kernel, {g_pending, e}});
+  g_pending = nullptr;
+}
 
 namespace {
 
@@ -214,6 +253,24 @@ const char* saf_status_string(saf_status s) {
 }
 
 int saf_last_launch_count(void) { return g_launches; }
+
+saf_status saf_trace_enable(int enable) {
+  g_trace.on = enable != 0;
+  g_trace.recs.clear();
+  g_trace.next_event = 0;
+  return SAF_OK;
+}
+
+int saf_trace_count(void) { return (int)g_trace.recs.size(); }
+
+saf_status saf_trace_get(int index, const char** kernel, float* ms) {
+  if (index < 0 || index >= (int)g_trace.recs.size() || !kernel || !ms) return SAF_ERR_INVALID_ARG;
+  const TraceRec& r = g_trace.recs[index];
+  if (cudaEventSynchronize(r.ev[1]) != cudaSuccess) return SAF_ERR_CUDA;
+  if (cudaEventElapsedTime(ms, r.ev[0], r.ev[1]) != cudaSuccess) return SAF_ERR_CUDA;
+  *kernel = r.name;
+  return SAF_OK;
+}
 
 size_t saf_hybrid_attn_workspace_size(const saf_attn_dims* dims, int want_param_grads) {
   (void)want_param_grads;  // the parameter-gradient pass needs no extra scratch

@@ -564,8 +564,9 @@ cudaError_t launch_dyn(const BwdLaunch& L, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   if (L.p.n_items == 0) return cudaSuccess;
   const int grid = L.p.n_items < L.num_sms ? L.p.n_items : L.num_sms;
+  trace_begin(s);
   bwd_dynamic_kernel<D><<<grid, 384, BwdSmem<D>::ALLOC, s>>>(L.tm_q, L.tm_k, L.tm_v, L.tm_do, L.p);
-  note_launch();
+  trace_end(s, "bwd_dynamic");
   return cudaGetLastError();
 }
 
@@ -576,8 +577,9 @@ cudaError_t launch_pg(const ParamGradLaunch& L, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   if (L.p.n_items == 0) return cudaSuccess;
   const int grid = L.p.n_items < L.num_sms ? L.p.n_items : L.num_sms;
+  trace_begin(s);
   param_grad_kernel<D><<<grid, 256, PgSmem<D>::ALLOC, s>>>(L.tm_v, L.tm_do, L.p);
-  note_launch();
+  trace_end(s, "param_grad");
   return cudaGetLastError();
 }
 

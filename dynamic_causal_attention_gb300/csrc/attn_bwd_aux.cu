@@ -91,30 +91,33 @@ int grid_for(size_t threads) {
 cudaError_t launch_bwd_pre(const BwdPre& p, cudaStream_t s) {
   const size_t threads = (size_t)p.B * p.H * p.T * (p.d_h / 8);
   const int blocks = (int)((threads + 255) / 256);
+  trace_begin(s);
   switch (p.d_h) {
     case 32: bwd_pre_kernel<32><<<blocks, 256, 0, s>>>(p); break;
     case 64: bwd_pre_kernel<64><<<blocks, 256, 0, s>>>(p); break;
     case 128: bwd_pre_kernel<128><<<blocks, 256, 0, s>>>(p); break;
     default: return cudaErrorInvalidValue;
   }
-  note_launch();
+  trace_end(s, "bwd_pre");
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.Dsum == nullptr || p.n_static == 0) return e;
+  trace_begin(s);
   dsum_kernel<<<dim3((p.T + 255) / 256, p.n_static), 256, 0, s>>>(p);
-  note_launch();
+  trace_end(s, "bwd_dsum");
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_post(const BwdPost& p, cudaStream_t s) {
   const float scale = 1.0f / sqrtf((float)p.d_h);
   const int blocks = grid_for((size_t)p.B * p.H * p.T * p.d_h / 8);
+  trace_begin(s);
   switch (p.d_h) {
     case 32: bwd_post_kernel<32><<<blocks, 256, 0, s>>>(p, scale); break;
     case 64: bwd_post_kernel<64><<<blocks, 256, 0, s>>>(p, scale); break;
     case 128: bwd_post_kernel<128><<<blocks, 256, 0, s>>>(p, scale); break;
     default: return cudaErrorInvalidValue;
   }
-  note_launch();
+  trace_end(s, "bwd_post");
   return cudaGetLastError();
 }
 

@@ -190,29 +190,33 @@ cudaError_t launch_static_prep(const StaticPrep& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
+  trace_begin(s);
   static_prep_kernel<<<dim3((p.T + 255) / 256, p.n_static), 256, smem, s>>>(p);
-  note_launch();
+  trace_end(s, "static_prep");
   return cudaGetLastError();
 }
 
 cudaError_t launch_f32_to_bf16(const float* src, void* dst, size_t n, cudaStream_t s) {
+  trace_begin(s);
   f32_to_bf16_kernel<<<elementwise_blocks(n / 4), 256, 0, s>>>(
       src, static_cast<__nv_bfloat16*>(dst), n);
-  note_launch();
+  trace_end(s, "f32_to_bf16");
   return cudaGetLastError();
 }
 
 cudaError_t launch_bf16_to_f32(const void* src, float* dst, size_t n, cudaStream_t s) {
+  trace_begin(s);
   bf16_to_f32_kernel<<<elementwise_blocks(n / 4), 256, 0, s>>>(
       static_cast<const __nv_bfloat16*>(src), dst, n);
-  note_launch();
+  trace_end(s, "bf16_to_f32");
   return cudaGetLastError();
 }
 
 cudaError_t launch_zero_u32(void* dst, size_t n_words, cudaStream_t s) {
+  trace_begin(s);
   zero_u32_kernel<<<elementwise_blocks(n_words / 4), 256, 0, s>>>(static_cast<uint32_t*>(dst),
                                                                   n_words);
-  note_launch();
+  trace_end(s, "zero");
   return cudaGetLastError();
 }
 
@@ -705,8 +709,9 @@ cudaError_t launch_fused(const FwdLaunch& L, cudaStream_t s) {
   }
   if (L.p.n_items == 0) return cudaSuccess;
   const int grid = L.p.n_items < L.num_sms ? L.p.n_items : L.num_sms;
+  trace_begin(s);
   kern<<<grid, 256, S::ALLOC, s>>>(L.tm_q, L.tm_k, L.tm_v, L.p);
-  note_launch();
+  trace_end(s, TRANSPOSED ? "static_dv" : "hybrid_fwd");
   return cudaGetLastError();
 }
 

@@ -173,19 +173,22 @@ cudaError_t launch_calib_accumulate(const CalibLaunch& p, cudaStream_t s) {
   const uint64_t units = 2ull * (uint64_t)(p.T / 4) * (uint64_t)(p.T / 4 + 1) * (uint64_t)p.head_count;
   const uint64_t want = (units + 255) / 256;
   const int blocks = (int)(want < (1u << 30) ? want : (1u << 30));
+  trace_begin(s);
   calib_accumulate_kernel<<<blocks, 256, 0, s>>>(p);
-  note_launch();
+  trace_end(s, "calib_accumulate");
   return cudaGetLastError();
 }
 
 cudaError_t launch_calib_finalize(const CalibFinalize& p, cudaStream_t s) {
   if (p.num_heads > kMaxCalibHeads) return cudaErrorInvalidValue;
+  trace_begin(s);
   calib_rows_kernel<<<dim3(p.T, p.num_heads), 128, 0, s>>>(p);
-  note_launch();
+  trace_end(s, "calib_rows");
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  trace_begin(s);
   calib_select_kernel<<<1, 1024, 0, s>>>(p);
-  note_launch();
+  trace_end(s, "calib_select");
   return cudaGetLastError();
 }
 

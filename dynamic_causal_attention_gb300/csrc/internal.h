@@ -10,8 +10,12 @@
 
 namespace saf {
 
-// Counts kernel launches made by the current API call (per host thread).
-void note_launch();
+// Launch bookkeeping (per host thread): trace_begin() before and trace_end()
+// after every kernel launch.  trace_end counts the launch for
+// saf_last_launch_count(); when the kernel trace is enabled the pair also
+// records two CUDA events on the launch stream around the kernel.
+void trace_begin(cudaStream_t s);
+void trace_end(cudaStream_t s, const char* kernel);
 
 // ------------------------------------------------------------ calibration
 struct CalibLaunch {

@@ -191,6 +191,17 @@ SAF_API const char* saf_status_string(saf_status status);
  * saf_hybrid_attn_fwd / _bwd / saf_calib_* call on this host thread. */
 SAF_API int saf_last_launch_count(void);
 
+/* Kernel trace (per host thread; for profiling, off by default).
+ * saf_trace_enable(1) clears the record and starts recording: every kernel
+ * this library launches from the thread is then bracketed by two CUDA events
+ * on its launch stream (up to 65536 launches).  saf_trace_enable(0) stops
+ * recording and clears the record.  saf_trace_get(i, ...) waits for the i-th
+ * recorded launch to finish and returns its kernel name (a static string) and
+ * its duration in milliseconds between the two events. */
+SAF_API saf_status saf_trace_enable(int enable);
+SAF_API int saf_trace_count(void);
+SAF_API saf_status saf_trace_get(int index, const char** kernel, float* ms);
+
 #ifdef __cplusplus
 }  /* extern "C" */
 #endif

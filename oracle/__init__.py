@@ -37,6 +37,8 @@ from .attention import (
     hybrid_attn_bwd,
     dynamic_head_fwd_rows,
     static_head_fwd_rows,
+    dynamic_head_bwd_rows,
+    static_head_bwd_rows,
 )
 from .calibration import (
     calib_mean,
@@ -59,6 +61,8 @@ __all__ = [
     "hybrid_attn_bwd",
     "dynamic_head_fwd_rows",
     "static_head_fwd_rows",
+    "dynamic_head_bwd_rows",
+    "static_head_bwd_rows",
     "calib_mean",
     "calib_svar",
     "calib_mean_svar",

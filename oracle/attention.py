@@ -25,6 +25,8 @@ __all__ = [
     "hybrid_attn_bwd",
     "dynamic_head_fwd_rows",
     "static_head_fwd_rows",
+    "dynamic_head_bwd_rows",
+    "static_head_bwd_rows",
 ]
 
 
@@ -243,3 +245,40 @@ def static_head_fwd_rows(alpha, rho, v, rows):
     L[m] = (alpha[None, :] + rho[np.clip(dist, 0, T - 1)])[m]
     P, lse = _causal_row_softmax(L)
     return P @ v, lse
+
+
+def dynamic_head_bwd_rows(q, k, v, dout, rows):
+    """Contribution of the query rows ``rows`` to the backward of one dynamic
+    head: (dq for those rows, their part of dk, their part of dv).  Summing the
+    parts over a partition of all rows gives dynamic_head_bwd."""
+    q, k, v, dout = _as64(q), _as64(k), _as64(v), _as64(dout)
+    T, d = k.shape
+    rows = np.asarray(rows)
+    S = (q[rows] @ k.T) / np.sqrt(d)
+    S = np.where(np.arange(T)[None, :] <= rows[:, None], S, -np.inf)
+    A, _ = _causal_row_softmax(S)
+    dv = A.T @ dout[rows]
+    dA = dout[rows] @ v.T
+    dS = A * (dA - (A * dA).sum(axis=1, keepdims=True))
+    return dS @ k / np.sqrt(d), dS.T @ q[rows] / np.sqrt(d), dv
+
+
+def static_head_bwd_rows(alpha, rho, v, dout, rows):
+    """Contribution of the query rows ``rows`` of one sequence to a frozen
+    head's backward: (its part of dv, of dalpha, of drho)."""
+    alpha, rho, v, dout = _as64(alpha), _as64(rho), _as64(v), _as64(dout)
+    T = alpha.shape[0]
+    rows = np.asarray(rows)
+    j = np.arange(T)[None, :]
+    dist = rows[:, None] - j
+    L = np.full((len(rows), T), -np.inf)
+    m = dist >= 0
+    L[m] = (alpha[None, :] + rho[np.clip(dist, 0, T - 1)])[m]
+    P, _ = _causal_row_softmax(L)
+    dv = P.T @ dout[rows]
+    dP = dout[rows] @ v.T
+    dl = P * (dP - (P * dP).sum(axis=1, keepdims=True))
+    dalpha = dl.sum(axis=0)
+    drho = np.zeros(T)
+    np.add.at(drho, np.clip(dist, 0, T - 1)[m], dl[m])
+    return dv, dalpha, drho

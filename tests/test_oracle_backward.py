@@ -109,3 +109,20 @@ def test_running_mean_pattern_backward_closed_form():
     dvs, _, _ = oracle.static_head_bwd(np.zeros(T), np.zeros(T), [RNG.normal(size=(T, d))], [dO])
     want = np.array([(dO[j:] / np.arange(j + 1, T + 1)[:, None]).sum(0) for j in range(T)])
     np.testing.assert_allclose(dvs[0], want, atol=1e-13)
+
+
+def test_row_block_parts_sum_to_full_backward():
+    T, d = 40, 4
+    q, k, v, dO = (RNG.normal(size=(T, d)) for _ in range(4))
+    alpha, rho = RNG.normal(size=T), RNG.normal(size=T)
+    dq, dk, dv = oracle.dynamic_head_bwd(q, k, v, dO)
+    blocks = [range(0, 13), range(13, 31), range(31, 40)]
+    parts = [oracle.dynamic_head_bwd_rows(q, k, v, dO, list(b)) for b in blocks]
+    np.testing.assert_allclose(np.concatenate([p[0] for p in parts]), dq, atol=1e-13)
+    np.testing.assert_allclose(sum(p[1] for p in parts), dk, atol=1e-13)
+    np.testing.assert_allclose(sum(p[2] for p in parts), dv, atol=1e-13)
+    dvs, da, dr = oracle.static_head_bwd(alpha, rho, [v], [dO])
+    parts = [oracle.static_head_bwd_rows(alpha, rho, v, dO, list(b)) for b in blocks]
+    np.testing.assert_allclose(sum(p[0] for p in parts), dvs[0], atol=1e-13)
+    np.testing.assert_allclose(sum(p[1] for p in parts), da, atol=1e-13)
+    np.testing.assert_allclose(sum(p[2] for p in parts), dr, atol=1e-13)
