@@ -41,7 +41,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from dynamic_causal_attention_gb300.synthetic import (  # noqa: E402
-    ATTN_CONFIGS, CALIB_CONFIG, attn_inputs, sweep_config)
+    ATTN_CONFIGS, CALIB_CONFIG, PREFILL_SWEEP, attn_inputs, prefill_inputs,
+    static_heads_for_ratio, sweep_config)
 
 METRIC = "hybrid attn fwd+bwd useful TFLOP/s & tokens/s, % of GB300 bf16 tensor peak"
 L2_BYTES = 129 * 1024 * 1024
@@ -183,13 +184,24 @@ def barrier(world):
 
 
 def max_over_ranks(x, world):
+    """The largest x over all ranks (the slowest rank's time)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(local_ms, steps, flop_per_step, world):
+    """Whole-job useful TFLOP/s of `world` replicas that each ran `steps`
+    steps: every rank's work over the slowest rank's time.  Returns
+    (TFLOP/s, ms per step of the slowest rank)."""
+    ms = max_over_ranks(local_ms, world)
+    per = ms / steps
+    return world * flop_per_step / (per / 1e3) / 1e12, per
 
 
 # ---------------------------------------------------------------- saf arm
@@ -384,6 +396,60 @@ def layer_secondary(cfg, steps, warmup, peaks):
     return res
 
 
+def prefill_secondary(peaks):
+    """Forward-only causal prefill: the 124M head shape at batch 64 over
+    T = 512..16K with 0%, 25% and 50% of heads frozen, and batch 1 at
+    T = 4096.  Reports ms per forward and the speed ratio against 0%."""
+    import torch
+    from dynamic_causal_attention_gb300 import api
+    P = PREFILL_SWEEP
+    H, d = P["H"], P["d_h"]
+
+    def time_fwd(B, T, r, reps):
+        mask = np.zeros(H, dtype=np.uint8)
+        for h in static_heads_for_ratio(H, r):
+            mask[h] = 1
+        q, k, v, alpha, rho = prefill_inputs(B, H, T, d)
+        layer = api.HybridAttention(B, H, T, d, mask)
+        out = torch.empty_like(v)
+        lse = torch.empty((B, H, T), dtype=torch.float32, device="cuda")
+        for _ in range(2):
+            layer.forward(q, k, v, alpha, rho, out=out, lse=lse)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(reps):
+            layer.forward(q, k, v, alpha, rho, out=out, lse=lse)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        u = d * T * T / 2.0
+        hs = int(mask.sum())
+        flop = B * (4 * u * (H - hs) + 2 * u * hs)
+        del q, k, v, out, lse, layer
+        torch.cuda.empty_cache()
+        return ms, flop / (ms / 1e3) / 1e12
+
+    res = {}
+    for T in P["T"]:
+        row = {}
+        base = None
+        for r in P["ratios"]:
+            ms, tf = time_fwd(P["B"], T, r, 5 if T >= 8192 else 10)
+            base = ms if r == 0.0 else base
+            row[f"r={r:g}"] = {"ms": round(ms, 4), "TFLOP_per_s": round(tf, 1),
+                               "speedup_vs_r0": round(base / ms, 3)}
+        res[f"T={T}"] = row
+    b1 = {}
+    base = None
+    for r in P["ratios"]:
+        ms, tf = time_fwd(1, P["batch1_T"], r, 50)
+        base = ms if r == 0.0 else base
+        b1[f"r={r:g}"] = {"ms": round(ms, 4), "speedup_vs_r0": round(base / ms, 3)}
+    res[f"batch1_T={P['batch1_T']}"] = b1
+    return {"workload": f"causal prefill, forward only, B={P['B']} H={H} d_h={d}", "sweep": res}
+
+
 # ---------------------------------------------------------------- oracle leg
 def oracle_sample(inp, cfg, s, rows_per_block=1024):
     """One bounded sample of the layer for the float64 oracle: query rows
@@ -475,10 +541,8 @@ def run_saf(args):
     sampler = ClockSampler(local) if rank == 0 else None
     ms, clocks, kernels = time_steps(run, args.steps, args.warmup, world, trace=True,
                                      sampler=sampler)
-    ms_max = max_over_ranks(ms, world)
-    per = ms_max / args.steps
     f, b = useful_flops(cfg)
-    value = world * (f + b) / (per / 1e3) / 1e12
+    value, per = job_throughput(ms, args.steps, f + b, world)
     launches = run.launches
 
     # dominant kernel of the timed region
@@ -521,6 +585,7 @@ def run_saf(args):
             sweep[f"r={r:g}"] = {k: s[k] for k in ("ms_per_step", "TFLOP_per_s", "tokens_per_s",
                                                   "frac_of_bf16_peak")}
         secondary["static_ratio_sweep_124m"] = sweep
+        secondary["prefill"] = prefill_secondary(peaks)
     barrier(world)
     if rank != 0:
         return

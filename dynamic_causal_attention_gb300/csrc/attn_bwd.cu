@@ -14,10 +14,14 @@
 //     S^T  = K_J Q_I^T,  dP^T = V_J dO_I^T           (tcgen05, fp32 in TMEM)
 //     P^T  = exp2(S^T * log2e/sqrt(d) - lse2(i)),   dS^T = P^T * (dP^T - D(i))
 //                                                   (compute warps, 1 row/thread)
-//     dV_J += P^T dO_I,  dK_J += dS^T Q_I,  dQ_I = dS K_J   (tcgen05)
-// dQ_I is read from TMEM by a second warpgroup and added into an fp32
-// accumulator with vector atomics; a post-pass scales it by 1/sqrt(d) and
-// converts it.
+//     dV_J += P^T dO_I,  dK_J += dS^T Q_I           (tcgen05, A operand in TMEM)
+//     dQ_I  = dS K_J                                (tcgen05, dS^T tile in smem
+//                                                    read as an MN-major A)
+// The compute warps write P^T and dS^T as packed bf16 over the TMEM columns
+// of S^T and dP^T they have just read, so the dV/dK products read only dO and
+// Q from shared memory.  dQ_I is read from TMEM by a second warpgroup and
+// added into an fp32 accumulator with vector atomics; a post-pass scales it by
+// 1/sqrt(d) and converts it.
 //
 // param_grad_kernel (K5): items (h_static, J).  For I = J..nI-1 the batch-
 // summed dP^T(j, i) = sum_b V_b(j) . dO_b(i) is one MMA chain with K = B*d;
@@ -42,27 +46,35 @@ constexpr uint32_t kTmemCols = 512;
 template <int D>
 struct BwdSmem {
   using G = TileGeom<D>;
-  static constexpr int QST = (D == 128) ? 1 : 2;
+  // Q_I, dO_I stages; d_h = 128 keeps two stages by dropping the alignment
+  // slack (the dynamic shared base is checked at run time instead).
+  static constexpr int QST = (D == 128) ? 2 : 3;
   static constexpr int STAGE = 2 * G::TILE_BYTES + 1024;  // Q_I, dO_I, lse2[128], D[128]
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + G::TILE_BYTES;
   static constexpr int OFF_Q = OFF_V + G::TILE_BYTES;
-  static constexpr int OFF_PT = OFF_Q + QST * STAGE;
-  static constexpr int OFF_DST = OFF_PT + SqTile::BYTES;
+  static constexpr int OFF_DST = OFF_Q + QST * STAGE;
   static constexpr int OFF_BAR = OFF_DST + SqTile::BYTES;
-  static constexpr int NBAR = 2 + 2 * QST + 8;
+  static constexpr int NBAR = 2 + 2 * QST + 9;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int ALLOC = OFF_MISC + 16 + 1024;
+  static constexpr int BYTES = OFF_MISC + 16;
+  static constexpr int SLACK = (BYTES + 1024 <= 232448) ? 1024 : 0;
+  static constexpr int ALLOC = BYTES + SLACK;
   static_assert(ALLOC <= 232448, "shared memory budget exceeded");
-  // TMEM columns
-  static constexpr uint32_t T_S = 0, T_DP = 128, T_DV = 256, T_DK = 256 + D;
+  // TMEM columns.  S^T (fp32) at 0; P^T (bf16, packed) is written over its
+  // first 64 columns once read.  dP^T at 128; dS^T over its first 64 columns.
+  static constexpr uint32_t T_S = 0, T_DP = 128, T_PT = 0, T_DST = 128;
+  static constexpr uint32_t T_DV = 256, T_DK = 256 + D;
+  // d_h = 128 leaves no free columns: dQ reuses the S^T/P^T columns once the
+  // dV MMAs that read P^T have completed.
   static constexpr bool DQ_ALIAS = (256 + 3 * D > 512);
   static constexpr uint32_t T_DQ = DQ_ALIAS ? 0 : 256 + 2 * D;
 };
 
 enum : int {
   kSiteBProdKV = 101, kSiteBProdQ, kSiteBMmaKV, kSiteBMmaQ, kSiteBMmaS, kSiteBMmaP, kSiteBMmaKD,
-  kSiteBMmaDQ, kSiteBCmpQ, kSiteBCmpS, kSiteBCmpP, kSiteBCmpKD, kSiteBDq
+  kSiteBMmaDQ, kSiteBCmpQ, kSiteBCmpS, kSiteBCmpP, kSiteBCmpKD, kSiteBDq, kSiteBMmaTS,
+  kSiteBAlign
 };
 
 struct BItem {
@@ -91,16 +103,21 @@ __global__ void __launch_bounds__(384, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
+  if (L::SLACK == 0 && smem != smem_raw) {
+    // no room to realign: report and leave without touching anything
+    if (threadIdx.x == 0) atomicCAS(p.status, 0, kSiteBAlign);
+    return;
+  }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
   uint64_t* kv_full = bars + 0;
   uint64_t* kv_empty = bars + 1;
   uint64_t* q_full = bars + 2;
   uint64_t* q_empty = q_full + L::QST;
-  uint64_t* s_full = q_empty + L::QST;
-  uint64_t* s_free = s_full + 1;
-  uint64_t* p_full = s_free + 1;
-  uint64_t* p_empty = p_full + 1;
-  uint64_t* dq_full = p_empty + 1;
+  uint64_t* s_full = q_empty + L::QST;   // S^T, dP^T ready
+  uint64_t* p_full = s_full + 1;         // P^T, dS^T written (TMEM + smem)
+  uint64_t* p_empty = p_full + 1;        // the dS^T smem tile is free again
+  uint64_t* ts_done = p_empty + 1;       // dV/dK MMAs of the step completed
+  uint64_t* dq_full = ts_done + 1;
   uint64_t* dq_empty = dq_full + 1;
   uint64_t* kd_full = dq_empty + 1;
   uint64_t* kd_empty = kd_full + 1;
@@ -114,9 +131,9 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(kv_empty, 1);
     for (int s = 0; s < L::QST; ++s) { mbar_init(q_full + s, 1); mbar_init(q_empty + s, 1); }
     mbar_init(s_full, 1);
-    mbar_init(s_free, 128);
     mbar_init(p_full, 128);
     mbar_init(p_empty, 1);
+    mbar_init(ts_done, 1);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, 128);
     mbar_init(kd_full, 1);
@@ -140,7 +157,6 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t sK = smem_u32(smem + L::OFF_K);
   const uint32_t sV = smem_u32(smem + L::OFF_V);
-  const uint32_t sPT = smem_u32(smem + L::OFF_PT);
   const uint32_t sDST = smem_u32(smem + L::OFF_DST);
   const int H = p.H, T = p.T;
 
@@ -186,7 +202,7 @@ __global__ void __launch_bounds__(384, 1)
       constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);
       constexpr uint32_t id_acc = idesc_bf16(128, D, false, true);
       constexpr uint32_t id_dq = idesc_bf16(128, D, true, true);
-      uint32_t kvc = 0, qc = 0, sc = 0, pc = 0, dqc = 0, kdc = 0;
+      uint32_t kvc = 0, qc = 0, pc = 0, tc = 0, dqc = 0, kdc = 0;
       for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
         const BItem w = decode_bwd(p, it);
         mbar_wait(kv_full, kvc & 1, wc, kSiteBMmaKV);
@@ -194,7 +210,9 @@ __global__ void __launch_bounds__(384, 1)
         for (int t = 0; t < w.nsteps; ++t) {
           const int qs = qc % L::QST;
           mbar_wait(q_full + qs, (qc / L::QST) & 1, wc, kSiteBMmaQ);
-          mbar_wait(s_free, (sc & 1) ^ 1, wc, kSiteBMmaS);
+          // S^T / dP^T columns hold the previous step's P^T / dS^T (operands
+          // of its dV/dK MMAs) and, for d_h = 128, its dQ: wait for them.
+          if (tc > 0) mbar_wait(ts_done, (tc - 1) & 1, wc, kSiteBMmaTS);
           if (L::DQ_ALIAS) mbar_wait(dq_empty, (dqc & 1) ^ 1, wc, kSiteBMmaDQ);
           tc_fence_after();
           const uint32_t sQ = smem_u32(smem + L::OFF_Q + qs * L::STAGE);
@@ -208,19 +226,24 @@ __global__ void __launch_bounds__(384, 1)
             mma_bf16_ss(tmem + L::T_DP, G::kmajor_desc(sV, kk), G::kmajor_desc(sDO, kk), id_s,
                         kk > 0);
           mma_commit(s_full);
-          ++sc;
           mbar_wait(p_full, pc & 1, wc, kSiteBMmaP);
           if (t == 0) mbar_wait(kd_empty, (kdc & 1) ^ 1, wc, kSiteBMmaKD);
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ss(tmem + L::T_DV, SqTile::kmajor_desc(sPT, kk), G::mnmajor_desc(sDO, kk),
-                        id_acc, (t > 0 || kk > 0));
+            mma_bf16_ts(tmem + L::T_DV, tmem + L::T_PT + kk * 8, G::mnmajor_desc(sDO, kk), id_acc,
+                        (t > 0 || kk > 0));
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ss(tmem + L::T_DK, SqTile::kmajor_desc(sDST, kk), G::mnmajor_desc(sQ, kk),
-                        id_acc, (t > 0 || kk > 0));
-          if (!L::DQ_ALIAS) mbar_wait(dq_empty, (dqc & 1) ^ 1, wc, kSiteBMmaDQ);
+            mma_bf16_ts(tmem + L::T_DK, tmem + L::T_DST + kk * 8, G::mnmajor_desc(sQ, kk), id_acc,
+                        (t > 0 || kk > 0));
+          mma_commit(ts_done);
+          ++tc;
+          if (L::DQ_ALIAS) {
+            mbar_wait(ts_done, (tc - 1) & 1, wc, kSiteBMmaTS);  // P^T read: columns free
+          } else {
+            mbar_wait(dq_empty, (dqc & 1) ^ 1, wc, kSiteBMmaDQ);
+          }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
@@ -255,11 +278,12 @@ __global__ void __launch_bounds__(384, 1)
         mbar_wait(p_empty, (pc & 1) ^ 1, wc, kSiteBCmpP);
         tc_fence_after();
         const bool diag = (t == 0);
+        const uint32_t trow = tmem + lane_base;
 #pragma unroll 1
         for (int c0 = 0; c0 < 128; c0 += 32) {
           uint32_t sv[32], dv[32];
-          tmem_ld_x32(tmem + lane_base + L::T_S + c0, sv);
-          tmem_ld_x32(tmem + lane_base + L::T_DP + c0, dv);
+          tmem_ld_x32(trow + L::T_S + c0, sv);
+          tmem_ld_x32(trow + L::T_DP + c0, dv);
           tmem_wait_ld(sv);
           tmem_wait_ld(dv);
           uint32_t pk[16], dk[16];
@@ -275,17 +299,19 @@ __global__ void __launch_bounds__(384, 1)
             pk[k >> 1] = pack_bf16x2(p0, p1);
             dk[k >> 1] = pack_bf16x2(g0, g1);
           }
+          // P^T and dS^T over the columns just read (K-major A operands of
+          // the dV and dK MMAs), and dS^T into shared memory for dQ.
+          tmem_st_x16(trow + L::T_PT + (c0 >> 1), pk);
+          tmem_st_x16(trow + L::T_DST + (c0 >> 1), dk);
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const uint32_t unit = (uint32_t)(c0 >> 3) + u;
-            st_shared_v4(SqTile::unit_addr(sPT, r, unit), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2],
-                         pk[4 * u + 3]);
             st_shared_v4(SqTile::unit_addr(sDST, r, unit), dk[4 * u], dk[4 * u + 1],
                          dk[4 * u + 2], dk[4 * u + 3]);
           }
         }
+        tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(s_free);
         fence_proxy_async_smem();
         mbar_arrive(p_full);
         ++qc;

@@ -71,21 +71,29 @@ __device__ __forceinline__ void block_minmax(float& mx, float& mn, float* red) {
   }
 }
 
-// grid (ceil(T / 256), n_static), 256 threads, dynamic smem 2*T floats.
+// grid (T / 64, n_static), 256 threads (8 warps), dynamic smem 2 * T floats.
+// Each block owns 64 rows; each warp computes the convolution of 8 rows with
+// its 32 lanes splitting the causal sum, reduced across lanes in a fixed order.
+constexpr int kPrepRows = 64;
+
 __global__ void __launch_bounds__(256) static_prep_kernel(StaticPrep p) {
   extern __shared__ float sh[];
   __shared__ float red[64];
   const int T = p.T, hs = blockIdx.y, h = p.heads[hs];
+  const int row0 = blockIdx.x * kPrepRows;
+  const int nload = row0 + kPrepRows;  // entries 0 .. row0 + 63 are needed
   float* sa = sh;
   float* sr = sh + T;
   const float* alpha = p.alpha + (size_t)h * T;
   const float* rho = p.rho + (size_t)h * T;
-  // finite max/min of alpha and rho
+  // finite max/min of alpha and rho over the whole head (every block agrees)
   float amax = -INFINITY, amin = INFINITY, rmax = -INFINITY, rmin = INFINITY;
   for (int t = threadIdx.x; t < T; t += blockDim.x) {
     const float a = alpha[t], r = rho[t];
-    sa[t] = a;
-    sr[t] = r;
+    if (t < nload) {
+      sa[t] = a;
+      sr[t] = r;
+    }
     if (isfinite(a)) { amax = fmaxf(amax, a); amin = fminf(amin, a); }
     if (isfinite(r)) { rmax = fmaxf(rmax, r); rmin = fminf(rmin, r); }
   }
@@ -98,43 +106,67 @@ __global__ void __launch_bounds__(256) static_prep_kernel(StaticPrep p) {
   float* row_tab = p.row_tab + (size_t)hs * T;
   float* logZ = p.logZ + (size_t)hs * T;
   if (blockIdx.x == 0 && threadIdx.x == 0) p.mode[hs] = exact ? 1 : 0;
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
   if (!exact) {
-    // transform in place to a = exp(alpha - max), r = exp(rho - max)
+    // a = exp(alpha - max), r = exp(rho - max) in place
     __syncthreads();
-    for (int t = threadIdx.x; t < T; t += blockDim.x) {
+    for (int t = threadIdx.x; t < nload; t += blockDim.x) {
       sa[t] = all_masked ? 0.f : expf(sa[t] - amax);
       sr[t] = all_masked ? 0.f : expf(sr[t] - rmax);
     }
     __syncthreads();
-    if (i < T) {
+    for (int m = 0; m < kPrepRows / 8; ++m) {
+      const int i = row0 + warp * (kPrepRows / 8) + m;
       float z = 0.f;
-      for (int k = 0; k <= i; ++k) z = fmaf(sa[k], sr[i - k], z);
-      row_tab[i] = z > 0.f ? 1.0f / z : 0.f;
-      logZ[i] = z > 0.f ? logf(z) + amax + rmax : -INFINITY;
-      a_tab[i] = sa[i];
-      r_tab[127 + i] = sr[i];
+      for (int k = lane; k <= i; k += 32) z = fmaf(sa[k], sr[i - k], z);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+      if (lane == 0) {
+        row_tab[i] = z > 0.f ? 1.0f / z : 0.f;
+        logZ[i] = z > 0.f ? logf(z) + amax + rmax : -INFINITY;
+      }
+    }
+    for (int t = threadIdx.x; t < kPrepRows; t += blockDim.x) {
+      a_tab[row0 + t] = sa[row0 + t];
+      r_tab[127 + row0 + t] = sr[row0 + t];
     }
     if (blockIdx.x == 0 && threadIdx.x < 127) r_tab[threadIdx.x] = 0.f;
     if (blockIdx.x == 0 && threadIdx.x == 127) r_tab[T + 127] = 0.f;
   } else {
-    if (i < T) {
-      float m = -INFINITY, s = 0.f;
-      for (int k = 0; k <= i; ++k) {
+    __syncthreads();
+    for (int m = 0; m < kPrepRows / 8; ++m) {
+      const int i = row0 + warp * (kPrepRows / 8) + m;
+      // per-lane online log-sum-exp, then a fixed-order merge across lanes
+      float mx = -INFINITY, sm = 0.f;
+      for (int k = lane; k <= i; k += 32) {
         const float t = sa[k] + sr[i - k];
-        if (t > m) {
-          s = s * expf(m - t) + 1.f;
-          m = t;
+        if (t > mx) {
+          sm = sm * expf(mx - t) + 1.f;
+          mx = t;
         } else if (t > -INFINITY) {
-          s += expf(t - m);
+          sm += expf(t - mx);
         }
       }
-      const float lz = (m > -INFINITY) ? m + logf(s) : -INFINITY;
-      logZ[i] = lz;
-      row_tab[i] = (m > -INFINITY) ? -lz * kLog2e : -INFINITY;
-      a_tab[i] = sa[i] * kLog2e;
-      r_tab[127 + i] = sr[i] * kLog2e;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float mo = __shfl_xor_sync(0xffffffffu, mx, o);
+        const float so = __shfl_xor_sync(0xffffffffu, sm, o);
+        const float mn = fmaxf(mx, mo);
+        if (mn > -INFINITY) {
+          sm = sm * expf(mx - mn) + so * expf(mo - mn);
+          mx = mn;
+        }
+      }
+      if (lane == 0) {
+        const float lz = (mx > -INFINITY) ? mx + logf(sm) : -INFINITY;
+        logZ[i] = lz;
+        row_tab[i] = (mx > -INFINITY) ? -lz * kLog2e : -INFINITY;
+      }
+    }
+    for (int t = threadIdx.x; t < kPrepRows; t += blockDim.x) {
+      a_tab[row0 + t] = sa[row0 + t] * kLog2e;
+      r_tab[127 + row0 + t] = sr[row0 + t] * kLog2e;
     }
     if (blockIdx.x == 0 && threadIdx.x < 127) r_tab[threadIdx.x] = -INFINITY;
     if (blockIdx.x == 0 && threadIdx.x == 127) r_tab[T + 127] = -INFINITY;
@@ -191,7 +223,7 @@ cudaError_t launch_static_prep(const StaticPrep& p, cudaStream_t s) {
     attr_set = true;
   }
   trace_begin(s);
-  static_prep_kernel<<<dim3((p.T + 255) / 256, p.n_static), 256, smem, s>>>(p);
+  static_prep_kernel<<<dim3(p.T / kPrepRows, p.n_static), 256, smem, s>>>(p);
   trace_end(s, "static_prep");
   return cudaGetLastError();
 }
@@ -226,14 +258,13 @@ namespace {
 template <int D>
 struct FwdSmem {
   using G = TileGeom<D>;
-  static constexpr int KST = (D == 128) ? 2 : 3;  // K ring (also holds static aux)
-  static constexpr int VST = (D == 128) ? 2 : 3;  // V ring
+  static constexpr int KST = (D == 128) ? 3 : 4;  // K ring (also holds static aux)
+  static constexpr int VST = (D == 128) ? 3 : 4;  // V ring
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + G::TILE_BYTES;
   static constexpr int OFF_V = OFF_K + KST * G::TILE_BYTES;
-  static constexpr int OFF_P = OFF_V + VST * G::TILE_BYTES;
-  static constexpr int OFF_BAR = OFF_P + 2 * SqTile::BYTES;
-  static constexpr int NBAR = 2 + 2 * KST + 2 * VST + 4 + 4 + 2;
+  static constexpr int OFF_BAR = OFF_V + VST * G::TILE_BYTES;
+  static constexpr int NBAR = 2 + 2 * KST + 2 * VST + 2 + 2 + 2 + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int ALLOC = BYTES + 1024;  // slack to align the base to 1024 B
@@ -245,8 +276,10 @@ struct FwdSmem {
   static constexpr int AUX_BYTES = 512 + 1024;
 };
 
-// TMEM columns: S double buffer at 0 and 128, O accumulator at 256 (up to 256
-// columns: d_h for a dynamic item, group * d_h for a static item).
+// TMEM columns: two 128-column buffers at 0 and 128 hold S (fp32) and then,
+// over its first 64 columns, P as packed bf16 (the A operand of O += P V);
+// static items keep their generated tiles there.  The O accumulator sits at
+// 256 (d_h columns for a dynamic item, group * d_h for a static item).
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 0;
 constexpr uint32_t kTmemO = 256;
@@ -312,11 +345,10 @@ __global__ void __launch_bounds__(256, 1)
   uint64_t* k_empty = k_full + L::KST;
   uint64_t* v_full = k_empty + L::KST;
   uint64_t* v_empty = v_full + L::VST;
-  uint64_t* s_full = v_empty + L::VST;
-  uint64_t* s_empty = s_full + 2;
-  uint64_t* p_full = s_empty + 2;
-  uint64_t* p_empty = p_full + 2;
-  uint64_t* o_full = p_empty + 2;
+  uint64_t* s_full = v_empty + L::VST;   // S ready (MMA -> compute)
+  uint64_t* s_empty = s_full + 2;        // buffer free again: its P V MMAs done (MMA -> all)
+  uint64_t* p_full = s_empty + 2;        // P / G written, O rescaled (compute -> MMA)
+  uint64_t* o_full = p_full + 2;
   uint64_t* o_empty = o_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
@@ -330,9 +362,8 @@ __global__ void __launch_bounds__(256, 1)
     for (int s = 0; s < L::VST; ++s) { mbar_init(v_full + s, 1); mbar_init(v_empty + s, 1); }
     for (int s = 0; s < 2; ++s) {
       mbar_init(s_full + s, 1);
-      mbar_init(s_empty + s, 128);
+      mbar_init(s_empty + s, 1);
       mbar_init(p_full + s, 128);
-      mbar_init(p_empty + s, 1);
     }
     mbar_init(o_full, 1);
     mbar_init(o_empty, 128);
@@ -355,7 +386,6 @@ __global__ void __launch_bounds__(256, 1)
   const uint32_t sQ = smem_u32(smem + L::OFF_Q);
   const uint32_t sK = smem_u32(smem + L::OFF_K);
   const uint32_t sV = smem_u32(smem + L::OFF_V);
-  const uint32_t sP = smem_u32(smem + L::OFF_P);
   const int H = p.H, T = p.T;
 
   if (warp == 0) {
@@ -430,58 +460,58 @@ __global__ void __launch_bounds__(256, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16(128, D, false, true);
-      uint32_t qc = 0, kc = 0, vc = 0, sc = 0, pc = 0, oc = 0;
+      uint32_t qc = 0, kc = 0, vc = 0, sc = 0, oc = 0;
       for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
         const Item w = decode_item<TRANSPOSED>(p, it);
+        const uint32_t sc0 = sc;
         if (!w.is_static) {
           mbar_wait(q_full, qc & 1, wc, kSiteMmaQ);
           ++qc;
           for (int j = 0; j <= w.nsteps; ++j) {
             if (j < w.nsteps) {
+              const uint32_t u = sc0 + j;
               const int ks = kc % L::KST;
               mbar_wait(k_full + ks, (kc / L::KST) & 1, wc, kSiteMmaK);
-              const int sb = sc & 1;
-              mbar_wait(s_empty + sb, ((sc >> 1) & 1) ^ 1, wc, kSiteMmaS);
+              mbar_wait(s_empty + (u & 1), ((u >> 1) & 1) ^ 1, wc, kSiteMmaS);
               tc_fence_after();
               const uint32_t kt = sK + ks * G::TILE_BYTES;
 #pragma unroll
               for (int kk = 0; kk < G::KSTEPS; ++kk)
-                mma_bf16_ss(tmem + kTmemS + sb * 128, G::kmajor_desc(sQ, kk),
+                mma_bf16_ss(tmem + kTmemS + (u & 1) * 128, G::kmajor_desc(sQ, kk),
                             G::kmajor_desc(kt, kk), idesc_s, kk > 0);
               mma_commit(k_empty + ks);
-              mma_commit(s_full + sb);
+              mma_commit(s_full + (u & 1));
               if (j == w.nsteps - 1) mma_commit(q_empty);
               ++kc;
-              ++sc;
             }
             if (j >= 1) {
+              const uint32_t u = sc0 + j - 1;
               const int vs = vc % L::VST;
               mbar_wait(v_full + vs, (vc / L::VST) & 1, wc, kSiteMmaV);
-              const int pb = pc & 1;
-              mbar_wait(p_full + pb, (pc >> 1) & 1, wc, kSiteMmaP);
+              mbar_wait(p_full + (u & 1), (u >> 1) & 1, wc, kSiteMmaP);
               if (j == 1) mbar_wait(o_empty, (oc & 1) ^ 1, wc, kSiteMmaO);
               tc_fence_after();
               const uint32_t vt = sV + vs * G::TILE_BYTES;
-              const uint32_t pt = sP + pb * SqTile::BYTES;
+              const uint32_t pa = tmem + kTmemS + (u & 1) * 128;
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk)
-                mma_bf16_ss(tmem + kTmemO, SqTile::kmajor_desc(pt, kk), G::mnmajor_desc(vt, kk),
-                            idesc_pv, (j > 1 || kk > 0));
+                mma_bf16_ts(tmem + kTmemO, pa + kk * 8, G::mnmajor_desc(vt, kk), idesc_pv,
+                            (j > 1 || kk > 0));
               mma_commit(v_empty + vs);
-              mma_commit(p_empty + pb);
+              mma_commit(s_empty + (u & 1));
               ++vc;
-              ++pc;
             }
           }
+          sc = sc0 + w.nsteps;
           mma_commit(o_full);
           ++oc;
         } else {
           for (int step = 0; step < w.nsteps; ++step) {
             ++kc;  // the aux entry of this step is consumed by the compute warps
-            const int pb = pc & 1;
-            mbar_wait(p_full + pb, (pc >> 1) & 1, wc, kSiteMmaP);
+            const uint32_t u = sc0 + step;
+            mbar_wait(p_full + (u & 1), (u >> 1) & 1, wc, kSiteMmaP);
             if (step == 0) mbar_wait(o_empty, (oc & 1) ^ 1, wc, kSiteMmaO);
-            const uint32_t pt = sP + pb * SqTile::BYTES;
+            const uint32_t ga = tmem + kTmemS + (u & 1) * 128;
             for (int bb = 0; bb < w.nb; ++bb) {
               const int vs = vc % L::VST;
               mbar_wait(v_full + vs, (vc / L::VST) & 1, wc, kSiteMmaV);
@@ -489,14 +519,17 @@ __global__ void __launch_bounds__(256, 1)
               const uint32_t vt = sV + vs * G::TILE_BYTES;
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk)
-                mma_bf16_ss(tmem + kTmemO + bb * D, SqTile::kmajor_desc(pt, kk),
-                            G::mnmajor_desc(vt, kk), idesc_pv, (step > 0 || kk > 0));
+                mma_bf16_ts(tmem + kTmemO + bb * D, ga + kk * 8, G::mnmajor_desc(vt, kk),
+                            idesc_pv, (step > 0 || kk > 0));
               mma_commit(v_empty + vs);
               ++vc;
             }
-            mma_commit(p_empty + pb);
-            ++pc;
+            // every use of a TMEM buffer completes one phase of both of its
+            // barriers, so that the compute warps can count uses uniformly
+            mma_commit(s_full + (u & 1));
+            mma_commit(s_empty + (u & 1));
           }
+          sc = sc0 + w.nsteps;
           mma_commit(o_full);
           ++oc;
         }
@@ -506,15 +539,17 @@ __global__ void __launch_bounds__(256, 1)
     // ---------------------------------------------------------- compute WG
     const int r = threadIdx.x - 128;             // tile row == TMEM lane
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    uint32_t kc = 0, sc = 0, pc = 0, oc = 0;
+    uint32_t kc = 0, sc = 0, oc = 0;
     for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
       const Item w = decode_item<TRANSPOSED>(p, it);
+      const uint32_t sc0 = sc;
       if (!w.is_static) {
         kc += w.nsteps;
         float m_run = -INFINITY, l_run = 0.f;
         for (int j = 0; j < w.nsteps; ++j) {
-          const int sb = sc & 1;
-          mbar_wait(s_full + sb, (sc >> 1) & 1, wc, kSiteCmpS);
+          const uint32_t u = sc0 + j;
+          const uint32_t sb = u & 1;
+          mbar_wait(s_full + sb, (u >> 1) & 1, wc, kSiteCmpS);
           tc_fence_after();
           uint32_t sr[128];
           {
@@ -532,26 +567,65 @@ __global__ void __launch_bounds__(256, 1)
             tmem_wait_ld(a2);
             tmem_wait_ld(a3);
           }
-          tc_fence_before();
-          mbar_arrive(s_empty + sb);
-          ++sc;
-          const bool diag = (j == w.X);
-          float mt = -INFINITY;
+          // Row max of the raw scores: eight independent partial maxima so
+          // that the dependency chains stay short.  Only the diagonal tile
+          // needs the causal mask.
+          if (j == w.X) {
 #pragma unroll
-          for (int c = 0; c < 128; ++c) {
-            float v = __uint_as_float(sr[c]) * p.scale_log2;
-            if (diag && c > r) v = -INFINITY;
-            sr[c] = __float_as_uint(v);
-            mt = fmaxf(mt, v);
+            for (int c = 0; c < 128; ++c)
+              if (c > r) sr[c] = 0xff800000u;  // -inf
           }
+          float mx[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mx[k] = fmaxf(__uint_as_float(sr[k]), __uint_as_float(sr[k + 8]));
+#pragma unroll
+          for (int c = 16; c < 128; c += 16)
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              mx[k] = fmax3(mx[k], __uint_as_float(sr[c + k]), __uint_as_float(sr[c + 8 + k]));
+          const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                 fmaxf(mx[6], mx[7])) * p.scale_log2;
           const float m_new = fmaxf(m_run, mt);
           const bool need = m_new > m_run + 8.0f;
           const float m_use = need ? m_new : m_run;
           const float corr = need ? fast_exp2(m_run - m_new) : 1.0f;
-          // Rescale O (in TMEM) when some row of this warp moved its max.
+          // p = exp2(s * scale_log2 - m_use): one packed FMA per pair, two
+          // exponentials, one packed add into four partial row sums.
+          const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
+          const uint64_t nm2 = f2_pack(-m_use, -m_use);
+          // P goes over the first 64 columns of this S buffer (already read
+          // into registers), 16 packed columns at a time.
+          uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+          const uint32_t pdst = tmem + lane_base + kTmemS + sb * 128;
+#pragma unroll
+          for (int q0 = 0; q0 < 64; q0 += 16) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int qq = 0; qq < 16; ++qq) {
+              const int q = q0 + qq;
+              float x0, x1;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * q]), __uint_as_float(sr[2 * q + 1])),
+                               sc2, nm2),
+                        x0, x1);
+              const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
+              acc[qq & 3] = f2_add(acc[qq & 3], f2_pack(e0, e1));
+              pk[qq] = pack_bf16x2(e0, e1);
+            }
+            tmem_st_x16(pdst + q0, pk);
+          }
+          float rs;
+          {
+            const uint64_t t = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
+            float lo, hi;
+            f2_unpack(t, lo, hi);
+            rs = lo + hi;
+          }
+          // Rescale O (in TMEM) when some row of this warp moved its max: the
+          // previous tile's P V must have finished first.
           if (j > 0 && __any_sync(0xffffffffu, need)) {
-            const uint32_t pprev = pc - 1;
-            mbar_wait(p_empty + (pprev & 1), (pprev >> 1) & 1, wc, kSiteCmpPV);
+            const uint32_t up = u - 1;
+            mbar_wait(s_empty + (up & 1), (up >> 1) & 1, wc, kSiteCmpPV);
             tc_fence_after();
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 16) {
@@ -563,31 +637,14 @@ __global__ void __launch_bounds__(256, 1)
               for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
               tmem_st_x16(ta, o);
             }
-            tmem_wait_st();
           }
-          const int pb = pc & 1;
-          mbar_wait(p_empty + pb, ((pc >> 1) & 1) ^ 1, wc, kSiteCmpP);
-          const uint32_t pt = sP + pb * SqTile::BYTES;
-          float rs = 0.f;
-#pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            float e[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              e[k] = fast_exp2(__uint_as_float(sr[u * 8 + k]) - m_use);
-              rs += e[k];
-            }
-            st_shared_v4(SqTile::unit_addr(pt, r, u), pack_bf16x2(e[0], e[1]),
-                         pack_bf16x2(e[2], e[3]), pack_bf16x2(e[4], e[5]),
-                         pack_bf16x2(e[6], e[7]));
-          }
+          tmem_wait_st();
           l_run = l_run * corr + rs;
           m_run = m_use;
-          fence_proxy_async_smem();
           tc_fence_before();
-          mbar_arrive(p_full + pb);
-          ++pc;
+          mbar_arrive(p_full + sb);
         }
+        sc = sc0 + w.nsteps;
         // epilogue: O / l -> out, lse
         mbar_wait(o_full, oc & 1, wc, kSiteCmpO);
         tc_fence_after();
@@ -616,44 +673,49 @@ __global__ void __launch_bounds__(256, 1)
         mbar_arrive(o_empty);
         ++oc;
       } else {
-        // static item: generate G (or G^T) tiles, then the epilogue
+        // static item: generate G (or G^T) tiles into TMEM, then the epilogue
         const bool exact = p.mode[w.hs] != 0;
         // per-row value: forward 1/Z'(i) or -log2 Z(i); transposed a(j)
         const float rowv = TRANSPOSED ? p.a_tab[(size_t)w.hs * T + w.X * 128 + r]
                                       : p.row_tab[(size_t)w.hs * T + w.X * 128 + r];
         for (int step = 0; step < w.nsteps; ++step) {
+          const uint32_t u = sc0 + step;
           const int ks = kc % L::KST;
           mbar_wait(k_full + ks, (kc / L::KST) & 1, wc, kSiteCmpAux);
           const float* aux = reinterpret_cast<const float*>(smem + L::OFF_K + ks * G::TILE_BYTES);
           const float* colv = aux;                 // 128 values
           const float* win = aux + L::AUX_WIN / 4; // window, centre at 127
-          const int pb = pc & 1;
-          mbar_wait(p_empty + pb, ((pc >> 1) & 1) ^ 1, wc, kSiteCmpP);
-          const uint32_t pt = sP + pb * SqTile::BYTES;
-#pragma unroll 2
-          for (int u = 0; u < 16; ++u) {
-            float e[8];
+          // the TMEM buffer must be free: the MMAs of two steps back are done
+          mbar_wait(s_empty + (u & 1), ((u >> 1) & 1) ^ 1, wc, kSiteCmpP);
+          tc_fence_after();
+          const uint32_t gdst = tmem + lane_base + kTmemS + (u & 1) * 128;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const int c = u * 8 + k;
-              // forward: element (i = row, j = col), distance r - c
-              // transposed: element (j = row, i = col), distance c - r
-              const float wv = TRANSPOSED ? win[127 + c - r] : win[127 + r - c];
-              e[k] = exact ? fast_exp2(colv[c] + wv + rowv) : colv[c] * wv * rowv;
+          for (int q0 = 0; q0 < 64; q0 += 16) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int qq = 0; qq < 16; ++qq) {
+              float e[2];
+#pragma unroll
+              for (int k = 0; k < 2; ++k) {
+                const int c = 2 * (q0 + qq) + k;
+                // forward: element (i = row, j = col), distance r - c
+                // transposed: element (j = row, i = col), distance c - r
+                const float wv = TRANSPOSED ? win[127 + c - r] : win[127 + r - c];
+                e[k] = exact ? fast_exp2(colv[c] + wv + rowv) : colv[c] * wv * rowv;
+              }
+              pk[qq] = pack_bf16x2(e[0], e[1]);
             }
-            st_shared_v4(SqTile::unit_addr(pt, r, u), pack_bf16x2(e[0], e[1]),
-                         pack_bf16x2(e[2], e[3]), pack_bf16x2(e[4], e[5]),
-                         pack_bf16x2(e[6], e[7]));
+            tmem_st_x16(gdst + q0, pk);
           }
-          fence_proxy_async_smem();
-          tc_fence_before();
-          mbar_arrive(p_full + pb);
-          ++pc;
           // all 128 threads have read the aux slot: release it once
           named_bar_sync(1, 128);
           if (r == 0) mbar_arrive(k_empty + ks);
           ++kc;
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(p_full + (u & 1));
         }
+        sc = sc0 + w.nsteps;
         mbar_wait(o_full, oc & 1, wc, kSiteCmpO);
         tc_fence_after();
         const int trow = w.X * 128 + r;
@@ -679,7 +741,6 @@ __global__ void __launch_bounds__(256, 1)
           }
           if (!TRANSPOSED && p.lse) p.lse[orow] = p.logZ[(size_t)w.hs * T + trow];
         }
-        (void)exact;
         tc_fence_before();
         mbar_arrive(o_empty);
         ++oc;

@@ -43,6 +43,8 @@ __all__ = [
     "attn_inputs",
     "calib_temperatures",
     "calib_probabilities",
+    "prefill_inputs",
+    "PREFILL_SWEEP",
 ]
 
 
@@ -176,3 +178,33 @@ def calib_probabilities(N: int, num_heads: int, T: int, d_h: int = 64,
         out[n - n_begin] = torch.softmax(logits, dim=-1)
         del q, k, logits
     return out
+
+
+# Forward-only causal prefill sweep (App. D.3 of the notes: the 124M model's
+# head shape, batch 64, T from 512 to 16K, 25% and 50% of heads frozen, plus
+# batch 1 at T = 4096 where launch overhead dominates).
+PREFILL_SWEEP = {
+    "B": 64, "H": 12, "d_h": 64,
+    "T": (512, 1024, 2048, 4096, 8192, 16384),
+    "ratios": (0.0, 0.25, 0.5),
+    "batch1_T": 4096,
+}
+
+
+def prefill_inputs(B: int, H: int, T: int, d_h: int, seed: int = 0, device: str = "cuda"):
+    """Q, K, V ~ N(0,1) as bf16 device tensors drawn with a seeded torch
+    generator on ``device`` (large prefill shapes are drawn where they are
+    used), and alpha ~ N(0,1), rho(d) = -log(1+d) + N(0, 0.3) as fp32."""
+    import torch
+
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed) * 7919 + T)
+    shp = (B, H, T, d_h)
+    q = torch.randn(shp, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+    k = torch.randn(shp, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+    v = torch.randn(shp, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+    rng = np.random.Generator(np.random.PCG64(seed + T))
+    alpha = rng.standard_normal((H, T), dtype=np.float32)
+    rho = (-np.log1p(np.arange(T, dtype=np.float64))[None, :]
+           + rng.normal(0.0, 0.3, size=(H, T))).astype(np.float32)
+    return q, k, v, torch.from_numpy(alpha).to(device), torch.from_numpy(rho).to(device)

@@ -17,7 +17,9 @@ Statically Defined?" (the close-reading notes of Li, Tai, Fonseca and Cohen):
 * backward: §3.3 / App. D.2 (the static head's attention backward is only
   dV = P^T dZ; the alpha/rho gradients are the plain chain rule of Eq. (3));
 * calibration: §3.1, the sample mean A_hat and Eq. (1) s_var, then the global
-  ascending sort and the first k = round(r L H) heads.
+  ascending sort and the first k = round(r L H) heads;
+* compact fit: Eq. (3)/(4) and App. A.2, alpha/rho fitted to A_hat by Adam on
+  the row-wise cross-entropy, gated by a mean row KL of 0.2 nat.
 
 Parity status: every function here is pinned by ``tests/test_oracle_*.py``
 against closed forms, hand-worked fixtures in ``tests/golden/``, finite
@@ -39,6 +41,14 @@ from .attention import (
     static_head_fwd_rows,
     dynamic_head_bwd_rows,
     static_head_bwd_rows,
+)
+from .fit import (
+    marginals,
+    fit_loss,
+    fit_gradient,
+    mean_row_kl,
+    compact_fit,
+    select_fitted,
 )
 from .calibration import (
     calib_mean,
@@ -69,4 +79,10 @@ __all__ = [
     "num_select",
     "select_heads",
     "reconstruction_risk",
+    "marginals",
+    "fit_loss",
+    "fit_gradient",
+    "mean_row_kl",
+    "compact_fit",
+    "select_fitted",
 ]

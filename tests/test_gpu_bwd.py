@@ -29,6 +29,9 @@ def gpu_fwd_bwd(api, inp, mask, grads, dtype=torch.bfloat16):
     alpha = to_dev(inp["alpha"], torch.float32)
     rho = to_dev(inp["rho"], torch.float32)
     out, lse = layer.forward(q, k, v, alpha, rho)
+    torch.cuda.synchronize()
+    st, site = layer.device_status()
+    assert st == 0, f"forward: device wait timed out at site {site}"
     res = layer.backward(q, k, v, out, lse, do, alpha, rho, want_param_grads=grads)
     torch.cuda.synchronize()
     st, site = layer.device_status()
@@ -75,6 +78,17 @@ def test_hybrid_bwd_matches_oracle(api, d_h, B, H, T, static, grads):
     inp = attn_inputs(cfg, seed=21 + d_h)
     got = gpu_fwd_bwd(api, inp, cfg.head_is_static, grads)
     compare(got, oracle_bwd(inp, cfg.head_is_static, grads), cfg.head_is_static, f"d{d_h}", grads)
+
+
+@pytest.mark.parametrize("d_h,grads", [(64, False), (128, True)])
+def test_many_items_per_cta(api, d_h, grads):
+    # More work items than SMs in every kernel of the backward.
+    cfg = AttnConfig("many", B=8, H=12, T=512, d_h=d_h, dtype="bf16",
+                     static_heads=(2, 7, 9))
+    inp = attn_inputs(cfg, seed=43)
+    got = gpu_fwd_bwd(api, inp, cfg.head_is_static, grads)
+    compare(got, oracle_bwd(inp, cfg.head_is_static, grads), cfg.head_is_static,
+            f"many d{d_h}", grads)
 
 
 def test_identity_pattern_backward(api):

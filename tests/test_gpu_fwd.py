@@ -69,6 +69,18 @@ def test_hybrid_fwd_matches_oracle(api, d_h, B, H, T, static):
     compare(out, lse, ref_out, ref_lse, cfg.head_is_static, f"d{d_h}")
 
 
+@pytest.mark.parametrize("d_h", [64, 128])
+def test_many_items_per_cta(api, d_h):
+    # More work items than SMs: every persistent CTA runs a mixed sequence of
+    # static and dynamic items, so the pipelines carry state across items.
+    cfg = AttnConfig("many", B=8, H=12, T=512, d_h=d_h, dtype="bf16",
+                     static_heads=(2, 7, 9))
+    inp = attn_inputs(cfg, seed=41)
+    out, lse = gpu_fwd(api, inp, cfg.head_is_static)
+    ref_out, ref_lse = oracle_fwd(inp, cfg.head_is_static)
+    compare(out, lse, ref_out, ref_lse, cfg.head_is_static, f"many d{d_h}")
+
+
 def test_identity_pattern_copies_v(api):
     B, H, T, d = 2, 1, 256, 64
     cfg = AttnConfig("id", B=B, H=H, T=T, d_h=d, dtype="bf16", static_heads=(0,))
