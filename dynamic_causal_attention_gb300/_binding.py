@@ -29,6 +29,7 @@ EXPORTED = (
     "saf_hybrid_attn_workspace_size",
     "saf_hybrid_attn_fwd",
     "saf_hybrid_attn_bwd",
+    "saf_hybrid_attn_fwd_noalloc",
     "saf_calib_create",
     "saf_calib_accumulate",
     "saf_calib_num_select",
@@ -77,6 +78,9 @@ _lib.saf_hybrid_attn_bwd.argtypes = [ctypes.POINTER(saf_attn_dims), _vp, _vp, _v
                                      _vp, _vp, _vp, ctypes.c_char_p, _vp, _vp, _vp, _vp, _vp,
                                      _vp, _sz, _vp]
 _lib.saf_hybrid_attn_bwd.restype = _i
+_lib.saf_hybrid_attn_fwd_noalloc.argtypes = [ctypes.POINTER(saf_attn_dims), _vp, _vp, _vp, _vp,
+                                             _vp, ctypes.c_char_p, _vp, _vp, _vp]
+_lib.saf_hybrid_attn_fwd_noalloc.restype = _i
 _lib.saf_calib_create.argtypes = [ctypes.POINTER(_vp), _i, _i]
 _lib.saf_calib_create.restype = _i
 _lib.saf_calib_accumulate.argtypes = [_vp, _vp, _i, _i, _i, _vp]
@@ -150,6 +154,12 @@ def saf_hybrid_attn_bwd(dims, Q, K, V, out, lse, dout, alpha, rho, head_is_stati
     return _lib.saf_hybrid_attn_bwd(ctypes.byref(dims), Q, K, V, out, lse, dout, alpha, rho,
                                     bytes(head_is_static), dQ, dK, dV, dalpha, drho,
                                     workspace, int(ws_bytes), stream)
+
+
+def saf_hybrid_attn_fwd_noalloc(dims, Q, K, V, alpha, rho, head_is_static: bytes, out, lse,
+                                stream) -> int:
+    return _lib.saf_hybrid_attn_fwd_noalloc(ctypes.byref(dims), Q, K, V, alpha, rho,
+                                            bytes(head_is_static), out, lse, stream)
 
 
 def saf_calib_create(num_heads: int, T: int):

@@ -135,6 +135,36 @@ SAF_API saf_status saf_hybrid_attn_bwd(const saf_attn_dims* dims,
                                void* workspace, size_t ws_bytes,
                                void* stream);
 
+/* saf_hybrid_attn_fwd without a workspace: for callers that cannot allocate
+ * device memory when they run the layer.  An inference engine's plugin, for
+ * example, may only enqueue work on the buffers it is handed: the engine has
+ * planned all device memory ahead of time (often inside a captured CUDA
+ * graph) and an allocation at that point would break its plan.  Such callers
+ * pass only inputs and outputs here.  The paper has no counterpart to this
+ * call; it is an interface convenience.
+ *
+ * Arguments and results are those of saf_hybrid_attn_fwd with dims->dtype ==
+ * SAF_BF16 (fp32 I/O would need staging buffers: SAF_ERR_UNSUPPORTED).  The
+ * scratch (the frozen heads' tables, log Z and the status word) lives in one
+ * file-scope device array of 4 MiB that every GPU which loads the library
+ * holds until the process exits; a shape whose tables need more,
+ * n_static * (4 T + 128) * 4 bytes plus at most 1.5 KiB of status word and
+ * alignment, is rejected with SAF_ERR_UNSUPPORTED before anything is launched.  Nothing is allocated:
+ * no cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Every call on a device shares the one array and it keeps the last
+ * call's contents, so calls whose work overlaps on the GPU (different streams,
+ * or several host threads) race on it: serialise them.  The status word is
+ * cleared at the start of every call but cannot be read back through
+ * saf_get_device_status (there is no workspace to name). */
+SAF_API saf_status saf_hybrid_attn_fwd_noalloc(const saf_attn_dims* dims,
+                                       const void* Q, const void* K, const void* V,
+                                       const float* alpha, const float* rho,
+                                       const uint8_t* head_is_static,
+                                       void* out, float* lse, void* stream);
+
 /* Calibration state for `num_heads` heads (all layers, flat index
  * l * H + h) of sequence length T (a positive multiple of 4, <= 16384).
  * Allocates the per-element running mean and M2 (2 * num_heads * T * T fp32)

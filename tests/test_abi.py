@@ -105,3 +105,19 @@ def test_calib_argument_checks(binding):
     assert binding.saf_calib_accumulate(None, 16, 1, 0, 1, None) == binding.SAF_ERR_INVALID_ARG
     assert binding.saf_calib_finalize(None, 0, None, 16, None, None) == binding.SAF_ERR_INVALID_ARG
     assert binding.saf_calib_destroy(None) == binding.SAF_OK
+
+
+def test_noalloc_forward_rejects_what_its_scratch_cannot_hold(binding):
+    d = binding._dims
+    # 64 frozen heads at T = 16384 need ~16.8 MB of tables: beyond the 4 MiB array
+    hs = bytes([1] * 64)
+    st = binding.saf_hybrid_attn_fwd_noalloc(d(1, 64, 16384, 64, 0), 16, 16, 16, 16, 16, hs,
+                                             16, 16, None)
+    assert st == binding.SAF_ERR_UNSUPPORTED
+    # fp32 I/O would need staging buffers
+    st = binding.saf_hybrid_attn_fwd_noalloc(d(1, 4, 128, 32, 1), 16, 16, 16, 16, 16,
+                                             bytes([1, 0, 0, 0]), 16, 16, None)
+    assert st == binding.SAF_ERR_UNSUPPORTED
+    st = binding.saf_hybrid_attn_fwd_noalloc(d(1, 4, 128, 32, 0), 16, 16, None, 16, 16,
+                                             bytes([1, 0, 0, 0]), 16, 16, None)
+    assert st == binding.SAF_ERR_INVALID_ARG
