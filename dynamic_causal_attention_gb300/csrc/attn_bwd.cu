@@ -49,7 +49,7 @@ struct BwdSmem {
   // Q_I, dO_I stages; d_h = 128 keeps two stages by dropping the alignment
   // slack (the dynamic shared base is checked at run time instead).
   static constexpr int QST = (D == 128) ? 2 : 3;
-  static constexpr int STAGE = 2 * G::TILE_BYTES + 1024;  // Q_I, dO_I, lse2[128], D[128]
+  static constexpr int STAGE = 2 * G::TILE_BYTES + 1024;  // Q_I, dO_I, -lse2[128], -D[128]
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + G::TILE_BYTES;
   static constexpr int OFF_Q = OFF_V + G::TILE_BYTES;
@@ -61,14 +61,19 @@ struct BwdSmem {
   static constexpr int SLACK = (BYTES + 1024 <= 232448) ? 1024 : 0;
   static constexpr int ALLOC = BYTES + SLACK;
   static_assert(ALLOC <= 232448, "shared memory budget exceeded");
-  // TMEM columns.  S^T (fp32) at 0; P^T (bf16, packed) is written over its
-  // first 64 columns once read.  dP^T at 128; dS^T over its first 64 columns.
-  static constexpr uint32_t T_S = 0, T_DP = 128, T_PT = 0, T_DST = 128;
+  // TMEM columns.  S^T (fp32) at 0, dP^T at 128.  Each compute half (64 of
+  // the 128 query columns) writes its P^T, packed bf16, over the first 32
+  // columns of its own S^T half, and its dS^T over the first 32 of its dP^T
+  // half: P^T k-steps 0..3 sit at 0.., 4..7 at 64.. (dS^T likewise + 128).
+  static constexpr uint32_t T_S = 0, T_DP = 128;
   static constexpr uint32_t T_DV = 256, T_DK = 256 + D;
   // d_h = 128 leaves no free columns: dQ reuses the S^T/P^T columns once the
   // dV MMAs that read P^T have completed.
   static constexpr bool DQ_ALIAS = (256 + 3 * D > 512);
   static constexpr uint32_t T_DQ = DQ_ALIAS ? 0 : 256 + 2 * D;
+  __device__ static __forceinline__ uint32_t a_col(int kk) {
+    return (uint32_t)((kk < 4) ? kk * 8 : 64 + (kk - 4) * 8);
+  }
 };
 
 enum : int {
@@ -92,8 +97,11 @@ __device__ __forceinline__ BItem decode_bwd(const BwdParams& p, int it) {
   return r;
 }
 
+// Threads: warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM owner,
+// warps 4..11 two compute halves (query columns 0..63 and 64..127 of every
+// key row; a row per thread), warps 12..15 the dQ warps.
 template <int D>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(512, 1)
     bwd_dynamic_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
@@ -131,13 +139,13 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(kv_empty, 1);
     for (int s = 0; s < L::QST; ++s) { mbar_init(q_full + s, 1); mbar_init(q_empty + s, 1); }
     mbar_init(s_full, 1);
-    mbar_init(p_full, 128);
+    mbar_init(p_full, 256);
     mbar_init(p_empty, 1);
     mbar_init(ts_done, 1);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, 128);
     mbar_init(kd_full, 1);
-    mbar_init(kd_empty, 128);
+    mbar_init(kd_empty, 256);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -203,45 +211,62 @@ __global__ void __launch_bounds__(384, 1)
       constexpr uint32_t id_acc = idesc_bf16(128, D, false, true);
       constexpr uint32_t id_dq = idesc_bf16(128, D, true, true);
       uint32_t kvc = 0, qc = 0, pc = 0, tc = 0, dqc = 0, kdc = 0;
+      // S^T and dP^T of the step whose Q/dO sit in stage `qs_of`.
+      auto issue_s = [&](uint32_t qcount) {
+        const int qs = qcount % L::QST;
+        mbar_wait(q_full + qs, (qcount / L::QST) & 1, wc, kSiteBMmaQ);
+        tc_fence_after();
+        const uint32_t sQ = smem_u32(smem + L::OFF_Q + qs * L::STAGE);
+        const uint32_t sDO = sQ + G::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < G::KSTEPS; ++kk)
+          mma_bf16_ss(tmem + L::T_S, G::kmajor_desc(sK, kk), G::kmajor_desc(sQ, kk), id_s,
+                      kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < G::KSTEPS; ++kk)
+          mma_bf16_ss(tmem + L::T_DP, G::kmajor_desc(sV, kk), G::kmajor_desc(sDO, kk), id_s,
+                      kk > 0);
+        mma_commit(s_full);
+      };
       for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
         const BItem w = decode_bwd(p, it);
         mbar_wait(kv_full, kvc & 1, wc, kSiteBMmaKV);
         ++kvc;
+        // S^T/dP^T columns still hold the previous step's P^T/dS^T and, for
+        // d_h = 128, its dQ: both must be consumed first.
+        if (tc > 0) mbar_wait(ts_done, (tc - 1) & 1, wc, kSiteBMmaTS);
+        if (L::DQ_ALIAS) mbar_wait(dq_empty, (dqc & 1) ^ 1, wc, kSiteBMmaDQ);
+        issue_s(qc);
         for (int t = 0; t < w.nsteps; ++t) {
           const int qs = qc % L::QST;
-          mbar_wait(q_full + qs, (qc / L::QST) & 1, wc, kSiteBMmaQ);
-          // S^T / dP^T columns hold the previous step's P^T / dS^T (operands
-          // of its dV/dK MMAs) and, for d_h = 128, its dQ: wait for them.
-          if (tc > 0) mbar_wait(ts_done, (tc - 1) & 1, wc, kSiteBMmaTS);
-          if (L::DQ_ALIAS) mbar_wait(dq_empty, (dqc & 1) ^ 1, wc, kSiteBMmaDQ);
-          tc_fence_after();
           const uint32_t sQ = smem_u32(smem + L::OFF_Q + qs * L::STAGE);
           const uint32_t sDO = sQ + G::TILE_BYTES;
-#pragma unroll
-          for (int kk = 0; kk < G::KSTEPS; ++kk)
-            mma_bf16_ss(tmem + L::T_S, G::kmajor_desc(sK, kk), G::kmajor_desc(sQ, kk), id_s,
-                        kk > 0);
-#pragma unroll
-          for (int kk = 0; kk < G::KSTEPS; ++kk)
-            mma_bf16_ss(tmem + L::T_DP, G::kmajor_desc(sV, kk), G::kmajor_desc(sDO, kk), id_s,
-                        kk > 0);
-          mma_commit(s_full);
           mbar_wait(p_full, pc & 1, wc, kSiteBMmaP);
           if (t == 0) mbar_wait(kd_empty, (kdc & 1) ^ 1, wc, kSiteBMmaKD);
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ts(tmem + L::T_DV, tmem + L::T_PT + kk * 8, G::mnmajor_desc(sDO, kk), id_acc,
-                        (t > 0 || kk > 0));
+            mma_bf16_ts(tmem + L::T_DV, tmem + L::T_S + L::a_col(kk), G::mnmajor_desc(sDO, kk),
+                        id_acc, (t > 0 || kk > 0));
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ts(tmem + L::T_DK, tmem + L::T_DST + kk * 8, G::mnmajor_desc(sQ, kk), id_acc,
-                        (t > 0 || kk > 0));
+            mma_bf16_ts(tmem + L::T_DK, tmem + L::T_DP + L::a_col(kk), G::mnmajor_desc(sQ, kk),
+                        id_acc, (t > 0 || kk > 0));
           mma_commit(ts_done);
+          mma_commit(q_empty + qs);
           ++tc;
-          if (L::DQ_ALIAS) {
-            mbar_wait(ts_done, (tc - 1) & 1, wc, kSiteBMmaTS);  // P^T read: columns free
+          ++qc;
+          ++pc;
+          if (!L::DQ_ALIAS) {
+            // next step's scores first, so that the compute warps can start
+            // while dQ of this step runs
+            if (t + 1 < w.nsteps) {
+              mbar_wait(ts_done, (tc - 1) & 1, wc, kSiteBMmaTS);
+              issue_s(qc);
+            }
+            mbar_wait(dq_empty, (dqc & 1) ^ 1, wc, kSiteBMmaDQ);
           } else {
+            mbar_wait(ts_done, (tc - 1) & 1, wc, kSiteBMmaTS);  // P^T read: columns free
             mbar_wait(dq_empty, (dqc & 1) ^ 1, wc, kSiteBMmaDQ);
           }
           tc_fence_after();
@@ -249,63 +274,83 @@ __global__ void __launch_bounds__(384, 1)
           for (int kk = 0; kk < 8; ++kk)
             mma_bf16_ss(tmem + L::T_DQ, SqTile::mnmajor_desc(sDST, kk), G::mnmajor_desc(sK, kk),
                         id_dq, kk > 0);
-          mma_commit(q_empty + qs);
           mma_commit(p_empty);
           mma_commit(dq_full);
-          ++qc;
-          ++pc;
           ++dqc;
+          if (L::DQ_ALIAS && t + 1 < w.nsteps) {
+            mbar_wait(dq_empty, (dqc & 1) ^ 1, wc, kSiteBMmaDQ);
+            issue_s(qc);
+          }
         }
         mma_commit(kd_full);
         mma_commit(kv_empty);
         ++kdc;
       }
     }
-  } else if (warp >= 4 && warp < 8) {
-    // ---------------------------------------------------------- compute WG
-    const int r = threadIdx.x - 128;  // key row j within the tile == TMEM lane
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+  } else if (warp >= 4 && warp < 12) {
+    // ---------------------------------------------------------- compute halves
+    const int hf = (warp - 4) >> 2;          // query columns 64*hf .. 64*hf + 63
+    const int r = (warp & 3) * 32 + lane;    // key row j within the tile == TMEM lane
+    const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
     uint32_t qc = 0, sc = 0, pc = 0, kdc = 0;
     for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
       const BItem w = decode_bwd(p, it);
       for (int t = 0; t < w.nsteps; ++t) {
         const int qs = qc % L::QST;
         mbar_wait(q_full + qs, (qc / L::QST) & 1, wc, kSiteBCmpQ);
-        const float* lse_s = reinterpret_cast<const float*>(smem + L::OFF_Q + qs * L::STAGE +
-                                                            2 * G::TILE_BYTES);
-        const float* d_s = lse_s + 128;
+        const float* nl_s = reinterpret_cast<const float*>(smem + L::OFF_Q + qs * L::STAGE +
+                                                           2 * G::TILE_BYTES) + 64 * hf;
+        const float* nd_s = nl_s + 128;
         mbar_wait(s_full, sc & 1, wc, kSiteBCmpS);
-        mbar_wait(p_empty, (pc & 1) ^ 1, wc, kSiteBCmpP);
         tc_fence_after();
         const bool diag = (t == 0);
-        const uint32_t trow = tmem + lane_base;
 #pragma unroll 1
-        for (int c0 = 0; c0 < 128; c0 += 32) {
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          const int col = 64 * hf + c0;      // first query column of this chunk
           uint32_t sv[32], dv[32];
-          tmem_ld_x32(trow + L::T_S + c0, sv);
-          tmem_ld_x32(trow + L::T_DP + c0, dv);
+          tmem_ld_x32(trow + L::T_S + col, sv);
+          tmem_ld_x32(trow + L::T_DP + col, dv);
           tmem_wait_ld(sv);
           tmem_wait_ld(dv);
           uint32_t pk[16], dk[16];
 #pragma unroll
-          for (int k = 0; k < 32; k += 2) {
-            const int c = c0 + k;
-            float p0 = fast_exp2(fmaf(__uint_as_float(sv[k]), p.scale_log2, -lse_s[c]));
-            float p1 = fast_exp2(fmaf(__uint_as_float(sv[k + 1]), p.scale_log2, -lse_s[c + 1]));
-            if (diag && c < r) p0 = 0.f;
-            if (diag && c + 1 < r) p1 = 0.f;
-            const float g0 = p0 * (__uint_as_float(dv[k]) - d_s[c]);
-            const float g1 = p1 * (__uint_as_float(dv[k + 1]) - d_s[c + 1]);
-            pk[k >> 1] = pack_bf16x2(p0, p1);
-            dk[k >> 1] = pack_bf16x2(g0, g1);
+          for (int k4 = 0; k4 < 32; k4 += 4) {
+            const float4 nl = *reinterpret_cast<const float4*>(nl_s + c0 + k4);
+            const float4 nd = *reinterpret_cast<const float4*>(nd_s + c0 + k4);
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const int k = k4 + 2 * h2;
+              const float l0 = h2 ? nl.z : nl.x, l1 = h2 ? nl.w : nl.y;
+              const float e0 = h2 ? nd.z : nd.x, e1 = h2 ? nd.w : nd.y;
+              float x0, x1;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[k]), __uint_as_float(sv[k + 1])), sc2,
+                               f2_pack(l0, l1)),
+                        x0, x1);
+              float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+              if (diag) {
+                if (col + k < r) p0 = 0.f;
+                if (col + k + 1 < r) p1 = 0.f;
+              }
+              const uint64_t pp = f2_pack(p0, p1);
+              const uint64_t g2 = f2_mul(
+                  pp, f2_add(f2_pack(__uint_as_float(dv[k]), __uint_as_float(dv[k + 1])),
+                             f2_pack(e0, e1)));
+              float g0, g1;
+              f2_unpack(g2, g0, g1);
+              pk[k >> 1] = pack_bf16x2(p0, p1);
+              dk[k >> 1] = pack_bf16x2(g0, g1);
+            }
           }
-          // P^T and dS^T over the columns just read (K-major A operands of
-          // the dV and dK MMAs), and dS^T into shared memory for dQ.
-          tmem_st_x16(trow + L::T_PT + (c0 >> 1), pk);
-          tmem_st_x16(trow + L::T_DST + (c0 >> 1), dk);
+          // P^T and dS^T over this half's columns just read (K-major A
+          // operands of dV and dK), and dS^T into shared memory for dQ.
+          tmem_st_x16(trow + L::T_S + 64 * hf + (c0 >> 1), pk);
+          tmem_st_x16(trow + L::T_DP + 64 * hf + (c0 >> 1), dk);
+          // the dS^T tile in shared memory is read by the previous step's dQ
+          if (c0 == 0) mbar_wait(p_empty, (pc & 1) ^ 1, wc, kSiteBCmpP);
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const uint32_t unit = (uint32_t)(c0 >> 3) + u;
+            const uint32_t unit = (uint32_t)(col >> 3) + u;
             st_shared_v4(SqTile::unit_addr(sDST, r, unit), dk[4 * u], dk[4 * u + 1],
                          dk[4 * u + 2], dk[4 * u + 3]);
           }
@@ -318,40 +363,37 @@ __global__ void __launch_bounds__(384, 1)
         ++sc;
         ++pc;
       }
-      // epilogue: dV_J, dK_J (scaled) -> global
+      // epilogue: half 0 writes dV_J, half 1 writes dK_J (scaled)
       mbar_wait(kd_full, kdc & 1, wc, kSiteBCmpKD);
       tc_fence_after();
       const size_t orow = (size_t)(w.b * H + w.h) * T + (size_t)w.J * 128 + r;
-#pragma unroll 1
-      for (int which = 0; which < 2; ++which) {
-        __nv_bfloat16* dst = (which == 0 ? p.dV : p.dK) + orow * D;
-        const float sc_out = which == 0 ? 1.0f : p.scale;
-        const uint32_t col = which == 0 ? L::T_DV : L::T_DK;
+      __nv_bfloat16* dst = (hf == 0 ? p.dV : p.dK) + orow * D;
+      const float sc_out = hf == 0 ? 1.0f : p.scale;
+      const uint32_t colb = hf == 0 ? L::T_DV : L::T_DK;
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 16) {
-          uint32_t o[16];
-          tmem_ld_x16(tmem + lane_base + col + c0, o);
-          tmem_wait_ld(o);
-          uint4 v0, v1;
-          v0.x = pack_bf16x2(__uint_as_float(o[0]) * sc_out, __uint_as_float(o[1]) * sc_out);
-          v0.y = pack_bf16x2(__uint_as_float(o[2]) * sc_out, __uint_as_float(o[3]) * sc_out);
-          v0.z = pack_bf16x2(__uint_as_float(o[4]) * sc_out, __uint_as_float(o[5]) * sc_out);
-          v0.w = pack_bf16x2(__uint_as_float(o[6]) * sc_out, __uint_as_float(o[7]) * sc_out);
-          v1.x = pack_bf16x2(__uint_as_float(o[8]) * sc_out, __uint_as_float(o[9]) * sc_out);
-          v1.y = pack_bf16x2(__uint_as_float(o[10]) * sc_out, __uint_as_float(o[11]) * sc_out);
-          v1.z = pack_bf16x2(__uint_as_float(o[12]) * sc_out, __uint_as_float(o[13]) * sc_out);
-          v1.w = pack_bf16x2(__uint_as_float(o[14]) * sc_out, __uint_as_float(o[15]) * sc_out);
-          *reinterpret_cast<uint4*>(dst + c0) = v0;
-          *reinterpret_cast<uint4*>(dst + c0 + 8) = v1;
-        }
+      for (int c0 = 0; c0 < D; c0 += 16) {
+        uint32_t o[16];
+        tmem_ld_x16(trow + colb + c0, o);
+        tmem_wait_ld(o);
+        uint4 v0, v1;
+        v0.x = pack_bf16x2(__uint_as_float(o[0]) * sc_out, __uint_as_float(o[1]) * sc_out);
+        v0.y = pack_bf16x2(__uint_as_float(o[2]) * sc_out, __uint_as_float(o[3]) * sc_out);
+        v0.z = pack_bf16x2(__uint_as_float(o[4]) * sc_out, __uint_as_float(o[5]) * sc_out);
+        v0.w = pack_bf16x2(__uint_as_float(o[6]) * sc_out, __uint_as_float(o[7]) * sc_out);
+        v1.x = pack_bf16x2(__uint_as_float(o[8]) * sc_out, __uint_as_float(o[9]) * sc_out);
+        v1.y = pack_bf16x2(__uint_as_float(o[10]) * sc_out, __uint_as_float(o[11]) * sc_out);
+        v1.z = pack_bf16x2(__uint_as_float(o[12]) * sc_out, __uint_as_float(o[13]) * sc_out);
+        v1.w = pack_bf16x2(__uint_as_float(o[14]) * sc_out, __uint_as_float(o[15]) * sc_out);
+        *reinterpret_cast<uint4*>(dst + c0) = v0;
+        *reinterpret_cast<uint4*>(dst + c0 + 8) = v1;
       }
       tc_fence_before();
       mbar_arrive(kd_empty);
       ++kdc;
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 12) {
     // ---------------------------------------------------------- dQ warps
-    const int r = threadIdx.x - 256;  // query row i within the tile == TMEM lane
+    const int r = (warp & 3) * 32 + lane;  // query row i within the tile == TMEM lane
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     uint32_t dqc = 0;
     for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
@@ -591,7 +633,7 @@ cudaError_t launch_dyn(const BwdLaunch& L, cudaStream_t s) {
   if (L.p.n_items == 0) return cudaSuccess;
   const int grid = L.p.n_items < L.num_sms ? L.p.n_items : L.num_sms;
   trace_begin(s);
-  bwd_dynamic_kernel<D><<<grid, 384, BwdSmem<D>::ALLOC, s>>>(L.tm_q, L.tm_k, L.tm_v, L.tm_do, L.p);
+  bwd_dynamic_kernel<D><<<grid, 512, BwdSmem<D>::ALLOC, s>>>(L.tm_q, L.tm_k, L.tm_v, L.tm_do, L.p);
   trace_end(s, "bwd_dynamic");
   return cudaGetLastError();
 }

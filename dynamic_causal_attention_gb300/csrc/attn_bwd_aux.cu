@@ -1,8 +1,9 @@
 // attn_bwd_aux.cu — the small bandwidth-bound passes around the backward
 // kernels of the hybrid layer:
 //   bwd_pre   D(b,h,i) = sum_d dO(b,h,i,d) * out(b,h,i,d) (the softmax
-//             backward's row term), lse2 = lse * log2(e), and for frozen heads
-//             the batch sums of D that the alpha/rho gradients need;
+//             backward's row term), stored negated, and -lse * log2(e) (the
+//             dynamic backward adds both), plus for frozen heads the batch
+//             sums of D that the alpha/rho gradients need;
 //   bwd_post  dQ = (1/sqrt(d_h)) * fp32 accumulator -> bf16, and zeros for the
 //             dQ/dK rows of frozen heads (they have no query/key path).
 #include <cuda_bf16.h>
@@ -42,8 +43,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(BwdPre p) {
   for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
   (void)lane;
   if (row < rows && sub == 0) {
-    p.Dvec[row] = acc;
-    p.lse2[row] = p.lse[row] * 1.4426950408889634f;
+    p.Dvec[row] = -acc;
+    p.lse2[row] = -p.lse[row] * 1.4426950408889634f;
   }
 }
 
@@ -52,7 +53,7 @@ __global__ void dsum_kernel(BwdPre p) {
   if (i >= p.T) return;
   const int h = p.static_heads[hs];
   float s = 0.f;
-  for (int b = 0; b < p.B; ++b) s += p.Dvec[((size_t)b * p.H + h) * p.T + i];
+  for (int b = 0; b < p.B; ++b) s -= p.Dvec[((size_t)b * p.H + h) * p.T + i];
   p.Dsum[(size_t)hs * p.T + i] = s;
 }
 

@@ -46,8 +46,8 @@ struct BwdPre {
   const __nv_bfloat16* out;
   const __nv_bfloat16* dout;
   const float* lse;
-  float* Dvec;        // [B, H, T]
-  float* lse2;        // [B, H, T]  lse * log2(e)
+  float* Dvec;        // [B, H, T]  -D
+  float* lse2;        // [B, H, T]  -lse * log2(e)
   float* Dsum;        // [n_static, T] (nullable): sum over b of D
   int n_static;
   uint8_t static_heads[kMaxHeads];
@@ -61,8 +61,8 @@ struct BwdParams {
   float scale_log2;           // log2(e) / sqrt(d_h)
   float scale;                // 1 / sqrt(d_h)
   uint8_t dynamic_heads[kMaxHeads];
-  const float* lse2;          // [B, H, T]  lse * log2(e)
-  const float* Dvec;          // [B, H, T]
+  const float* lse2;          // [B, H, T]  -lse * log2(e)
+  const float* Dvec;          // [B, H, T]  -D
   float* dq_acc;              // [B, H, T, d_h] fp32, zeroed
   __nv_bfloat16* dK;
   __nv_bfloat16* dV;
