@@ -27,10 +27,11 @@
 // range(alpha) + range(rho) > 80 the products could underflow in fp32, and
 // the head falls back to the exact form exp2(alpha2(j) + rho2(i-j) - log2 Z(i)).
 //
-// Warp roles in K2 (256 threads): warp 0 issues TMA copies, warp 1 issues
+// Warp roles in K2 (384 threads): warp 0 issues TMA copies, warp 1 issues
 // tcgen05 MMAs (one elected lane), warp 2 owns the TMEM allocation, warps
-// 4..7 are the compute warpgroup (softmax / tile generation / epilogue), one
-// tile row per thread, matching TMEM lanes 0..127.
+// 4..11 are two compute warpgroups (softmax / tile generation / epilogue):
+// each tile row belongs to one thread of each, which split its 128 key
+// columns and exchange row maxima and sums through shared memory.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -258,12 +259,13 @@ namespace {
 template <int D>
 struct FwdSmem {
   using G = TileGeom<D>;
-  static constexpr int KST = (D == 128) ? 3 : 4;  // K ring (also holds static aux)
-  static constexpr int VST = (D == 128) ? 3 : 4;  // V ring
+  static constexpr int KST = (D == 128) ? 2 : 4;  // K ring (also holds static aux)
+  static constexpr int VST = (D == 128) ? 3 : 4;  // V ring (consumed a step after K)
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + G::TILE_BYTES;
   static constexpr int OFF_V = OFF_K + KST * G::TILE_BYTES;
-  static constexpr int OFF_BAR = OFF_V + VST * G::TILE_BYTES;
+  static constexpr int OFF_X = OFF_V + VST * G::TILE_BYTES;  // row max / sum exchange
+  static constexpr int OFF_BAR = OFF_X + 3 * 2 * 128 * 4;
   static constexpr int NBAR = 2 + 2 * KST + 2 * VST + 2 + 2 + 2 + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
@@ -276,13 +278,18 @@ struct FwdSmem {
   static constexpr int AUX_BYTES = 512 + 1024;
 };
 
-// TMEM columns: two 128-column buffers at 0 and 128 hold S (fp32) and then,
-// over its first 64 columns, P as packed bf16 (the A operand of O += P V);
-// static items keep their generated tiles there.  The O accumulator sits at
-// 256 (d_h columns for a dynamic item, group * d_h for a static item).
+// TMEM columns: two 128-column buffers at 0 and 128 hold S (fp32).  Each
+// compute half (key columns 0..63 or 64..127 of the tile) writes its P, as
+// packed bf16, over the first 32 columns of its own S half, so P k-steps 0..3
+// sit at buffer + 0.. and 4..7 at buffer + 64..; static items keep their
+// generated tiles in the same places.  The O accumulator sits at 256 (d_h
+// columns for a dynamic item, group * d_h for a static item).
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 0;
 constexpr uint32_t kTmemO = 256;
+__device__ __forceinline__ uint32_t p_col(int kk) {
+  return (uint32_t)((kk < 4) ? kk * 8 : 64 + (kk - 4) * 8);
+}
 
 enum : int {
   kSiteProdQ = 1, kSiteProdK, kSiteProdV, kSiteMmaQ, kSiteMmaK, kSiteMmaS, kSiteMmaV,
@@ -328,13 +335,32 @@ __device__ __forceinline__ Item decode_item(const FwdParams& p, int it) {
   return r;
 }
 
+// Store 16 packed bf16x2 values of one tile row from fp32 pairs.
+__device__ __forceinline__ void store_row16(__nv_bfloat16* dst, const uint32_t (&o)[16], float s) {
+  uint4 v0, v1;
+  v0.x = pack_bf16x2(__uint_as_float(o[0]) * s, __uint_as_float(o[1]) * s);
+  v0.y = pack_bf16x2(__uint_as_float(o[2]) * s, __uint_as_float(o[3]) * s);
+  v0.z = pack_bf16x2(__uint_as_float(o[4]) * s, __uint_as_float(o[5]) * s);
+  v0.w = pack_bf16x2(__uint_as_float(o[6]) * s, __uint_as_float(o[7]) * s);
+  v1.x = pack_bf16x2(__uint_as_float(o[8]) * s, __uint_as_float(o[9]) * s);
+  v1.y = pack_bf16x2(__uint_as_float(o[10]) * s, __uint_as_float(o[11]) * s);
+  v1.z = pack_bf16x2(__uint_as_float(o[12]) * s, __uint_as_float(o[13]) * s);
+  v1.w = pack_bf16x2(__uint_as_float(o[14]) * s, __uint_as_float(o[15]) * s);
+  *reinterpret_cast<uint4*>(dst) = v0;
+  *reinterpret_cast<uint4*>(dst + 8) = v1;
+}
+
+// Threads: warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM owner, warps
+// 4..11 two compute halves (warps 4..7 key columns 0..63, warps 8..11 key
+// columns 64..127 of each tile; a row per thread, two threads per row).
 template <int D, bool TRANSPOSED>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     hybrid_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   using G = TileGeom<D>;
   using L = FwdSmem<D>;
+  constexpr int DH = D / 2;  // output columns per compute half
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
@@ -350,6 +376,8 @@ __global__ void __launch_bounds__(256, 1)
   uint64_t* p_full = s_empty + 2;        // P / G written, O rescaled (compute -> MMA)
   uint64_t* o_full = p_full + 2;
   uint64_t* o_empty = o_full + 1;
+  float* xmax = reinterpret_cast<float*>(smem + L::OFF_X);  // [2 parity][2 halves][128]
+  float* xsum = xmax + 2 * 2 * 128;                         // [2 halves][128]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
   const WaitCtl wc{abort_flag, p.status};
@@ -363,10 +391,10 @@ __global__ void __launch_bounds__(256, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(s_full + s, 1);
       mbar_init(s_empty + s, 1);
-      mbar_init(p_full + s, 128);
+      mbar_init(p_full + s, 256);
     }
     mbar_init(o_full, 1);
-    mbar_init(o_empty, 128);
+    mbar_init(o_empty, 256);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -495,7 +523,7 @@ __global__ void __launch_bounds__(256, 1)
               const uint32_t pa = tmem + kTmemS + (u & 1) * 128;
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk)
-                mma_bf16_ts(tmem + kTmemO, pa + kk * 8, G::mnmajor_desc(vt, kk), idesc_pv,
+                mma_bf16_ts(tmem + kTmemO, pa + p_col(kk), G::mnmajor_desc(vt, kk), idesc_pv,
                             (j > 1 || kk > 0));
               mma_commit(v_empty + vs);
               mma_commit(s_empty + (u & 1));
@@ -519,7 +547,7 @@ __global__ void __launch_bounds__(256, 1)
               const uint32_t vt = sV + vs * G::TILE_BYTES;
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk)
-                mma_bf16_ts(tmem + kTmemO + bb * D, ga + kk * 8, G::mnmajor_desc(vt, kk),
+                mma_bf16_ts(tmem + kTmemO + bb * D, ga + p_col(kk), G::mnmajor_desc(vt, kk),
                             idesc_pv, (step > 0 || kk > 0));
               mma_commit(v_empty + vs);
               ++vc;
@@ -536,9 +564,12 @@ __global__ void __launch_bounds__(256, 1)
       }
     }
   } else if (warp >= 4) {
-    // ---------------------------------------------------------- compute WG
-    const int r = threadIdx.x - 128;             // tile row == TMEM lane
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    // ---------------------------------------------------------- compute halves
+    const int hf = (warp - 4) >> 2;              // key columns 64*hf .. 64*hf + 63
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;                // tile row == TMEM lane
+    const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
+    const int pair_bar = 2 + q4;                 // the two warps that share these rows
     uint32_t kc = 0, sc = 0, oc = 0;
     for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
       const Item w = decode_item<TRANSPOSED>(p, it);
@@ -549,57 +580,53 @@ __global__ void __launch_bounds__(256, 1)
         for (int j = 0; j < w.nsteps; ++j) {
           const uint32_t u = sc0 + j;
           const uint32_t sb = u & 1;
+          const uint32_t sbase = trow + kTmemS + sb * 128 + 64 * hf;
           mbar_wait(s_full + sb, (u >> 1) & 1, wc, kSiteCmpS);
           tc_fence_after();
-          uint32_t sr[128];
+          uint32_t sr[64];
           {
             uint32_t (&a0)[32] = *reinterpret_cast<uint32_t(*)[32]>(sr);
             uint32_t (&a1)[32] = *reinterpret_cast<uint32_t(*)[32]>(sr + 32);
-            uint32_t (&a2)[32] = *reinterpret_cast<uint32_t(*)[32]>(sr + 64);
-            uint32_t (&a3)[32] = *reinterpret_cast<uint32_t(*)[32]>(sr + 96);
-            const uint32_t ta = tmem + lane_base + kTmemS + sb * 128;
-            tmem_ld_x32(ta, a0);
-            tmem_ld_x32(ta + 32, a1);
-            tmem_ld_x32(ta + 64, a2);
-            tmem_ld_x32(ta + 96, a3);
+            tmem_ld_x32(sbase, a0);
+            tmem_ld_x32(sbase + 32, a1);
             tmem_wait_ld(a0);
             tmem_wait_ld(a1);
-            tmem_wait_ld(a2);
-            tmem_wait_ld(a3);
           }
-          // Row max of the raw scores: eight independent partial maxima so
-          // that the dependency chains stay short.  Only the diagonal tile
-          // needs the causal mask.
+          // Causal mask on the diagonal tile: key column 64*hf + c > row r.
           if (j == w.X) {
 #pragma unroll
-            for (int c = 0; c < 128; ++c)
-              if (c > r) sr[c] = 0xff800000u;  // -inf
+            for (int c = 0; c < 64; ++c)
+              if (64 * hf + c > r) sr[c] = 0xff800000u;  // -inf
           }
+          // Partial row max over this half (eight short chains), then the
+          // other half's through shared memory.
           float mx[8];
 #pragma unroll
           for (int k = 0; k < 8; ++k)
             mx[k] = fmaxf(__uint_as_float(sr[k]), __uint_as_float(sr[k + 8]));
 #pragma unroll
-          for (int c = 16; c < 128; c += 16)
+          for (int c = 16; c < 64; c += 16)
 #pragma unroll
             for (int k = 0; k < 8; ++k)
               mx[k] = fmax3(mx[k], __uint_as_float(sr[c + k]), __uint_as_float(sr[c + 8 + k]));
-          const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
-                                 fmaxf(mx[6], mx[7])) * p.scale_log2;
+          const float mh = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                 fmaxf(mx[6], mx[7]));
+          float* xm = xmax + (u & 1) * 256;
+          xm[hf * 128 + r] = mh;
+          named_bar_sync(pair_bar, 64);
+          const float mt = fmaxf(mh, xm[(1 - hf) * 128 + r]) * p.scale_log2;
           const float m_new = fmaxf(m_run, mt);
           const bool need = m_new > m_run + 8.0f;
           const float m_use = need ? m_new : m_run;
           const float corr = need ? fast_exp2(m_run - m_new) : 1.0f;
           // p = exp2(s * scale_log2 - m_use): one packed FMA per pair, two
-          // exponentials, one packed add into four partial row sums.
+          // exponentials, a packed add into four partial sums; P goes over the
+          // first 32 columns of this half (already read), 16 at a time.
           const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
           const uint64_t nm2 = f2_pack(-m_use, -m_use);
-          // P goes over the first 64 columns of this S buffer (already read
-          // into registers), 16 packed columns at a time.
           uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-          const uint32_t pdst = tmem + lane_base + kTmemS + sb * 128;
 #pragma unroll
-          for (int q0 = 0; q0 < 64; q0 += 16) {
+          for (int q0 = 0; q0 < 32; q0 += 16) {
             uint32_t pk[16];
 #pragma unroll
             for (int qq = 0; qq < 16; ++qq) {
@@ -612,7 +639,7 @@ __global__ void __launch_bounds__(256, 1)
               acc[qq & 3] = f2_add(acc[qq & 3], f2_pack(e0, e1));
               pk[qq] = pack_bf16x2(e0, e1);
             }
-            tmem_st_x16(pdst + q0, pk);
+            tmem_st_x16(sbase + q0, pk);
           }
           float rs;
           {
@@ -621,16 +648,16 @@ __global__ void __launch_bounds__(256, 1)
             f2_unpack(t, lo, hi);
             rs = lo + hi;
           }
-          // Rescale O (in TMEM) when some row of this warp moved its max: the
-          // previous tile's P V must have finished first.
+          // Rescale this half's O columns when some row of the warp moved its
+          // max: the previous tile's P V must have finished first.
           if (j > 0 && __any_sync(0xffffffffu, need)) {
             const uint32_t up = u - 1;
             mbar_wait(s_empty + (up & 1), (up >> 1) & 1, wc, kSiteCmpPV);
             tc_fence_after();
 #pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 16) {
+            for (int c0 = 0; c0 < DH; c0 += 16) {
               uint32_t o[16];
-              const uint32_t ta = tmem + lane_base + kTmemO + c0;
+              const uint32_t ta = trow + kTmemO + hf * DH + c0;
               tmem_ld_x16(ta, o);
               tmem_wait_ld(o);
 #pragma unroll
@@ -645,30 +672,24 @@ __global__ void __launch_bounds__(256, 1)
           mbar_arrive(p_full + sb);
         }
         sc = sc0 + w.nsteps;
-        // epilogue: O / l -> out, lse
+        // epilogue: O / l -> out (each half its d_h / 2 columns), lse
+        xsum[hf * 128 + r] = l_run;
+        named_bar_sync(pair_bar, 64);
+        const float l_tot = l_run + xsum[(1 - hf) * 128 + r];
+        named_bar_sync(pair_bar, 64);  // xsum may be rewritten by the next item
         mbar_wait(o_full, oc & 1, wc, kSiteCmpO);
         tc_fence_after();
-        const float inv_l = 1.0f / l_run;
+        const float inv_l = 1.0f / l_tot;
         const size_t orow = ((size_t)(w.b * H + w.h) * T + (size_t)w.X * 128 + r);
-        __nv_bfloat16* dst = p.out + orow * D;
+        __nv_bfloat16* dst = p.out + orow * D + hf * DH;
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 16) {
+        for (int c0 = 0; c0 < DH; c0 += 16) {
           uint32_t o[16];
-          tmem_ld_x16(tmem + lane_base + kTmemO + c0, o);
+          tmem_ld_x16(trow + kTmemO + hf * DH + c0, o);
           tmem_wait_ld(o);
-          uint4 v0, v1;
-          v0.x = pack_bf16x2(__uint_as_float(o[0]) * inv_l, __uint_as_float(o[1]) * inv_l);
-          v0.y = pack_bf16x2(__uint_as_float(o[2]) * inv_l, __uint_as_float(o[3]) * inv_l);
-          v0.z = pack_bf16x2(__uint_as_float(o[4]) * inv_l, __uint_as_float(o[5]) * inv_l);
-          v0.w = pack_bf16x2(__uint_as_float(o[6]) * inv_l, __uint_as_float(o[7]) * inv_l);
-          v1.x = pack_bf16x2(__uint_as_float(o[8]) * inv_l, __uint_as_float(o[9]) * inv_l);
-          v1.y = pack_bf16x2(__uint_as_float(o[10]) * inv_l, __uint_as_float(o[11]) * inv_l);
-          v1.z = pack_bf16x2(__uint_as_float(o[12]) * inv_l, __uint_as_float(o[13]) * inv_l);
-          v1.w = pack_bf16x2(__uint_as_float(o[14]) * inv_l, __uint_as_float(o[15]) * inv_l);
-          *reinterpret_cast<uint4*>(dst + c0) = v0;
-          *reinterpret_cast<uint4*>(dst + c0 + 8) = v1;
+          store_row16(dst + c0, o, inv_l);
         }
-        if (p.lse) p.lse[orow] = (m_run + log2f(l_run)) * kLn2;
+        if (hf == 0 && p.lse) p.lse[orow] = (m_run + log2f(l_tot)) * kLn2;
         tc_fence_before();
         mbar_arrive(o_empty);
         ++oc;
@@ -683,33 +704,34 @@ __global__ void __launch_bounds__(256, 1)
           const int ks = kc % L::KST;
           mbar_wait(k_full + ks, (kc / L::KST) & 1, wc, kSiteCmpAux);
           const float* aux = reinterpret_cast<const float*>(smem + L::OFF_K + ks * G::TILE_BYTES);
-          const float* colv = aux;                 // 128 values
+          const float* colv = aux + 64 * hf;       // this half's 64 column values
           const float* win = aux + L::AUX_WIN / 4; // window, centre at 127
           // the TMEM buffer must be free: the MMAs of two steps back are done
           mbar_wait(s_empty + (u & 1), ((u >> 1) & 1) ^ 1, wc, kSiteCmpP);
           tc_fence_after();
-          const uint32_t gdst = tmem + lane_base + kTmemS + (u & 1) * 128;
+          const uint32_t gdst = trow + kTmemS + (u & 1) * 128 + 64 * hf;
 #pragma unroll
-          for (int q0 = 0; q0 < 64; q0 += 16) {
+          for (int q0 = 0; q0 < 32; q0 += 16) {
             uint32_t pk[16];
 #pragma unroll
             for (int qq = 0; qq < 16; ++qq) {
               float e[2];
 #pragma unroll
               for (int k = 0; k < 2; ++k) {
-                const int c = 2 * (q0 + qq) + k;
+                const int cl = 2 * (q0 + qq) + k;  // column within the half
+                const int c = 64 * hf + cl;
                 // forward: element (i = row, j = col), distance r - c
                 // transposed: element (j = row, i = col), distance c - r
                 const float wv = TRANSPOSED ? win[127 + c - r] : win[127 + r - c];
-                e[k] = exact ? fast_exp2(colv[c] + wv + rowv) : colv[c] * wv * rowv;
+                e[k] = exact ? fast_exp2(colv[cl] + wv + rowv) : colv[cl] * wv * rowv;
               }
               pk[qq] = pack_bf16x2(e[0], e[1]);
             }
             tmem_st_x16(gdst + q0, pk);
           }
-          // all 128 threads have read the aux slot: release it once
-          named_bar_sync(1, 128);
-          if (r == 0) mbar_arrive(k_empty + ks);
+          // all 256 compute threads have read the aux slot: release it once
+          named_bar_sync(1, 256);
+          if (hf == 0 && r == 0) mbar_arrive(k_empty + ks);
           ++kc;
           tmem_wait_st();
           tc_fence_before();
@@ -718,28 +740,18 @@ __global__ void __launch_bounds__(256, 1)
         sc = sc0 + w.nsteps;
         mbar_wait(o_full, oc & 1, wc, kSiteCmpO);
         tc_fence_after();
-        const int trow = w.X * 128 + r;
+        const int trow_i = w.X * 128 + r;
         for (int bb = 0; bb < w.nb; ++bb) {
-          const size_t orow = ((size_t)((w.b + bb) * H + w.h) * T + trow);
-          __nv_bfloat16* dst = p.out + orow * D;
+          const size_t orow = ((size_t)((w.b + bb) * H + w.h) * T + trow_i);
+          __nv_bfloat16* dst = p.out + orow * D + hf * DH;
 #pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 16) {
+          for (int c0 = 0; c0 < DH; c0 += 16) {
             uint32_t o[16];
-            tmem_ld_x16(tmem + lane_base + kTmemO + bb * D + c0, o);
+            tmem_ld_x16(trow + kTmemO + bb * D + hf * DH + c0, o);
             tmem_wait_ld(o);
-            uint4 v0, v1;
-            v0.x = pack_bf16x2(__uint_as_float(o[0]), __uint_as_float(o[1]));
-            v0.y = pack_bf16x2(__uint_as_float(o[2]), __uint_as_float(o[3]));
-            v0.z = pack_bf16x2(__uint_as_float(o[4]), __uint_as_float(o[5]));
-            v0.w = pack_bf16x2(__uint_as_float(o[6]), __uint_as_float(o[7]));
-            v1.x = pack_bf16x2(__uint_as_float(o[8]), __uint_as_float(o[9]));
-            v1.y = pack_bf16x2(__uint_as_float(o[10]), __uint_as_float(o[11]));
-            v1.z = pack_bf16x2(__uint_as_float(o[12]), __uint_as_float(o[13]));
-            v1.w = pack_bf16x2(__uint_as_float(o[14]), __uint_as_float(o[15]));
-            *reinterpret_cast<uint4*>(dst + c0) = v0;
-            *reinterpret_cast<uint4*>(dst + c0 + 8) = v1;
+            store_row16(dst + c0, o, 1.0f);
           }
-          if (!TRANSPOSED && p.lse) p.lse[orow] = p.logZ[(size_t)w.hs * T + trow];
+          if (!TRANSPOSED && hf == 0 && p.lse) p.lse[orow] = p.logZ[(size_t)w.hs * T + trow_i];
         }
         tc_fence_before();
         mbar_arrive(o_empty);
@@ -771,7 +783,7 @@ cudaError_t launch_fused(const FwdLaunch& L, cudaStream_t s) {
   if (L.p.n_items == 0) return cudaSuccess;
   const int grid = L.p.n_items < L.num_sms ? L.p.n_items : L.num_sms;
   trace_begin(s);
-  kern<<<grid, 256, S::ALLOC, s>>>(L.tm_q, L.tm_k, L.tm_v, L.p);
+  kern<<<grid, 384, S::ALLOC, s>>>(L.tm_q, L.tm_k, L.tm_v, L.p);
   trace_end(s, TRANSPOSED ? "static_dv" : "hybrid_fwd");
   return cudaGetLastError();
 }
