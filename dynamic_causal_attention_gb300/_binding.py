@@ -34,6 +34,7 @@ EXPORTED = (
     "saf_calib_accumulate",
     "saf_calib_num_select",
     "saf_calib_finalize",
+    "saf_fit_compact",
     "saf_calib_reset",
     "saf_calib_destroy",
     "saf_get_device_status",
@@ -89,6 +90,9 @@ _lib.saf_calib_num_select.argtypes = [ctypes.c_double, _i]
 _lib.saf_calib_num_select.restype = _i
 _lib.saf_calib_finalize.argtypes = [_vp, _i, _vp, _vp, _vp, _vp]
 _lib.saf_calib_finalize.restype = _i
+_lib.saf_fit_compact.argtypes = [_vp, _i, _i, _vp, _i, _i, ctypes.c_float, _i, ctypes.c_float,
+                                 _vp, _vp, _vp, _vp, _vp, _vp]
+_lib.saf_fit_compact.restype = _i
 _lib.saf_calib_reset.argtypes = [_vp]
 _lib.saf_calib_reset.restype = _i
 _lib.saf_calib_destroy.argtypes = [_vp]
@@ -178,6 +182,13 @@ def saf_calib_num_select(r: float, num_heads: int) -> int:
 
 def saf_calib_finalize(handle, k, A_hat, s_var, selected, stream) -> int:
     return _lib.saf_calib_finalize(handle, int(k), A_hat, s_var, selected, stream)
+
+
+def saf_fit_compact(A_hat, num_heads, T, candidates, n_candidates, k, kl_max, steps, lr,
+                    alpha, rho, kl, selected, n_selected, stream) -> int:
+    return _lib.saf_fit_compact(A_hat, int(num_heads), int(T), candidates, int(n_candidates),
+                                int(k), float(kl_max), int(steps), float(lr), alpha, rho, kl,
+                                selected, n_selected, stream)
 
 
 def saf_calib_reset(handle) -> int:

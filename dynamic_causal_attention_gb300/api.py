@@ -12,7 +12,7 @@ import torch
 
 from . import _binding as B
 
-__all__ = ["HybridAttention", "Calibration", "num_select", "SafError"]
+__all__ = ["HybridAttention", "Calibration", "fit_compact", "num_select", "SafError"]
 
 SafError = B.SafError
 
@@ -127,6 +127,25 @@ class Calibration:
             self.close()
         except Exception:
             pass
+
+
+def fit_compact(A_hat, candidates, k, kl_max=0.2, steps=400, lr=1e-2):
+    """Fit alpha/rho to A_hat [num_heads, T, T] for each candidate head (device
+    int32, priority order) and select the first k that pass the KL gate.
+    Returns (alpha [n, T], rho [n, T], kl [n], selected [n_selected])."""
+    num_heads, T, _ = A_hat.shape
+    n = candidates.numel()
+    dev = A_hat.device
+    alpha = torch.empty((n, T), dtype=torch.float32, device=dev)
+    rho = torch.empty((n, T), dtype=torch.float32, device=dev)
+    kl = torch.empty(n, dtype=torch.float32, device=dev)
+    sel = torch.empty(max(k, 1), dtype=torch.int32, device=dev)
+    n_sel = torch.zeros(1, dtype=torch.int32, device=dev)
+    st = B.saf_fit_compact(_ptr(A_hat), num_heads, T, _ptr(candidates), n, k, kl_max, steps, lr,
+                           _ptr(alpha), _ptr(rho), _ptr(kl), _ptr(sel), _ptr(n_sel),
+                           _stream(dev))
+    _check(st, "saf_fit_compact")
+    return alpha, rho, kl, sel[: int(n_sel.item())]
 
 
 def num_select(r: float, num_heads: int) -> int:

@@ -575,6 +575,38 @@ saf_status saf_calib_finalize(void* handle, int k, float* A_hat, float* s_var, i
   return cuda_status(launch_calib_finalize(p, static_cast<cudaStream_t>(stream)));
 }
 
+saf_status saf_fit_compact(const float* A_hat, int num_heads, int T, const int32_t* candidates,
+                           int n_candidates, int k, float kl_max, int steps, float lr,
+                           float* alpha, float* rho, float* kl, int32_t* selected,
+                           int32_t* n_selected, void* stream) {
+  g_launches = 0;
+  if (!A_hat || !candidates || !alpha || !rho || !kl || !n_selected) return SAF_ERR_INVALID_ARG;
+  if (num_heads < 1 || T < 1 || n_candidates < 1 || steps < 0 || k < 0 || k > n_candidates)
+    return SAF_ERR_INVALID_ARG;
+  if (k > 0 && !selected) return SAF_ERR_INVALID_ARG;
+  if (!(lr > 0.f) || !(kl_max >= 0.f)) return SAF_ERR_INVALID_ARG;
+  if (T > 4096) return SAF_ERR_UNSUPPORTED;
+  if (!aligned16(A_hat) || !aligned16(alpha) || !aligned16(rho)) return SAF_ERR_INVALID_ARG;
+  FitParams p;
+  p.A_hat = A_hat;
+  p.T = T;
+  p.candidates = candidates;
+  p.n_candidates = n_candidates;
+  p.k = k;
+  p.kl_max = kl_max;
+  p.steps = steps;
+  p.lr = lr;
+  p.beta1 = 0.9f;
+  p.beta2 = 0.999f;
+  p.eps = 1e-8f;
+  p.alpha = alpha;
+  p.rho = rho;
+  p.kl = kl;
+  p.selected = selected;
+  p.n_selected = n_selected;
+  return cuda_status(launch_fit(p, static_cast<cudaStream_t>(stream)));
+}
+
 saf_status saf_calib_reset(void* handle) {
   CalibHandle* h = static_cast<CalibHandle*>(handle);
   if (!h) return SAF_ERR_INVALID_ARG;

@@ -44,6 +44,25 @@ struct CalibFinalize {
 };
 cudaError_t launch_calib_finalize(const CalibFinalize& p, cudaStream_t s);
 
+// ------------------------------------------------------------ compact fit
+struct FitParams {
+  const float* A_hat;        // [num_heads, T, T]
+  int T;
+  const int32_t* candidates; // [n_candidates] head indices, priority order
+  int n_candidates;
+  int k;
+  float kl_max;
+  int steps;
+  float lr, beta1, beta2, eps;
+  float* alpha;              // [n_candidates, T]
+  float* rho;                // [n_candidates, T]
+  float* kl;                 // [n_candidates]
+  int32_t* selected;         // [k] (nullable when k == 0)
+  int32_t* n_selected;       // [1]
+};
+size_t fit_smem_bytes(int T);
+cudaError_t launch_fit(const FitParams& p, cudaStream_t s);
+
 // ------------------------------------------------------------ attention
 constexpr int kMaxHeads = 256;
 

@@ -198,6 +198,31 @@ SAF_API int saf_calib_num_select(double r, int num_heads);
 SAF_API saf_status saf_calib_finalize(void* handle, int k, float* A_hat, float* s_var,
                               int32_t* selected, void* stream);
 
+/* Compact pattern fit ("When Can Attention Heads Be Statically Defined?",
+ * §3 Eq. (3)/(4) and App. A.2).  For each candidate head, alpha and rho are
+ * fitted to its mean pattern A_hat by `steps` Adam steps (rate `lr`, beta =
+ * (0.9, 0.999), eps = 1e-8) on the row-averaged cross-entropy, starting from
+ * the log of A_hat's column and diagonal means; the gradient uses only the
+ * column and diagonal sums of A_hat (Eq. (4)).  Then the candidates are
+ * walked in the given order and the first k whose fitted pattern has mean row
+ * KL(A_hat || P_hat) <= kl_max (0.2 nat in the paper) are selected; a head
+ * over the gate is skipped.
+ *   A_hat       device fp32 [num_heads, T, T] (e.g. from saf_calib_finalize);
+ *               T <= 4096.
+ *   candidates  device int32 [n_candidates]: head indices in priority order
+ *               (ascending s_var: saf_calib_finalize with k = num_heads).
+ *   alpha, rho  device fp32 [n_candidates, T]: the fitted vectors.
+ *   kl          device fp32 [n_candidates]: mean row KL of each fit, in nats.
+ *   selected    device int32 [k] (NULL when k == 0); n_selected device int32
+ *               [1]: how many heads passed (<= k; the rest of `selected` is
+ *               left untouched).
+ * One CTA per candidate; no workspace is needed. */
+SAF_API saf_status saf_fit_compact(const float* A_hat, int num_heads, int T,
+                           const int32_t* candidates, int n_candidates, int k,
+                           float kl_max, int steps, float lr,
+                           float* alpha, float* rho, float* kl,
+                           int32_t* selected, int32_t* n_selected, void* stream);
+
 /* Forget all accumulated samples (the allocation is kept). */
 SAF_API saf_status saf_calib_reset(void* handle);
 
