@@ -113,6 +113,22 @@ bool encode_rows(CUtensorMap* m, const void* base, uint64_t rows, int d) {
   return r == CUDA_SUCCESS;
 }
 
+// 2-D view [rows, d] of an fp32 tensor, box of 128 rows x 32 columns (128 B,
+// 128-byte swizzle): the staging layout of the backward's dQ reduction.
+bool encode_rows_f32(CUtensorMap* m, const void* base, uint64_t rows, int d) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)d * 4};
+  const cuuint32_t box[2] = {32u, 128u};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------ workspace
 struct WsLayout {
   size_t status, a_tab, r_tab, row_tab, logZ, mode;
@@ -219,7 +235,7 @@ void fill_fwd_params(FwdParams& p, const saf_attn_dims& d, const HeadSplit& hs, 
   p.nI = d.T / 128;
   p.n_static = hs.n_static;
   p.n_dynamic = transposed ? 0 : hs.n_dynamic;
-  p.group = 256 / d.d_h < d.B ? 256 / d.d_h : d.B;
+  p.group = static_group(d.d_h, d.B);
   p.n_groups = (d.B + p.group - 1) / p.group;
   p.n_items = p.nI * (p.n_static * p.n_groups + (transposed ? 0 : d.B * hs.n_dynamic));
   p.scale_log2 = 1.4426950408889634f / sqrtf((float)d.d_h);
@@ -400,11 +416,11 @@ saf_status saf_hybrid_attn_bwd(const saf_attn_dims* dims, const void* Q, const v
   pre.Dsum = dalpha ? reinterpret_cast<float*>(ws + L.Dsum) : nullptr;
   pre.n_static = hs.n_static;
   memcpy(pre.static_heads, hs.st, sizeof(pre.static_heads));
+  float* dq_acc = reinterpret_cast<float*>(ws + L.dq_acc);
+  pre.dq_acc = hs.n_dynamic > 0 ? dq_acc : nullptr;
   SAF_TRY(launch_bwd_pre(pre, s));
 
-  float* dq_acc = reinterpret_cast<float*>(ws + L.dq_acc);
   if (hs.n_dynamic > 0) {
-    SAF_TRY(launch_zero_u32(dq_acc, elems, s));
     BwdLaunch bl;
     memset(&bl, 0, sizeof(bl));
     BwdParams& p = bl.p;
@@ -421,7 +437,8 @@ saf_status saf_hybrid_attn_bwd(const saf_attn_dims* dims, const void* Q, const v
     p.dV = static_cast<__nv_bfloat16*>(dv16);
     p.status = reinterpret_cast<int*>(ws + L.status);
     if (!encode_rows(&bl.tm_q, q16, rows, d.d_h) || !encode_rows(&bl.tm_k, k16, rows, d.d_h) ||
-        !encode_rows(&bl.tm_v, v16, rows, d.d_h) || !encode_rows(&bl.tm_do, do16, rows, d.d_h))
+        !encode_rows(&bl.tm_v, v16, rows, d.d_h) || !encode_rows(&bl.tm_do, do16, rows, d.d_h) ||
+        !encode_rows_f32(&bl.tm_dq, dq_acc, rows, d.d_h))
       return SAF_ERR_CUDA;
     bl.d_h = d.d_h;
     bl.num_sms = sm_count();

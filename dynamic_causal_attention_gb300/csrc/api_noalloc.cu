@@ -167,7 +167,7 @@ extern "C" saf_status saf_hybrid_attn_fwd_noalloc(const saf_attn_dims* dims, con
   p.nI = d.T / 128;
   p.n_static = n_static;
   p.n_dynamic = n_dynamic;
-  p.group = 256 / d.d_h < d.B ? 256 / d.d_h : d.B;
+  p.group = static_group(d.d_h, d.B);
   p.n_groups = (d.B + p.group - 1) / p.group;
   p.n_items = p.nI * (n_static * p.n_groups + d.B * n_dynamic);
   p.scale_log2 = 1.4426950408889634f / sqrtf((float)d.d_h);

@@ -20,7 +20,9 @@
 // The compute warps write P^T and dS^T as packed bf16 over the TMEM columns
 // of S^T and dP^T they have just read, so the dV/dK products read only dO and
 // Q from shared memory.  dQ_I is read from TMEM by a second warpgroup and
-// added into an fp32 accumulator with vector atomics; a post-pass scales it by
+// added into an fp32 accumulator (zeroed by the pre-pass): for d_h <= 64 the
+// tile is staged in shared memory and added with one TMA tensor reduce per 32
+// columns, for d_h = 128 with vector atomics.  A post-pass scales it by
 // 1/sqrt(d) and converts it.
 //
 // param_grad_kernel (K5): items (h_static, J).  For I = J..nI-1 the batch-
@@ -54,7 +56,12 @@ struct BwdSmem {
   static constexpr int OFF_V = OFF_K + G::TILE_BYTES;
   static constexpr int OFF_Q = OFF_V + G::TILE_BYTES;
   static constexpr int OFF_DST = OFF_Q + QST * STAGE;
-  static constexpr int OFF_BAR = OFF_DST + SqTile::BYTES;
+  // dQ staging for the tensor reduce-add (d_h <= 64): [d_h / 32] chunks of
+  // [128 rows x 128 B], 128-byte swizzled.  d_h = 128 adds with atomics.
+  static constexpr bool DQ_TMA = (D <= 64);
+  static constexpr int DQS_BYTES = DQ_TMA ? 128 * D * 4 : 0;
+  static constexpr int OFF_DQS = OFF_DST + SqTile::BYTES;
+  static constexpr int OFF_BAR = OFF_DQS + DQS_BYTES;
   static constexpr int NBAR = 2 + 2 * QST + 9;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
@@ -105,7 +112,8 @@ __global__ void __launch_bounds__(512, 1)
     bwd_dynamic_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
-                       const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+                       const __grid_constant__ CUtensorMap tm_do,
+                       const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
   using G = TileGeom<D>;
   using L = BwdSmem<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -402,23 +410,56 @@ __global__ void __launch_bounds__(512, 1)
         const int I = w.J + t;
         mbar_wait(dq_full, dqc & 1, wc, kSiteBDq);
         tc_fence_after();
-        float* dst = p.dq_acc + ((size_t)(w.b * H + w.h) * T + (size_t)I * 128 + r) * D;
+        if constexpr (L::DQ_TMA) {
+          // TMEM -> registers -> swizzled staging tile -> one tensor
+          // reduce-add per 32-column chunk, issued by one thread.
+          uint32_t o[D];
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 16) {
-          uint32_t o[16];
-          tmem_ld_x16(tmem + lane_base + L::T_DQ + c0, o);
-          tmem_wait_ld(o);
+          for (int c0 = 0; c0 < D; c0 += 16)
+            tmem_ld_x16(tmem + lane_base + L::T_DQ + c0,
+                        *reinterpret_cast<uint32_t(*)[16]>(o + c0));
 #pragma unroll
-          for (int e = 0; e < 16; e += 4)
-            atomicAdd(reinterpret_cast<float4*>(dst + c0 + e),
-                      make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]),
-                                  __uint_as_float(o[e + 2]), __uint_as_float(o[e + 3])));
+          for (int c0 = 0; c0 < D; c0 += 16)
+            tmem_wait_ld(*reinterpret_cast<uint32_t(*)[16]>(o + c0));
+          tc_fence_before();
+          mbar_arrive(dq_empty);
+          if (r == 0) bulk_wait_group_read0();  // the previous tile has been read
+          named_bar_sync(6, 128);
+          const uint32_t stg = smem_u32(smem + L::OFF_DQS);
+#pragma unroll
+          for (int u = 0; u < D / 4; ++u)
+            st_shared_v4(stg + (uint32_t)(u >> 3) * 16384u + sw128_offset(r, (uint32_t)(u & 7)),
+                         o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
+          fence_proxy_async_smem();
+          named_bar_sync(6, 128);
+          if (r == 0) {
+            const int row = (w.b * H + w.h) * T + I * 128;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c)
+              tma_reduce_add_2d(&tm_dq, smem + L::OFF_DQS + c * 16384, c * 32, row);
+            bulk_commit_group();
+          }
+        } else {
+          float* dst = p.dq_acc + ((size_t)(w.b * H + w.h) * T + (size_t)I * 128 + r) * D;
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 16) {
+            uint32_t o[16];
+            tmem_ld_x16(tmem + lane_base + L::T_DQ + c0, o);
+            tmem_wait_ld(o);
+#pragma unroll
+            for (int e = 0; e < 16; e += 4)
+              atomicAdd(reinterpret_cast<float4*>(dst + c0 + e),
+                        make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]),
+                                    __uint_as_float(o[e + 2]), __uint_as_float(o[e + 3])));
+          }
+          tc_fence_before();
+          mbar_arrive(dq_empty);
         }
-        tc_fence_before();
-        mbar_arrive(dq_empty);
         ++dqc;
       }
     }
+    // every reduction issued must have completed before the CTA exits
+    if (L::DQ_TMA && r == 0) bulk_wait_group0();
   }
 
   tc_fence_before();
@@ -633,7 +674,8 @@ cudaError_t launch_dyn(const BwdLaunch& L, cudaStream_t s) {
   if (L.p.n_items == 0) return cudaSuccess;
   const int grid = L.p.n_items < L.num_sms ? L.p.n_items : L.num_sms;
   trace_begin(s);
-  bwd_dynamic_kernel<D><<<grid, 512, BwdSmem<D>::ALLOC, s>>>(L.tm_q, L.tm_k, L.tm_v, L.tm_do, L.p);
+  bwd_dynamic_kernel<D><<<grid, 512, BwdSmem<D>::ALLOC, s>>>(L.tm_q, L.tm_k, L.tm_v, L.tm_do,
+                                                              L.tm_dq, L.p);
   trace_end(s, "bwd_dynamic");
   return cudaGetLastError();
 }

@@ -3,7 +3,8 @@
 //   bwd_pre   D(b,h,i) = sum_d dO(b,h,i,d) * out(b,h,i,d) (the softmax
 //             backward's row term), stored negated, and -lse * log2(e) (the
 //             dynamic backward adds both), plus for frozen heads the batch
-//             sums of D that the alpha/rho gradients need;
+//             sums of D that the alpha/rho gradients need; it also zeroes the
+//             fp32 dQ accumulator;
 //   bwd_post  dQ = (1/sqrt(d_h)) * fp32 accumulator -> bf16, and zeros for the
 //             dQ/dK rows of frozen heads (they have no query/key path).
 #include <cuda_bf16.h>
@@ -42,6 +43,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(BwdPre p) {
 #pragma unroll
   for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
   (void)lane;
+  if (row < rows && p.dq_acc) {
+    float4* z = reinterpret_cast<float4*>(p.dq_acc + row * D + sub * 8);
+    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   if (row < rows && sub == 0) {
     p.Dvec[row] = -acc;
     p.lse2[row] = -p.lse[row] * 1.4426950408889634f;

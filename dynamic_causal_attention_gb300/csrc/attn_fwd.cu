@@ -259,6 +259,10 @@ namespace {
 template <int D>
 struct FwdSmem {
   using G = TileGeom<D>;
+  // TMEM S/P buffers: three for d_h <= 64 (then S of tile j + 1 only waits for
+  // P V of tile j - 2), two for d_h = 128 (the O accumulator needs the rest).
+  static constexpr int NBUF = (D <= 64) ? 3 : 2;
+  static constexpr uint32_t TMEM_O = NBUF * 128;
   static constexpr int KST = (D == 128) ? 2 : 4;  // K ring (also holds static aux)
   static constexpr int VST = (D == 128) ? 3 : 4;  // V ring (consumed a step after K)
   static constexpr int OFF_Q = 0;
@@ -266,7 +270,7 @@ struct FwdSmem {
   static constexpr int OFF_V = OFF_K + KST * G::TILE_BYTES;
   static constexpr int OFF_X = OFF_V + VST * G::TILE_BYTES;  // row max / sum exchange
   static constexpr int OFF_BAR = OFF_X + 3 * 2 * 128 * 4;
-  static constexpr int NBAR = 2 + 2 * KST + 2 * VST + 2 + 2 + 2 + 2;
+  static constexpr int NBAR = 2 + 2 * KST + 2 * VST + 3 * NBUF + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int ALLOC = BYTES + 1024;  // slack to align the base to 1024 B
@@ -278,15 +282,14 @@ struct FwdSmem {
   static constexpr int AUX_BYTES = 512 + 1024;
 };
 
-// TMEM columns: two 128-column buffers at 0 and 128 hold S (fp32).  Each
-// compute half (key columns 0..63 or 64..127 of the tile) writes its P, as
-// packed bf16, over the first 32 columns of its own S half, so P k-steps 0..3
-// sit at buffer + 0.. and 4..7 at buffer + 64..; static items keep their
-// generated tiles in the same places.  The O accumulator sits at 256 (d_h
+// TMEM columns: NBUF 128-column buffers from 0 hold S (fp32).  Each compute
+// half (key columns 0..63 or 64..127 of the tile) writes its P, as packed
+// bf16, over the first 32 columns of its own S half, so P k-steps 0..3 sit at
+// buffer + 0.. and 4..7 at buffer + 64..; static items keep their generated
+// tiles in the same places.  The O accumulator follows the buffers (d_h
 // columns for a dynamic item, group * d_h for a static item).
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 0;
-constexpr uint32_t kTmemO = 256;
 __device__ __forceinline__ uint32_t p_col(int kk) {
   return (uint32_t)((kk < 4) ? kk * 8 : 64 + (kk - 4) * 8);
 }
@@ -371,10 +374,12 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* k_empty = k_full + L::KST;
   uint64_t* v_full = k_empty + L::KST;
   uint64_t* v_empty = v_full + L::VST;
+  constexpr int NB = L::NBUF;
+  constexpr uint32_t kTmemO = L::TMEM_O;
   uint64_t* s_full = v_empty + L::VST;   // S ready (MMA -> compute)
-  uint64_t* s_empty = s_full + 2;        // buffer free again: its P V MMAs done (MMA -> all)
-  uint64_t* p_full = s_empty + 2;        // P / G written, O rescaled (compute -> MMA)
-  uint64_t* o_full = p_full + 2;
+  uint64_t* s_empty = s_full + NB;       // buffer free again: its P V MMAs done (MMA -> all)
+  uint64_t* p_full = s_empty + NB;       // P / G written, O rescaled (compute -> MMA)
+  uint64_t* o_full = p_full + NB;
   uint64_t* o_empty = o_full + 1;
   float* xmax = reinterpret_cast<float*>(smem + L::OFF_X);  // [2 parity][2 halves][128]
   float* xsum = xmax + 2 * 2 * 128;                         // [2 halves][128]
@@ -388,7 +393,7 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(q_empty, 1);
     for (int s = 0; s < L::KST; ++s) { mbar_init(k_full + s, 1); mbar_init(k_empty + s, 1); }
     for (int s = 0; s < L::VST; ++s) { mbar_init(v_full + s, 1); mbar_init(v_empty + s, 1); }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < NB; ++s) {
       mbar_init(s_full + s, 1);
       mbar_init(s_empty + s, 1);
       mbar_init(p_full + s, 256);
@@ -500,15 +505,16 @@ __global__ void __launch_bounds__(384, 1)
               const uint32_t u = sc0 + j;
               const int ks = kc % L::KST;
               mbar_wait(k_full + ks, (kc / L::KST) & 1, wc, kSiteMmaK);
-              mbar_wait(s_empty + (u & 1), ((u >> 1) & 1) ^ 1, wc, kSiteMmaS);
+              const uint32_t b = u % NB;
+              mbar_wait(s_empty + b, ((u / NB) & 1) ^ 1, wc, kSiteMmaS);
               tc_fence_after();
               const uint32_t kt = sK + ks * G::TILE_BYTES;
 #pragma unroll
               for (int kk = 0; kk < G::KSTEPS; ++kk)
-                mma_bf16_ss(tmem + kTmemS + (u & 1) * 128, G::kmajor_desc(sQ, kk),
+                mma_bf16_ss(tmem + kTmemS + b * 128, G::kmajor_desc(sQ, kk),
                             G::kmajor_desc(kt, kk), idesc_s, kk > 0);
               mma_commit(k_empty + ks);
-              mma_commit(s_full + (u & 1));
+              mma_commit(s_full + b);
               if (j == w.nsteps - 1) mma_commit(q_empty);
               ++kc;
             }
@@ -516,17 +522,17 @@ __global__ void __launch_bounds__(384, 1)
               const uint32_t u = sc0 + j - 1;
               const int vs = vc % L::VST;
               mbar_wait(v_full + vs, (vc / L::VST) & 1, wc, kSiteMmaV);
-              mbar_wait(p_full + (u & 1), (u >> 1) & 1, wc, kSiteMmaP);
+              mbar_wait(p_full + (u % NB), (u / NB) & 1, wc, kSiteMmaP);
               if (j == 1) mbar_wait(o_empty, (oc & 1) ^ 1, wc, kSiteMmaO);
               tc_fence_after();
               const uint32_t vt = sV + vs * G::TILE_BYTES;
-              const uint32_t pa = tmem + kTmemS + (u & 1) * 128;
+              const uint32_t pa = tmem + kTmemS + (u % NB) * 128;
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk)
                 mma_bf16_ts(tmem + kTmemO, pa + p_col(kk), G::mnmajor_desc(vt, kk), idesc_pv,
                             (j > 1 || kk > 0));
               mma_commit(v_empty + vs);
-              mma_commit(s_empty + (u & 1));
+              mma_commit(s_empty + (u % NB));
               ++vc;
             }
           }
@@ -537,9 +543,9 @@ __global__ void __launch_bounds__(384, 1)
           for (int step = 0; step < w.nsteps; ++step) {
             ++kc;  // the aux entry of this step is consumed by the compute warps
             const uint32_t u = sc0 + step;
-            mbar_wait(p_full + (u & 1), (u >> 1) & 1, wc, kSiteMmaP);
+            mbar_wait(p_full + (u % NB), (u / NB) & 1, wc, kSiteMmaP);
             if (step == 0) mbar_wait(o_empty, (oc & 1) ^ 1, wc, kSiteMmaO);
-            const uint32_t ga = tmem + kTmemS + (u & 1) * 128;
+            const uint32_t ga = tmem + kTmemS + (u % NB) * 128;
             for (int bb = 0; bb < w.nb; ++bb) {
               const int vs = vc % L::VST;
               mbar_wait(v_full + vs, (vc / L::VST) & 1, wc, kSiteMmaV);
@@ -554,8 +560,8 @@ __global__ void __launch_bounds__(384, 1)
             }
             // every use of a TMEM buffer completes one phase of both of its
             // barriers, so that the compute warps can count uses uniformly
-            mma_commit(s_full + (u & 1));
-            mma_commit(s_empty + (u & 1));
+            mma_commit(s_full + (u % NB));
+            mma_commit(s_empty + (u % NB));
           }
           sc = sc0 + w.nsteps;
           mma_commit(o_full);
@@ -579,9 +585,9 @@ __global__ void __launch_bounds__(384, 1)
         float m_run = -INFINITY, l_run = 0.f;
         for (int j = 0; j < w.nsteps; ++j) {
           const uint32_t u = sc0 + j;
-          const uint32_t sb = u & 1;
+          const uint32_t sb = u % NB;
           const uint32_t sbase = trow + kTmemS + sb * 128 + 64 * hf;
-          mbar_wait(s_full + sb, (u >> 1) & 1, wc, kSiteCmpS);
+          mbar_wait(s_full + sb, (u / NB) & 1, wc, kSiteCmpS);
           tc_fence_after();
           uint32_t sr[64];
           {
@@ -652,7 +658,7 @@ __global__ void __launch_bounds__(384, 1)
           // max: the previous tile's P V must have finished first.
           if (j > 0 && __any_sync(0xffffffffu, need)) {
             const uint32_t up = u - 1;
-            mbar_wait(s_empty + (up & 1), (up >> 1) & 1, wc, kSiteCmpPV);
+            mbar_wait(s_empty + (up % NB), (up / NB) & 1, wc, kSiteCmpPV);
             tc_fence_after();
 #pragma unroll
             for (int c0 = 0; c0 < DH; c0 += 16) {
@@ -707,9 +713,9 @@ __global__ void __launch_bounds__(384, 1)
           const float* colv = aux + 64 * hf;       // this half's 64 column values
           const float* win = aux + L::AUX_WIN / 4; // window, centre at 127
           // the TMEM buffer must be free: the MMAs of two steps back are done
-          mbar_wait(s_empty + (u & 1), ((u >> 1) & 1) ^ 1, wc, kSiteCmpP);
+          mbar_wait(s_empty + (u % NB), ((u / NB) & 1) ^ 1, wc, kSiteCmpP);
           tc_fence_after();
-          const uint32_t gdst = trow + kTmemS + (u & 1) * 128 + 64 * hf;
+          const uint32_t gdst = trow + kTmemS + (u % NB) * 128 + 64 * hf;
 #pragma unroll
           for (int q0 = 0; q0 < 32; q0 += 16) {
             uint32_t pk[16];
@@ -735,7 +741,7 @@ __global__ void __launch_bounds__(384, 1)
           ++kc;
           tmem_wait_st();
           tc_fence_before();
-          mbar_arrive(p_full + (u & 1));
+          mbar_arrive(p_full + (u % NB));
         }
         sc = sc0 + w.nsteps;
         mbar_wait(o_full, oc & 1, wc, kSiteCmpO);

@@ -30,6 +30,14 @@ struct FwdParams {
   int* status;                // device status word
 };
 
+// Sequences per static work item: the TMEM columns left for the O
+// accumulator (512 minus the S/P buffers) divided by d_h.
+inline int static_group(int d_h, int B) {
+  const int cols = d_h <= 64 ? 128 : 256;
+  const int g = cols / d_h;
+  return g < B ? g : B;
+}
+
 struct FwdLaunch {
   CUtensorMap tm_q, tm_k, tm_v;  // [B*H*T, d_h] bf16 views; tm_v = dO when transposed
   FwdParams p;
@@ -49,6 +57,7 @@ struct BwdPre {
   float* Dvec;        // [B, H, T]  -D
   float* lse2;        // [B, H, T]  -lse * log2(e)
   float* Dsum;        // [n_static, T] (nullable): sum over b of D
+  float* dq_acc;      // [B, H, T, d_h] fp32 zeroed here (nullable)
   int n_static;
   uint8_t static_heads[kMaxHeads];
 };
@@ -70,6 +79,7 @@ struct BwdParams {
 };
 struct BwdLaunch {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;
+  CUtensorMap tm_dq;             // fp32 [B*H*T, d_h] view of dq_acc (d_h <= 64)
   BwdParams p;
   int d_h;
   int num_sms;
