@@ -87,10 +87,20 @@ def load_peaks():
                 "source": "fallback"}
 
 
-def source_hash():
+# Source files that define each timed kernel: a recorded DRAM-traffic figure
+# counts only while these are unchanged.
+KERNEL_SOURCES = {
+    "hybrid_fwd": ("attn_fwd.cu", "attn_common.cuh", "ptx.cuh", "attn_kernels.h"),
+    "static_dv": ("attn_fwd.cu", "attn_common.cuh", "ptx.cuh", "attn_kernels.h"),
+    "bwd_dynamic": ("attn_bwd.cu", "attn_common.cuh", "ptx.cuh", "attn_kernels.h"),
+    "param_grad": ("attn_bwd.cu", "attn_common.cuh", "ptx.cuh", "attn_kernels.h"),
+}
+
+
+def source_hash(kernel):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dynamic_causal_attention_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in KERNEL_SOURCES.get(kernel, ()):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode())
             h.update(fh.read())
@@ -98,18 +108,20 @@ def source_hash():
 
 
 def ncu_traffic(kernel, workload):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources; else None."""
-    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    """DRAM bytes (read + write) per launch from the committed ncu record
+    (profiles/dram_traffic.txt: workload, kernel, bytes, source hash), if it
+    was taken on the kernel's current sources; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     try:
         with open(path) as f:
-            d = json.load(f)
-        e = d[workload][kernel]
-        if d.get("source_hash") != source_hash():
-            return None
-        return float(e["bytes_per_launch"])
-    except Exception:
-        return None
+            for line in f:
+                parts = line.split()
+                if len(parts) == 4 and not line.startswith("#") and parts[0] == workload \
+                        and parts[1] == kernel and parts[3] == source_hash(kernel):
+                    return float(parts[2])
+    except OSError:
+        pass
+    return None
 
 
 # ---------------------------------------------------------------- clocks

@@ -57,6 +57,7 @@ from .calibration import (
     num_select,
     select_heads,
     reconstruction_risk,
+    calib_kl_score,
 )
 
 __all__ = [
@@ -79,6 +80,7 @@ __all__ = [
     "num_select",
     "select_heads",
     "reconstruction_risk",
+    "calib_kl_score",
     "marginals",
     "fit_loss",
     "fit_gradient",

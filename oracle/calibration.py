@@ -22,6 +22,7 @@ __all__ = [
     "num_select",
     "select_heads",
     "reconstruction_risk",
+    "calib_kl_score",
 ]
 
 
@@ -75,3 +76,20 @@ def reconstruction_risk(P: np.ndarray, A: np.ndarray) -> float:
     N, T, _ = A.shape
     dev = A - np.asarray(P, dtype=np.float64)[None]
     return float((dev * dev).sum() / (N * T * T))
+
+
+def calib_kl_score(A: np.ndarray, A_hat: np.ndarray | None = None) -> float:
+    """Row-wise forward-KL score of one head: the mean over the N samples and
+    the T rows of KL(A_n(i, :) || A_hat(i, :)), in nats.  This is the
+    alternative selector the notes compare against s_var (§3.1 and App. B.2);
+    its formula is not printed there, and this mean over samples and rows is
+    the reading taken.  Terms with A_n(i, j) = 0 contribute nothing."""
+    A = np.asarray(A, dtype=np.float64)
+    N, T, _ = A.shape
+    if A_hat is None:
+        A_hat = calib_mean(A)
+    total = 0.0
+    for n in range(N):
+        m = A[n] > 0
+        total += float((A[n][m] * (np.log(A[n][m]) - np.log(A_hat[m]))).sum())
+    return total / (N * T)

@@ -90,3 +90,26 @@ def test_selection_matches_brute_force_with_index_tiebreak():
             want.append(best)
             left.remove(best)
         assert list(got) == want
+
+
+def test_kl_score_closed_forms():
+    # identical samples: every row KL is zero
+    A = np.repeat(_random_causal_rows(1, 10), 5, axis=0)
+    assert abs(oracle.calib_kl_score(A)) < 1e-14
+    # two samples whose rows are point masses at different keys: for the row
+    # i >= 1 with masses on j0 != j1, A_hat = (1/2, 1/2) there and each sample's
+    # KL is log 2; row 0 has a single key and contributes nothing
+    T = 6
+    A = np.zeros((2, T, T))
+    for i in range(T):
+        A[0, i, 0] = 1.0
+        A[1, i, i] = 1.0
+    want = (T - 1) * 2 * np.log(2.0) / (2 * T)
+    assert abs(oracle.calib_kl_score(A) - want) < 1e-14
+
+
+def test_kl_score_is_nonnegative_and_permutation_invariant():
+    A = _random_causal_rows(9, 12)
+    s = oracle.calib_kl_score(A)
+    assert s > 0
+    assert abs(oracle.calib_kl_score(A[RNG.permutation(9)]) - s) < 1e-14
