@@ -25,15 +25,19 @@ SAF_ERR_TIMEOUT = 5
 SAF_BF16 = 0
 SAF_F32 = 1
 
+SAF_CALIB_TRACK_KL = 1
+
 EXPORTED = (
     "saf_hybrid_attn_workspace_size",
     "saf_hybrid_attn_fwd",
     "saf_hybrid_attn_bwd",
     "saf_hybrid_attn_fwd_noalloc",
     "saf_calib_create",
+    "saf_calib_create_ex",
     "saf_calib_accumulate",
     "saf_calib_num_select",
     "saf_calib_finalize",
+    "saf_calib_finalize_kl",
     "saf_fit_compact",
     "saf_calib_reset",
     "saf_calib_destroy",
@@ -84,6 +88,10 @@ _lib.saf_hybrid_attn_fwd_noalloc.argtypes = [ctypes.POINTER(saf_attn_dims), _vp,
 _lib.saf_hybrid_attn_fwd_noalloc.restype = _i
 _lib.saf_calib_create.argtypes = [ctypes.POINTER(_vp), _i, _i]
 _lib.saf_calib_create.restype = _i
+_lib.saf_calib_create_ex.argtypes = [ctypes.POINTER(_vp), _i, _i, ctypes.c_uint]
+_lib.saf_calib_create_ex.restype = _i
+_lib.saf_calib_finalize_kl.argtypes = [_vp, _i, _vp, _vp, _vp]
+_lib.saf_calib_finalize_kl.restype = _i
 _lib.saf_calib_accumulate.argtypes = [_vp, _vp, _i, _i, _i, _vp]
 _lib.saf_calib_accumulate.restype = _i
 _lib.saf_calib_num_select.argtypes = [ctypes.c_double, _i]
@@ -170,6 +178,16 @@ def saf_calib_create(num_heads: int, T: int):
     h = _vp()
     st = _lib.saf_calib_create(ctypes.byref(h), int(num_heads), int(T))
     return st, h.value
+
+
+def saf_calib_create_ex(num_heads: int, T: int, flags: int):
+    h = _vp()
+    st = _lib.saf_calib_create_ex(ctypes.byref(h), int(num_heads), int(T), int(flags))
+    return st, h.value
+
+
+def saf_calib_finalize_kl(handle, k, s_kl, selected, stream) -> int:
+    return _lib.saf_calib_finalize_kl(handle, int(k), s_kl, selected, stream)
 
 
 def saf_calib_accumulate(handle, A, n, head_begin, head_count, stream) -> int:

@@ -90,11 +90,12 @@ class HybridAttention:
 class Calibration:
     """Streaming calibration state for ``num_heads`` heads of length T."""
 
-    def __init__(self, num_heads: int, T: int, device="cuda"):
+    def __init__(self, num_heads: int, T: int, device="cuda", track_kl=False):
         self.device = torch.device(device)
         with torch.cuda.device(self.device):
-            st, self.handle = B.saf_calib_create(num_heads, T)
-        _check(st, "saf_calib_create")
+            st, self.handle = B.saf_calib_create_ex(
+                num_heads, T, B.SAF_CALIB_TRACK_KL if track_kl else 0)
+        _check(st, "saf_calib_create_ex")
         self.num_heads, self.T = num_heads, T
 
     def accumulate(self, A, head_begin=0):
@@ -113,6 +114,14 @@ class Calibration:
                                   _stream(self.device))
         _check(st, "saf_calib_finalize")
         return A_hat, s_var, sel[:k]
+
+    def finalize_kl(self, k):
+        """Forward-KL selector: (s_kl [num_heads], the k lowest-scoring heads)."""
+        s_kl = torch.empty(self.num_heads, dtype=torch.float32, device=self.device)
+        sel = torch.empty(max(k, 1), dtype=torch.int32, device=self.device)
+        st = B.saf_calib_finalize_kl(self.handle, k, _ptr(s_kl), _ptr(sel), _stream(self.device))
+        _check(st, "saf_calib_finalize_kl")
+        return s_kl, sel[:k]
 
     def reset(self):
         _check(B.saf_calib_reset(self.handle), "saf_calib_reset")

@@ -507,28 +507,33 @@ struct CalibHandle {
   int num_heads = 0, T = 0;
   float* mean = nullptr;
   float* m2 = nullptr;
+  float* ent = nullptr;  // sum_n x log x (only with SAF_CALIB_TRACK_KL)
   double* partials = nullptr;
   int* status = nullptr;
   std::vector<int> counts;
 };
 }  // namespace
 
-saf_status saf_calib_create(void** handle, int num_heads, int T) {
+saf_status saf_calib_create_ex(void** handle, int num_heads, int T, unsigned flags) {
   g_launches = 0;
   if (!handle) return SAF_ERR_INVALID_ARG;
   *handle = nullptr;
   if (num_heads < 1 || T < 4 || T % 4 != 0) return SAF_ERR_INVALID_ARG;
+  if ((flags & ~(unsigned)SAF_CALIB_TRACK_KL) != 0) return SAF_ERR_INVALID_ARG;
   if (T > kMaxT || num_heads > 8192) return SAF_ERR_UNSUPPORTED;
   CalibHandle* h = new CalibHandle();
   h->num_heads = num_heads;
   h->T = T;
   h->counts.assign(num_heads, 0);
   const size_t n = (size_t)num_heads * T * T;
+  const bool kl = (flags & SAF_CALIB_TRACK_KL) != 0;
   if (cudaMalloc(&h->mean, n * 4) != cudaSuccess || cudaMalloc(&h->m2, n * 4) != cudaSuccess ||
+      (kl && cudaMalloc(&h->ent, n * 4) != cudaSuccess) ||
       cudaMalloc(&h->partials, (size_t)num_heads * T * 8) != cudaSuccess ||
       cudaMalloc(&h->status, 256) != cudaSuccess || cudaMemset(h->status, 0, 256) != cudaSuccess) {
     cudaFree(h->mean);
     cudaFree(h->m2);
+    cudaFree(h->ent);
     cudaFree(h->partials);
     cudaFree(h->status);
     delete h;
@@ -536,6 +541,10 @@ saf_status saf_calib_create(void** handle, int num_heads, int T) {
   }
   *handle = h;
   return SAF_OK;
+}
+
+saf_status saf_calib_create(void** handle, int num_heads, int T) {
+  return saf_calib_create_ex(handle, num_heads, T, 0u);
 }
 
 saf_status saf_calib_accumulate(void* handle, const float* A, int n, int head_begin,
@@ -557,6 +566,7 @@ saf_status saf_calib_accumulate(void* handle, const float* A, int n, int head_be
   p.count0 = c0;
   p.mean = h->mean;
   p.m2 = h->m2;
+  p.ent = h->ent;
   const cudaError_t e = launch_calib_accumulate(p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return SAF_ERR_CUDA;
   for (int i = head_begin; i < head_begin + head_count; ++i) h->counts[i] += n;
@@ -589,7 +599,34 @@ saf_status saf_calib_finalize(void* handle, int k, float* A_hat, float* s_var, i
   p.A_hat = A_hat;
   p.s_var = s_var;
   p.selected = selected;
+  p.ent = nullptr;
   return cuda_status(launch_calib_finalize(p, static_cast<cudaStream_t>(stream)));
+}
+
+saf_status saf_calib_finalize_kl(void* handle, int k, float* s_kl, int32_t* selected,
+                                 void* stream) {
+  g_launches = 0;
+  CalibHandle* h = static_cast<CalibHandle*>(handle);
+  if (!h || !s_kl || !aligned16(s_kl)) return SAF_ERR_INVALID_ARG;
+  if (k < 0 || k > h->num_heads || (k > 0 && !selected)) return SAF_ERR_INVALID_ARG;
+  if (!h->ent) return SAF_ERR_STATE;
+  const int N = h->counts[0];
+  for (int c : h->counts)
+    if (c != N) return SAF_ERR_STATE;
+  if (N < 1) return SAF_ERR_STATE;
+  CalibFinalize p;
+  p.num_heads = h->num_heads;
+  p.T = h->T;
+  p.N = N;
+  p.k = k;
+  p.mean = h->mean;
+  p.m2 = h->m2;
+  p.row_partials = h->partials;
+  p.A_hat = nullptr;
+  p.s_var = s_kl;
+  p.selected = selected;
+  p.ent = h->ent;
+  return cuda_status(launch_calib_finalize_kl(p, static_cast<cudaStream_t>(stream)));
 }
 
 saf_status saf_fit_compact(const float* A_hat, int num_heads, int T, const int32_t* candidates,
@@ -637,6 +674,7 @@ saf_status saf_calib_destroy(void* handle) {
   cudaDeviceSynchronize();
   cudaFree(h->mean);
   cudaFree(h->m2);
+  cudaFree(h->ent);
   cudaFree(h->partials);
   cudaFree(h->status);
   delete h;

@@ -25,12 +25,15 @@
 // columns, for d_h = 128 with vector atomics.  A post-pass scales it by
 // 1/sqrt(d) and converts it.
 //
-// param_grad_kernel (K5): items (h_static, J).  For I = J..nI-1 the batch-
-// summed dP^T(j, i) = sum_b V_b(j) . dO_b(i) is one MMA chain with K = B*d;
-// the compute warps form dl = P(i,j) (dP - sum_b D_b(i)) with P(i,j) rebuilt
-// from the static tables, keep the column sums (alpha) per thread, and
-// accumulate the diagonal sums (rho) in shared memory, flushed to global with
-// atomics once per tile.
+// param_grad_kernel (K5): items (h_static, J), handed out in snake order.
+// For I = J..nI-1 the batch-summed dP^T(j, i) = sum_b V_b(j) . dO_b(i) is one
+// MMA chain with K = B*d; eight compute warps (a 32-row group x a 64-column
+// half each) form dl = P(i,j) (dP - sum_b D_b(i)) with P(i,j) rebuilt from the
+// static tables and keep the row sums (alpha) in registers.  For the diagonal
+// sums (rho) each warp writes its 32 x 32 block of dl to shared memory by
+// diagonal, so that lane q adds up diagonals q and q + 32 with vector loads;
+// the per-warp sums of a tile are combined in a fixed order and added to
+// global with one atomic per distance.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -474,13 +477,19 @@ __global__ void __launch_bounds__(512, 1)
 template <int D>
 struct PgSmem {
   using G = TileGeom<D>;
-  static constexpr int ST = (D == 128) ? 3 : 4;        // (V_b[J], dO_b[I]) pairs
+  static constexpr int ST = (D == 128) ? 2 : (D == 64 ? 3 : 4);  // (V_b[J], dO_b[I]) pairs
   static constexpr int STAGE = 2 * G::TILE_BYTES;
-  static constexpr int AUX = 2048;                     // col values, D sums, window
+  static constexpr int AUX = 2048;                     // col values, D sums, r window
+  // Per compute warp, its 32 x 32 block of dl laid out by diagonal: row
+  // e = k - rr + 32 (k column, rr row of the block), 36 floats a row.
+  static constexpr int SKW_ROW = 36;
+  static constexpr int SKW = 64 * SKW_ROW * 4;
+  static constexpr int CW = 8 * 96 * 4;                // per-warp diagonal sums, x2
   static constexpr int OFF_ST = 0;
   static constexpr int OFF_AUX = OFF_ST + ST * STAGE;
-  static constexpr int OFF_WIN = OFF_AUX + 2 * AUX;    // 256 floats of diagonal sums
-  static constexpr int OFF_BAR = OFF_WIN + 1024;
+  static constexpr int OFF_SKW = OFF_AUX + 2 * AUX;
+  static constexpr int OFF_CW = OFF_SKW + 8 * SKW;
+  static constexpr int OFF_BAR = OFF_CW + 2 * CW;
   static constexpr int NBAR = 2 * ST + 4 + 4;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int ALLOC = OFF_MISC + 16 + 1024;
@@ -489,8 +498,15 @@ struct PgSmem {
 
 enum : int { kSitePgProd = 201, kSitePgProdAux, kSitePgMma, kSitePgMmaAcc, kSitePgAux, kSitePgAcc };
 
+// Item of round k for this CTA: even rounds run forwards, odd rounds
+// backwards, so the CTA that drew one of the longest items (small J) in one
+// round draws one of the shortest in the next.
+__device__ __forceinline__ int snake_item(int k, int cta, int grid) {
+  return (k & 1) ? (k + 1) * grid - 1 - cta : k * grid + cta;
+}
+
 template <int D>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     param_grad_kernel(const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_do, const ParamGradParams p) {
   using G = TileGeom<D>;
@@ -508,7 +524,6 @@ __global__ void __launch_bounds__(256, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
   const WaitCtl wc{abort_flag, p.status};
-  float* win = reinterpret_cast<float*>(smem + L::OFF_WIN);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -517,7 +532,7 @@ __global__ void __launch_bounds__(256, 1)
       mbar_init(aux_full + s, 1);
       mbar_init(aux_empty + s, 1);
       mbar_init(acc_full + s, 1);
-      mbar_init(acc_empty + s, 128);
+      mbar_init(acc_empty + s, 256);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -525,6 +540,13 @@ __global__ void __launch_bounds__(256, 1)
   if (warp == 2) {
     tmem_alloc(tmem_slot, 256);
     tmem_relinquish();
+  }
+  // Cells of the diagonal blocks that no (row, column) pair maps to are read
+  // as zeros, and nothing ever writes them.
+  {
+    float4* z = reinterpret_cast<float4*>(smem + L::OFF_SKW);
+    for (int t = threadIdx.x; t < 8 * L::SKW / 16; t += blockDim.x)
+      z[t] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   tc_fence_before();
   __syncthreads();
@@ -535,7 +557,9 @@ __global__ void __launch_bounds__(256, 1)
   if (warp == 0) {
     if (lane == 0) {
       uint32_t sc = 0, ac = 0;
-      for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+      for (int k = 0;; ++k) {
+        const int it = snake_item(k, blockIdx.x, gridDim.x);
+        if (it >= p.n_items) break;
         const int J = it / p.n_static, hs = it - J * p.n_static, h = p.static_heads[hs];
         for (int I = J; I < p.nI; ++I) {
           const int as = ac & 1;
@@ -572,7 +596,9 @@ __global__ void __launch_bounds__(256, 1)
     if (lane == 0) {
       constexpr uint32_t id = idesc_bf16(128, 128, false, false);
       uint32_t sc = 0, cc = 0;
-      for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+      for (int k = 0;; ++k) {
+        const int it = snake_item(k, blockIdx.x, gridDim.x);
+        if (it >= p.n_items) break;
         const int J = it / p.n_static;
         for (int I = J; I < p.nI; ++I) {
           const int ab = cc & 1;
@@ -596,57 +622,119 @@ __global__ void __launch_bounds__(256, 1)
       }
     }
   } else if (warp >= 4) {
-    const int r = threadIdx.x - 128;  // key row j within tile J
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    // Warp (rg, hf): key rows r = 32 rg + lane of tile J, query columns
+    // 64 hf .. 64 hf + 63 of tile I.
+    const int rg = warp & 3, hf = (warp - 4) >> 2, w8 = warp - 4;
+    const int r = rg * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(rg * 32) << 16;
+    float* skw = reinterpret_cast<float*>(smem + L::OFF_SKW + w8 * L::SKW);
+    // row lane writes block column k to skw[(k - lane + 32) * 36 + lane]
+    float* skw_w = skw + (32 - lane) * L::SKW_ROW + lane;
+    // lane q sums the block diagonals e = q and e = q + 32
+    const float4* skw_lo = reinterpret_cast<const float4*>(skw + lane * L::SKW_ROW);
+    const float4* skw_hi = reinterpret_cast<const float4*>(skw + (lane + 32) * L::SKW_ROW);
+    const uint64_t m1 = f2_pack(-1.f, -1.f);
     uint32_t ac = 0, cc = 0;
-    for (int t = r; t < 256; t += 128) win[t] = 0.f;
-    named_bar_sync(1, 128);
-    for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+    for (int k = 0;; ++k) {
+      const int it = snake_item(k, blockIdx.x, gridDim.x);
+      if (it >= p.n_items) break;
       const int J = it / p.n_static, hs = it - J * p.n_static, h = p.static_heads[hs];
       const bool exact = p.mode[hs] != 0;
       const float rowv = p.a_tab[(size_t)hs * T + J * 128 + r];
-      float dalpha = 0.f;
+      const uint64_t row2 = f2_pack(rowv, rowv);
+      uint64_t dal2 = 0;
       for (int I = J; I < p.nI; ++I) {
         const int as = ac & 1;
         mbar_wait(aux_full + as, (ac >> 1) & 1, wc, kSitePgAux);
         const float* aux = reinterpret_cast<const float*>(smem + L::OFF_AUX + as * L::AUX);
-        const float* colv = aux;          // 1/Z'(i) or -log2 Z(i)
-        const float* dsum = aux + 128;    // sum_b D_b(i)
-        const float* rwin = aux + 256;    // r(i - j), centre 127
+        const float* colv = aux + 64 * hf;        // 1/Z'(i) or -log2 Z(i)
+        const float* dsum = aux + 128 + 64 * hf;  // sum_b D_b(i)
+        const float* rwin = aux + 256 + 127 + 64 * hf - r;  // r(i - j), i - j = c - r
         const int ab = cc & 1;
         mbar_wait(acc_full + ab, (cc >> 1) & 1, wc, kSitePgAcc);
         tc_fence_after();
+        // diagonal sums of this warp: d = 127 + 64 hf - 32 rg - 32 + 32 m + lane
+        float dg0 = 0.f, dg1 = 0.f, dg2 = 0.f;
 #pragma unroll 1
-        for (int c0 = 0; c0 < 128; c0 += 32) {
+        for (int ch = 0; ch < 2; ++ch) {
           uint32_t v[32];
-          tmem_ld_x32(tmem + lane_base + ab * 128 + c0, v);
+          tmem_ld_x32(tmem + lane_base + ab * 128 + 64 * hf + 32 * ch, v);
           tmem_wait_ld(v);
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const int c = c0 + k;
-            const float wv = rwin[127 + c - r];
-            const float pij = exact ? fast_exp2(rowv + wv + colv[c]) : rowv * wv * colv[c];
-            const float dl = pij * (__uint_as_float(v[k]) - dsum[c]);
-            dalpha += dl;
-            atomicAdd(&win[127 + c - r], dl);
+          for (int k4 = 0; k4 < 32; k4 += 4) {
+            const int c = 32 * ch + k4;
+            const float4 cv = *reinterpret_cast<const float4*>(colv + c);
+            const float4 ds = *reinterpret_cast<const float4*>(dsum + c);
+#pragma unroll
+            for (int e = 0; e < 4; e += 2) {
+              const float w0 = rwin[c + e], w1 = rwin[c + e + 1];
+              const uint64_t cv2 = e ? f2_pack(cv.z, cv.w) : f2_pack(cv.x, cv.y);
+              const uint64_t ds2 = e ? f2_pack(ds.z, ds.w) : f2_pack(ds.x, ds.y);
+              uint64_t p2;
+              if (exact) {
+                float a0, a1;
+                f2_unpack(f2_add(f2_add(f2_pack(w0, w1), cv2), row2), a0, a1);
+                p2 = f2_pack(fast_exp2(a0), fast_exp2(a1));
+              } else {
+                p2 = f2_mul(f2_mul(f2_pack(w0, w1), cv2), row2);
+              }
+              const uint64_t x2 = f2_fma(ds2, m1, f2_pack(__uint_as_float(v[k4 + e]),
+                                                          __uint_as_float(v[k4 + e + 1])));
+              const uint64_t dl2 = f2_mul(p2, x2);
+              dal2 = f2_add(dal2, dl2);
+              float d0, d1;
+              f2_unpack(dl2, d0, d1);
+              skw_w[(k4 + e) * L::SKW_ROW] = d0;
+              skw_w[(k4 + e + 1) * L::SKW_ROW] = d1;
+            }
           }
+          __syncwarp();
+          uint64_t lo_a = 0, lo_b = 0, hi_a = 0, hi_b = 0;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float4 x = skw_lo[j];
+            const float4 y = skw_hi[j];
+            lo_a = f2_add(lo_a, f2_pack(x.x, x.y));
+            lo_b = f2_add(lo_b, f2_pack(x.z, x.w));
+            hi_a = f2_add(hi_a, f2_pack(y.x, y.y));
+            hi_b = f2_add(hi_b, f2_pack(y.z, y.w));
+          }
+          __syncwarp();
+          float t0, t1, t2, t3;
+          f2_unpack(f2_add(lo_a, lo_b), t0, t1);
+          f2_unpack(f2_add(hi_a, hi_b), t2, t3);
+          const float elo = t0 + t1, ehi = t2 + t3;  // block diagonals lane, lane + 32
+          if (ch == 0) { dg0 += elo; dg1 += ehi; } else { dg1 += elo; dg2 += ehi; }
         }
         tc_fence_before();
         mbar_arrive(acc_empty + ab);
         ++cc;
-        named_bar_sync(1, 128);
-        if (r == 0) mbar_arrive(aux_empty + as);
+        float* cw = reinterpret_cast<float*>(smem + L::OFF_CW + (ac & 1) * L::CW);
+        cw[w8 * 96 + lane] = dg0;
+        cw[w8 * 96 + 32 + lane] = dg1;
+        cw[w8 * 96 + 64 + lane] = dg2;
+        named_bar_sync(1, 256);
+        if (threadIdx.x == 128) mbar_arrive(aux_empty + as);
         ++ac;
-        // flush the diagonal sums of this tile: distance (I-J)*128 - 127 + t
-        for (int t = r; t < 256; t += 128) {
+        // tile diagonal t = c - r + 127, global distance (I - J) * 128 - 127 + t;
+        // the per-warp sums are added in a fixed order
+        const int t = threadIdx.x - 128;
+        if (t < 255) {
+          float vs = 0.f;
+#pragma unroll
+          for (int w = 0; w < 8; ++w) {
+            const int o = t - (95 + 64 * (w >> 2) - 32 * (w & 3));
+            if (o >= 0 && o < 96) vs += cw[w * 96 + o];
+          }
           const int delta = (I - J) * 128 - 127 + t;
-          const float vsum = win[t];
-          win[t] = 0.f;
-          if (delta >= 0 && delta < T && vsum != 0.f) atomicAdd(&p.drho[(size_t)h * T + delta], vsum);
+          if (delta >= 0 && delta < T && vs != 0.f) atomicAdd(&p.drho[(size_t)h * T + delta], vs);
         }
-        named_bar_sync(1, 128);
       }
-      p.dalpha[(size_t)h * T + J * 128 + r] = dalpha;
+      float da0, da1;
+      f2_unpack(dal2, da0, da1);
+      // the two column halves of row r add into a zeroed entry: 0 + a + b is
+      // the same in either order
+      atomicAdd(&p.dalpha[(size_t)h * T + J * 128 + r], da0 + da1);
     }
   }
 
@@ -688,7 +776,7 @@ cudaError_t launch_pg(const ParamGradLaunch& L, cudaStream_t s) {
   if (L.p.n_items == 0) return cudaSuccess;
   const int grid = L.p.n_items < L.num_sms ? L.p.n_items : L.num_sms;
   trace_begin(s);
-  param_grad_kernel<D><<<grid, 256, PgSmem<D>::ALLOC, s>>>(L.tm_v, L.tm_do, L.p);
+  param_grad_kernel<D><<<grid, 384, PgSmem<D>::ALLOC, s>>>(L.tm_v, L.tm_do, L.p);
   trace_end(s, "param_grad");
   return cudaGetLastError();
 }

@@ -16,6 +16,10 @@
 //          M2   = M2_a + M2_b + delta^2 * na * nb / n.
 // s_var sums M2 over the triangle in fp64 with a fixed reduction order, so
 // results are deterministic run to run.
+//
+// Optionally the state also keeps sum_n x log x per element, from which the
+// row-wise forward-KL selector (the alternative to s_var that the notes
+// compare, App. B.2) follows without a second pass over A.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -46,6 +50,10 @@ __device__ __forceinline__ float4 masked(float4 v, int row, int col0) {
   return v;
 }
 
+// x log x with the limit 0 at x = 0.
+__device__ __forceinline__ float xlogx(float x) { return x > 0.f ? x * __logf(x) : 0.f; }
+
+template <bool KL>
 __global__ void __launch_bounds__(256) calib_accumulate_kernel(CalibLaunch p) {
   const int T = p.T;
   const uint32_t units_per_head = 2u * (uint32_t)(T / 4) * (uint32_t)(T / 4 + 1);
@@ -60,10 +68,11 @@ __global__ void __launch_bounds__(256) calib_accumulate_kernel(CalibLaunch p) {
     const size_t in_off = ((size_t)hl * T + row) * (size_t)T + col0;
     const size_t st_off = ((size_t)(p.head_begin + hl) * T + row) * (size_t)T + col0;
 
-    float4 mean = make_float4(0.f, 0.f, 0.f, 0.f), m2 = mean;
+    float4 mean = make_float4(0.f, 0.f, 0.f, 0.f), m2 = mean, ent = mean;
     if (p.count0 > 0) {
       mean = *reinterpret_cast<const float4*>(p.mean + st_off);
       m2 = *reinterpret_cast<const float4*>(p.m2 + st_off);
+      if (KL) ent = *reinterpret_cast<const float4*>(p.ent + st_off);
     }
     int cnt = p.count0;
     const float* src = p.A + in_off;
@@ -80,6 +89,10 @@ __global__ void __launch_bounds__(256) calib_accumulate_kernel(CalibLaunch p) {
         if (k < m) {
           x[k] = masked(x[k], row, col0);
           mb.x += x[k].x; mb.y += x[k].y; mb.z += x[k].z; mb.w += x[k].w;
+          if (KL) {
+            ent.x += xlogx(x[k].x); ent.y += xlogx(x[k].y);
+            ent.z += xlogx(x[k].z); ent.w += xlogx(x[k].w);
+          }
         }
       mb.x *= inv_m; mb.y *= inv_m; mb.z *= inv_m; mb.w *= inv_m;
       float4 qb = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -106,7 +119,33 @@ __global__ void __launch_bounds__(256) calib_accumulate_kernel(CalibLaunch p) {
     }
     *reinterpret_cast<float4*>(p.mean + st_off) = mean;
     *reinterpret_cast<float4*>(p.m2 + st_off) = m2;
+    if (KL) *reinterpret_cast<float4*>(p.ent + st_off) = ent;
   }
+}
+
+// KL score rows: sum_j (sum_n x log x - N A_hat log A_hat) over the lower
+// part of one row, in fp64 (sum_n KL(A_n,i || A_hat_i) = that difference,
+// because sum_n A_n = N A_hat).
+__global__ void __launch_bounds__(128) calib_kl_rows_kernel(CalibFinalize p) {
+  const int row = blockIdx.x, h = blockIdx.y, T = p.T;
+  const size_t base = ((size_t)h * T + row) * (size_t)T;
+  const float N = (float)p.N;
+  double acc = 0.0;
+  for (int c4 = threadIdx.x; c4 * 4 <= row; c4 += blockDim.x) {
+    const int col0 = c4 * 4;
+    const float4 mu = masked(*reinterpret_cast<const float4*>(p.mean + base + col0), row, col0);
+    const float4 e = masked(*reinterpret_cast<const float4*>(p.ent + base + col0), row, col0);
+    acc += (double)(e.x - N * xlogx(mu.x)) + (double)(e.y - N * xlogx(mu.y)) +
+           (double)(e.z - N * xlogx(mu.z)) + (double)(e.w - N * xlogx(mu.w));
+  }
+  __shared__ double red[128];
+  red[threadIdx.x] = acc;
+  __syncthreads();
+  for (int s = 64; s > 0; s >>= 1) {
+    if (threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) p.row_partials[(size_t)h * T + row] = red[0];
 }
 
 // One block per (row, head): writes the full row of A_hat (zeros above the
@@ -140,10 +179,9 @@ __global__ void __launch_bounds__(128) calib_rows_kernel(CalibFinalize p) {
 // exact top-k by rank over the unique 64-bit keys (bits(s_var) << 32 | index).
 constexpr int kMaxCalibHeads = 8192;
 
-__global__ void __launch_bounds__(1024) calib_select_kernel(CalibFinalize p) {
+__global__ void __launch_bounds__(1024) calib_select_kernel(CalibFinalize p, double denom) {
   __shared__ float sv[kMaxCalibHeads];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-  const double denom = (double)(p.N - 1) * (double)p.T * (double)p.T;
   for (int h = warp; h < p.num_heads; h += nwarps) {
     double acc = 0.0;
     for (int r = lane; r < p.T; r += 32) acc += p.row_partials[(size_t)h * p.T + r];
@@ -174,7 +212,10 @@ cudaError_t launch_calib_accumulate(const CalibLaunch& p, cudaStream_t s) {
   const uint64_t want = (units + 255) / 256;
   const int blocks = (int)(want < (1u << 30) ? want : (1u << 30));
   trace_begin(s);
-  calib_accumulate_kernel<<<blocks, 256, 0, s>>>(p);
+  if (p.ent)
+    calib_accumulate_kernel<true><<<blocks, 256, 0, s>>>(p);
+  else
+    calib_accumulate_kernel<false><<<blocks, 256, 0, s>>>(p);
   trace_end(s, "calib_accumulate");
   return cudaGetLastError();
 }
@@ -187,7 +228,20 @@ cudaError_t launch_calib_finalize(const CalibFinalize& p, cudaStream_t s) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   trace_begin(s);
-  calib_select_kernel<<<1, 1024, 0, s>>>(p);
+  calib_select_kernel<<<1, 1024, 0, s>>>(p, (double)(p.N - 1) * (double)p.T * (double)p.T);
+  trace_end(s, "calib_select");
+  return cudaGetLastError();
+}
+
+cudaError_t launch_calib_finalize_kl(const CalibFinalize& p, cudaStream_t s) {
+  if (p.num_heads > kMaxCalibHeads || p.ent == nullptr) return cudaErrorInvalidValue;
+  trace_begin(s);
+  calib_kl_rows_kernel<<<dim3(p.T, p.num_heads), 128, 0, s>>>(p);
+  trace_end(s, "calib_kl_rows");
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  trace_begin(s);
+  calib_select_kernel<<<1, 1024, 0, s>>>(p, (double)p.N * (double)p.T);
   trace_end(s, "calib_select");
   return cudaGetLastError();
 }

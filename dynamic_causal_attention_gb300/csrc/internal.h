@@ -27,6 +27,7 @@ struct CalibLaunch {
   int count0;         // samples already merged into these heads
   float* mean;        // [num_heads, T, T]
   float* m2;          // [num_heads, T, T]
+  float* ent;         // [num_heads, T, T] sum_n x log x, or null (not tracked)
 };
 cudaError_t launch_calib_accumulate(const CalibLaunch& p, cudaStream_t s);
 
@@ -41,8 +42,11 @@ struct CalibFinalize {
   float* A_hat;          // nullable
   float* s_var;
   int32_t* selected;     // nullable when k == 0
+  const float* ent;      // KL score only: sum_n x log x state
 };
 cudaError_t launch_calib_finalize(const CalibFinalize& p, cudaStream_t s);
+// Forward-KL score per head (into p.s_var) and its exact top-k.
+cudaError_t launch_calib_finalize_kl(const CalibFinalize& p, cudaStream_t s);
 
 // ------------------------------------------------------------ compact fit
 struct FitParams {

@@ -171,6 +171,12 @@ SAF_API saf_status saf_hybrid_attn_fwd_noalloc(const saf_attn_dims* dims,
  * on the current device.  *handle receives an opaque pointer. */
 SAF_API saf_status saf_calib_create(void** handle, int num_heads, int T);
 
+/* saf_calib_create with options.  flags = SAF_CALIB_TRACK_KL also keeps, per
+ * element, the sum over samples of x log x (one more num_heads * T * T fp32
+ * array), which saf_calib_finalize_kl needs; flags = 0 is saf_calib_create. */
+#define SAF_CALIB_TRACK_KL 1u
+SAF_API saf_status saf_calib_create_ex(void** handle, int num_heads, int T, unsigned flags);
+
 /* Streams n more calibration samples into the state (§3.1).
  *   A  device fp32 [n, head_count, T, T]: the causal attention probabilities of
  *      heads head_begin .. head_begin+head_count-1 for n sequences.  Only the
@@ -197,6 +203,18 @@ SAF_API int saf_calib_num_select(double r, int num_heads);
  *             to s_var. */
 SAF_API saf_status saf_calib_finalize(void* handle, int k, float* A_hat, float* s_var,
                               int32_t* selected, void* stream);
+
+/* The row-wise forward-KL selector that the notes compare with s_var (§3.1,
+ * App. B.2; its formula is not printed, the reading here is the mean over
+ * samples and rows):  s_kl = (1/(N T)) sum_n sum_i KL(A_n(i,:) || A_hat(i,:)),
+ * computed from the tracked state as sum_n x log x - N A_hat log A_hat, summed
+ * in fp64.  Needs a handle made with SAF_CALIB_TRACK_KL (SAF_ERR_STATE
+ * otherwise) and the same N >= 1 samples for every head.
+ *   s_kl      device fp32 [num_heads].
+ *   selected  device int32 [k]: the k heads with the smallest s_kl in
+ *             ascending (s_kl, index) order (NULL when k == 0). */
+SAF_API saf_status saf_calib_finalize_kl(void* handle, int k, float* s_kl, int32_t* selected,
+                                 void* stream);
 
 /* Compact pattern fit ("When Can Attention Heads Be Statically Defined?",
  * §3 Eq. (3)/(4) and App. A.2).  For each candidate head, alpha and rho are

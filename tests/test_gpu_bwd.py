@@ -143,3 +143,17 @@ def test_full_size_one_head_of_each_class(api, name):
     if grads:
         assert_close(da[hs], ra, f"{name} dalpha")
         assert_close(dr[hs], rr, f"{name} drho")
+
+
+def test_param_grads_several_rounds_both_generator_modes(api):
+    # More (head, key tile) items than SMs, so each CTA takes items from
+    # several rounds of the snake order; heads 0 and 5 have a parameter range
+    # above 80 and use the exact exponential, the others the factored form.
+    B, H, T, d = 1, 8, 2560, 32
+    cfg = AttnConfig("rounds", B=B, H=H, T=T, d_h=d, dtype="bf16",
+                     static_heads=tuple(range(H)))
+    inp = attn_inputs(cfg, seed=57)
+    for h in (0, 5):
+        inp["alpha"][h] += np.linspace(-45.0, 45.0, T)
+    got = gpu_fwd_bwd(api, inp, cfg.head_is_static, True)
+    compare(got, oracle_bwd(inp, cfg.head_is_static, True), cfg.head_is_static, "rounds", True)

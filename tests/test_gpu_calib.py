@@ -152,3 +152,29 @@ def test_full_size_calibration(api):
             assert np.abs(got - ref_hat).max() <= 1e-5 * np.abs(ref_hat).max()
     check_stats(None, s_var, sel, None, ref_s, k, "full")
     cal.close()
+
+
+def test_forward_kl_selector_matches_oracle(api):
+    N, nh, T, k = 10, 6, 64, 2
+    A = calib_probabilities(N, nh, T, d_h=16, seed=21)
+    ref = np.array([oracle.calib_kl_score(A[:, h].double().numpy()) for h in range(nh)])
+    cal = api.Calibration(nh, T, track_kl=True)
+    cal.accumulate(A[:4].cuda())
+    cal.accumulate(A[4:].cuda())          # chunked like a stream of batches
+    s_kl, sel = cal.finalize_kl(k)
+    _, s_var, sel_var = cal.finalize(k)   # the variance path is unaffected
+    torch.cuda.synchronize()
+    s_kl = s_kl.cpu().numpy()
+    np.testing.assert_allclose(s_kl, ref, rtol=1e-4, atol=1e-7)
+    np.testing.assert_array_equal(sel.cpu().numpy(), host_topk(s_kl, k))
+    ref_s = oracle.calib_mean_svar(A.numpy())[1]
+    np.testing.assert_allclose(s_var.cpu().numpy(), ref_s, rtol=1e-5)
+    cal.close()
+    # without tracking the KL score is refused
+    from dynamic_causal_attention_gb300 import _binding as B
+    cal = api.Calibration(nh, T)
+    cal.accumulate(A.cuda())
+    with pytest.raises(B.SafError) as e:
+        cal.finalize_kl(k)
+    assert e.value.status == B.SAF_ERR_STATE
+    cal.close()
