@@ -51,6 +51,14 @@ constexpr uint32_t kTmemCols = 512;
 template <int D>
 struct BwdSmem {
   using G = TileGeom<D>;
+  // d_h = 128 leaves no free TMEM columns: dQ reuses the S^T/P^T columns once
+  // the dV MMAs that read P^T have completed.
+  static constexpr bool DQ_ALIAS = (256 + 3 * D > 512);
+  // d_h <= 64: P^T and dS^T go to shared memory (SS MMAs for dV, dK), so the
+  // S^T/dP^T columns are free as soon as the compute warps have loaded them
+  // and the next step's scores overlap this step's softmax.  d_h = 128 keeps
+  // P^T and dS^T in TMEM (TS MMAs): shared memory has no room for the tile.
+  static constexpr bool PS = !DQ_ALIAS;
   // Q_I, dO_I stages; d_h = 128 keeps two stages by dropping the alignment
   // slack (the dynamic shared base is checked at run time instead).
   static constexpr int QST = (D == 128) ? 2 : 3;
@@ -59,13 +67,15 @@ struct BwdSmem {
   static constexpr int OFF_V = OFF_K + G::TILE_BYTES;
   static constexpr int OFF_Q = OFF_V + G::TILE_BYTES;
   static constexpr int OFF_DST = OFF_Q + QST * STAGE;
-  // dQ staging for the tensor reduce-add (d_h <= 64): [d_h / 32] chunks of
-  // [128 rows x 128 B], 128-byte swizzled.  d_h = 128 adds with atomics.
+  // dQ staging for the tensor reduce-add (d_h <= 64): one [128 rows x 128 B]
+  // chunk (32 fp32 columns), 128-byte swizzled, reused for each chunk of the
+  // row.  d_h = 128 adds with atomics.
   static constexpr bool DQ_TMA = (D <= 64);
-  static constexpr int DQS_BYTES = DQ_TMA ? 128 * D * 4 : 0;
+  static constexpr int DQS_BYTES = DQ_TMA ? 128 * 32 * 4 : 0;
   static constexpr int OFF_DQS = OFF_DST + SqTile::BYTES;
-  static constexpr int OFF_BAR = OFF_DQS + DQS_BYTES;
-  static constexpr int NBAR = 2 + 2 * QST + 9;
+  static constexpr int OFF_PT = OFF_DQS + DQS_BYTES;   // P^T tile (PS only)
+  static constexpr int OFF_BAR = OFF_PT + (PS ? SqTile::BYTES : 0);
+  static constexpr int NBAR = 2 + 2 * QST + 10;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int SLACK = (BYTES + 1024 <= 232448) ? 1024 : 0;
@@ -77,9 +87,6 @@ struct BwdSmem {
   // half: P^T k-steps 0..3 sit at 0.., 4..7 at 64.. (dS^T likewise + 128).
   static constexpr uint32_t T_S = 0, T_DP = 128;
   static constexpr uint32_t T_DV = 256, T_DK = 256 + D;
-  // d_h = 128 leaves no free columns: dQ reuses the S^T/P^T columns once the
-  // dV MMAs that read P^T have completed.
-  static constexpr bool DQ_ALIAS = (256 + 3 * D > 512);
   static constexpr uint32_t T_DQ = DQ_ALIAS ? 0 : 256 + 2 * D;
   __device__ static __forceinline__ uint32_t a_col(int kk) {
     return (uint32_t)((kk < 4) ? kk * 8 : 64 + (kk - 4) * 8);
@@ -140,6 +147,7 @@ __global__ void __launch_bounds__(512, 1)
   uint64_t* dq_empty = dq_full + 1;
   uint64_t* kd_full = dq_empty + 1;
   uint64_t* kd_empty = kd_full + 1;
+  uint64_t* s_free = kd_empty + 1;       // S^T, dP^T loaded by the compute warps (PS)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
   const WaitCtl wc{abort_flag, p.status};
@@ -157,6 +165,7 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(dq_empty, 128);
     mbar_init(kd_full, 1);
     mbar_init(kd_empty, 256);
+    mbar_init(s_free, 256);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -177,6 +186,7 @@ __global__ void __launch_bounds__(512, 1)
   const uint32_t sK = smem_u32(smem + L::OFF_K);
   const uint32_t sV = smem_u32(smem + L::OFF_V);
   const uint32_t sDST = smem_u32(smem + L::OFF_DST);
+  const uint32_t sPT = smem_u32(smem + L::OFF_PT);
   const int H = p.H, T = p.T;
 
   if (warp == 0) {
@@ -239,7 +249,58 @@ __global__ void __launch_bounds__(512, 1)
                       kk > 0);
         mma_commit(s_full);
       };
-      for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+      uint32_t sfc = 0;
+      if constexpr (L::PS) {
+        for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+          const BItem w = decode_bwd(p, it);
+          mbar_wait(kv_full, kvc & 1, wc, kSiteBMmaKV);
+          ++kvc;
+          // the previous item's last S^T/dP^T must have been loaded
+          if (it != (int)blockIdx.x) {
+            mbar_wait(s_free, sfc & 1, wc, kSiteBMmaS);
+            ++sfc;
+          }
+          issue_s(qc);
+          for (int t = 0; t < w.nsteps; ++t) {
+            const int qs = qc % L::QST;
+            const uint32_t sQ = smem_u32(smem + L::OFF_Q + qs * L::STAGE);
+            const uint32_t sDO = sQ + G::TILE_BYTES;
+            if (t + 1 < w.nsteps) {
+              // next step's scores as soon as this step's are in registers
+              mbar_wait(s_free, sfc & 1, wc, kSiteBMmaS);
+              ++sfc;
+              issue_s(qc + 1);
+            }
+            mbar_wait(p_full, pc & 1, wc, kSiteBMmaP);
+            if (t == 0) mbar_wait(kd_empty, (kdc & 1) ^ 1, wc, kSiteBMmaKD);
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_bf16_ss(tmem + L::T_DV, SqTile::kmajor_desc(sPT, kk), G::mnmajor_desc(sDO, kk),
+                          id_acc, (t > 0 || kk > 0));
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_bf16_ss(tmem + L::T_DK, SqTile::kmajor_desc(sDST, kk), G::mnmajor_desc(sQ, kk),
+                          id_acc, (t > 0 || kk > 0));
+            mma_commit(q_empty + qs);
+            ++qc;
+            ++pc;
+            mbar_wait(dq_empty, (dqc & 1) ^ 1, wc, kSiteBMmaDQ);
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_bf16_ss(tmem + L::T_DQ, SqTile::mnmajor_desc(sDST, kk), G::mnmajor_desc(sK, kk),
+                          id_dq, kk > 0);
+            mma_commit(p_empty);
+            mma_commit(dq_full);
+            ++dqc;
+          }
+          mma_commit(kd_full);
+          mma_commit(kv_empty);
+          ++kdc;
+        }
+      }
+      for (int it = blockIdx.x; !L::PS && it < p.n_items; it += gridDim.x) {
         const BItem w = decode_bwd(p, it);
         mbar_wait(kv_full, kvc & 1, wc, kSiteBMmaKV);
         ++kvc;
@@ -324,6 +385,11 @@ __global__ void __launch_bounds__(512, 1)
           tmem_ld_x32(trow + L::T_DP + col, dv);
           tmem_wait_ld(sv);
           tmem_wait_ld(dv);
+          if (L::PS && c0 == 32) {
+            // every S^T/dP^T column this thread reads is in registers
+            tc_fence_before();
+            mbar_arrive(s_free);
+          }
           uint32_t pk[16], dk[16];
 #pragma unroll
           for (int k4 = 0; k4 < 32; k4 += 4) {
@@ -353,20 +419,25 @@ __global__ void __launch_bounds__(512, 1)
               dk[k >> 1] = pack_bf16x2(g0, g1);
             }
           }
-          // P^T and dS^T over this half's columns just read (K-major A
-          // operands of dV and dK), and dS^T into shared memory for dQ.
-          tmem_st_x16(trow + L::T_S + 64 * hf + (c0 >> 1), pk);
-          tmem_st_x16(trow + L::T_DP + 64 * hf + (c0 >> 1), dk);
-          // the dS^T tile in shared memory is read by the previous step's dQ
+          if constexpr (!L::PS) {
+            // P^T and dS^T over this half's columns just read (K-major A
+            // operands of dV and dK), and dS^T into shared memory for dQ.
+            tmem_st_x16(trow + L::T_S + 64 * hf + (c0 >> 1), pk);
+            tmem_st_x16(trow + L::T_DP + 64 * hf + (c0 >> 1), dk);
+          }
+          // the shared tiles are read by the previous step's dV/dK/dQ
           if (c0 == 0) mbar_wait(p_empty, (pc & 1) ^ 1, wc, kSiteBCmpP);
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const uint32_t unit = (uint32_t)(col >> 3) + u;
             st_shared_v4(SqTile::unit_addr(sDST, r, unit), dk[4 * u], dk[4 * u + 1],
                          dk[4 * u + 2], dk[4 * u + 3]);
+            if constexpr (L::PS)
+              st_shared_v4(SqTile::unit_addr(sPT, r, unit), pk[4 * u], pk[4 * u + 1],
+                           pk[4 * u + 2], pk[4 * u + 3]);
           }
         }
-        tmem_wait_st();
+        if constexpr (!L::PS) tmem_wait_st();
         tc_fence_before();
         fence_proxy_async_smem();
         mbar_arrive(p_full);
@@ -426,21 +497,22 @@ __global__ void __launch_bounds__(512, 1)
             tmem_wait_ld(*reinterpret_cast<uint32_t(*)[16]>(o + c0));
           tc_fence_before();
           mbar_arrive(dq_empty);
-          if (r == 0) bulk_wait_group_read0();  // the previous tile has been read
-          named_bar_sync(6, 128);
           const uint32_t stg = smem_u32(smem + L::OFF_DQS);
+          const int row = (w.b * H + w.h) * T + I * 128;
 #pragma unroll
-          for (int u = 0; u < D / 4; ++u)
-            st_shared_v4(stg + (uint32_t)(u >> 3) * 16384u + sw128_offset(r, (uint32_t)(u & 7)),
-                         o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
-          fence_proxy_async_smem();
-          named_bar_sync(6, 128);
-          if (r == 0) {
-            const int row = (w.b * H + w.h) * T + I * 128;
+          for (int c = 0; c < D / 32; ++c) {
+            if (r == 0) bulk_wait_group_read0();  // the staging chunk has been read
+            named_bar_sync(6, 128);
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c)
-              tma_reduce_add_2d(&tm_dq, smem + L::OFF_DQS + c * 16384, c * 32, row);
-            bulk_commit_group();
+            for (int u = 0; u < 8; ++u)
+              st_shared_v4(stg + sw128_offset(r, (uint32_t)u), o[32 * c + 4 * u],
+                           o[32 * c + 4 * u + 1], o[32 * c + 4 * u + 2], o[32 * c + 4 * u + 3]);
+            fence_proxy_async_smem();
+            named_bar_sync(6, 128);
+            if (r == 0) {
+              tma_reduce_add_2d(&tm_dq, smem + L::OFF_DQS, c * 32, row);
+              bulk_commit_group();
+            }
           }
         } else {
           float* dst = p.dq_acc + ((size_t)(w.b * H + w.h) * T + (size_t)I * 128 + r) * D;

@@ -282,6 +282,39 @@ struct FwdSmem {
   static constexpr int AUX_BYTES = 512 + 1024;
 };
 
+// One thread's 64 columns of a generated tile, written as packed bf16 to
+// TMEM columns tdst .. tdst + 31.  colv_s: shared address of the half's 64
+// column values; win_s: the distance window (centre at entry 127); rc = the
+// row minus the half's first column.  Forward element (i = row, j = col):
+// distance rc - cl; transposed (j = row, i = col): distance cl - rc.
+// Factored: colv * r(distance) * rowv; exact: exp2(colv + r(distance) + rowv).
+template <bool TRANSPOSED, bool EXACT>
+__device__ __forceinline__ void gen_tile(uint32_t colv_s, uint32_t win_s, int rc, uint64_t row2,
+                                         uint32_t tdst) {
+  // address of window entry 127 + distance for column 0 of the half
+  const uint32_t w0 = win_s + 4u * (uint32_t)(127 + (TRANSPOSED ? -rc : rc));
+#pragma unroll
+  for (int q0 = 0; q0 < 32; q0 += 16) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int qq = 0; qq < 16; ++qq) {
+      const int cl = 2 * (q0 + qq);
+      const uint64_t cv = lds_f32x2(colv_s + 4u * cl);
+      const float wa = lds_f32(TRANSPOSED ? w0 + 4u * cl : w0 - 4u * cl);
+      const float wb = lds_f32(TRANSPOSED ? w0 + 4u * (cl + 1) : w0 - 4u * (cl + 1));
+      const uint64_t wv = f2_pack(wa, wb);
+      if (EXACT) {
+        float x0, x1;
+        f2_unpack(f2_add(f2_add(cv, wv), row2), x0, x1);
+        pk[qq] = pack_bf16x2(fast_exp2(x0), fast_exp2(x1));
+      } else {
+        pk[qq] = pack_bf16x2_f2(f2_mul(f2_mul(cv, wv), row2));
+      }
+    }
+    tmem_st_x16(tdst + q0, pk);
+  }
+}
+
 // TMEM columns: NBUF 128-column buffers from 0 hold S (fp32).  Each compute
 // half (key columns 0..63 or 64..127 of the tile) writes its P, as packed
 // bf16, over the first 32 columns of its own S half, so P k-steps 0..3 sit at
@@ -705,6 +738,7 @@ __global__ void __launch_bounds__(384, 1)
         // per-row value: forward 1/Z'(i) or -log2 Z(i); transposed a(j)
         const float rowv = TRANSPOSED ? p.a_tab[(size_t)w.hs * T + w.X * 128 + r]
                                       : p.row_tab[(size_t)w.hs * T + w.X * 128 + r];
+        const uint64_t row2 = f2_pack(rowv, rowv);
         for (int step = 0; step < w.nsteps; ++step) {
           const uint32_t u = sc0 + step;
           const int ks = kc % L::KST;
@@ -716,25 +750,10 @@ __global__ void __launch_bounds__(384, 1)
           mbar_wait(s_empty + (u % NB), ((u / NB) & 1) ^ 1, wc, kSiteCmpP);
           tc_fence_after();
           const uint32_t gdst = trow + kTmemS + (u % NB) * 128 + 64 * hf;
-#pragma unroll
-          for (int q0 = 0; q0 < 32; q0 += 16) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int qq = 0; qq < 16; ++qq) {
-              float e[2];
-#pragma unroll
-              for (int k = 0; k < 2; ++k) {
-                const int cl = 2 * (q0 + qq) + k;  // column within the half
-                const int c = 64 * hf + cl;
-                // forward: element (i = row, j = col), distance r - c
-                // transposed: element (j = row, i = col), distance c - r
-                const float wv = TRANSPOSED ? win[127 + c - r] : win[127 + r - c];
-                e[k] = exact ? fast_exp2(colv[cl] + wv + rowv) : colv[cl] * wv * rowv;
-              }
-              pk[qq] = pack_bf16x2(e[0], e[1]);
-            }
-            tmem_st_x16(gdst + q0, pk);
-          }
+          if (exact)
+            gen_tile<TRANSPOSED, true>(smem_u32(colv), smem_u32(win), r - 64 * hf, row2, gdst);
+          else
+            gen_tile<TRANSPOSED, false>(smem_u32(colv), smem_u32(win), r - 64 * hf, row2, gdst);
           // all 256 compute threads have read the aux slot: release it once
           named_bar_sync(1, 256);
           if (hf == 0 && r == 0) mbar_arrive(k_empty + ks);
