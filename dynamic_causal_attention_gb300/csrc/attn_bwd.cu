@@ -75,7 +75,7 @@ struct BwdSmem {
   static constexpr int OFF_DQS = OFF_DST + SqTile::BYTES;
   static constexpr int OFF_PT = OFF_DQS + DQS_BYTES;   // P^T tile (PS only)
   static constexpr int OFF_BAR = OFF_PT + (PS ? SqTile::BYTES : 0);
-  static constexpr int NBAR = 2 + 2 * QST + 10;
+  static constexpr int NBAR = 2 + 2 * QST + 11;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int SLACK = (BYTES + 1024 <= 232448) ? 1024 : 0;
@@ -148,6 +148,7 @@ __global__ void __launch_bounds__(512, 1)
   uint64_t* kd_full = dq_empty + 1;
   uint64_t* kd_empty = kd_full + 1;
   uint64_t* s_free = kd_empty + 1;       // S^T, dP^T loaded by the compute warps (PS)
+  uint64_t* pt_empty = s_free + 1;       // the P^T tile is free again (PS)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
   const WaitCtl wc{abort_flag, p.status};
@@ -166,6 +167,7 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(kd_full, 1);
     mbar_init(kd_empty, 256);
     mbar_init(s_free, 256);
+    mbar_init(pt_empty, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -278,6 +280,7 @@ __global__ void __launch_bounds__(512, 1)
             for (int kk = 0; kk < 8; ++kk)
               mma_bf16_ss(tmem + L::T_DV, SqTile::kmajor_desc(sPT, kk), G::mnmajor_desc(sDO, kk),
                           id_acc, (t > 0 || kk > 0));
+            mma_commit(pt_empty);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
               mma_bf16_ss(tmem + L::T_DK, SqTile::kmajor_desc(sDST, kk), G::mnmajor_desc(sQ, kk),
@@ -374,22 +377,83 @@ __global__ void __launch_bounds__(512, 1)
         const float* nl_s = reinterpret_cast<const float*>(smem + L::OFF_Q + qs * L::STAGE +
                                                            2 * G::TILE_BYTES) + 64 * hf;
         const float* nd_s = nl_s + 128;
+        const uint32_t nl_a = smem_u32(nl_s);  // -lse2 at +0, -D at +512 bytes
         mbar_wait(s_full, sc & 1, wc, kSiteBCmpS);
         tc_fence_after();
         const bool diag = (t == 0);
+        if constexpr (L::PS) {
+          // Four 16-column chunks; the TMEM loads of chunk k + 1 are issued
+          // right after chunk k's have landed, so they fly while chunk k is
+          // computed (tcgen05.wait::ld waits for every load in flight).
+          uint32_t sv[2][16], dv[2][16];
+          uint32_t dsk[32];  // this step's dS^T row, stored once the last dQ has read the tile
+          tmem_ld_x16(trow + L::T_S + 64 * hf, sv[0]);
+          tmem_ld_x16(trow + L::T_DP + 64 * hf, dv[0]);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int b = k & 1;
+            const int col = 64 * hf + 16 * k;  // first query column of this chunk
+            tmem_wait_ld(sv[b]);
+            tmem_wait_ld(dv[b]);
+            if (k + 1 < 4) {
+              tmem_ld_x16(trow + L::T_S + col + 16, sv[b ^ 1]);
+              tmem_ld_x16(trow + L::T_DP + col + 16, dv[b ^ 1]);
+            } else {
+              // every S^T/dP^T column this thread reads is in registers
+              tc_fence_before();
+              mbar_arrive(s_free);
+            }
+            if (diag) {
+              // causal mask of the diagonal tile: query column < key row
+#pragma unroll
+              for (int e = 0; e < 16; ++e)
+                if (col + e < r) sv[b][e] = 0xff800000u;  // -inf: P = 0, dS = 0
+            }
+            uint32_t pk[8];
+#pragma unroll
+            for (int k4 = 0; k4 < 16; k4 += 4) {
+              const float4 nl = lds_f32x4(nl_a + 4u * (16 * k + k4));
+              const float4 nd = lds_f32x4(nl_a + 512u + 4u * (16 * k + k4));
+#pragma unroll
+              for (int h2 = 0; h2 < 2; ++h2) {
+                const int e = k4 + 2 * h2;
+                const float l0 = h2 ? nl.z : nl.x, l1 = h2 ? nl.w : nl.y;
+                const float e0 = h2 ? nd.z : nd.x, e1 = h2 ? nd.w : nd.y;
+                float x0, x1;
+                f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[b][e]), __uint_as_float(sv[b][e + 1])),
+                                 sc2, f2_pack(l0, l1)),
+                          x0, x1);
+                const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+                const uint64_t g2 = f2_mul(
+                    f2_pack(p0, p1),
+                    f2_add(f2_pack(__uint_as_float(dv[b][e]), __uint_as_float(dv[b][e + 1])),
+                           f2_pack(e0, e1)));
+                pk[e >> 1] = pack_bf16x2(p0, p1);
+                dsk[8 * k + (e >> 1)] = pack_bf16x2_f2(g2);
+              }
+            }
+            // the P^T tile is read by the previous step's dV
+            if (k == 0) mbar_wait(pt_empty, (pc & 1) ^ 1, wc, kSiteBCmpP);
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+              st_shared_v4(SqTile::unit_addr(sPT, r, (uint32_t)(col >> 3) + u), pk[4 * u],
+                           pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+          }
+          // the dS^T tile is read by the previous step's dK and dQ
+          mbar_wait(p_empty, (pc & 1) ^ 1, wc, kSiteBCmpP);
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            st_shared_v4(SqTile::unit_addr(sDST, r, (uint32_t)(8 * hf) + u), dsk[4 * u],
+                         dsk[4 * u + 1], dsk[4 * u + 2], dsk[4 * u + 3]);
+        }
 #pragma unroll 1
-        for (int c0 = 0; c0 < 64; c0 += 32) {
+        for (int c0 = 0; !L::PS && c0 < 64; c0 += 32) {
           const int col = 64 * hf + c0;      // first query column of this chunk
           uint32_t sv[32], dv[32];
           tmem_ld_x32(trow + L::T_S + col, sv);
           tmem_ld_x32(trow + L::T_DP + col, dv);
           tmem_wait_ld(sv);
           tmem_wait_ld(dv);
-          if (L::PS && c0 == 32) {
-            // every S^T/dP^T column this thread reads is in registers
-            tc_fence_before();
-            mbar_arrive(s_free);
-          }
           uint32_t pk[16], dk[16];
 #pragma unroll
           for (int k4 = 0; k4 < 32; k4 += 4) {
@@ -419,22 +483,17 @@ __global__ void __launch_bounds__(512, 1)
               dk[k >> 1] = pack_bf16x2(g0, g1);
             }
           }
-          if constexpr (!L::PS) {
-            // P^T and dS^T over this half's columns just read (K-major A
-            // operands of dV and dK), and dS^T into shared memory for dQ.
-            tmem_st_x16(trow + L::T_S + 64 * hf + (c0 >> 1), pk);
-            tmem_st_x16(trow + L::T_DP + 64 * hf + (c0 >> 1), dk);
-          }
-          // the shared tiles are read by the previous step's dV/dK/dQ
+          // P^T and dS^T over this half's columns just read (K-major A
+          // operands of dV and dK), and dS^T into shared memory for dQ.
+          tmem_st_x16(trow + L::T_S + 64 * hf + (c0 >> 1), pk);
+          tmem_st_x16(trow + L::T_DP + 64 * hf + (c0 >> 1), dk);
+          // the dS^T tile in shared memory is read by the previous step's dQ
           if (c0 == 0) mbar_wait(p_empty, (pc & 1) ^ 1, wc, kSiteBCmpP);
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const uint32_t unit = (uint32_t)(col >> 3) + u;
             st_shared_v4(SqTile::unit_addr(sDST, r, unit), dk[4 * u], dk[4 * u + 1],
                          dk[4 * u + 2], dk[4 * u + 3]);
-            if constexpr (L::PS)
-              st_shared_v4(SqTile::unit_addr(sPT, r, unit), pk[4 * u], pk[4 * u + 1],
-                           pk[4 * u + 2], pk[4 * u + 3]);
           }
         }
         if constexpr (!L::PS) tmem_wait_st();

@@ -348,6 +348,13 @@ __device__ __forceinline__ uint64_t lds_f32x2(uint32_t addr) {
   asm volatile("ld.shared.b64 %0, [%1];" : "=l"(v) : "r"(addr));
   return v;
 }
+__device__ __forceinline__ float4 lds_f32x4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
+  return v;
+}
 __device__ __forceinline__ uint32_t pack_bf16x2_f2(uint64_t v) {
   float lo, hi;
   f2_unpack(v, lo, hi);
