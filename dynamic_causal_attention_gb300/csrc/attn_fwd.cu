@@ -28,8 +28,8 @@
 // the head falls back to the exact form exp2(alpha2(j) + rho2(i-j) - log2 Z(i)).
 //
 // Warp roles in K2 (384 threads): warp 0 issues TMA copies, warp 1 issues
-// tcgen05 MMAs (one elected lane), warp 2 owns the TMEM allocation, warps
-// 4..11 are two compute warpgroups (softmax / tile generation / epilogue):
+// the S = Q K^T MMAs and warp 3 the P V MMAs (one lane each), warp 2 owns the
+// TMEM allocation, warps 4..11 are two compute warpgroups (softmax / tile generation / epilogue):
 // each tile row belongs to one thread of each, which split its 128 key
 // columns and exchange row maxima and sums through shared memory.
 #include <cuda.h>
@@ -522,59 +522,72 @@ __global__ void __launch_bounds__(384, 1)
         if (vc > (uint32_t)s) mbar_drain(v_full + s, ((vc - 1 - s) / L::VST) & 1);
     }
   } else if (warp == 1) {
-    // ---------------------------------------------------------- MMA issuer
+    // ---------------------------------------------------------- S issuer
+    // S = Q K^T of every dynamic step.  A second warp issues the P V
+    // products, so that a score MMA never queues behind a wait for the
+    // softmax: each issuing thread blocks while its MMAs are accepted.
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16(128, D, false, true);
-      uint32_t qc = 0, kc = 0, vc = 0, sc = 0, oc = 0;
+      uint32_t qc = 0, kc = 0, sc = 0;
       for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
         const Item w = decode_item<TRANSPOSED>(p, it);
         const uint32_t sc0 = sc;
         if (!w.is_static) {
           mbar_wait(q_full, qc & 1, wc, kSiteMmaQ);
           ++qc;
-          for (int j = 0; j <= w.nsteps; ++j) {
-            if (j < w.nsteps) {
-              const uint32_t u = sc0 + j;
-              const int ks = kc % L::KST;
-              mbar_wait(k_full + ks, (kc / L::KST) & 1, wc, kSiteMmaK);
-              const uint32_t b = u % NB;
-              mbar_wait(s_empty + b, ((u / NB) & 1) ^ 1, wc, kSiteMmaS);
-              tc_fence_after();
-              const uint32_t kt = sK + ks * G::TILE_BYTES;
+          for (int j = 0; j < w.nsteps; ++j) {
+            const uint32_t u = sc0 + j;
+            const int ks = kc % L::KST;
+            mbar_wait(k_full + ks, (kc / L::KST) & 1, wc, kSiteMmaK);
+            const uint32_t b = u % NB;
+            mbar_wait(s_empty + b, ((u / NB) & 1) ^ 1, wc, kSiteMmaS);
+            tc_fence_after();
+            const uint32_t kt = sK + ks * G::TILE_BYTES;
 #pragma unroll
-              for (int kk = 0; kk < G::KSTEPS; ++kk)
-                mma_bf16_ss(tmem + kTmemS + b * 128, G::kmajor_desc(sQ, kk),
-                            G::kmajor_desc(kt, kk), idesc_s, kk > 0);
-              mma_commit(k_empty + ks);
-              mma_commit(s_full + b);
-              if (j == w.nsteps - 1) mma_commit(q_empty);
-              ++kc;
-            }
-            if (j >= 1) {
-              const uint32_t u = sc0 + j - 1;
-              const int vs = vc % L::VST;
-              mbar_wait(v_full + vs, (vc / L::VST) & 1, wc, kSiteMmaV);
-              mbar_wait(p_full + (u % NB), (u / NB) & 1, wc, kSiteMmaP);
-              if (j == 1) mbar_wait(o_empty, (oc & 1) ^ 1, wc, kSiteMmaO);
-              tc_fence_after();
-              const uint32_t vt = sV + vs * G::TILE_BYTES;
-              const uint32_t pa = tmem + kTmemS + (u % NB) * 128;
-#pragma unroll
-              for (int kk = 0; kk < 8; ++kk)
-                mma_bf16_ts(tmem + kTmemO, pa + p_col(kk), G::mnmajor_desc(vt, kk), idesc_pv,
-                            (j > 1 || kk > 0));
-              mma_commit(v_empty + vs);
-              mma_commit(s_empty + (u % NB));
-              ++vc;
-            }
+            for (int kk = 0; kk < G::KSTEPS; ++kk)
+              mma_bf16_ss(tmem + kTmemS + b * 128, G::kmajor_desc(sQ, kk), G::kmajor_desc(kt, kk),
+                          idesc_s, kk > 0);
+            mma_commit(k_empty + ks);
+            mma_commit(s_full + b);
+            if (j == w.nsteps - 1) mma_commit(q_empty);
+            ++kc;
           }
-          sc = sc0 + w.nsteps;
+        } else {
+          kc += w.nsteps;  // the aux entries of static steps are consumed by the compute warps
+        }
+        sc = sc0 + w.nsteps;
+      }
+    }
+  } else if (warp == 3) {
+    // ---------------------------------------------------------- P V issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_pv = idesc_bf16(128, D, false, true);
+      uint32_t vc = 0, sc = 0, oc = 0;
+      for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+        const Item w = decode_item<TRANSPOSED>(p, it);
+        const uint32_t sc0 = sc;
+        if (!w.is_static) {
+          for (int j = 0; j < w.nsteps; ++j) {
+            const uint32_t u = sc0 + j;
+            const int vs = vc % L::VST;
+            mbar_wait(v_full + vs, (vc / L::VST) & 1, wc, kSiteMmaV);
+            mbar_wait(p_full + (u % NB), (u / NB) & 1, wc, kSiteMmaP);
+            if (j == 0) mbar_wait(o_empty, (oc & 1) ^ 1, wc, kSiteMmaO);
+            tc_fence_after();
+            const uint32_t vt = sV + vs * G::TILE_BYTES;
+            const uint32_t pa = tmem + kTmemS + (u % NB) * 128;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_bf16_ts(tmem + kTmemO, pa + p_col(kk), G::mnmajor_desc(vt, kk), idesc_pv,
+                          (j > 0 || kk > 0));
+            mma_commit(v_empty + vs);
+            mma_commit(s_empty + (u % NB));
+            ++vc;
+          }
           mma_commit(o_full);
           ++oc;
         } else {
           for (int step = 0; step < w.nsteps; ++step) {
-            ++kc;  // the aux entry of this step is consumed by the compute warps
             const uint32_t u = sc0 + step;
             mbar_wait(p_full + (u % NB), (u / NB) & 1, wc, kSiteMmaP);
             if (step == 0) mbar_wait(o_empty, (oc & 1) ^ 1, wc, kSiteMmaO);
@@ -596,10 +609,10 @@ __global__ void __launch_bounds__(384, 1)
             mma_commit(s_full + (u % NB));
             mma_commit(s_empty + (u % NB));
           }
-          sc = sc0 + w.nsteps;
           mma_commit(o_full);
           ++oc;
         }
+        sc = sc0 + w.nsteps;
       }
     }
   } else if (warp >= 4) {
