@@ -114,7 +114,8 @@ __device__ __forceinline__ BItem decode_bwd(const BwdParams& p, int it) {
   return r;
 }
 
-// Threads: warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM owner,
+// Threads: warp 0 TMA producer, warp 1 MMA issuer (for d_h <= 64 only the
+// S^T/dP^T products; warp 3 issues dV, dK and dQ), warp 2 TMEM owner,
 // warps 4..11 two compute halves (query columns 0..63 and 64..127 of every
 // key row; a row per thread), warps 12..15 the dQ warps.
 template <int D>
@@ -253,6 +254,7 @@ __global__ void __launch_bounds__(512, 1)
       };
       uint32_t sfc = 0;
       if constexpr (L::PS) {
+        // S^T and dP^T only; warp 3 issues dV, dK and dQ.
         for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
           const BItem w = decode_bwd(p, it);
           mbar_wait(kv_full, kvc & 1, wc, kSiteBMmaKV);
@@ -263,44 +265,14 @@ __global__ void __launch_bounds__(512, 1)
             ++sfc;
           }
           issue_s(qc);
-          for (int t = 0; t < w.nsteps; ++t) {
-            const int qs = qc % L::QST;
-            const uint32_t sQ = smem_u32(smem + L::OFF_Q + qs * L::STAGE);
-            const uint32_t sDO = sQ + G::TILE_BYTES;
-            if (t + 1 < w.nsteps) {
-              // next step's scores as soon as this step's are in registers
-              mbar_wait(s_free, sfc & 1, wc, kSiteBMmaS);
-              ++sfc;
-              issue_s(qc + 1);
-            }
-            mbar_wait(p_full, pc & 1, wc, kSiteBMmaP);
-            if (t == 0) mbar_wait(kd_empty, (kdc & 1) ^ 1, wc, kSiteBMmaKD);
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_bf16_ss(tmem + L::T_DV, SqTile::kmajor_desc(sPT, kk), G::mnmajor_desc(sDO, kk),
-                          id_acc, (t > 0 || kk > 0));
-            mma_commit(pt_empty);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_bf16_ss(tmem + L::T_DK, SqTile::kmajor_desc(sDST, kk), G::mnmajor_desc(sQ, kk),
-                          id_acc, (t > 0 || kk > 0));
-            mma_commit(q_empty + qs);
+          ++qc;
+          for (int t = 0; t + 1 < w.nsteps; ++t) {
+            // next step's scores as soon as this step's are in registers
+            mbar_wait(s_free, sfc & 1, wc, kSiteBMmaS);
+            ++sfc;
+            issue_s(qc);
             ++qc;
-            ++pc;
-            mbar_wait(dq_empty, (dqc & 1) ^ 1, wc, kSiteBMmaDQ);
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_bf16_ss(tmem + L::T_DQ, SqTile::mnmajor_desc(sDST, kk), G::mnmajor_desc(sK, kk),
-                          id_dq, kk > 0);
-            mma_commit(p_empty);
-            mma_commit(dq_full);
-            ++dqc;
           }
-          mma_commit(kd_full);
-          mma_commit(kv_empty);
-          ++kdc;
         }
       }
       for (int it = blockIdx.x; !L::PS && it < p.n_items; it += gridDim.x) {
@@ -359,6 +331,50 @@ __global__ void __launch_bounds__(512, 1)
         }
         mma_commit(kd_full);
         mma_commit(kv_empty);
+        ++kdc;
+      }
+    }
+  } else if (warp == 3) {
+    // ---------------------------------------------------------- dV/dK/dQ issuer (PS)
+    if (L::PS && lane == 0) {
+      constexpr uint32_t id_acc = idesc_bf16(128, D, false, true);
+      constexpr uint32_t id_dq = idesc_bf16(128, D, true, true);
+      uint32_t kvc = 0, qc = 0, pc = 0, dqc = 0, kdc = 0;
+      for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+        const BItem w = decode_bwd(p, it);
+        mbar_wait(kv_full, kvc & 1, wc, kSiteBMmaKV);  // K_J is the B operand of dQ
+        ++kvc;
+        for (int t = 0; t < w.nsteps; ++t) {
+          const int qs = qc % L::QST;
+          const uint32_t sQ = smem_u32(smem + L::OFF_Q + qs * L::STAGE);
+          const uint32_t sDO = sQ + G::TILE_BYTES;
+          mbar_wait(p_full, pc & 1, wc, kSiteBMmaP);
+          if (t == 0) mbar_wait(kd_empty, (kdc & 1) ^ 1, wc, kSiteBMmaKD);
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tmem + L::T_DV, SqTile::kmajor_desc(sPT, kk), G::mnmajor_desc(sDO, kk),
+                        id_acc, (t > 0 || kk > 0));
+          mma_commit(pt_empty);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tmem + L::T_DK, SqTile::kmajor_desc(sDST, kk), G::mnmajor_desc(sQ, kk),
+                        id_acc, (t > 0 || kk > 0));
+          mma_commit(q_empty + qs);  // S^T/dP^T of this stage completed before p_full
+          ++qc;
+          ++pc;
+          mbar_wait(dq_empty, (dqc & 1) ^ 1, wc, kSiteBMmaDQ);
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tmem + L::T_DQ, SqTile::mnmajor_desc(sDST, kk), G::mnmajor_desc(sK, kk),
+                        id_dq, kk > 0);
+          mma_commit(p_empty);
+          mma_commit(dq_full);
+          ++dqc;
+        }
+        mma_commit(kd_full);
+        mma_commit(kv_empty);  // the item's S^T/dP^T all completed before its last p_full
         ++kdc;
       }
     }
