@@ -72,9 +72,11 @@ __device__ __forceinline__ void block_minmax(float& mx, float& mn, float* red) {
   }
 }
 
-// grid (T / 64, n_static), 256 threads (8 warps), dynamic smem 2 * T floats.
-// Each block owns 64 rows; each warp computes the convolution of 8 rows with
-// its 32 lanes splitting the causal sum, reduced across lanes in a fixed order.
+// grid (T / 64, n_static), 256 threads (8 warps), dynamic smem 2 * T + 8
+// floats.  Each block owns 64 rows; each warp computes the convolution of 8
+// rows together (eight independent accumulators, one load of a(k) for all
+// of them) with its 32 lanes splitting the causal sum, reduced across lanes
+// in a fixed order.
 constexpr int kPrepRows = 64;
 
 __global__ void __launch_bounds__(256) static_prep_kernel(StaticPrep p) {
@@ -84,7 +86,7 @@ __global__ void __launch_bounds__(256) static_prep_kernel(StaticPrep p) {
   const int row0 = blockIdx.x * kPrepRows;
   const int nload = row0 + kPrepRows;  // entries 0 .. row0 + 63 are needed
   float* sa = sh;
-  float* sr = sh + T;
+  float* sr = sh + T + 8;  // sr[-8 .. -1] = 0: the last stride reads past d = 0
   const float* alpha = p.alpha + (size_t)h * T;
   const float* rho = p.rho + (size_t)h * T;
   // finite max/min of alpha and rho over the whole head (every block agrees)
@@ -116,17 +118,32 @@ __global__ void __launch_bounds__(256) static_prep_kernel(StaticPrep p) {
       sa[t] = all_masked ? 0.f : expf(sa[t] - amax);
       sr[t] = all_masked ? 0.f : expf(sr[t] - rmax);
     }
+    if (threadIdx.x < 8) sr[(int)threadIdx.x - 8] = 0.f;
     __syncthreads();
-    for (int m = 0; m < kPrepRows / 8; ++m) {
-      const int i = row0 + warp * (kPrepRows / 8) + m;
-      float z = 0.f;
-      for (int k = lane; k <= i; k += 32) z = fmaf(sa[k], sr[i - k], z);
+    const int ib = row0 + warp * (kPrepRows / 8);  // this warp's first row
+    float z[8];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-      if (lane == 0) {
-        row_tab[i] = z > 0.f ? 1.0f / z : 0.f;
-        logZ[i] = z > 0.f ? logf(z) + amax + rmax : -INFINITY;
-      }
+    for (int m = 0; m < 8; ++m) z[m] = 0.f;
+    // k <= ib + 7 covers every row; k > i reads the zero pad (i - k >= -7)
+    for (int k = lane; k <= ib + 7; k += 32) {
+      const float av = sa[k];
+      const float* rp = sr + (ib - k);
+#pragma unroll
+      for (int m = 0; m < 8; ++m) z[m] = fmaf(av, rp[m], z[m]);
+    }
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) z[m] += __shfl_xor_sync(0xffffffffu, z[m], o);
+    }
+    if (lane < 8) {
+      float zz = z[0];
+#pragma unroll
+      for (int m = 1; m < 8; ++m)
+        if (lane == m) zz = z[m];
+      const int i = ib + lane;
+      row_tab[i] = zz > 0.f ? 1.0f / zz : 0.f;
+      logZ[i] = zz > 0.f ? logf(zz) + amax + rmax : -INFINITY;
     }
     for (int t = threadIdx.x; t < kPrepRows; t += blockDim.x) {
       a_tab[row0 + t] = sa[row0 + t];
@@ -215,7 +232,7 @@ int elementwise_blocks(size_t n) {
 
 cudaError_t launch_static_prep(const StaticPrep& p, cudaStream_t s) {
   if (p.n_static == 0) return cudaSuccess;
-  const size_t smem = 2 * (size_t)p.T * sizeof(float);
+  const size_t smem = (2 * (size_t)p.T + 8) * sizeof(float);
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(static_prep_kernel,
@@ -485,7 +502,9 @@ __global__ void __launch_bounds__(384, 1)
                           v_full + vs, c * G::CHUNK, row0 + j * 128);
           }
         } else {
-          for (int step = 0; step < w.nsteps; ++step) {
+          // The tables of a step go into the K ring one step ahead of its V
+          // tiles, so that the compute warps never wait behind a V slot.
+          auto load_aux = [&](int step) {
             // inner tile Y: J (forward) or I (transposed)
             const int Y = TRANSPOSED ? (w.X + step) : step;
             const int dist0 = TRANSPOSED ? (Y - w.X) : (w.X - Y);  // (I - J) in tiles
@@ -501,6 +520,11 @@ __global__ void __launch_bounds__(384, 1)
             bulk_load(aux + L::AUX_COL, col_src, 512, k_full + ks);
             bulk_load(aux + L::AUX_WIN, p.r_tab + (size_t)w.hs * (T + 128) + dist0 * 128, 1024,
                       k_full + ks);
+          };
+          load_aux(0);
+          for (int step = 0; step < w.nsteps; ++step) {
+            const int Y = TRANSPOSED ? (w.X + step) : step;
+            if (step + 1 < w.nsteps) load_aux(step + 1);
             for (int bb = 0; bb < w.nb; ++bb) {
               const int vs = vc % L::VST;
               mbar_wait(v_empty + vs, ((vc / L::VST) & 1) ^ 1, wc, kSiteProdV);
