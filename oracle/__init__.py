@@ -58,6 +58,7 @@ from .calibration import (
     select_heads,
     reconstruction_risk,
     calib_kl_score,
+    sharp_mean_pattern,
 )
 
 __all__ = [
@@ -81,6 +82,7 @@ __all__ = [
     "select_heads",
     "reconstruction_risk",
     "calib_kl_score",
+    "sharp_mean_pattern",
     "marginals",
     "fit_loss",
     "fit_gradient",

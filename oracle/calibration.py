@@ -23,6 +23,7 @@ __all__ = [
     "select_heads",
     "reconstruction_risk",
     "calib_kl_score",
+    "sharp_mean_pattern",
 ]
 
 
@@ -93,3 +94,21 @@ def calib_kl_score(A: np.ndarray, A_hat: np.ndarray | None = None) -> float:
         m = A[n] > 0
         total += float((A[n][m] * (np.log(A[n][m]) - np.log(A_hat[m]))).sum())
     return total / (N * T)
+
+
+def sharp_mean_pattern(L: np.ndarray) -> np.ndarray:
+    """The sharp-mean fixed pattern of one head (one of the candidate fixed
+    patterns listed with the probability mean in §3, compared in §5.1 /
+    Fig. 3): the pre-softmax logits are
+    averaged over the N samples first, and each row of that mean then goes
+    through a causal softmax.  L: [N, T, T]; only j <= i is read.  Returns
+    [T, T] with exact zeros above the diagonal."""
+    L = np.asarray(L, dtype=np.float64)
+    N, T, _ = L.shape
+    M = L.sum(axis=0) / N
+    P = np.zeros((T, T))
+    for i in range(T):
+        row = M[i, : i + 1]
+        e = np.exp(row - row.max())
+        P[i, : i + 1] = e / e.sum()
+    return P

@@ -113,3 +113,37 @@ def test_kl_score_is_nonnegative_and_permutation_invariant():
     s = oracle.calib_kl_score(A)
     assert s > 0
     assert abs(oracle.calib_kl_score(A[RNG.permutation(9)]) - s) < 1e-14
+
+
+def test_sharp_mean_reduces_to_the_library_softmax_for_one_sample():
+    # N = 1: the mean of the logits is the logits; compare with torch's softmax
+    import torch
+    T = 9
+    L = RNG.normal(size=(1, T, T)) * 3.0
+    mask = np.tril(np.ones((T, T), dtype=bool))
+    ref = torch.softmax(torch.from_numpy(np.where(mask, L[0], -np.inf)), dim=-1).numpy()
+    np.testing.assert_allclose(oracle.sharp_mean_pattern(L), ref, rtol=1e-13, atol=1e-15)
+
+
+def test_sharp_mean_closed_form_and_jensen_gap():
+    # T = 2, row 1: logits (0, 0) and (2, 0) average to (1, 0), so the pattern
+    # row is (e, 1) / (e + 1); the post-softmax mean of the same two rows is
+    # ((1/2 + e^2/(e^2 + 1)) / 2, ...), which differs.
+    L = np.zeros((2, 2, 2))
+    L[1, 1, 0] = 2.0
+    P = oracle.sharp_mean_pattern(L)
+    e = np.e
+    np.testing.assert_allclose(P, [[1.0, 0.0], [e / (e + 1), 1 / (e + 1)]], rtol=1e-14)
+    soft = 0.5 * (0.5 + e * e / (e * e + 1))
+    assert abs(P[1, 0] - soft) > 1e-3
+
+
+def test_sharp_mean_rows_are_causal_distributions_and_shift_invariant():
+    T = 11
+    L = RNG.normal(size=(4, T, T))
+    P = oracle.sharp_mean_pattern(L)
+    np.testing.assert_allclose(P.sum(axis=1), 1.0, rtol=1e-13)
+    assert np.all(np.triu(P, 1) == 0)
+    # adding a per-(sample, row) constant to the logits changes nothing
+    shift = RNG.normal(size=(4, T, 1))
+    np.testing.assert_allclose(oracle.sharp_mean_pattern(L + shift), P, rtol=1e-12, atol=1e-15)
