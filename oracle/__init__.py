@@ -37,6 +37,8 @@ from .attention import (
     static_head_bwd,
     hybrid_attn_fwd,
     hybrid_attn_bwd,
+    gqa_hybrid_attn_fwd,
+    gqa_hybrid_attn_bwd,
     dynamic_head_fwd_rows,
     static_head_fwd_rows,
     dynamic_head_bwd_rows,
@@ -71,6 +73,8 @@ __all__ = [
     "static_head_bwd",
     "hybrid_attn_fwd",
     "hybrid_attn_bwd",
+    "gqa_hybrid_attn_fwd",
+    "gqa_hybrid_attn_bwd",
     "dynamic_head_fwd_rows",
     "static_head_fwd_rows",
     "dynamic_head_bwd_rows",

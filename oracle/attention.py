@@ -216,6 +216,43 @@ def hybrid_attn_bwd(Q, K, V, alpha, rho, head_is_static, dout,
     return dQ, dK, dV, dalpha, drho
 
 
+def _kv_expand(X, H):
+    """[B, H_kv, T, d] -> [B, H, T, d]: kv head c serves query heads
+    c*g .. c*g + g - 1, g = H / H_kv."""
+    X = _as64(X)
+    H_kv = X.shape[1]
+    if H % H_kv != 0:
+        raise ValueError("H must be a multiple of H_kv")
+    return np.repeat(X, H // H_kv, axis=1)
+
+
+def gqa_hybrid_attn_fwd(Q, K, V, alpha, rho, head_is_static):
+    """Grouped-query form of the hybrid layer (the GQA path of §3.3 / App. D.2:
+    K and V are shared by groups of query heads, so freezing a query head
+    removes only its query path and it still mixes its group's V).
+
+    Q: [B, H, T, d_h]; K, V: [B, H_kv, T, d_h], H a multiple of H_kv; query
+    head h reads kv head h // (H / H_kv).  Same outputs as hybrid_attn_fwd.
+    """
+    H = np.asarray(Q).shape[1]
+    return hybrid_attn_fwd(Q, _kv_expand(K, H), _kv_expand(V, H), alpha, rho, head_is_static)
+
+
+def gqa_hybrid_attn_bwd(Q, K, V, alpha, rho, head_is_static, dout, want_param_grads=True):
+    """Gradients of sum(dout * out) for the grouped-query layer: dK and dV of a
+    kv head are the sums over the query heads it serves ([B, H_kv, T, d_h]);
+    dQ, dalpha, drho are per query head, as in hybrid_attn_bwd."""
+    Q = _as64(Q)
+    B, H, T, d = Q.shape
+    H_kv = np.asarray(K).shape[1]
+    dQ, dKe, dVe, da, dr = hybrid_attn_bwd(Q, _kv_expand(K, H), _kv_expand(V, H), alpha, rho,
+                                           head_is_static, dout, want_param_grads)
+    g = H // H_kv
+    dK = dKe.reshape(B, H_kv, g, T, d).sum(axis=2)
+    dV = dVe.reshape(B, H_kv, g, T, d).sum(axis=2)
+    return dQ, dK, dV, da, dr
+
+
 # --------------------------------------------------------------------------
 # Row-restricted forms (the same definitions evaluated on a subset of query
 # rows), for spot checks of full-size outputs.
