@@ -38,6 +38,7 @@ EXPORTED = (
     "saf_calib_num_select",
     "saf_calib_finalize",
     "saf_calib_finalize_kl",
+    "saf_calib_finalize_sharp",
     "saf_fit_compact",
     "saf_calib_reset",
     "saf_calib_destroy",
@@ -52,7 +53,7 @@ EXPORTED = (
 
 class saf_attn_dims(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("T", ctypes.c_int),
-                ("d_h", ctypes.c_int), ("dtype", ctypes.c_int)]
+                ("d_h", ctypes.c_int), ("dtype", ctypes.c_int), ("H_kv", ctypes.c_int)]
 
 
 class SafError(RuntimeError):
@@ -92,6 +93,8 @@ _lib.saf_calib_create_ex.argtypes = [ctypes.POINTER(_vp), _i, _i, ctypes.c_uint]
 _lib.saf_calib_create_ex.restype = _i
 _lib.saf_calib_finalize_kl.argtypes = [_vp, _i, _vp, _vp, _vp]
 _lib.saf_calib_finalize_kl.restype = _i
+_lib.saf_calib_finalize_sharp.argtypes = [_vp, _vp, _vp]
+_lib.saf_calib_finalize_sharp.restype = _i
 _lib.saf_calib_accumulate.argtypes = [_vp, _vp, _i, _i, _i, _vp]
 _lib.saf_calib_accumulate.restype = _i
 _lib.saf_calib_num_select.argtypes = [ctypes.c_double, _i]
@@ -123,8 +126,8 @@ def lib():
     return _lib
 
 
-def _dims(B, H, T, d_h, dtype):
-    return saf_attn_dims(int(B), int(H), int(T), int(d_h), int(dtype))
+def _dims(B, H, T, d_h, dtype, H_kv=0):
+    return saf_attn_dims(int(B), int(H), int(T), int(d_h), int(dtype), int(H_kv))
 
 
 def saf_status_string(status: int) -> str:
@@ -188,6 +191,10 @@ def saf_calib_create_ex(num_heads: int, T: int, flags: int):
 
 def saf_calib_finalize_kl(handle, k, s_kl, selected, stream) -> int:
     return _lib.saf_calib_finalize_kl(handle, int(k), s_kl, selected, stream)
+
+
+def saf_calib_finalize_sharp(handle, pattern, stream) -> int:
+    return _lib.saf_calib_finalize_sharp(handle, pattern, stream)
 
 
 def saf_calib_accumulate(handle, A, n, head_begin, head_count, stream) -> int:

@@ -35,16 +35,18 @@ class HybridAttention:
 
     ``head_is_static`` marks the frozen heads (host booleans, length H).
     ``dtype`` is torch.bfloat16 or torch.float32 (fp32 I/O is computed in
-    bf16 inside the library).
+    bf16 inside the library).  ``H_kv`` < H groups the K/V heads: query head
+    h reads K/V head h // (H // H_kv), and K, V, dK, dV are [B, H_kv, T, d_h].
     """
 
     def __init__(self, B_: int, H: int, T: int, d_h: int, head_is_static,
-                 dtype=torch.bfloat16, device="cuda", want_param_grads=False):
+                 dtype=torch.bfloat16, device="cuda", want_param_grads=False, H_kv=None):
         self.shape = (B_, H, T, d_h)
+        self.H_kv = H if H_kv is None else H_kv
         self.dtype = dtype
         self.device = torch.device(device)
         code = B.SAF_BF16 if dtype == torch.bfloat16 else B.SAF_F32
-        self.dims = B._dims(B_, H, T, d_h, code)
+        self.dims = B._dims(B_, H, T, d_h, code, self.H_kv)
         self.head_is_static = bytes(np.asarray(head_is_static, dtype=np.uint8).tolist())
         assert len(self.head_is_static) == H
         self.ws_bytes = B.saf_hybrid_attn_workspace_size(self.dims, int(want_param_grads))
@@ -68,8 +70,8 @@ class HybridAttention:
                  grads=None):
         B_, H, T, d = self.shape
         if grads is None:
-            mk = lambda: torch.empty((B_, H, T, d), dtype=self.dtype, device=self.device)
-            dq, dk, dv = mk(), mk(), mk()
+            mk = lambda h: torch.empty((B_, h, T, d), dtype=self.dtype, device=self.device)
+            dq, dk, dv = mk(H), mk(self.H_kv), mk(self.H_kv)
             da = dr = None
             if want_param_grads:
                 da = torch.empty((H, T), dtype=torch.float32, device=self.device)
@@ -122,6 +124,15 @@ class Calibration:
         st = B.saf_calib_finalize_kl(self.handle, k, _ptr(s_kl), _ptr(sel), _stream(self.device))
         _check(st, "saf_calib_finalize_kl")
         return s_kl, sel[:k]
+
+    def finalize_sharp(self):
+        """Sharp-mean pattern [num_heads, T, T] of a handle fed logits: the
+        causal softmax of each row of the logits' mean."""
+        out = torch.empty((self.num_heads, self.T, self.T), dtype=torch.float32,
+                          device=self.device)
+        st = B.saf_calib_finalize_sharp(self.handle, _ptr(out), _stream(self.device))
+        _check(st, "saf_calib_finalize_sharp")
+        return out
 
     def reset(self):
         _check(B.saf_calib_reset(self.handle), "saf_calib_reset")

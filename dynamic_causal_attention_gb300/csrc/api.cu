@@ -133,14 +133,18 @@ bool encode_rows_f32(CUtensorMap* m, const void* base, uint64_t rows, int d) {
 struct WsLayout {
   size_t status, a_tab, r_tab, row_tab, logZ, mode;
   size_t q16, k16, v16, o16, do16, dq16, dk16, dv16;
-  size_t Dvec, lse2, Dsum, dq_acc;
+  size_t Dvec, lse2, Dsum, dq_acc, dv_acc;
   size_t total;
 };
+
+int kv_heads(const saf_attn_dims& d) { return d.H_kv > 0 ? d.H_kv : d.H; }
 
 WsLayout ws_layout(const saf_attn_dims& d) {
   WsLayout L;
   const size_t B = d.B, H = d.H, T = d.T, D = d.d_h;
+  const size_t Hkv = (size_t)kv_heads(d);
   const size_t elems = B * H * T * D;
+  const size_t elems_kv = B * Hkv * T * D;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t o = off;
@@ -155,18 +159,21 @@ WsLayout ws_layout(const saf_attn_dims& d) {
   L.mode = take(H * 4);
   const bool f32 = d.dtype == SAF_F32;
   const size_t stage = f32 ? elems * 2 : 0;
+  const size_t stage_kv = f32 ? elems_kv * 2 : 0;
   L.q16 = take(stage);
-  L.k16 = take(stage);
-  L.v16 = take(stage);
+  L.k16 = take(stage_kv);
+  L.v16 = take(stage_kv);
   L.o16 = take(stage);
   L.do16 = take(stage);
   L.dq16 = take(stage);
-  L.dk16 = take(stage);
-  L.dv16 = take(stage);
+  L.dk16 = take(stage_kv);
+  L.dv16 = take(stage_kv);
   L.Dvec = take(B * H * T * 4);
   L.lse2 = take(B * H * T * 4);
   L.Dsum = take(H * T * 4);
   L.dq_acc = take(elems * 4);
+  // grouped K/V: the frozen query heads' dV, summed per K/V head in fp32
+  L.dv_acc = take(Hkv < H ? elems_kv * 4 : 0);
   L.total = off;
   return L;
 }
@@ -175,6 +182,7 @@ saf_status check_dims(const saf_attn_dims* d) {
   if (!d) return SAF_ERR_INVALID_ARG;
   if (d->B < 1 || d->H < 1 || d->T < 1 || d->d_h < 1) return SAF_ERR_INVALID_ARG;
   if (d->dtype != SAF_BF16 && d->dtype != SAF_F32) return SAF_ERR_INVALID_ARG;
+  if (d->H_kv < 0 || (d->H_kv > 0 && d->H % d->H_kv != 0)) return SAF_ERR_INVALID_ARG;
   if (d->H > kMaxHeads) return SAF_ERR_UNSUPPORTED;
   if (d->T % 128 != 0 || d->T > kMaxT) return SAF_ERR_UNSUPPORTED;
   if (d->d_h != 32 && d->d_h != 64 && d->d_h != 128) return SAF_ERR_UNSUPPORTED;
@@ -233,6 +241,8 @@ void fill_fwd_params(FwdParams& p, const saf_attn_dims& d, const HeadSplit& hs, 
   p.H = d.H;
   p.T = d.T;
   p.nI = d.T / 128;
+  p.H_kv = kv_heads(d);
+  p.group_kv = d.H / p.H_kv;
   p.n_static = hs.n_static;
   p.n_dynamic = transposed ? 0 : hs.n_dynamic;
   p.group = static_group(d.d_h, d.B);
@@ -315,6 +325,7 @@ saf_status saf_hybrid_attn_fwd(const saf_attn_dims* dims, const void* Q, const v
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const size_t elems = (size_t)d.B * d.H * d.T * d.d_h;
+  const size_t elems_kv = (size_t)d.B * kv_heads(d) * d.T * d.d_h;
   SAF_TRY(cudaMemsetAsync(ws + L.status, 0, sizeof(int), s));
 
   const void *q16 = Q, *k16 = K, *v16 = V;
@@ -322,9 +333,9 @@ saf_status saf_hybrid_attn_fwd(const saf_attn_dims* dims, const void* Q, const v
   if (d.dtype == SAF_F32) {
     if (hs.n_dynamic > 0) {
       SAF_TRY(launch_f32_to_bf16(static_cast<const float*>(Q), ws + L.q16, elems, s));
-      SAF_TRY(launch_f32_to_bf16(static_cast<const float*>(K), ws + L.k16, elems, s));
+      SAF_TRY(launch_f32_to_bf16(static_cast<const float*>(K), ws + L.k16, elems_kv, s));
     }
-    SAF_TRY(launch_f32_to_bf16(static_cast<const float*>(V), ws + L.v16, elems, s));
+    SAF_TRY(launch_f32_to_bf16(static_cast<const float*>(V), ws + L.v16, elems_kv, s));
     q16 = ws + L.q16;
     k16 = ws + L.k16;
     v16 = ws + L.v16;
@@ -338,11 +349,12 @@ saf_status saf_hybrid_attn_fwd(const saf_attn_dims* dims, const void* Q, const v
   fl.p.out = static_cast<__nv_bfloat16*>(o16);
   fl.p.lse = lse;
   const uint64_t rows = (uint64_t)d.B * d.H * d.T;
+  const uint64_t rows_kv = (uint64_t)d.B * kv_heads(d) * d.T;
   // Q/K maps must be valid descriptors even when only static heads exist.
-  const void* qb = q16 ? q16 : v16;
+  const void* qb = q16 ? q16 : o16;
   const void* kb = k16 ? k16 : v16;
-  if (!encode_rows(&fl.tm_q, qb, rows, d.d_h) || !encode_rows(&fl.tm_k, kb, rows, d.d_h) ||
-      !encode_rows(&fl.tm_v, v16, rows, d.d_h))
+  if (!encode_rows(&fl.tm_q, qb, rows, d.d_h) || !encode_rows(&fl.tm_k, kb, rows_kv, d.d_h) ||
+      !encode_rows(&fl.tm_v, v16, rows_kv, d.d_h))
     return SAF_ERR_CUDA;
   fl.d_h = d.d_h;
   fl.transposed = false;
@@ -379,18 +391,28 @@ saf_status saf_hybrid_attn_bwd(const saf_attn_dims* dims, const void* Q, const v
   if (ws_bytes < L.total) return SAF_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int Hkv = kv_heads(d), gkv = d.H / Hkv;
   const size_t elems = (size_t)d.B * d.H * d.T * d.d_h;
+  const size_t elems_kv = (size_t)d.B * Hkv * d.T * d.d_h;
   const uint64_t rows = (uint64_t)d.B * d.H * d.T;
+  const uint64_t rows_kv = (uint64_t)d.B * Hkv * d.T;
   SAF_TRY(cudaMemsetAsync(ws + L.status, 0, sizeof(int), s));
+
+  // K/V heads: which serve dynamic query heads, which serve frozen ones
+  uint8_t kv_has_dyn[kMaxHeads], kv_has_static[kMaxHeads];
+  memset(kv_has_dyn, 0, sizeof(kv_has_dyn));
+  memset(kv_has_static, 0, sizeof(kv_has_static));
+  for (int h = 0; h < d.H; ++h) (hs.is_static[h] ? kv_has_static : kv_has_dyn)[h / gkv] = 1;
+  float* dv_acc = (gkv > 1 && hs.n_static > 0) ? reinterpret_cast<float*>(ws + L.dv_acc) : nullptr;
 
   const void *q16 = Q, *k16 = K, *v16 = V, *o16 = out, *do16 = dout;
   void *dq16 = dQ, *dk16 = dK, *dv16 = dV;
   if (d.dtype == SAF_F32) {
     if (hs.n_dynamic > 0) {
       SAF_TRY(launch_f32_to_bf16(static_cast<const float*>(Q), ws + L.q16, elems, s));
-      SAF_TRY(launch_f32_to_bf16(static_cast<const float*>(K), ws + L.k16, elems, s));
+      SAF_TRY(launch_f32_to_bf16(static_cast<const float*>(K), ws + L.k16, elems_kv, s));
     }
-    SAF_TRY(launch_f32_to_bf16(static_cast<const float*>(V), ws + L.v16, elems, s));
+    SAF_TRY(launch_f32_to_bf16(static_cast<const float*>(V), ws + L.v16, elems_kv, s));
     SAF_TRY(launch_f32_to_bf16(static_cast<const float*>(out), ws + L.o16, elems, s));
     SAF_TRY(launch_f32_to_bf16(static_cast<const float*>(dout), ws + L.do16, elems, s));
     q16 = ws + L.q16;
@@ -420,36 +442,16 @@ saf_status saf_hybrid_attn_bwd(const saf_attn_dims* dims, const void* Q, const v
   pre.dq_acc = hs.n_dynamic > 0 ? dq_acc : nullptr;
   SAF_TRY(launch_bwd_pre(pre, s));
 
-  if (hs.n_dynamic > 0) {
-    BwdLaunch bl;
-    memset(&bl, 0, sizeof(bl));
-    BwdParams& p = bl.p;
-    p.B = d.B; p.H = d.H; p.T = d.T; p.nI = d.T / 128;
-    p.n_dynamic = hs.n_dynamic;
-    p.n_items = p.nI * d.B * hs.n_dynamic;
-    p.scale = 1.0f / sqrtf((float)d.d_h);
-    p.scale_log2 = 1.4426950408889634f * p.scale;
-    memcpy(p.dynamic_heads, hs.dy, sizeof(p.dynamic_heads));
-    p.lse2 = pre.lse2;
-    p.Dvec = pre.Dvec;
-    p.dq_acc = dq_acc;
-    p.dK = static_cast<__nv_bfloat16*>(dk16);
-    p.dV = static_cast<__nv_bfloat16*>(dv16);
-    p.status = reinterpret_cast<int*>(ws + L.status);
-    if (!encode_rows(&bl.tm_q, q16, rows, d.d_h) || !encode_rows(&bl.tm_k, k16, rows, d.d_h) ||
-        !encode_rows(&bl.tm_v, v16, rows, d.d_h) || !encode_rows(&bl.tm_do, do16, rows, d.d_h) ||
-        !encode_rows_f32(&bl.tm_dq, dq_acc, rows, d.d_h))
-      return SAF_ERR_CUDA;
-    bl.d_h = d.d_h;
-    bl.num_sms = sm_count();
-    SAF_TRY(launch_bwd_dynamic(bl, s));
-  }
   if (hs.n_static > 0) {
-    // dV = P^T dO for the frozen heads: the forward's static engine, transposed.
+    // dV = P^T dO for the frozen heads: the forward's static engine,
+    // transposed.  With grouped K/V it adds into an fp32 sum per K/V head,
+    // which the dynamic pass (or the post-pass) folds into dV.
+    if (dv_acc) SAF_TRY(cudaMemsetAsync(dv_acc, 0, elems_kv * sizeof(float), s));
     FwdLaunch fl;
     memset(&fl, 0, sizeof(fl));
     fill_fwd_params(fl.p, d, hs, ws, L, true);
     fl.p.out = static_cast<__nv_bfloat16*>(dv16);
+    fl.p.out_acc = dv_acc;
     fl.p.lse = nullptr;
     if (!encode_rows(&fl.tm_q, do16, rows, d.d_h) || !encode_rows(&fl.tm_k, do16, rows, d.d_h) ||
         !encode_rows(&fl.tm_v, do16, rows, d.d_h))
@@ -459,6 +461,39 @@ saf_status saf_hybrid_attn_bwd(const saf_attn_dims* dims, const void* Q, const v
     fl.num_sms = sm_count();
     SAF_TRY(launch_hybrid_fwd(fl, s));
   }
+  if (hs.n_dynamic > 0) {
+    BwdLaunch bl;
+    memset(&bl, 0, sizeof(bl));
+    BwdParams& p = bl.p;
+    p.B = d.B; p.H = d.H; p.T = d.T; p.nI = d.T / 128;
+    p.H_kv = Hkv;
+    int nd = 0;
+    for (int kv = 0; kv < Hkv; ++kv) {
+      p.dyn_begin[kv] = (uint16_t)nd;
+      for (int h = kv * gkv; h < (kv + 1) * gkv; ++h)
+        if (!hs.is_static[h]) p.dyn_by_kv[nd++] = (uint8_t)h;
+      p.dyn_count[kv] = (uint16_t)(nd - p.dyn_begin[kv]);
+      if (p.dyn_count[kv] > 0) p.kv_list[p.n_kv++] = (uint8_t)kv;
+      p.kv_has_static[kv] = kv_has_static[kv];
+    }
+    p.n_items = p.nI * d.B * p.n_kv;
+    p.scale = 1.0f / sqrtf((float)d.d_h);
+    p.scale_log2 = 1.4426950408889634f * p.scale;
+    p.dv_acc = dv_acc;
+    p.lse2 = pre.lse2;
+    p.Dvec = pre.Dvec;
+    p.dq_acc = dq_acc;
+    p.dK = static_cast<__nv_bfloat16*>(dk16);
+    p.dV = static_cast<__nv_bfloat16*>(dv16);
+    p.status = reinterpret_cast<int*>(ws + L.status);
+    if (!encode_rows(&bl.tm_q, q16, rows, d.d_h) || !encode_rows(&bl.tm_k, k16, rows_kv, d.d_h) ||
+        !encode_rows(&bl.tm_v, v16, rows_kv, d.d_h) || !encode_rows(&bl.tm_do, do16, rows, d.d_h) ||
+        !encode_rows_f32(&bl.tm_dq, dq_acc, rows, d.d_h))
+      return SAF_ERR_CUDA;
+    bl.d_h = d.d_h;
+    bl.num_sms = sm_count();
+    SAF_TRY(launch_bwd_dynamic(bl, s));
+  }
   if (dalpha) {
     SAF_TRY(launch_zero_u32(dalpha, (size_t)d.H * d.T, s));
     SAF_TRY(launch_zero_u32(drho, (size_t)d.H * d.T, s));
@@ -467,6 +502,8 @@ saf_status saf_hybrid_attn_bwd(const saf_attn_dims* dims, const void* Q, const v
       memset(&gl, 0, sizeof(gl));
       ParamGradParams& p = gl.p;
       p.B = d.B; p.H = d.H; p.T = d.T; p.nI = d.T / 128;
+      p.H_kv = Hkv;
+      p.group_kv = gkv;
       p.n_static = hs.n_static;
       p.n_items = hs.n_static * p.nI;
       memcpy(p.static_heads, hs.st, sizeof(p.static_heads));
@@ -478,7 +515,7 @@ saf_status saf_hybrid_attn_bwd(const saf_attn_dims* dims, const void* Q, const v
       p.dalpha = dalpha;
       p.drho = drho;
       p.status = reinterpret_cast<int*>(ws + L.status);
-      if (!encode_rows(&gl.tm_v, v16, rows, d.d_h) || !encode_rows(&gl.tm_do, do16, rows, d.d_h))
+      if (!encode_rows(&gl.tm_v, v16, rows_kv, d.d_h) || !encode_rows(&gl.tm_do, do16, rows, d.d_h))
         return SAF_ERR_CUDA;
       gl.d_h = d.d_h;
       gl.num_sms = sm_count();
@@ -487,16 +524,19 @@ saf_status saf_hybrid_attn_bwd(const saf_attn_dims* dims, const void* Q, const v
   }
   BwdPost post;
   memset(&post, 0, sizeof(post));
-  post.B = d.B; post.H = d.H; post.T = d.T; post.d_h = d.d_h;
+  post.B = d.B; post.H = d.H; post.T = d.T; post.d_h = d.d_h; post.H_kv = Hkv;
   post.dq_acc = dq_acc;
   post.dQ = static_cast<__nv_bfloat16*>(dq16);
   post.dK = static_cast<__nv_bfloat16*>(dk16);
+  post.dV = static_cast<__nv_bfloat16*>(dv16);
+  post.dv_acc = dv_acc;
   memcpy(post.is_static, hs.is_static, sizeof(post.is_static));
+  for (int kv = 0; kv < Hkv; ++kv) post.kv_no_dyn[kv] = kv_has_dyn[kv] ? 0 : 1;
   SAF_TRY(launch_bwd_post(post, s));
   if (d.dtype == SAF_F32) {
     SAF_TRY(launch_bf16_to_f32(dq16, static_cast<float*>(dQ), elems, s));
-    SAF_TRY(launch_bf16_to_f32(dk16, static_cast<float*>(dK), elems, s));
-    SAF_TRY(launch_bf16_to_f32(dv16, static_cast<float*>(dV), elems, s));
+    SAF_TRY(launch_bf16_to_f32(dk16, static_cast<float*>(dK), elems_kv, s));
+    SAF_TRY(launch_bf16_to_f32(dv16, static_cast<float*>(dV), elems_kv, s));
   }
   return SAF_OK;
 }
@@ -627,6 +667,18 @@ saf_status saf_calib_finalize_kl(void* handle, int k, float* s_kl, int32_t* sele
   p.selected = selected;
   p.ent = h->ent;
   return cuda_status(launch_calib_finalize_kl(p, static_cast<cudaStream_t>(stream)));
+}
+
+saf_status saf_calib_finalize_sharp(void* handle, float* pattern, void* stream) {
+  g_launches = 0;
+  CalibHandle* h = static_cast<CalibHandle*>(handle);
+  if (!h || !pattern) return SAF_ERR_INVALID_ARG;
+  const int N = h->counts[0];
+  for (int c : h->counts)
+    if (c != N) return SAF_ERR_STATE;
+  if (N < 1) return SAF_ERR_STATE;
+  return cuda_status(
+      launch_calib_sharp(h->mean, h->num_heads, h->T, pattern, static_cast<cudaStream_t>(stream)));
 }
 
 saf_status saf_fit_compact(const float* A_hat, int num_heads, int T, const int32_t* candidates,

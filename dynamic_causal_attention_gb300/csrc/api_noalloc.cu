@@ -119,6 +119,8 @@ extern "C" saf_status saf_hybrid_attn_fwd_noalloc(const saf_attn_dims* dims, con
   if (d.H > kMaxHeads || d.T % 128 != 0 || d.T > 16384) return SAF_ERR_UNSUPPORTED;
   if (d.d_h != 32 && d.d_h != 64 && d.d_h != 128) return SAF_ERR_UNSUPPORTED;
   if ((uint64_t)d.B * d.H * d.T >= (1ull << 31)) return SAF_ERR_UNSUPPORTED;
+  if (d.H_kv < 0 || (d.H_kv > 0 && d.H % d.H_kv != 0)) return SAF_ERR_INVALID_ARG;
+  const int Hkv = d.H_kv > 0 ? d.H_kv : d.H;
   int n_static = 0, n_dynamic = 0;
   uint8_t st[kMaxHeads], dy[kMaxHeads];
   for (int h = 0; h < d.H; ++h) {
@@ -165,6 +167,8 @@ extern "C" saf_status saf_hybrid_attn_fwd_noalloc(const saf_attn_dims* dims, con
   p.H = d.H;
   p.T = d.T;
   p.nI = d.T / 128;
+  p.H_kv = Hkv;
+  p.group_kv = d.H / Hkv;
   p.n_static = n_static;
   p.n_dynamic = n_dynamic;
   p.group = static_group(d.d_h, d.B);
@@ -182,10 +186,11 @@ extern "C" saf_status saf_hybrid_attn_fwd_noalloc(const saf_attn_dims* dims, con
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
   const uint64_t rows = (uint64_t)d.B * d.H * d.T;
-  const void* qb = Q ? Q : V;
+  const uint64_t rows_kv = (uint64_t)d.B * Hkv * d.T;
+  const void* qb = Q ? Q : out;
   const void* kb = K ? K : V;
-  if (!encode_rows_na(&fl.tm_q, qb, rows, d.d_h) || !encode_rows_na(&fl.tm_k, kb, rows, d.d_h) ||
-      !encode_rows_na(&fl.tm_v, V, rows, d.d_h))
+  if (!encode_rows_na(&fl.tm_q, qb, rows, d.d_h) || !encode_rows_na(&fl.tm_k, kb, rows_kv, d.d_h) ||
+      !encode_rows_na(&fl.tm_v, V, rows_kv, d.d_h))
     return SAF_ERR_CUDA;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||

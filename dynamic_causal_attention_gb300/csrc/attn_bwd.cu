@@ -99,19 +99,32 @@ enum : int {
   kSiteBAlign
 };
 
+// Item (b, K/V head kv, key tile J): the query tiles I = J..nI-1 of every
+// dynamic query head that K/V head serves, head by head; dK_J and dV_J
+// collect all of them.
 struct BItem {
-  int b, h, J, nsteps;
+  int b, kv, J, span, db, nsteps;  // span = nI - J query tiles per head
 };
 
 __device__ __forceinline__ BItem decode_bwd(const BwdParams& p, int it) {
   BItem r;
-  const int per = p.B * p.n_dynamic;
+  const int per = p.B * p.n_kv;
   r.J = it / per;
   const int rem = it - r.J * per;
-  r.b = rem / p.n_dynamic;
-  r.h = p.dynamic_heads[rem - r.b * p.n_dynamic];
-  r.nsteps = p.nI - r.J;
+  r.b = rem / p.n_kv;
+  r.kv = p.kv_list[rem - r.b * p.n_kv];
+  r.span = p.nI - r.J;
+  r.db = p.dyn_begin[r.kv];
+  r.nsteps = p.dyn_count[r.kv] * r.span;
   return r;
+}
+
+// Query head and query tile of step t of an item.
+__device__ __forceinline__ void step_of(const BwdParams& p, const BItem& w, int t, int& hq,
+                                        int& I) {
+  const int q = t / w.span;
+  hq = p.dyn_by_kv[w.db + q];
+  I = w.J + (t - q * w.span);
 }
 
 // Threads: warp 0 TMA producer, warp 1 MMA issuer (for d_h <= 64 only the
@@ -198,18 +211,20 @@ __global__ void __launch_bounds__(512, 1)
       uint32_t kvc = 0, qc = 0;
       for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
         const BItem w = decode_bwd(p, it);
-        const int row0 = (w.b * H + w.h) * T;
+        const int kvrow0 = (w.b * p.H_kv + w.kv) * T;
         mbar_wait(kv_empty, (kvc & 1) ^ 1, wc, kSiteBProdKV);
         ++kvc;
         mbar_arrive_expect_tx(kv_full, 2 * G::TILE_BYTES);
         for (int c = 0; c < G::NCHUNK; ++c) {
           tma_load_2d(smem + L::OFF_K + c * G::CHUNK_BYTES, &tm_k, kv_full, c * G::CHUNK,
-                      row0 + w.J * 128);
+                      kvrow0 + w.J * 128);
           tma_load_2d(smem + L::OFF_V + c * G::CHUNK_BYTES, &tm_v, kv_full, c * G::CHUNK,
-                      row0 + w.J * 128);
+                      kvrow0 + w.J * 128);
         }
         for (int t = 0; t < w.nsteps; ++t) {
-          const int I = w.J + t;
+          int hq, I;
+          step_of(p, w, t, hq, I);
+          const int row0 = (w.b * H + hq) * T;
           const int qs = qc % L::QST;
           mbar_wait(q_empty + qs, ((qc / L::QST) & 1) ^ 1, wc, kSiteBProdQ);
           ++qc;
@@ -396,7 +411,7 @@ __global__ void __launch_bounds__(512, 1)
         const uint32_t nl_a = smem_u32(nl_s);  // -lse2 at +0, -D at +512 bytes
         mbar_wait(s_full, sc & 1, wc, kSiteBCmpS);
         tc_fence_after();
-        const bool diag = (t == 0);
+        const bool diag = (t % w.span == 0);  // I == J: the causal diagonal
         if constexpr (L::PS) {
           // Four 16-column chunks; the TMEM loads of chunk k + 1 are issued
           // right after chunk k's have landed, so they fly while chunk k is
@@ -523,8 +538,11 @@ __global__ void __launch_bounds__(512, 1)
       // epilogue: half 0 writes dV_J, half 1 writes dK_J (scaled)
       mbar_wait(kd_full, kdc & 1, wc, kSiteBCmpKD);
       tc_fence_after();
-      const size_t orow = (size_t)(w.b * H + w.h) * T + (size_t)w.J * 128 + r;
+      const size_t orow = (size_t)(w.b * p.H_kv + w.kv) * T + (size_t)w.J * 128 + r;
       __nv_bfloat16* dst = (hf == 0 ? p.dV : p.dK) + orow * D;
+      // frozen query heads of this K/V head added their dV in fp32 beforehand
+      const float* addv =
+          (hf == 0 && p.dv_acc && p.kv_has_static[w.kv]) ? p.dv_acc + orow * D : nullptr;
       const float sc_out = hf == 0 ? 1.0f : p.scale;
       const uint32_t colb = hf == 0 ? L::T_DV : L::T_DK;
 #pragma unroll
@@ -532,6 +550,16 @@ __global__ void __launch_bounds__(512, 1)
         uint32_t o[16];
         tmem_ld_x16(trow + colb + c0, o);
         tmem_wait_ld(o);
+        if (addv) {
+#pragma unroll
+          for (int e = 0; e < 16; e += 4) {
+            const float4 a = *reinterpret_cast<const float4*>(addv + c0 + e);
+            o[e] = __float_as_uint(__uint_as_float(o[e]) + a.x);
+            o[e + 1] = __float_as_uint(__uint_as_float(o[e + 1]) + a.y);
+            o[e + 2] = __float_as_uint(__uint_as_float(o[e + 2]) + a.z);
+            o[e + 3] = __float_as_uint(__uint_as_float(o[e + 3]) + a.w);
+          }
+        }
         uint4 v0, v1;
         v0.x = pack_bf16x2(__uint_as_float(o[0]) * sc_out, __uint_as_float(o[1]) * sc_out);
         v0.y = pack_bf16x2(__uint_as_float(o[2]) * sc_out, __uint_as_float(o[3]) * sc_out);
@@ -556,7 +584,8 @@ __global__ void __launch_bounds__(512, 1)
     for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
       const BItem w = decode_bwd(p, it);
       for (int t = 0; t < w.nsteps; ++t) {
-        const int I = w.J + t;
+        int hq, I;
+        step_of(p, w, t, hq, I);
         mbar_wait(dq_full, dqc & 1, wc, kSiteBDq);
         tc_fence_after();
         if constexpr (L::DQ_TMA) {
@@ -573,7 +602,7 @@ __global__ void __launch_bounds__(512, 1)
           tc_fence_before();
           mbar_arrive(dq_empty);
           const uint32_t stg = smem_u32(smem + L::OFF_DQS);
-          const int row = (w.b * H + w.h) * T + I * 128;
+          const int row = (w.b * H + hq) * T + I * 128;
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             if (r == 0) bulk_wait_group_read0();  // the staging chunk has been read
@@ -590,7 +619,7 @@ __global__ void __launch_bounds__(512, 1)
             }
           }
         } else {
-          float* dst = p.dq_acc + ((size_t)(w.b * H + w.h) * T + (size_t)I * 128 + r) * D;
+          float* dst = p.dq_acc + ((size_t)(w.b * H + hq) * T + (size_t)I * 128 + r) * D;
 #pragma unroll
           for (int c0 = 0; c0 < D; c0 += 16) {
             uint32_t o[16];
@@ -723,11 +752,12 @@ __global__ void __launch_bounds__(384, 1)
             mbar_wait(st_empty + s, ((sc / L::ST) & 1) ^ 1, wc, kSitePgProd);
             ++sc;
             uint8_t* st = smem + L::OFF_ST + s * L::STAGE;
-            const int row0 = (b * H + h) * T;
+            const int row0 = (b * H + h) * T;                          // dO rows
+            const int vrow0 = (b * p.H_kv + h / p.group_kv) * T;      // V rows
             mbar_arrive_expect_tx(st_full + s, 2 * G::TILE_BYTES);
             for (int c = 0; c < G::NCHUNK; ++c) {
               tma_load_2d(st + c * G::CHUNK_BYTES, &tm_v, st_full + s, c * G::CHUNK,
-                          row0 + J * 128);
+                          vrow0 + J * 128);
               tma_load_2d(st + G::TILE_BYTES + c * G::CHUNK_BYTES, &tm_do, st_full + s,
                           c * G::CHUNK, row0 + I * 128);
             }

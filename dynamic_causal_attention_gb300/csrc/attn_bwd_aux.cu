@@ -70,10 +70,26 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(BwdPost p, float scale) {
        t += (size_t)gridDim.x * blockDim.x) {
     const size_t e = t * 8;
     const int h = (int)((e / ((size_t)p.T * D)) % p.H);
+    // the same element index in the [B, H_kv, T, d_h] tensors, while in range
+    if (e < (size_t)p.B * p.H_kv * p.T * D) {
+      const int kv = (int)((e / ((size_t)p.T * D)) % p.H_kv);
+      if (p.kv_no_dyn[kv]) {
+        *reinterpret_cast<uint4*>(p.dK + e) = make_uint4(0u, 0u, 0u, 0u);
+        if (p.dv_acc) {
+          const float4 a = *reinterpret_cast<const float4*>(p.dv_acc + e);
+          const float4 b = *reinterpret_cast<const float4*>(p.dv_acc + e + 4);
+          uint4 v;
+          v.x = pack_bf16x2(a.x, a.y);
+          v.y = pack_bf16x2(a.z, a.w);
+          v.z = pack_bf16x2(b.x, b.y);
+          v.w = pack_bf16x2(b.z, b.w);
+          *reinterpret_cast<uint4*>(p.dV + e) = v;
+        }
+      }
+    }
     uint4 q;
     if (p.is_static[h]) {
       q = make_uint4(0u, 0u, 0u, 0u);
-      *reinterpret_cast<uint4*>(p.dK + e) = q;
     } else {
       const float4 a = *reinterpret_cast<const float4*>(p.dq_acc + e);
       const float4 b = *reinterpret_cast<const float4*>(p.dq_acc + e + 4);

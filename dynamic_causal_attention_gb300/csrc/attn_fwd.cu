@@ -478,7 +478,8 @@ __global__ void __launch_bounds__(384, 1)
       for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
         const Item w = decode_item<TRANSPOSED>(p, it);
         if (!w.is_static) {
-          const int row0 = (w.b * H + w.h) * T;
+          const int row0 = (w.b * H + w.h) * T;                           // Q rows
+          const int kv0 = (w.b * p.H_kv + w.h / p.group_kv) * T;          // K/V rows
           mbar_wait(q_empty, (qc & 1) ^ 1, wc, kSiteProdQ);
           ++qc;
           mbar_arrive_expect_tx(q_full, G::TILE_BYTES);
@@ -492,14 +493,14 @@ __global__ void __launch_bounds__(384, 1)
             mbar_arrive_expect_tx(k_full + ks, G::TILE_BYTES);
             for (int c = 0; c < G::NCHUNK; ++c)
               tma_load_2d(smem + L::OFF_K + ks * G::TILE_BYTES + c * G::CHUNK_BYTES, &tm_k,
-                          k_full + ks, c * G::CHUNK, row0 + j * 128);
+                          k_full + ks, c * G::CHUNK, kv0 + j * 128);
             const int vs = vc % L::VST;
             mbar_wait(v_empty + vs, ((vc / L::VST) & 1) ^ 1, wc, kSiteProdV);
             ++vc;
             mbar_arrive_expect_tx(v_full + vs, G::TILE_BYTES);
             for (int c = 0; c < G::NCHUNK; ++c)
               tma_load_2d(smem + L::OFF_V + vs * G::TILE_BYTES + c * G::CHUNK_BYTES, &tm_v,
-                          v_full + vs, c * G::CHUNK, row0 + j * 128);
+                          v_full + vs, c * G::CHUNK, kv0 + j * 128);
           }
         } else {
           // The tables of a step go into the K ring one step ahead of its V
@@ -530,7 +531,9 @@ __global__ void __launch_bounds__(384, 1)
               mbar_wait(v_empty + vs, ((vc / L::VST) & 1) ^ 1, wc, kSiteProdV);
               ++vc;
               mbar_arrive_expect_tx(v_full + vs, G::TILE_BYTES);
-              const int row0 = ((w.b + bb) * H + w.h) * T;
+              // forward: V of the head's K/V group; transposed: dO of the head
+              const int row0 = TRANSPOSED ? ((w.b + bb) * H + w.h) * T
+                                          : ((w.b + bb) * p.H_kv + w.h / p.group_kv) * T;
               for (int c = 0; c < G::NCHUNK; ++c)
                 tma_load_2d(smem + L::OFF_V + vs * G::TILE_BYTES + c * G::CHUNK_BYTES, &tm_v,
                             v_full + vs, c * G::CHUNK, row0 + Y * 128);
@@ -805,6 +808,24 @@ __global__ void __launch_bounds__(384, 1)
         const int trow_i = w.X * 128 + r;
         for (int bb = 0; bb < w.nb; ++bb) {
           const size_t orow = ((size_t)((w.b + bb) * H + w.h) * T + trow_i);
+          if (TRANSPOSED && p.out_acc) {
+            // grouped K/V: several query heads add into one K/V head's dV
+            const size_t arow =
+                ((size_t)((w.b + bb) * p.H_kv + w.h / p.group_kv) * T + trow_i);
+            float* dst = p.out_acc + arow * D + hf * DH;
+#pragma unroll
+            for (int c0 = 0; c0 < DH; c0 += 16) {
+              uint32_t o[16];
+              tmem_ld_x16(trow + kTmemO + bb * D + hf * DH + c0, o);
+              tmem_wait_ld(o);
+#pragma unroll
+              for (int e = 0; e < 16; e += 4)
+                atomicAdd(reinterpret_cast<float4*>(dst + c0 + e),
+                          make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]),
+                                      __uint_as_float(o[e + 2]), __uint_as_float(o[e + 3])));
+            }
+            continue;
+          }
           __nv_bfloat16* dst = p.out + orow * D + hf * DH;
 #pragma unroll
           for (int c0 = 0; c0 < DH; c0 += 16) {

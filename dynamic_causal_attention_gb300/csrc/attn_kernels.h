@@ -14,6 +14,7 @@ namespace saf {
 // form, which computes dV = P^T dO for the frozen heads).
 struct FwdParams {
   int B, H, T, nI;            // nI = T / 128
+  int H_kv, group_kv;         // K/V heads; query heads per K/V head (1: one each)
   int n_static, n_dynamic;    // head counts
   int group, n_groups;        // sequences per static item, groups per head
   int n_items;
@@ -26,6 +27,8 @@ struct FwdParams {
   const float* logZ;          // [n_static, T]
   const int* mode;            // [n_static]
   __nv_bfloat16* out;         // forward: out; transposed: dV
+  float* out_acc;             // transposed with group_kv > 1: fp32 dV [B, H_kv, T, d_h],
+                              // added to with atomics (out is then unused)
   float* lse;                 // forward only (nullable)
   int* status;                // device status word
 };
@@ -39,7 +42,9 @@ inline int static_group(int d_h, int B) {
 }
 
 struct FwdLaunch {
-  CUtensorMap tm_q, tm_k, tm_v;  // [B*H*T, d_h] bf16 views; tm_v = dO when transposed
+  // bf16 views [B*H*T, d_h] (Q) and [B*H_kv*T, d_h] (K, V); tm_v = dO
+  // ([B*H*T, d_h]) when transposed
+  CUtensorMap tm_q, tm_k, tm_v;
   FwdParams p;
   int d_h;
   bool transposed;
@@ -66,10 +71,18 @@ cudaError_t launch_bwd_pre(const BwdPre& p, cudaStream_t s);
 // Dynamic-head backward (KV-tile parallel).
 struct BwdParams {
   int B, H, T, nI;
-  int n_dynamic, n_items;
+  int H_kv;                   // K/V heads (H: one per query head)
+  int n_kv, n_items;          // K/V heads that serve a dynamic query head; items
   float scale_log2;           // log2(e) / sqrt(d_h)
   float scale;                // 1 / sqrt(d_h)
-  uint8_t dynamic_heads[kMaxHeads];
+  // The dynamic query heads grouped by K/V head: K/V head kv_list[i] serves
+  // dyn_by_kv[dyn_begin[kv] .. dyn_begin[kv] + dyn_count[kv] - 1].
+  uint8_t kv_list[kMaxHeads];
+  uint16_t dyn_begin[kMaxHeads], dyn_count[kMaxHeads];
+  uint8_t dyn_by_kv[kMaxHeads];
+  uint8_t kv_has_static[kMaxHeads];
+  const float* dv_acc;        // [B, H_kv, T, d_h] fp32 dV of the frozen heads, added to
+                              // the dV of K/V heads with kv_has_static (nullable)
   const float* lse2;          // [B, H, T]  -lse * log2(e)
   const float* Dvec;          // [B, H, T]  -D
   float* dq_acc;              // [B, H, T, d_h] fp32, zeroed
@@ -89,6 +102,7 @@ cudaError_t launch_bwd_dynamic(const BwdLaunch& L, cudaStream_t s);
 // Static-head alpha/rho gradients.
 struct ParamGradParams {
   int B, H, T, nI;
+  int H_kv, group_kv;         // V rows of query head h: K/V head h / group_kv
   int n_static, n_items;
   uint8_t static_heads[kMaxHeads];
   const float* a_tab;
@@ -108,13 +122,18 @@ struct ParamGradLaunch {
 };
 cudaError_t launch_param_grads(const ParamGradLaunch& L, cudaStream_t s);
 
-// dQ: fp32 accumulator -> output dtype (scaled); zero dQ/dK rows of static heads.
+// dQ: fp32 accumulator -> output dtype (scaled); zero dQ rows of static
+// heads and dK rows of K/V heads that serve no dynamic head; dV of those K/V
+// heads from the fp32 static accumulator when there is one.
 struct BwdPost {
-  int B, H, T, d_h;
+  int B, H, T, d_h, H_kv;
   const float* dq_acc;
   __nv_bfloat16* dQ;
   __nv_bfloat16* dK;
+  __nv_bfloat16* dV;
+  const float* dv_acc;        // nullable
   uint8_t is_static[kMaxHeads];
+  uint8_t kv_no_dyn[kMaxHeads];
 };
 cudaError_t launch_bwd_post(const BwdPost& p, cudaStream_t s);
 

@@ -175,6 +175,38 @@ __global__ void __launch_bounds__(128) calib_rows_kernel(CalibFinalize p) {
   if (threadIdx.x == 0) p.row_partials[(size_t)h * T + row] = red[0];
 }
 
+// Sharp-mean pattern: one block per (row, head) applies a causal softmax to
+// the row of the running mean of the accumulated logits: maximum, then the
+// sum of exponentials in fp64 (fixed-order block reduction), then the
+// normalised row with exact zeros above the diagonal.
+__global__ void __launch_bounds__(128) calib_sharp_rows_kernel(const float* __restrict__ mean,
+                                                               int T, float* __restrict__ out) {
+  const int row = blockIdx.x, h = blockIdx.y;
+  const size_t base = ((size_t)h * T + row) * (size_t)T;
+  __shared__ float fred[128];
+  __shared__ double dred[128];
+  float mx = -INFINITY;
+  for (int j = threadIdx.x; j <= row; j += blockDim.x) mx = fmaxf(mx, mean[base + j]);
+  fred[threadIdx.x] = mx;
+  __syncthreads();
+  for (int s = 64; s > 0; s >>= 1) {
+    if (threadIdx.x < s) fred[threadIdx.x] = fmaxf(fred[threadIdx.x], fred[threadIdx.x + s]);
+    __syncthreads();
+  }
+  mx = fred[0];
+  double acc = 0.0;
+  for (int j = threadIdx.x; j <= row; j += blockDim.x) acc += (double)expf(mean[base + j] - mx);
+  dred[threadIdx.x] = acc;
+  __syncthreads();
+  for (int s = 64; s > 0; s >>= 1) {
+    if (threadIdx.x < s) dred[threadIdx.x] += dred[threadIdx.x + s];
+    __syncthreads();
+  }
+  const float inv = (float)(1.0 / dred[0]);
+  for (int j = threadIdx.x; j < T; j += blockDim.x)
+    out[base + j] = (j <= row) ? expf(mean[base + j] - mx) * inv : 0.f;
+}
+
 // One block: s_var per head (one warp per head, fixed-order sums) and the
 // exact top-k by rank over the unique 64-bit keys (bits(s_var) << 32 | index).
 constexpr int kMaxCalibHeads = 8192;
@@ -243,6 +275,14 @@ cudaError_t launch_calib_finalize_kl(const CalibFinalize& p, cudaStream_t s) {
   trace_begin(s);
   calib_select_kernel<<<1, 1024, 0, s>>>(p, (double)p.N * (double)p.T);
   trace_end(s, "calib_select");
+  return cudaGetLastError();
+}
+
+cudaError_t launch_calib_sharp(const float* mean, int num_heads, int T, float* out,
+                               cudaStream_t s) {
+  trace_begin(s);
+  calib_sharp_rows_kernel<<<dim3(T, num_heads), 128, 0, s>>>(mean, T, out);
+  trace_end(s, "calib_sharp_rows");
   return cudaGetLastError();
 }
 

@@ -47,6 +47,9 @@ struct CalibFinalize {
 cudaError_t launch_calib_finalize(const CalibFinalize& p, cudaStream_t s);
 // Forward-KL score per head (into p.s_var) and its exact top-k.
 cudaError_t launch_calib_finalize_kl(const CalibFinalize& p, cudaStream_t s);
+// Sharp-mean pattern: causal softmax of each row of the running mean.
+cudaError_t launch_calib_sharp(const float* mean, int num_heads, int T, float* out,
+                               cudaStream_t s);
 
 // ------------------------------------------------------------ compact fit
 struct FitParams {

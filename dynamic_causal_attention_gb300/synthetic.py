@@ -148,14 +148,17 @@ def calib_temperatures(num_heads: int, seed: int = 0) -> np.ndarray:
 
 def calib_probabilities(N: int, num_heads: int, T: int, d_h: int = 64,
                         seed: int = 0, device: str = "cpu", out=None,
-                        n_begin: int = 0, n_count: int | None = None):
+                        n_begin: int = 0, n_count: int | None = None,
+                        want_logits: bool = False):
     """Row-stochastic causal probability matrices, float32 [n, heads, T, T].
 
     Sample n of head h is torch.softmax over Q K^T / (sqrt(d_h) tau_h) with
     -inf above the diagonal, where Q, K ~ N(0,1) are drawn from a torch
     generator seeded with (seed, n).  Returns a torch tensor on ``device``
     (written into ``out`` when given).  ``n_begin``/``n_count`` select a
-    slice of the N samples so that callers can stream them.
+    slice of the N samples so that callers can stream them.  With
+    ``want_logits`` the pre-softmax logits are returned instead, zero above
+    the diagonal.
     """
     import torch
 
@@ -174,8 +177,11 @@ def calib_probabilities(N: int, num_heads: int, T: int, d_h: int = 64,
         q = torch.randn((num_heads, T, d_h), generator=g, device=device)
         k = torch.randn((num_heads, T, d_h), generator=g, device=device)
         logits = torch.matmul(q, k.transpose(1, 2)) * scale[:, None, None]
-        logits.masked_fill_(mask, float("-inf"))
-        out[n - n_begin] = torch.softmax(logits, dim=-1)
+        if want_logits:
+            out[n - n_begin] = logits.masked_fill_(mask, 0.0)
+        else:
+            logits.masked_fill_(mask, float("-inf"))
+            out[n - n_begin] = torch.softmax(logits, dim=-1)
         del q, k, logits
     return out
 

@@ -67,15 +67,24 @@ typedef enum saf_dtype {
                   * results written back as fp32                                      */
 } saf_dtype;
 
-/* Shape of one attention layer.  Q, K, V, out, dout, dQ, dK, dV are
- * [B, H, T, d_h] row-major; lse is [B, H, T] fp32; alpha, rho, dalpha, drho
- * are [H, T] fp32 (only the rows of static heads are read or written). */
+/* Shape of one attention layer.  Q, out, dout, dQ are [B, H, T, d_h]
+ * row-major; K, V, dK, dV are [B, H_kv, T, d_h]; lse is [B, H, T] fp32;
+ * alpha, rho, dalpha, drho are [H, T] fp32 (only the rows of static heads are
+ * read or written).
+ *
+ * Grouped K/V (the GQA path of "When Can Attention Heads Be Statically
+ * Defined?", §3.3 / App. D.2): with H_kv < H, query head h reads K/V head
+ * h / (H / H_kv).  A frozen query head still mixes its group's V (only its
+ * query path is gone); dK and dV of a K/V head sum the gradients of every
+ * query head it serves, and dK of a K/V head that serves no dynamic head is
+ * zero.  H_kv = 0 means H_kv = H (one K/V head per query head). */
 typedef struct saf_attn_dims {
   int B;        /* batch size, >= 1                                    */
-  int H;        /* heads in the layer, 1..256                          */
+  int H;        /* query heads in the layer, 1..256                    */
   int T;        /* sequence length, a positive multiple of 128         */
   int d_h;      /* head dimension: 32, 64 or 128                       */
   saf_dtype dtype;
+  int H_kv;     /* K/V heads: 0 (= H) or a divisor of H                */
 } saf_attn_dims;
 
 /* Bytes of device workspace that saf_hybrid_attn_fwd / _bwd need for `dims`
@@ -215,6 +224,17 @@ SAF_API saf_status saf_calib_finalize(void* handle, int k, float* A_hat, float* 
  *             ascending (s_kl, index) order (NULL when k == 0). */
 SAF_API saf_status saf_calib_finalize_kl(void* handle, int k, float* s_kl, int32_t* selected,
                                  void* stream);
+
+/* Sharp-mean pattern ("When Can Attention Heads Be Statically Defined?", one
+ * of the candidate fixed patterns of §3, compared in §5.1 / Fig. 3): when the
+ * handle has been fed pre-softmax logits instead of probabilities (the same
+ * [n, head_count, T, T] layout; the lower triangle j <= i must be finite,
+ * the rest is ignored), the pattern is the causal softmax of each row of the
+ * logits' mean over the N >= 1 samples.
+ *   pattern  device fp32 [num_heads, T, T]: each row a causal distribution,
+ *            exact zeros above the diagonal.
+ * SAF_ERR_STATE if no samples were accumulated or heads differ in N. */
+SAF_API saf_status saf_calib_finalize_sharp(void* handle, float* pattern, void* stream);
 
 /* Compact pattern fit ("When Can Attention Heads Be Statically Defined?",
  * §3 Eq. (3)/(4) and App. A.2).  For each candidate head, alpha and rho are

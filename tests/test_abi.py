@@ -62,6 +62,13 @@ def test_workspace_size_and_unsupported_shapes(binding):
     assert binding.saf_hybrid_attn_workspace_size(d(1, 4, 128, 48, 0), 0) == 0   # d_h
     assert binding.saf_hybrid_attn_workspace_size(d(1, 300, 128, 64, 0), 0) == 0  # H
     assert binding.saf_hybrid_attn_workspace_size(d(0, 4, 128, 64, 0), 0) == 0   # B
+    # grouped K/V: H_kv must divide H; the grouped layout needs the extra dV sum
+    ws_mha = binding.saf_hybrid_attn_workspace_size(d(2, 8, 256, 64, 0), 0)
+    ws_gqa = binding.saf_hybrid_attn_workspace_size(d(2, 8, 256, 64, 0, 2), 0)
+    assert ws_mha == binding.saf_hybrid_attn_workspace_size(d(2, 8, 256, 64, 0, 8), 0)
+    assert ws_gqa > 0 and ws_gqa != ws_mha
+    assert binding.saf_hybrid_attn_workspace_size(d(2, 8, 256, 64, 0, 3), 0) == 0
+    assert binding.saf_hybrid_attn_workspace_size(d(2, 8, 256, 64, 0, -1), 0) == 0
 
 
 def test_invalid_arguments_rejected_before_launch(binding):

@@ -178,3 +178,19 @@ def test_forward_kl_selector_matches_oracle(api):
         cal.finalize_kl(k)
     assert e.value.status == B.SAF_ERR_STATE
     cal.close()
+
+
+def test_sharp_mean_pattern_matches_oracle(api):
+    N, nh, T = 7, 5, 96
+    L = calib_probabilities(N, nh, T, d_h=16, seed=33, want_logits=True)
+    cal = api.Calibration(nh, T)
+    cal.accumulate(L[:3].cuda())
+    cal.accumulate(L[3:].cuda())
+    P = cal.finalize_sharp()
+    torch.cuda.synchronize()
+    P = P.cpu().numpy()
+    for h in range(nh):
+        ref = oracle.sharp_mean_pattern(L[:, h].double().numpy())
+        np.testing.assert_allclose(P[h], ref, rtol=2e-5, atol=1e-7)
+    assert np.all(np.triu(P, 1) == 0)
+    cal.close()
