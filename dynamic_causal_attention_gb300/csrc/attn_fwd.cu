@@ -292,6 +292,10 @@ struct FwdSmem {
   static constexpr uint32_t TMEM_O = NBUF * 128;
   static constexpr int KST = (D == 128) ? 2 : 4;  // K ring (also holds static aux)
   static constexpr int VST = (D == 128) ? 3 : 4;  // V ring (consumed a step after K)
+  // d_h = 64: a static step's two V tiles in an even-aligned slot pair are one
+  // N = 128 operand (a tile is one 128-byte-swizzled chunk, so the slot
+  // stride equals the chunk stride of a [128 x 128] MN-major operand).
+  static constexpr bool PAIR_V = (D == 64) && (VST % 2 == 0);
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + G::TILE_BYTES;
   static constexpr int OFF_V = OFF_K + KST * G::TILE_BYTES;
@@ -536,6 +540,13 @@ __global__ void __launch_bounds__(384, 1)
           for (int step = 0; step < w.nsteps; ++step) {
             const int Y = TRANSPOSED ? (w.X + step) : step;
             if (step + 1 < w.nsteps) load_aux(step + 1);
+            if (L::PAIR_V && w.nb == 2 && (vc & 1)) {
+              // the pair must start at an even slot: one slot carries nothing
+              const int vs = vc % L::VST;
+              mbar_wait(v_empty + vs, ((vc / L::VST) & 1) ^ 1, wc, kSiteProdV);
+              ++vc;
+              mbar_arrive(v_full + vs);
+            }
             for (int bb = 0; bb < w.nb; ++bb) {
               const int vs = vc % L::VST;
               mbar_wait(v_empty + vs, ((vc / L::VST) & 1) ^ 1, wc, kSiteProdV);
@@ -599,6 +610,7 @@ __global__ void __launch_bounds__(384, 1)
     // ---------------------------------------------------------- P V issuer
     if (lane == 0) {
       constexpr uint32_t idesc_pv = idesc_bf16(128, D, false, true);
+      constexpr uint32_t idesc_pair = idesc_bf16(128, 2 * D, false, true);
       uint32_t vc = 0, sc = 0, oc = 0;
       for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
         const Item w = decode_item<TRANSPOSED>(p, it);
@@ -629,17 +641,41 @@ __global__ void __launch_bounds__(384, 1)
             mbar_wait(p_full + (u % NB), (u / NB) & 1, wc, kSiteMmaP);
             if (step == 0) mbar_wait(o_empty, (oc & 1) ^ 1, wc, kSiteMmaO);
             const uint32_t ga = tmem + kTmemS + (u % NB) * 128;
-            for (int bb = 0; bb < w.nb; ++bb) {
+            if (L::PAIR_V && w.nb == 2) {
+              // Two sequences' V tiles in adjacent slots form one [128 x 2 d_h]
+              // MN-major operand (the slot stride is the chunk stride), so one
+              // N = 2 d_h product fills O_b0 | O_b1.
+              if (vc & 1) {
+                const int vs = vc % L::VST;
+                mbar_wait(v_full + vs, (vc / L::VST) & 1, wc, kSiteMmaV);
+                mma_commit(v_empty + vs);
+                ++vc;
+              }
               const int vs = vc % L::VST;
               mbar_wait(v_full + vs, (vc / L::VST) & 1, wc, kSiteMmaV);
+              mbar_wait(v_full + vs + 1, ((vc + 1) / L::VST) & 1, wc, kSiteMmaV);
               tc_fence_after();
               const uint32_t vt = sV + vs * G::TILE_BYTES;
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk)
-                mma_bf16_ts(tmem + kTmemO + bb * D, ga + p_col(kk), G::mnmajor_desc(vt, kk),
-                            idesc_pv, (step > 0 || kk > 0));
+                mma_bf16_ts(tmem + kTmemO, ga + p_col(kk), G::mnmajor_desc(vt, kk), idesc_pair,
+                            (step > 0 || kk > 0));
               mma_commit(v_empty + vs);
-              ++vc;
+              mma_commit(v_empty + vs + 1);
+              vc += 2;
+            } else {
+              for (int bb = 0; bb < w.nb; ++bb) {
+                const int vs = vc % L::VST;
+                mbar_wait(v_full + vs, (vc / L::VST) & 1, wc, kSiteMmaV);
+                tc_fence_after();
+                const uint32_t vt = sV + vs * G::TILE_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                  mma_bf16_ts(tmem + kTmemO + bb * D, ga + p_col(kk), G::mnmajor_desc(vt, kk),
+                              idesc_pv, (step > 0 || kk > 0));
+                mma_commit(v_empty + vs);
+                ++vc;
+              }
             }
             // every use of a TMEM buffer completes one phase of both of its
             // barriers, so that the compute warps can count uses uniformly
