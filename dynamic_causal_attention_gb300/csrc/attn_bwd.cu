@@ -73,8 +73,7 @@ struct BwdSmem {
   static constexpr bool DQ_TMA = (D <= 64);
   static constexpr int DQS_BYTES = DQ_TMA ? 128 * 32 * 4 : 0;
   static constexpr int OFF_DQS = OFF_DST + SqTile::BYTES;
-  static constexpr int OFF_PT = OFF_DQS + DQS_BYTES;   // P^T tile (PS only)
-  static constexpr int OFF_BAR = OFF_PT + (PS ? SqTile::BYTES : 0);
+  static constexpr int OFF_BAR = OFF_DQS + DQS_BYTES;
   static constexpr int NBAR = 2 + 2 * QST + 11;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
@@ -88,6 +87,10 @@ struct BwdSmem {
   static constexpr uint32_t T_S = 0, T_DP = 128;
   static constexpr uint32_t T_DV = 256, T_DK = 256 + D;
   static constexpr uint32_t T_DQ = DQ_ALIAS ? 0 : 256 + 2 * D;
+  // PS: P^T as packed bf16 (query columns 2c, 2c+1 in column T_PT + c), the
+  // TMEM A operand of dV; 64 columns, free for d_h <= 64.
+  static constexpr uint32_t T_PT = 256 + 3 * D;
+  static_assert(!PS || T_PT + 64 <= 512, "P^T does not fit in TMEM");
   __device__ static __forceinline__ uint32_t a_col(int kk) {
     return (uint32_t)((kk < 4) ? kk * 8 : 64 + (kk - 4) * 8);
   }
@@ -202,7 +205,6 @@ __global__ void __launch_bounds__(512, 1)
   const uint32_t sK = smem_u32(smem + L::OFF_K);
   const uint32_t sV = smem_u32(smem + L::OFF_V);
   const uint32_t sDST = smem_u32(smem + L::OFF_DST);
-  const uint32_t sPT = smem_u32(smem + L::OFF_PT);
   const int H = p.H, T = p.T;
 
   if (warp == 0) {
@@ -368,7 +370,7 @@ __global__ void __launch_bounds__(512, 1)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ss(tmem + L::T_DV, SqTile::kmajor_desc(sPT, kk), G::mnmajor_desc(sDO, kk),
+            mma_bf16_ts(tmem + L::T_DV, tmem + L::T_PT + 8 * kk, G::mnmajor_desc(sDO, kk),
                         id_acc, (t > 0 || kk > 0));
           mma_commit(pt_empty);
 #pragma unroll
@@ -463,13 +465,14 @@ __global__ void __launch_bounds__(512, 1)
                 dsk[8 * k + (e >> 1)] = pack_bf16x2_f2(g2);
               }
             }
-            // the P^T tile is read by the previous step's dV
-            if (k == 0) mbar_wait(pt_empty, (pc & 1) ^ 1, wc, kSiteBCmpP);
-#pragma unroll
-            for (int u = 0; u < 2; ++u)
-              st_shared_v4(SqTile::unit_addr(sPT, r, (uint32_t)(col >> 3) + u), pk[4 * u],
-                           pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+            // P^T goes to TMEM, read there by the previous step's dV first
+            if (k == 0) {
+              mbar_wait(pt_empty, (pc & 1) ^ 1, wc, kSiteBCmpP);
+              tc_fence_after();
+            }
+            tmem_st_x8(trow + L::T_PT + (uint32_t)(col >> 1), pk);
           }
+          tmem_wait_st();
           // the dS^T tile is read by the previous step's dK and dQ
           mbar_wait(p_empty, (pc & 1) ^ 1, wc, kSiteBCmpP);
 #pragma unroll
