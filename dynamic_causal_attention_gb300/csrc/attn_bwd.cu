@@ -72,9 +72,11 @@ struct BwdSmem {
   // row.  d_h = 128 adds with atomics.
   static constexpr bool DQ_TMA = (D <= 64);
   static constexpr int DQS_BYTES = DQ_TMA ? 128 * 32 * 4 : 0;
-  static constexpr int OFF_DQS = OFF_DST + SqTile::BYTES;
+  // PS: two dS^T tiles, used by alternate steps
+  static constexpr int DST_BUFS = PS ? 2 : 1;
+  static constexpr int OFF_DQS = OFF_DST + DST_BUFS * SqTile::BYTES;
   static constexpr int OFF_BAR = OFF_DQS + DQS_BYTES;
-  static constexpr int NBAR = 2 + 2 * QST + 11;
+  static constexpr int NBAR = 2 + 2 * QST + 12;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int SLACK = (BYTES + 1024 <= 232448) ? 1024 : 0;
@@ -165,7 +167,8 @@ __global__ void __launch_bounds__(512, 1)
   uint64_t* kd_full = dq_empty + 1;
   uint64_t* kd_empty = kd_full + 1;
   uint64_t* s_free = kd_empty + 1;       // S^T, dP^T loaded by the compute warps (PS)
-  uint64_t* pt_empty = s_free + 1;       // the P^T tile is free again (PS)
+  uint64_t* pt_empty = s_free + 1;       // the P^T columns are free again (PS)
+  uint64_t* p_empty2 = pt_empty + 1;     // PS: dS^T tile 1 free again (tile 0: p_empty)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
   const WaitCtl wc{abort_flag, p.status};
@@ -185,6 +188,7 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(kd_empty, 256);
     mbar_init(s_free, 256);
     mbar_init(pt_empty, 1);
+    mbar_init(p_empty2, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -365,6 +369,7 @@ __global__ void __launch_bounds__(512, 1)
           const int qs = qc % L::QST;
           const uint32_t sQ = smem_u32(smem + L::OFF_Q + qs * L::STAGE);
           const uint32_t sDO = sQ + G::TILE_BYTES;
+          const uint32_t sDSTb = sDST + (pc & 1) * SqTile::BYTES;  // this step's dS^T tile
           mbar_wait(p_full, pc & 1, wc, kSiteBMmaP);
           if (t == 0) mbar_wait(kd_empty, (kdc & 1) ^ 1, wc, kSiteBMmaKD);
           tc_fence_after();
@@ -375,18 +380,18 @@ __global__ void __launch_bounds__(512, 1)
           mma_commit(pt_empty);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ss(tmem + L::T_DK, SqTile::kmajor_desc(sDST, kk), G::mnmajor_desc(sQ, kk),
+            mma_bf16_ss(tmem + L::T_DK, SqTile::kmajor_desc(sDSTb, kk), G::mnmajor_desc(sQ, kk),
                         id_acc, (t > 0 || kk > 0));
           mma_commit(q_empty + qs);  // S^T/dP^T of this stage completed before p_full
           ++qc;
-          ++pc;
           mbar_wait(dq_empty, (dqc & 1) ^ 1, wc, kSiteBMmaDQ);
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ss(tmem + L::T_DQ, SqTile::mnmajor_desc(sDST, kk), G::mnmajor_desc(sK, kk),
+            mma_bf16_ss(tmem + L::T_DQ, SqTile::mnmajor_desc(sDSTb, kk), G::mnmajor_desc(sK, kk),
                         id_dq, kk > 0);
-          mma_commit(p_empty);
+          mma_commit((pc & 1) ? p_empty2 : p_empty);
+          ++pc;
           mma_commit(dq_full);
           ++dqc;
         }
@@ -419,7 +424,7 @@ __global__ void __launch_bounds__(512, 1)
           // right after chunk k's have landed, so they fly while chunk k is
           // computed (tcgen05.wait::ld waits for every load in flight).
           uint32_t sv[2][16], dv[2][16];
-          uint32_t dsk[32];  // this step's dS^T row, stored once the last dQ has read the tile
+          const uint32_t sDSTb = sDST + (pc & 1) * SqTile::BYTES;  // this step's dS^T tile
           tmem_ld_x16(trow + L::T_S + 64 * hf, sv[0]);
           tmem_ld_x16(trow + L::T_DP + 64 * hf, dv[0]);
 #pragma unroll
@@ -442,7 +447,7 @@ __global__ void __launch_bounds__(512, 1)
               for (int e = 0; e < 16; ++e)
                 if (col + e < r) sv[b][e] = 0xff800000u;  // -inf: P = 0, dS = 0
             }
-            uint32_t pk[8];
+            uint32_t pk[8], dk[8];
 #pragma unroll
             for (int k4 = 0; k4 < 16; k4 += 4) {
               const float4 nl = lds_f32x4(nl_a + 4u * (16 * k + k4));
@@ -462,23 +467,23 @@ __global__ void __launch_bounds__(512, 1)
                     f2_add(f2_pack(__uint_as_float(dv[b][e]), __uint_as_float(dv[b][e + 1])),
                            f2_pack(e0, e1)));
                 pk[e >> 1] = pack_bf16x2(p0, p1);
-                dsk[8 * k + (e >> 1)] = pack_bf16x2_f2(g2);
+                dk[e >> 1] = pack_bf16x2_f2(g2);
               }
             }
-            // P^T goes to TMEM, read there by the previous step's dV first
             if (k == 0) {
+              // P^T goes to TMEM, read there by the previous step's dV first;
+              // this dS^T tile was last read by dK and dQ two steps back
               mbar_wait(pt_empty, (pc & 1) ^ 1, wc, kSiteBCmpP);
+              mbar_wait((pc & 1) ? p_empty2 : p_empty, ((pc >> 1) & 1) ^ 1, wc, kSiteBCmpP);
               tc_fence_after();
             }
             tmem_st_x8(trow + L::T_PT + (uint32_t)(col >> 1), pk);
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+              st_shared_v4(SqTile::unit_addr(sDSTb, r, (uint32_t)(col >> 3) + u), dk[4 * u],
+                           dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
           }
           tmem_wait_st();
-          // the dS^T tile is read by the previous step's dK and dQ
-          mbar_wait(p_empty, (pc & 1) ^ 1, wc, kSiteBCmpP);
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            st_shared_v4(SqTile::unit_addr(sDST, r, (uint32_t)(8 * hf) + u), dsk[4 * u],
-                         dsk[4 * u + 1], dsk[4 * u + 2], dsk[4 * u + 3]);
         }
 #pragma unroll 1
         for (int c0 = 0; !L::PS && c0 < 64; c0 += 32) {
