@@ -156,7 +156,7 @@ WsLayout ws_layout(const saf_attn_dims& d) {
   L.r_tab = take(H * (T + 128) * 4);
   L.row_tab = take(H * T * 4);
   L.logZ = take(H * T * 4);
-  L.mode = take(H * 4);
+  L.mode = take(H * 8);  // H ints of mode, then H floats of shift
   const bool f32 = d.dtype == SAF_F32;
   const size_t stage = f32 ? elems * 2 : 0;
   const size_t stage_kv = f32 ? elems_kv * 2 : 0;
@@ -231,6 +231,7 @@ StaticPrep make_prep(const saf_attn_dims& d, const HeadSplit& hs, const float* a
   sp.row_tab = reinterpret_cast<float*>(ws + L.row_tab);
   sp.logZ = reinterpret_cast<float*>(ws + L.logZ);
   sp.mode = reinterpret_cast<int*>(ws + L.mode);
+  sp.shift = reinterpret_cast<float*>(ws + L.mode) + d.H;
   return sp;
 }
 
@@ -256,6 +257,7 @@ void fill_fwd_params(FwdParams& p, const saf_attn_dims& d, const HeadSplit& hs, 
   p.row_tab = reinterpret_cast<const float*>(ws + L.row_tab);
   p.logZ = reinterpret_cast<const float*>(ws + L.logZ);
   p.mode = reinterpret_cast<const int*>(ws + L.mode);
+  p.shift = reinterpret_cast<const float*>(ws + L.mode) + d.H;
   p.status = reinterpret_cast<int*>(ws + L.status);
 }
 
@@ -437,6 +439,13 @@ saf_status saf_hybrid_attn_bwd(const saf_attn_dims* dims, const void* Q, const v
   pre.lse2 = reinterpret_cast<float*>(ws + L.lse2);
   pre.Dsum = dalpha ? reinterpret_cast<float*>(ws + L.Dsum) : nullptr;
   pre.n_static = hs.n_static;
+  memset(pre.static_slot, 255, sizeof(pre.static_slot));
+  for (int i = 0; i < hs.n_static; ++i) pre.static_slot[hs.st[i]] = (uint8_t)i;
+  if (hs.n_static > 0) {
+    pre.row_tab = reinterpret_cast<float*>(ws + L.row_tab);
+    pre.mode = reinterpret_cast<const int*>(ws + L.mode);
+    pre.shift = reinterpret_cast<const float*>(ws + L.mode) + d.H;
+  }
   memcpy(pre.static_heads, hs.st, sizeof(pre.static_heads));
   float* dq_acc = reinterpret_cast<float*>(ws + L.dq_acc);
   pre.dq_acc = hs.n_dynamic > 0 ? dq_acc : nullptr;

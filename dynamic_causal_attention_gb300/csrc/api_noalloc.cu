@@ -69,7 +69,7 @@ ScratchLayout scratch_layout(int n_static, int T) {
   L.r_tab = take(hs * (t + 128) * 4);
   L.row_tab = take(hs * t * 4);
   L.logZ = take(hs * t * 4);
-  L.mode = take(hs * 4);
+  L.mode = take(hs * 8);  // n_static ints of mode, then n_static floats of shift
   L.total = off;
   return L;
 }
@@ -157,6 +157,7 @@ extern "C" saf_status saf_hybrid_attn_fwd_noalloc(const saf_attn_dims* dims, con
     sp.row_tab = reinterpret_cast<float*>(ws + L.row_tab);
     sp.logZ = reinterpret_cast<float*>(ws + L.logZ);
     sp.mode = reinterpret_cast<int*>(ws + L.mode);
+    sp.shift = reinterpret_cast<float*>(ws + L.mode) + n_static;
     if (launch_static_prep(sp, s) != cudaSuccess) return SAF_ERR_CUDA;
   }
 
@@ -182,6 +183,7 @@ extern "C" saf_status saf_hybrid_attn_fwd_noalloc(const saf_attn_dims* dims, con
   p.row_tab = reinterpret_cast<const float*>(ws + L.row_tab);
   p.logZ = reinterpret_cast<const float*>(ws + L.logZ);
   p.mode = reinterpret_cast<const int*>(ws + L.mode);
+  p.shift = reinterpret_cast<const float*>(ws + L.mode) + n_static;
   p.status = reinterpret_cast<int*>(ws + L.status);
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;

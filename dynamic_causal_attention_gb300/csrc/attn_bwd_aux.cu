@@ -4,7 +4,8 @@
 //             backward's row term), stored negated, and -lse * log2(e) (the
 //             dynamic backward adds both), plus for frozen heads the batch
 //             sums of D that the alpha/rho gradients need; it also zeroes the
-//             fp32 dQ accumulator;
+//             fp32 dQ accumulator, and rebuilds the frozen heads' per-row table
+//             from the forward's lse (log Z);
 //   bwd_post  dQ = (1/sqrt(d_h)) * fp32 accumulator -> bf16, and zeros for the
 //             dQ/dK rows of frozen heads (they have no query/key path).
 #include <cuda_bf16.h>
@@ -49,8 +50,19 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(BwdPre p) {
     z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   if (row < rows && sub == 0) {
+    const float l = p.lse[row];
     p.Dvec[row] = -acc;
-    p.lse2[row] = -p.lse[row] * 1.4426950408889634f;
+    p.lse2[row] = -l * 1.4426950408889634f;
+    if (p.row_tab && row < (size_t)p.H * p.T) {  // sequence 0: rows (h, i)
+      const int h = (int)(row / p.T), i = (int)(row - (size_t)h * p.T);
+      const int hs = p.static_slot[h];
+      if (hs != 255) {
+        float v;
+        if (p.mode[hs]) v = -l * 1.4426950408889634f;
+        else v = (l > -INFINITY) ? expf(p.shift[hs] - l) : 0.f;
+        p.row_tab[(size_t)hs * p.T + i] = v;
+      }
+    }
   }
 }
 

@@ -73,10 +73,11 @@ __device__ __forceinline__ void block_minmax(float& mx, float& mn, float* red) {
 }
 
 // grid (T / 64, n_static), 256 threads (8 warps), dynamic smem 2 * T + 8
-// floats.  Each block owns 64 rows; each warp computes the convolution of 8
-// rows together (eight independent accumulators, one load of a(k) for all
-// of them) with its 32 lanes splitting the causal sum, reduced across lanes
-// in a fixed order.
+// floats.  Each block scans alpha/rho for their finite ranges and picks the
+// mode.  Factored heads: the block writes its 64 entries of the tables and,
+// block 0, the head's shift max alpha + max rho.  Exact heads: each warp
+// also forms log Z of 8 rows by an online log-sum-exp, its 32 lanes
+// splitting the causal sum, merged across lanes in a fixed order.
 constexpr int kPrepRows = 64;
 
 __global__ void __launch_bounds__(256) static_prep_kernel(StaticPrep p) {
@@ -118,46 +119,20 @@ __global__ void __launch_bounds__(256) static_prep_kernel(StaticPrep p) {
   float* r_tab = p.r_tab + (size_t)hs * (T + 128);
   float* row_tab = p.row_tab + (size_t)hs * T;
   float* logZ = p.logZ + (size_t)hs * T;
-  if (blockIdx.x == 0 && threadIdx.x == 0) p.mode[hs] = exact ? 1 : 0;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    p.mode[hs] = exact ? 1 : 0;
+    p.shift[hs] = (exact || all_masked) ? 0.f : amax + rmax;
+  }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
   if (!exact) {
-    // a = exp(alpha - max), r = exp(rho - max) in place
+    // a = exp(alpha - max), r = exp(rho - max) for this block's 64 entries.
+    // Z'(i) is not formed here: the forward sums it from its own tiles and
+    // the backward reads it back from the forward's lse.
     __syncthreads();
-    for (int t = threadIdx.x; t < nload; t += blockDim.x) {
-      sa[t] = all_masked ? 0.f : expf(sa[t] - amax);
-      sr[t] = all_masked ? 0.f : expf(sr[t] - rmax);
-    }
-    if (threadIdx.x < 8) sr[(int)threadIdx.x - 8] = 0.f;
-    __syncthreads();
-    const int ib = row0 + warp * (kPrepRows / 8);  // this warp's first row
-    float z[8];
-#pragma unroll
-    for (int m = 0; m < 8; ++m) z[m] = 0.f;
-    // k <= ib + 7 covers every row; k > i reads the zero pad (i - k >= -7)
-    for (int k = lane; k <= ib + 7; k += 32) {
-      const float av = sa[k];
-      const float* rp = sr + (ib - k);
-#pragma unroll
-      for (int m = 0; m < 8; ++m) z[m] = fmaf(av, rp[m], z[m]);
-    }
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) z[m] += __shfl_xor_sync(0xffffffffu, z[m], o);
-    }
-    if (lane < 8) {
-      float zz = z[0];
-#pragma unroll
-      for (int m = 1; m < 8; ++m)
-        if (lane == m) zz = z[m];
-      const int i = ib + lane;
-      row_tab[i] = zz > 0.f ? 1.0f / zz : 0.f;
-      logZ[i] = zz > 0.f ? logf(zz) + amax + rmax : -INFINITY;
-    }
     for (int t = threadIdx.x; t < kPrepRows; t += blockDim.x) {
-      a_tab[row0 + t] = sa[row0 + t];
-      r_tab[127 + row0 + t] = sr[row0 + t];
+      a_tab[row0 + t] = all_masked ? 0.f : expf(sa[row0 + t] - amax);
+      r_tab[127 + row0 + t] = all_masked ? 0.f : expf(sr[row0 + t] - rmax);
     }
     if (blockIdx.x == 0 && threadIdx.x < 127) r_tab[threadIdx.x] = 0.f;
     if (blockIdx.x == 0 && threadIdx.x == 127) r_tab[T + 127] = 0.f;
@@ -319,9 +294,14 @@ struct FwdSmem {
 // row minus the half's first column.  Forward element (i = row, j = col):
 // distance rc - cl; transposed (j = row, i = col): distance cl - rc.
 // Factored: colv * r(distance) * rowv; exact: exp2(colv + r(distance) + rowv).
-template <bool TRANSPOSED, bool EXACT>
+// With SUMS (factored forward) adds the row sums of the fp32 values and of
+// their bf16 roundings to zsum and zrnd.
+template <bool TRANSPOSED, bool EXACT, bool SUMS>
 __device__ __forceinline__ void gen_tile(uint32_t colv_s, uint32_t win_s, int rc, uint64_t row2,
-                                         uint32_t tdst) {
+                                         uint32_t tdst, float& zsum, float& zrnd) {
+  // SUMS: the fp32 sum of this thread's 64 values, and the sum of the same
+  // values after rounding to bf16 (what the MMA actually weighs V with)
+  uint64_t sum2 = 0, rnd2 = 0;
   // address of window entry 127 + distance for column 0 of the half
   const uint32_t w0 = win_s + 4u * (uint32_t)(127 + (TRANSPOSED ? -rc : rc));
 #pragma unroll
@@ -339,10 +319,23 @@ __device__ __forceinline__ void gen_tile(uint32_t colv_s, uint32_t win_s, int rc
         f2_unpack(f2_add(f2_add(cv, wv), row2), x0, x1);
         pk[qq] = pack_bf16x2(fast_exp2(x0), fast_exp2(x1));
       } else {
-        pk[qq] = pack_bf16x2_f2(f2_mul(f2_mul(cv, wv), row2));
+        const uint64_t g = f2_mul(f2_mul(cv, wv), row2);
+        pk[qq] = pack_bf16x2_f2(g);
+        if (SUMS) {
+          sum2 = f2_add(sum2, g);
+          rnd2 = f2_add(rnd2, f2_pack(__uint_as_float(pk[qq] << 16),
+                                      __uint_as_float(pk[qq] & 0xffff0000u)));
+        }
       }
     }
     tmem_st_x16(tdst + q0, pk);
+  }
+  if (SUMS) {
+    float lo, hi;
+    f2_unpack(sum2, lo, hi);
+    zsum += lo + hi;
+    f2_unpack(rnd2, lo, hi);
+    zrnd += lo + hi;
   }
 }
 
@@ -821,10 +814,16 @@ __global__ void __launch_bounds__(384, 1)
       } else {
         // static item: generate G (or G^T) tiles into TMEM, then the epilogue
         const bool exact = p.mode[w.hs] != 0;
-        // per-row value: forward 1/Z'(i) or -log2 Z(i); transposed a(j)
+        // per-row value: transposed a(j); forward exact -log2 Z(i); forward
+        // factored 1: the tiles hold a(j) r(i-j), whose row sums give Z'(i),
+        // and the epilogue divides by it
         const float rowv = TRANSPOSED ? p.a_tab[(size_t)w.hs * T + w.X * 128 + r]
-                                      : p.row_tab[(size_t)w.hs * T + w.X * 128 + r];
+                           : exact    ? p.row_tab[(size_t)w.hs * T + w.X * 128 + r]
+                                      : 1.0f;
         const uint64_t row2 = f2_pack(rowv, rowv);
+        // this half's share of Z'(i) (forward, factored): exact, and of the
+        // bf16 weights the products use
+        float zpart = 0.f, zround = 0.f;
         for (int step = 0; step < w.nsteps; ++step) {
           const uint32_t u = sc0 + step;
           const int ks = kc % L::KST;
@@ -837,9 +836,11 @@ __global__ void __launch_bounds__(384, 1)
           tc_fence_after();
           const uint32_t gdst = trow + kTmemS + (u % NB) * 128 + 64 * hf;
           if (exact)
-            gen_tile<TRANSPOSED, true>(smem_u32(colv), smem_u32(win), r - 64 * hf, row2, gdst);
+            gen_tile<TRANSPOSED, true, false>(smem_u32(colv), smem_u32(win), r - 64 * hf, row2,
+                                              gdst, zpart, zround);
           else
-            gen_tile<TRANSPOSED, false>(smem_u32(colv), smem_u32(win), r - 64 * hf, row2, gdst);
+            gen_tile<TRANSPOSED, false, !TRANSPOSED>(smem_u32(colv), smem_u32(win), r - 64 * hf,
+                                                     row2, gdst, zpart, zround);
           // all 256 compute threads have read the aux slot: release it once
           named_bar_sync(1, 256);
           if (hf == 0 && r == 0) mbar_arrive(k_empty + ks);
@@ -849,6 +850,21 @@ __global__ void __launch_bounds__(384, 1)
           mbar_arrive(p_full + (u % NB));
         }
         sc = sc0 + w.nsteps;
+        // forward, factored: Z'(i) = both halves' sums.  out = O divided by
+        // the sum of the bf16 weights the products used (so each row of the
+        // pattern that V is mixed with sums to one exactly: the identity
+        // pattern copies V), lse = log Z' (exact sum) + the head's shift
+        float oscale = 1.0f, lse_i = 0.f;
+        if (!TRANSPOSED && !exact) {
+          xsum[hf * 128 + r] = zpart;
+          xmax[hf * 128 + r] = zround;
+          named_bar_sync(pair_bar, 64);
+          const float z = zpart + xsum[(1 - hf) * 128 + r];
+          const float zr = zround + xmax[(1 - hf) * 128 + r];
+          named_bar_sync(pair_bar, 64);  // xsum may be rewritten by the next item
+          oscale = zr > 0.f ? 1.0f / zr : 0.f;
+          lse_i = z > 0.f ? logf(z) + p.shift[w.hs] : -INFINITY;
+        }
         mbar_wait(o_full, oc & 1, wc, kSiteCmpO);
         tc_fence_after();
         const int trow_i = w.X * 128 + r;
@@ -878,9 +894,10 @@ __global__ void __launch_bounds__(384, 1)
             uint32_t o[16];
             tmem_ld_x16(trow + kTmemO + bb * D + hf * DH + c0, o);
             tmem_wait_ld(o);
-            store_row16(dst + c0, o, 1.0f);
+            store_row16(dst + c0, o, oscale);
           }
-          if (!TRANSPOSED && hf == 0 && p.lse) p.lse[orow] = p.logZ[(size_t)w.hs * T + trow_i];
+          if (!TRANSPOSED && hf == 0 && p.lse)
+            p.lse[orow] = exact ? p.logZ[(size_t)w.hs * T + trow_i] : lse_i;
         }
         tc_fence_before();
         mbar_arrive(o_empty);

@@ -26,6 +26,7 @@ struct FwdParams {
   const float* row_tab;       // [n_static, T]
   const float* logZ;          // [n_static, T]
   const int* mode;            // [n_static]
+  const float* shift;         // [n_static] log Z = log Z' + shift (factored heads)
   __nv_bfloat16* out;         // forward: out; transposed: dV
   float* out_acc;             // transposed with group_kv > 1: fp32 dV [B, H_kv, T, d_h],
                               // added to with atomics (out is then unused)
@@ -65,6 +66,12 @@ struct BwdPre {
   float* dq_acc;      // [B, H, T, d_h] fp32 zeroed here (nullable)
   int n_static;
   uint8_t static_heads[kMaxHeads];
+  // Per-row table of the frozen heads from the forward's lse (sequence 0):
+  // factored 1/Z'(i) = exp(shift - lse), exact -lse * log2(e).  Nullable.
+  float* row_tab;     // [n_static, T]
+  const int* mode;
+  const float* shift;
+  uint8_t static_slot[kMaxHeads];  // head -> index among the frozen heads, 255 if dynamic
 };
 cudaError_t launch_bwd_pre(const BwdPre& p, cudaStream_t s);
 

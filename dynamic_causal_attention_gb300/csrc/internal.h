@@ -83,9 +83,10 @@ struct StaticPrep {
   const float* rho;          // [H, T]
   float* a_tab;              // [n_static, T]
   float* r_tab;              // [n_static, T + 128] (127 leading pads)
-  float* row_tab;            // [n_static, T] : 1/Z' (factored) or log2 Z (exact)
-  float* logZ;               // [n_static, T] natural log
+  float* row_tab;            // [n_static, T] : -log2 Z (exact heads only)
+  float* logZ;               // [n_static, T] natural log (exact heads only)
   int* mode;                 // [n_static] 0 factored, 1 exact
+  float* shift;              // [n_static] factored: max alpha + max rho (0 if all masked)
 };
 cudaError_t launch_static_prep(const StaticPrep& p, cudaStream_t s);
 

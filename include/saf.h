@@ -157,7 +157,7 @@ SAF_API saf_status saf_hybrid_attn_bwd(const saf_attn_dims* dims,
  * scratch (the frozen heads' tables, log Z and the status word) lives in one
  * file-scope device array of 4 MiB that every GPU which loads the library
  * holds until the process exits; a shape whose tables need more,
- * n_static * (4 T + 128) * 4 bytes plus at most 1.5 KiB of status word and
+ * n_static * (4 T + 130) * 4 bytes plus at most 1.5 KiB of status word and
  * alignment, is rejected with SAF_ERR_UNSUPPORTED before anything is launched.  Nothing is allocated:
  * no cudaMalloc, no cudaFree, no allocating library routine.
  *
