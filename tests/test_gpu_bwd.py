@@ -157,3 +157,39 @@ def test_param_grads_several_rounds_both_generator_modes(api):
         inp["alpha"][h] += np.linspace(-45.0, 45.0, T)
     got = gpu_fwd_bwd(api, inp, cfg.head_is_static, True)
     compare(got, oracle_bwd(inp, cfg.head_is_static, True), cfg.head_is_static, "rounds", True)
+
+
+def test_masked_keys_and_fully_masked_head(api):
+    # head 0: alpha = -inf everywhere (no row has a distribution: out = 0,
+    # lse = -inf, zero gradients); head 1: every even key masked, so row 0 is
+    # empty and the other rows see only odd keys
+    B, H, T, d = 2, 2, 256, 64
+    cfg = AttnConfig("mask", B=B, H=H, T=T, d_h=d, dtype="bf16", static_heads=(0, 1))
+    inp = attn_inputs(cfg, seed=13)
+    inp["alpha"][0] = -np.inf
+    inp["alpha"][1, 0::2] = -np.inf
+    layer = api.HybridAttention(B, H, T, d, cfg.head_is_static, want_param_grads=True)
+    q, k, v, do = (to_dev(inp[n], torch.bfloat16) for n in ("Q", "K", "V", "dO"))
+    alpha = to_dev(inp["alpha"], torch.float32)
+    rho = to_dev(inp["rho"], torch.float32)
+    out, lse = layer.forward(q, k, v, alpha, rho)
+    dq, dk, dv, da, dr = layer.backward(q, k, v, out, lse, do, alpha, rho, want_param_grads=True)
+    torch.cuda.synchronize()
+    out, lse, dv, da, dr = (to_np(x) for x in (out, lse, dv, da, dr))
+    assert np.all(out[:, 0] == 0) and np.all(np.isneginf(lse[:, 0]))
+    assert np.all(out[:, 1, 0] == 0) and np.all(np.isneginf(lse[:, 1, 0]))
+    V, dO = bf16_round(inp["V"]), bf16_round(inp["dO"])
+    ro, rl = oracle.hybrid_attn_fwd(inp["Q"], inp["K"], V, inp["alpha"], inp["rho"],
+                                    cfg.head_is_static)
+    assert_close(out[:, 1], ro[:, 1], "masked-keys out")
+    np.testing.assert_allclose(lse[:, 1, 1:], rl[:, 1, 1:], atol=1e-3)
+    rv, ra, rr = oracle.static_head_bwd(inp["alpha"][1], inp["rho"][1], [V[b, 1] for b in range(B)],
+                                        [dO[b, 1] for b in range(B)])
+    for b in range(B):
+        assert_close(dv[b, 1], rv[b], f"masked-keys dV b{b}")
+    assert np.all(dv[:, 0] == 0)
+    assert np.all(np.isfinite(da)) and np.all(np.isfinite(dr))
+    assert np.all(da[0] == 0) and np.all(dr[0] == 0)
+    assert np.all(da[1][0::2] == 0)
+    assert_close(da[1][1::2], ra[1::2], "masked-keys dalpha")
+    assert_close(dr[1], rr, "masked-keys drho")

@@ -85,3 +85,33 @@ def test_gqa_fp32_io(api):
     cfg, inp = gqa_inputs(1, 4, 2, 128, 32, (0,), seed=71)
     got = run(api, cfg, inp, 2, True, dtype=torch.float32)
     check(got, inp, cfg.head_is_static, True, "gqa fp32")
+
+
+def test_gqa_exact_range_frozen_head(api):
+    # a frozen query head whose alpha spans more than 80 uses the exact
+    # exponential; its group mixes it with dynamic heads
+    cfg, inp = gqa_inputs(2, 4, 2, 256, 64, (1, 2), seed=73)
+    inp["alpha"][1] += np.linspace(-45.0, 45.0, 256)
+    got = run(api, cfg, inp, 2, True)
+    check(got, inp, cfg.head_is_static, True, "gqa exact")
+
+
+def test_gqa_no_alloc_forward_matches(api):
+    # the allocation-free forward reads grouped K/V the same way
+    from dynamic_causal_attention_gb300 import _binding as B
+    cfg, inp = gqa_inputs(2, 8, 2, 256, 64, (1, 6), seed=79)
+    Bn, H, T, d = inp["Q"].shape
+    layer = api.HybridAttention(Bn, H, T, d, cfg.head_is_static, H_kv=2)
+    q, k, v = (to_dev(inp[n], torch.bfloat16) for n in ("Q", "K", "V"))
+    alpha = to_dev(inp["alpha"], torch.float32)
+    rho = to_dev(inp["rho"], torch.float32)
+    out, lse = layer.forward(q, k, v, alpha, rho)
+    out2 = torch.empty_like(out)
+    lse2 = torch.empty_like(lse)
+    st = B.saf_hybrid_attn_fwd_noalloc(layer.dims, q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                       alpha.data_ptr(), rho.data_ptr(), layer.head_is_static,
+                                       out2.data_ptr(), lse2.data_ptr(),
+                                       torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
