@@ -215,7 +215,8 @@ __global__ void __launch_bounds__(512, 1)
     // ---------------------------------------------------------- producer
     if (lane == 0) {
       uint32_t kvc = 0, qc = 0;
-      for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+      for (int kr = 0, it = snake_item(0, blockIdx.x, gridDim.x); it < p.n_items;
+         it = snake_item(++kr, blockIdx.x, gridDim.x)) {
         const BItem w = decode_bwd(p, it);
         const int kvrow0 = (w.b * p.H_kv + w.kv) * T;
         mbar_wait(kv_empty, (kvc & 1) ^ 1, wc, kSiteBProdKV);
@@ -276,7 +277,8 @@ __global__ void __launch_bounds__(512, 1)
       uint32_t sfc = 0;
       if constexpr (L::PS) {
         // S^T and dP^T only; warp 3 issues dV, dK and dQ.
-        for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+        for (int kr = 0, it = snake_item(0, blockIdx.x, gridDim.x); it < p.n_items;
+         it = snake_item(++kr, blockIdx.x, gridDim.x)) {
           const BItem w = decode_bwd(p, it);
           mbar_wait(kv_full, kvc & 1, wc, kSiteBMmaKV);
           ++kvc;
@@ -296,7 +298,8 @@ __global__ void __launch_bounds__(512, 1)
           }
         }
       }
-      for (int it = blockIdx.x; !L::PS && it < p.n_items; it += gridDim.x) {
+      for (int kr = 0, it = snake_item(0, blockIdx.x, gridDim.x); !L::PS && it < p.n_items;
+           it = snake_item(++kr, blockIdx.x, gridDim.x)) {
         const BItem w = decode_bwd(p, it);
         mbar_wait(kv_full, kvc & 1, wc, kSiteBMmaKV);
         ++kvc;
@@ -361,7 +364,8 @@ __global__ void __launch_bounds__(512, 1)
       constexpr uint32_t id_acc = idesc_bf16(128, D, false, true);
       constexpr uint32_t id_dq = idesc_bf16(128, D, true, true);
       uint32_t kvc = 0, qc = 0, pc = 0, dqc = 0, kdc = 0;
-      for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+      for (int kr = 0, it = snake_item(0, blockIdx.x, gridDim.x); it < p.n_items;
+         it = snake_item(++kr, blockIdx.x, gridDim.x)) {
         const BItem w = decode_bwd(p, it);
         mbar_wait(kv_full, kvc & 1, wc, kSiteBMmaKV);  // K_J is the B operand of dQ
         ++kvc;
@@ -407,7 +411,8 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
     uint32_t qc = 0, sc = 0, pc = 0, kdc = 0;
-    for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+    for (int kr = 0, it = snake_item(0, blockIdx.x, gridDim.x); it < p.n_items;
+         it = snake_item(++kr, blockIdx.x, gridDim.x)) {
       const BItem w = decode_bwd(p, it);
       for (int t = 0; t < w.nsteps; ++t) {
         const int qs = qc % L::QST;
@@ -589,7 +594,8 @@ __global__ void __launch_bounds__(512, 1)
     const int r = (warp & 3) * 32 + lane;  // query row i within the tile == TMEM lane
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     uint32_t dqc = 0;
-    for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+    for (int kr = 0, it = snake_item(0, blockIdx.x, gridDim.x); it < p.n_items;
+         it = snake_item(++kr, blockIdx.x, gridDim.x)) {
       const BItem w = decode_bwd(p, it);
       for (int t = 0; t < w.nsteps; ++t) {
         int hq, I;
@@ -682,12 +688,6 @@ struct PgSmem {
 
 enum : int { kSitePgProd = 201, kSitePgProdAux, kSitePgMma, kSitePgMmaAcc, kSitePgAux, kSitePgAcc };
 
-// Item of round k for this CTA: even rounds run forwards, odd rounds
-// backwards, so the CTA that drew one of the longest items (small J) in one
-// round draws one of the shortest in the next.
-__device__ __forceinline__ int snake_item(int k, int cta, int grid) {
-  return (k & 1) ? (k + 1) * grid - 1 - cta : k * grid + cta;
-}
 
 template <int D>
 __global__ void __launch_bounds__(384, 1)

@@ -68,4 +68,13 @@ struct SqTile {
   }
 };
 
+// Item of round k for CTA `cta` of a persistent grid of `grid` CTAs: even
+// rounds run forwards, odd rounds backwards, so that with items sorted
+// longest first the CTA that drew one of the longest items in one round
+// draws one of the shortest in the next.  Once an index is past the end,
+// every later round's is too.
+__device__ __forceinline__ int snake_item(int k, int cta, int grid) {
+  return (k & 1) ? (k + 1) * grid - 1 - cta : k * grid + cta;
+}
+
 }  // namespace saf

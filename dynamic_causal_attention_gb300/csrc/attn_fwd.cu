@@ -482,7 +482,8 @@ __global__ void __launch_bounds__(384, 1)
     // ---------------------------------------------------------- producer
     if (lane == 0) {
       uint32_t qc = 0, kc = 0, vc = 0;
-      for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+      for (int kr = 0, it = snake_item(0, blockIdx.x, gridDim.x); it < p.n_items;
+         it = snake_item(++kr, blockIdx.x, gridDim.x)) {
         const Item w = decode_item<TRANSPOSED>(p, it);
         if (!w.is_static) {
           const int row0 = (w.b * H + w.h) * T;                           // Q rows
@@ -570,7 +571,8 @@ __global__ void __launch_bounds__(384, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
       uint32_t qc = 0, kc = 0, sc = 0;
-      for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+      for (int kr = 0, it = snake_item(0, blockIdx.x, gridDim.x); it < p.n_items;
+         it = snake_item(++kr, blockIdx.x, gridDim.x)) {
         const Item w = decode_item<TRANSPOSED>(p, it);
         const uint32_t sc0 = sc;
         if (!w.is_static) {
@@ -605,7 +607,8 @@ __global__ void __launch_bounds__(384, 1)
       constexpr uint32_t idesc_pv = idesc_bf16(128, D, false, true);
       constexpr uint32_t idesc_pair = idesc_bf16(128, 2 * D, false, true);
       uint32_t vc = 0, sc = 0, oc = 0;
-      for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+      for (int kr = 0, it = snake_item(0, blockIdx.x, gridDim.x); it < p.n_items;
+         it = snake_item(++kr, blockIdx.x, gridDim.x)) {
         const Item w = decode_item<TRANSPOSED>(p, it);
         const uint32_t sc0 = sc;
         if (!w.is_static) {
@@ -689,7 +692,8 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
     const int pair_bar = 2 + q4;                 // the two warps that share these rows
     uint32_t kc = 0, sc = 0, oc = 0;
-    for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+    for (int kr = 0, it = snake_item(0, blockIdx.x, gridDim.x); it < p.n_items;
+         it = snake_item(++kr, blockIdx.x, gridDim.x)) {
       const Item w = decode_item<TRANSPOSED>(p, it);
       const uint32_t sc0 = sc;
       if (!w.is_static) {
