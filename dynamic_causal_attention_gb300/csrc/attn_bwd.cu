@@ -71,12 +71,15 @@ struct BwdSmem {
   // chunk (32 fp32 columns), 128-byte swizzled, reused for each chunk of the
   // row.  d_h = 128 adds with atomics.
   static constexpr bool DQ_TMA = (D <= 64);
+  // d_h = 128 has no room for a staging tile: dQ is staged through the dS^T
+  // tile (its two 16 KB halves alternate) once the dQ MMA has read it.
+  static constexpr bool DQ_DST = !DQ_TMA;
   static constexpr int DQS_BYTES = DQ_TMA ? 128 * 32 * 4 : 0;
   // PS: two dS^T tiles, used by alternate steps
   static constexpr int DST_BUFS = PS ? 2 : 1;
   static constexpr int OFF_DQS = OFF_DST + DST_BUFS * SqTile::BYTES;
   static constexpr int OFF_BAR = OFF_DQS + DQS_BYTES;
-  static constexpr int NBAR = 2 + 2 * QST + 12;
+  static constexpr int NBAR = 2 + 2 * QST + 13;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int SLACK = (BYTES + 1024 <= 232448) ? 1024 : 0;
@@ -169,6 +172,7 @@ __global__ void __launch_bounds__(512, 1)
   uint64_t* s_free = kd_empty + 1;       // S^T, dP^T loaded by the compute warps (PS)
   uint64_t* pt_empty = s_free + 1;       // the P^T columns are free again (PS)
   uint64_t* p_empty2 = pt_empty + 1;     // PS: dS^T tile 1 free again (tile 0: p_empty)
+  uint64_t* dqs_free = p_empty2 + 1;     // DQ_DST: the dQ reductions have read the tile
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
   const WaitCtl wc{abort_flag, p.status};
@@ -189,6 +193,7 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(s_free, 256);
     mbar_init(pt_empty, 1);
     mbar_init(p_empty2, 1);
+    mbar_init(dqs_free, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -532,7 +537,11 @@ __global__ void __launch_bounds__(512, 1)
           tmem_st_x16(trow + L::T_S + 64 * hf + (c0 >> 1), pk);
           tmem_st_x16(trow + L::T_DP + 64 * hf + (c0 >> 1), dk);
           // the dS^T tile in shared memory is read by the previous step's dQ
-          if (c0 == 0) mbar_wait(p_empty, (pc & 1) ^ 1, wc, kSiteBCmpP);
+          // (and, staged there, by its reductions)
+          if (c0 == 0) {
+            mbar_wait(p_empty, (pc & 1) ^ 1, wc, kSiteBCmpP);
+            if (L::DQ_DST) mbar_wait(dqs_free, (pc & 1) ^ 1, wc, kSiteBCmpP);
+          }
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const uint32_t unit = (uint32_t)(col >> 3) + u;
@@ -633,26 +642,42 @@ __global__ void __launch_bounds__(512, 1)
             }
           }
         } else {
-          float* dst = p.dq_acc + ((size_t)(w.b * H + hq) * T + (size_t)I * 128 + r) * D;
-#pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 16) {
-            uint32_t o[16];
-            tmem_ld_x16(tmem + lane_base + L::T_DQ + c0, o);
+          // d_h = 128: 32 columns at a time through the two halves of the
+          // dS^T tile (its dQ MMA has completed), one tensor reduce-add each
+          const int row = (w.b * H + hq) * T + I * 128;
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld_x32(tmem + lane_base + L::T_DQ + 32 * c, o);
             tmem_wait_ld(o);
+            if (c == D / 32 - 1) {
+              tc_fence_before();
+              mbar_arrive(dq_empty);  // every dQ column is in registers
+            }
+            const uint32_t slot = (uint32_t)(c & 1) * 16384u;
+            if (r == 0 && c >= 2) bulk_wait_group_read1();  // chunk c - 2 has left the slot
+            named_bar_sync(6, 128);
 #pragma unroll
-            for (int e = 0; e < 16; e += 4)
-              atomicAdd(reinterpret_cast<float4*>(dst + c0 + e),
-                        make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]),
-                                    __uint_as_float(o[e + 2]), __uint_as_float(o[e + 3])));
+            for (int u = 0; u < 8; ++u)
+              st_shared_v4(sDST + slot + sw128_offset(r, (uint32_t)u), o[4 * u], o[4 * u + 1],
+                           o[4 * u + 2], o[4 * u + 3]);
+            fence_proxy_async_smem();
+            named_bar_sync(6, 128);
+            if (r == 0) {
+              tma_reduce_add_2d(&tm_dq, smem + L::OFF_DST + slot, c * 32, row);
+              bulk_commit_group();
+            }
           }
-          tc_fence_before();
-          mbar_arrive(dq_empty);
+          if (r == 0) {
+            bulk_wait_group_read0();  // the tile may be rewritten with dS^T
+            mbar_arrive(dqs_free);
+          }
         }
         ++dqc;
       }
     }
     // every reduction issued must have completed before the CTA exits
-    if (L::DQ_TMA && r == 0) bulk_wait_group0();
+    if (r == 0) bulk_wait_group0();
   }
 
   tc_fence_before();
