@@ -79,7 +79,7 @@ struct BwdSmem {
   static constexpr int DST_BUFS = PS ? 2 : 1;
   static constexpr int OFF_DQS = OFF_DST + DST_BUFS * SqTile::BYTES;
   static constexpr int OFF_BAR = OFF_DQS + DQS_BYTES;
-  static constexpr int NBAR = 2 + 2 * QST + 13;
+  static constexpr int NBAR = 2 + 2 * QST + 16;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int SLACK = (BYTES + 1024 <= 232448) ? 1024 : 0;
@@ -91,7 +91,10 @@ struct BwdSmem {
   // half: P^T k-steps 0..3 sit at 0.., 4..7 at 64.. (dS^T likewise + 128).
   static constexpr uint32_t T_S = 0, T_DP = 128;
   static constexpr uint32_t T_DV = 256, T_DK = 256 + D;
-  static constexpr uint32_t T_DQ = DQ_ALIAS ? 0 : 256 + 2 * D;
+  // d_h = 128: dQ reuses the dP^T/dS^T columns once dK has read dS^T, so
+  // that the next step's S^T (over P^T, free once dV has read it) need not
+  // wait for dQ to be drained.
+  static constexpr uint32_t T_DQ = DQ_ALIAS ? 128 : 256 + 2 * D;
   // PS: P^T as packed bf16 (query columns 2c, 2c+1 in column T_PT + c), the
   // TMEM A operand of dV; 64 columns, free for d_h <= 64.
   static constexpr uint32_t T_PT = 256 + 3 * D;
@@ -164,7 +167,7 @@ __global__ void __launch_bounds__(512, 1)
   uint64_t* s_full = q_empty + L::QST;   // S^T, dP^T ready
   uint64_t* p_full = s_full + 1;         // P^T, dS^T written (TMEM + smem)
   uint64_t* p_empty = p_full + 1;        // the dS^T smem tile is free again
-  uint64_t* ts_done = p_empty + 1;       // dV/dK MMAs of the step completed
+  uint64_t* ts_done = p_empty + 1;       // (unused)
   uint64_t* dq_full = ts_done + 1;
   uint64_t* dq_empty = dq_full + 1;
   uint64_t* kd_full = dq_empty + 1;
@@ -173,6 +176,9 @@ __global__ void __launch_bounds__(512, 1)
   uint64_t* pt_empty = s_free + 1;       // the P^T columns are free again (PS)
   uint64_t* p_empty2 = pt_empty + 1;     // PS: dS^T tile 1 free again (tile 0: p_empty)
   uint64_t* dqs_free = p_empty2 + 1;     // DQ_DST: the dQ reductions have read the tile
+  uint64_t* dp_full = dqs_free + 1;      // DQ_ALIAS: dP^T ready (s_full: S^T ready)
+  uint64_t* dv_done = dp_full + 1;       // DQ_ALIAS: the step's dV has read P^T
+  uint64_t* dk_done = dv_done + 1;       // DQ_ALIAS: the step's dK has read dS^T
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
   const WaitCtl wc{abort_flag, p.status};
@@ -194,6 +200,9 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(pt_empty, 1);
     mbar_init(p_empty2, 1);
     mbar_init(dqs_free, 1);
+    mbar_init(dp_full, 1);
+    mbar_init(dv_done, 1);
+    mbar_init(dk_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -261,7 +270,7 @@ __global__ void __launch_bounds__(512, 1)
       constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);
       constexpr uint32_t id_acc = idesc_bf16(128, D, false, true);
       constexpr uint32_t id_dq = idesc_bf16(128, D, true, true);
-      uint32_t kvc = 0, qc = 0, pc = 0, tc = 0, dqc = 0, kdc = 0;
+      uint32_t kvc = 0, qc = 0, pc = 0, dqc = 0, kdc = 0;
       // S^T and dP^T of the step whose Q/dO sit in stage `qs_of`.
       auto issue_s = [&](uint32_t qcount) {
         const int qs = qcount % L::QST;
@@ -278,6 +287,29 @@ __global__ void __launch_bounds__(512, 1)
           mma_bf16_ss(tmem + L::T_DP, G::kmajor_desc(sV, kk), G::kmajor_desc(sDO, kk), id_s,
                       kk > 0);
         mma_commit(s_full);
+      };
+      // DQ_ALIAS: S^T and dP^T issued separately (same stage).
+      auto issue_st = [&](uint32_t qcount) {
+        const int qs = qcount % L::QST;
+        mbar_wait(q_full + qs, (qcount / L::QST) & 1, wc, kSiteBMmaQ);
+        tc_fence_after();
+        const uint32_t sQ = smem_u32(smem + L::OFF_Q + qs * L::STAGE);
+#pragma unroll
+        for (int kk = 0; kk < G::KSTEPS; ++kk)
+          mma_bf16_ss(tmem + L::T_S, G::kmajor_desc(sK, kk), G::kmajor_desc(sQ, kk), id_s,
+                      kk > 0);
+        mma_commit(s_full);
+      };
+      auto issue_dpt = [&](uint32_t qcount) {
+        const int qs = qcount % L::QST;
+        mbar_wait(q_full + qs, (qcount / L::QST) & 1, wc, kSiteBMmaQ);
+        tc_fence_after();
+        const uint32_t sDO = smem_u32(smem + L::OFF_Q + qs * L::STAGE) + G::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < G::KSTEPS; ++kk)
+          mma_bf16_ss(tmem + L::T_DP, G::kmajor_desc(sV, kk), G::kmajor_desc(sDO, kk), id_s,
+                      kk > 0);
+        mma_commit(dp_full);
       };
       uint32_t sfc = 0;
       if constexpr (L::PS) {
@@ -303,16 +335,18 @@ __global__ void __launch_bounds__(512, 1)
           }
         }
       }
+      uint32_t dvc = 0, dkc = 0;
       for (int kr = 0, it = snake_item(0, blockIdx.x, gridDim.x); !L::PS && it < p.n_items;
            it = snake_item(++kr, blockIdx.x, gridDim.x)) {
         const BItem w = decode_bwd(p, it);
         mbar_wait(kv_full, kvc & 1, wc, kSiteBMmaKV);
         ++kvc;
-        // S^T/dP^T columns still hold the previous step's P^T/dS^T and, for
-        // d_h = 128, its dQ: both must be consumed first.
-        if (tc > 0) mbar_wait(ts_done, (tc - 1) & 1, wc, kSiteBMmaTS);
-        if (L::DQ_ALIAS) mbar_wait(dq_empty, (dqc & 1) ^ 1, wc, kSiteBMmaDQ);
-        issue_s(qc);
+        // S^T over the previous step's P^T: its dV must have completed.
+        // dP^T over the previous step's dQ: it must have been drained.
+        if (dvc > 0) mbar_wait(dv_done, (dvc - 1) & 1, wc, kSiteBMmaTS);
+        issue_st(qc);
+        mbar_wait(dq_empty, (dqc & 1) ^ 1, wc, kSiteBMmaDQ);
+        issue_dpt(qc);
         for (int t = 0; t < w.nsteps; ++t) {
           const int qs = qc % L::QST;
           const uint32_t sQ = smem_u32(smem + L::OFF_Q + qs * L::STAGE);
@@ -324,27 +358,22 @@ __global__ void __launch_bounds__(512, 1)
           for (int kk = 0; kk < 8; ++kk)
             mma_bf16_ts(tmem + L::T_DV, tmem + L::T_S + L::a_col(kk), G::mnmajor_desc(sDO, kk),
                         id_acc, (t > 0 || kk > 0));
+          mma_commit(dv_done);
+          ++dvc;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_bf16_ts(tmem + L::T_DK, tmem + L::T_DP + L::a_col(kk), G::mnmajor_desc(sQ, kk),
                         id_acc, (t > 0 || kk > 0));
-          mma_commit(ts_done);
+          mma_commit(dk_done);
+          ++dkc;
           mma_commit(q_empty + qs);
-          ++tc;
           ++qc;
           ++pc;
-          if (!L::DQ_ALIAS) {
-            // next step's scores first, so that the compute warps can start
-            // while dQ of this step runs
-            if (t + 1 < w.nsteps) {
-              mbar_wait(ts_done, (tc - 1) & 1, wc, kSiteBMmaTS);
-              issue_s(qc);
-            }
-            mbar_wait(dq_empty, (dqc & 1) ^ 1, wc, kSiteBMmaDQ);
-          } else {
-            mbar_wait(ts_done, (tc - 1) & 1, wc, kSiteBMmaTS);  // P^T read: columns free
-            mbar_wait(dq_empty, (dqc & 1) ^ 1, wc, kSiteBMmaDQ);
+          if (t + 1 < w.nsteps) {
+            mbar_wait(dv_done, (dvc - 1) & 1, wc, kSiteBMmaTS);  // P^T read: S^T columns free
+            issue_st(qc);
           }
+          mbar_wait(dk_done, (dkc - 1) & 1, wc, kSiteBMmaTS);    // dS^T read: columns free
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
@@ -353,9 +382,9 @@ __global__ void __launch_bounds__(512, 1)
           mma_commit(p_empty);
           mma_commit(dq_full);
           ++dqc;
-          if (L::DQ_ALIAS && t + 1 < w.nsteps) {
-            mbar_wait(dq_empty, (dqc & 1) ^ 1, wc, kSiteBMmaDQ);
-            issue_s(qc);
+          if (t + 1 < w.nsteps) {
+            mbar_wait(dq_empty, (dqc & 1) ^ 1, wc, kSiteBMmaDQ);  // dQ drained
+            issue_dpt(qc);
           }
         }
         mma_commit(kd_full);
@@ -498,21 +527,17 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll 1
         for (int c0 = 0; !L::PS && c0 < 64; c0 += 32) {
           const int col = 64 * hf + c0;      // first query column of this chunk
-          uint32_t sv[32], dv[32];
+          // P from S^T first (dP^T may still be on its way), then dS
+          uint32_t sv[32], pk[16], dk[16];
           tmem_ld_x32(trow + L::T_S + col, sv);
-          tmem_ld_x32(trow + L::T_DP + col, dv);
           tmem_wait_ld(sv);
-          tmem_wait_ld(dv);
-          uint32_t pk[16], dk[16];
 #pragma unroll
           for (int k4 = 0; k4 < 32; k4 += 4) {
             const float4 nl = *reinterpret_cast<const float4*>(nl_s + c0 + k4);
-            const float4 nd = *reinterpret_cast<const float4*>(nd_s + c0 + k4);
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
               const int k = k4 + 2 * h2;
               const float l0 = h2 ? nl.z : nl.x, l1 = h2 ? nl.w : nl.y;
-              const float e0 = h2 ? nd.z : nd.x, e1 = h2 ? nd.w : nd.y;
               float x0, x1;
               f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[k]), __uint_as_float(sv[k + 1])), sc2,
                                f2_pack(l0, l1)),
@@ -522,19 +547,36 @@ __global__ void __launch_bounds__(512, 1)
                 if (col + k < r) p0 = 0.f;
                 if (col + k + 1 < r) p1 = 0.f;
               }
-              const uint64_t pp = f2_pack(p0, p1);
-              const uint64_t g2 = f2_mul(
-                  pp, f2_add(f2_pack(__uint_as_float(dv[k]), __uint_as_float(dv[k + 1])),
-                             f2_pack(e0, e1)));
-              float g0, g1;
-              f2_unpack(g2, g0, g1);
+              sv[k] = __float_as_uint(p0);  // P kept in fp32 for dS
+              sv[k + 1] = __float_as_uint(p1);
               pk[k >> 1] = pack_bf16x2(p0, p1);
-              dk[k >> 1] = pack_bf16x2(g0, g1);
             }
           }
-          // P^T and dS^T over this half's columns just read (K-major A
-          // operands of dV and dK), and dS^T into shared memory for dQ.
+          // P^T over this half's S^T columns just read (TMEM A operand of dV)
           tmem_st_x16(trow + L::T_S + 64 * hf + (c0 >> 1), pk);
+          if (c0 == 0 && L::DQ_ALIAS) {
+            mbar_wait(dp_full, sc & 1, wc, kSiteBCmpS);
+            tc_fence_after();
+          }
+          uint32_t dv[32];
+          tmem_ld_x32(trow + L::T_DP + col, dv);
+          tmem_wait_ld(dv);
+#pragma unroll
+          for (int k4 = 0; k4 < 32; k4 += 4) {
+            const float4 nd = *reinterpret_cast<const float4*>(nd_s + c0 + k4);
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const int k = k4 + 2 * h2;
+              const float e0 = h2 ? nd.z : nd.x, e1 = h2 ? nd.w : nd.y;
+              const uint64_t g2 = f2_mul(
+                  f2_pack(__uint_as_float(sv[k]), __uint_as_float(sv[k + 1])),
+                  f2_add(f2_pack(__uint_as_float(dv[k]), __uint_as_float(dv[k + 1])),
+                         f2_pack(e0, e1)));
+              dk[k >> 1] = pack_bf16x2_f2(g2);
+            }
+          }
+          // dS^T over this half's dP^T columns just read (A operand of dK),
+          // and into shared memory for dQ
           tmem_st_x16(trow + L::T_DP + 64 * hf + (c0 >> 1), dk);
           // the dS^T tile in shared memory is read by the previous step's dQ
           // (and, staged there, by its reductions)
