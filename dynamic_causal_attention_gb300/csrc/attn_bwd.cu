@@ -369,10 +369,7 @@ __global__ void __launch_bounds__(512, 1)
           mma_commit(q_empty + qs);
           ++qc;
           ++pc;
-          if (t + 1 < w.nsteps) {
-            mbar_wait(dv_done, (dvc - 1) & 1, wc, kSiteBMmaTS);  // P^T read: S^T columns free
-            issue_st(qc);
-          }
+          // dQ first, so that its drain overlaps the next step's S^T
           mbar_wait(dk_done, (dkc - 1) & 1, wc, kSiteBMmaTS);    // dS^T read: columns free
           tc_fence_after();
 #pragma unroll
@@ -383,6 +380,8 @@ __global__ void __launch_bounds__(512, 1)
           mma_commit(dq_full);
           ++dqc;
           if (t + 1 < w.nsteps) {
+            mbar_wait(dv_done, (dvc - 1) & 1, wc, kSiteBMmaTS);  // P^T read: S^T columns free
+            issue_st(qc);
             mbar_wait(dq_empty, (dqc & 1) ^ 1, wc, kSiteBMmaDQ);  // dQ drained
             issue_dpt(qc);
           }
