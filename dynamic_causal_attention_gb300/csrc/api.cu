@@ -246,7 +246,7 @@ void fill_fwd_params(FwdParams& p, const saf_attn_dims& d, const HeadSplit& hs, 
   p.group_kv = d.H / p.H_kv;
   p.n_static = hs.n_static;
   p.n_dynamic = transposed ? 0 : hs.n_dynamic;
-  p.group = static_group(d.d_h, d.B);
+  p.group = static_group(d.d_h, d.B, transposed);
   p.n_groups = (d.B + p.group - 1) / p.group;
   p.n_items = p.nI * (p.n_static * p.n_groups + (transposed ? 0 : d.B * hs.n_dynamic));
   p.scale_log2 = 1.4426950408889634f / sqrtf((float)d.d_h);

@@ -263,8 +263,11 @@ struct FwdSmem {
   using G = TileGeom<D>;
   // TMEM S/P buffers: three for d_h <= 64 (then S of tile j + 1 only waits for
   // P V of tile j - 2), two for d_h = 128 (the O accumulator needs the rest).
-  static constexpr int NBUF = (D <= 64) ? 3 : 2;
-  static constexpr uint32_t TMEM_O = NBUF * 128;
+  // Three 128-column S/P buffers; the rest holds O (128 columns: one
+  // sequence of a static group at d_h = 128, two at 64).  The transposed
+  // engine at d_h = 128 keeps two buffers so that O holds two sequences.
+  static constexpr int NBUF = 3;
+  static constexpr int NBUF_T = (D == 128) ? 2 : 3;
   static constexpr int KST = (D == 128) ? 2 : 4;  // K ring (also holds static aux)
   static constexpr int VST = (D == 128) ? 3 : 4;  // V ring (consumed a step after K)
   // d_h = 64: a static step's two V tiles in an even-aligned slot pair are one
@@ -276,7 +279,7 @@ struct FwdSmem {
   static constexpr int OFF_V = OFF_K + KST * G::TILE_BYTES;
   static constexpr int OFF_X = OFF_V + VST * G::TILE_BYTES;  // row max / sum exchange
   static constexpr int OFF_BAR = OFF_X + 3 * 2 * 128 * 4;
-  static constexpr int NBAR = 2 + 2 * KST + 2 * VST + 3 * NBUF + 2;
+  static constexpr int NBAR = 2 + 2 * KST + 2 * VST + 3 * NBUF + 2;  // NBUF >= NBUF_T
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int ALLOC = BYTES + 1024;  // slack to align the base to 1024 B
@@ -431,8 +434,8 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* k_empty = k_full + L::KST;
   uint64_t* v_full = k_empty + L::KST;
   uint64_t* v_empty = v_full + L::VST;
-  constexpr int NB = L::NBUF;
-  constexpr uint32_t kTmemO = L::TMEM_O;
+  constexpr int NB = TRANSPOSED ? L::NBUF_T : L::NBUF;
+  constexpr uint32_t kTmemO = NB * 128;
   uint64_t* s_full = v_empty + L::VST;   // S ready (MMA -> compute)
   uint64_t* s_empty = s_full + NB;       // buffer free again: its P V MMAs done (MMA -> all)
   uint64_t* p_full = s_empty + NB;       // P / G written, O rescaled (compute -> MMA)

@@ -35,9 +35,10 @@ struct FwdParams {
 };
 
 // Sequences per static work item: the TMEM columns left for the O
-// accumulator (512 minus the S/P buffers) divided by d_h.
-inline int static_group(int d_h, int B) {
-  const int cols = d_h <= 64 ? 128 : 256;
+// accumulator (512 minus the S/P buffers) divided by d_h.  Three buffers
+// leave 128 columns; the transposed engine at d_h = 128 keeps two (256).
+inline int static_group(int d_h, int B, bool transposed = false) {
+  const int cols = (transposed && d_h == 128) ? 256 : 128;
   const int g = cols / d_h;
   return g < B ? g : B;
 }
