@@ -79,7 +79,7 @@ struct BwdSmem {
   static constexpr int DST_BUFS = PS ? 2 : 1;
   static constexpr int OFF_DQS = OFF_DST + DST_BUFS * SqTile::BYTES;
   static constexpr int OFF_BAR = OFF_DQS + DQS_BYTES;
-  static constexpr int NBAR = 2 + 2 * QST + 16;
+  static constexpr int NBAR = 2 + 2 * QST + 15;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int SLACK = (BYTES + 1024 <= 232448) ? 1024 : 0;
@@ -167,8 +167,7 @@ __global__ void __launch_bounds__(512, 1)
   uint64_t* s_full = q_empty + L::QST;   // S^T, dP^T ready
   uint64_t* p_full = s_full + 1;         // P^T, dS^T written (TMEM + smem)
   uint64_t* p_empty = p_full + 1;        // the dS^T smem tile is free again
-  uint64_t* ts_done = p_empty + 1;       // (unused)
-  uint64_t* dq_full = ts_done + 1;
+  uint64_t* dq_full = p_empty + 1;
   uint64_t* dq_empty = dq_full + 1;
   uint64_t* kd_full = dq_empty + 1;
   uint64_t* kd_empty = kd_full + 1;
@@ -191,7 +190,6 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(s_full, 1);
     mbar_init(p_full, 256);
     mbar_init(p_empty, 1);
-    mbar_init(ts_done, 1);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, 128);
     mbar_init(kd_full, 1);

@@ -44,7 +44,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(BwdPre p) {
 #pragma unroll
   for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
   (void)lane;
-  if (row < rows && p.dq_acc) {
+  // the accumulator rows of frozen heads are never added to or read
+  if (row < rows && p.dq_acc && p.static_slot[(row / p.T) % p.H] == 255) {
     float4* z = reinterpret_cast<float4*>(p.dq_acc + row * D + sub * 8);
     z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
     z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
