@@ -356,7 +356,7 @@ saf_status saf_hybrid_attn_fwd(const saf_attn_dims* dims, const void* Q, const v
   const void* qb = q16 ? q16 : o16;
   const void* kb = k16 ? k16 : v16;
   if (!encode_rows(&fl.tm_q, qb, rows, d.d_h) || !encode_rows(&fl.tm_k, kb, rows_kv, d.d_h) ||
-      !encode_rows(&fl.tm_v, v16, rows_kv, d.d_h))
+      !encode_rows(&fl.tm_v, v16, rows_kv, d.d_h) || !encode_rows(&fl.tm_o, o16, rows, d.d_h))
     return SAF_ERR_CUDA;
   fl.d_h = d.d_h;
   fl.transposed = false;

@@ -192,7 +192,7 @@ extern "C" saf_status saf_hybrid_attn_fwd_noalloc(const saf_attn_dims* dims, con
   const void* qb = Q ? Q : out;
   const void* kb = K ? K : V;
   if (!encode_rows_na(&fl.tm_q, qb, rows, d.d_h) || !encode_rows_na(&fl.tm_k, kb, rows_kv, d.d_h) ||
-      !encode_rows_na(&fl.tm_v, V, rows_kv, d.d_h))
+      !encode_rows_na(&fl.tm_v, V, rows_kv, d.d_h) || !encode_rows_na(&fl.tm_o, out, rows, d.d_h))
     return SAF_ERR_CUDA;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||

@@ -277,7 +277,11 @@ struct FwdSmem {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + G::TILE_BYTES;
   static constexpr int OFF_V = OFF_K + KST * G::TILE_BYTES;
-  static constexpr int OFF_X = OFF_V + VST * G::TILE_BYTES;  // row max / sum exchange
+  // d_h = 64: a dynamic item's output tile is staged here (128-byte swizzled,
+  // as the tensor map expects) and written with one tensor store.
+  static constexpr bool OSTAGE = (D == 64);
+  static constexpr int OFF_OS = OFF_V + VST * G::TILE_BYTES;
+  static constexpr int OFF_X = OFF_OS + (OSTAGE ? G::TILE_BYTES : 0);  // row max / sum exchange
   static constexpr int OFF_BAR = OFF_X + 3 * 2 * 128 * 4;
   static constexpr int NBAR = 2 + 2 * KST + 2 * VST + 3 * NBUF + 2;  // NBUF >= NBUF_T
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
@@ -420,7 +424,8 @@ template <int D, bool TRANSPOSED>
 __global__ void __launch_bounds__(384, 1)
     hybrid_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+                      const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_o, const FwdParams p) {
   using G = TileGeom<D>;
   using L = FwdSmem<D>;
   constexpr int DH = D / 2;  // output columns per compute half
@@ -806,13 +811,43 @@ __global__ void __launch_bounds__(384, 1)
         tc_fence_after();
         const float inv_l = 1.0f / l_tot;
         const size_t orow = ((size_t)(w.b * H + w.h) * T + (size_t)w.X * 128 + r);
-        __nv_bfloat16* dst = p.out + orow * D + hf * DH;
+        if constexpr (L::OSTAGE && !TRANSPOSED) {
+          // O / l as bf16 into the staging tile, then one tensor store
+          uint32_t o[2][16];
+          tmem_ld_x16(trow + kTmemO + hf * DH, o[0]);
+          tmem_ld_x16(trow + kTmemO + hf * DH + 16, o[1]);
+          tmem_wait_ld(o[0]);
+          tmem_wait_ld(o[1]);
+          // the previous item's tensor store has read the staging tile
+          if (warp == 4 && lane == 0) bulk_wait_group_read0();
+          named_bar_sync(1, 256);
+          const uint32_t stg = smem_u32(smem + L::OFF_OS);
 #pragma unroll
-        for (int c0 = 0; c0 < DH; c0 += 16) {
-          uint32_t o[16];
-          tmem_ld_x16(trow + kTmemO + hf * DH + c0, o);
-          tmem_wait_ld(o);
-          store_row16(dst + c0, o, inv_l);
+          for (int h2 = 0; h2 < 2; ++h2) {
+            uint32_t v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              v[e] = pack_bf16x2(__uint_as_float(o[h2][2 * e]) * inv_l,
+                                 __uint_as_float(o[h2][2 * e + 1]) * inv_l);
+            const uint32_t u = (uint32_t)(hf * 4 + 2 * h2);
+            st_shared_v4(stg + sw128_offset(r, u), v[0], v[1], v[2], v[3]);
+            st_shared_v4(stg + sw128_offset(r, u + 1), v[4], v[5], v[6], v[7]);
+          }
+          fence_proxy_async_smem();
+          named_bar_sync(1, 256);
+          if (warp == 4 && lane == 0) {
+            tma_store_2d(&tm_o, smem + L::OFF_OS, 0, (w.b * H + w.h) * T + w.X * 128);
+            bulk_commit_group();
+          }
+        } else {
+          __nv_bfloat16* dst = p.out + orow * D + hf * DH;
+#pragma unroll
+          for (int c0 = 0; c0 < DH; c0 += 16) {
+            uint32_t o[16];
+            tmem_ld_x16(trow + kTmemO + hf * DH + c0, o);
+            tmem_wait_ld(o);
+            store_row16(dst + c0, o, inv_l);
+          }
         }
         if (hf == 0 && p.lse) p.lse[orow] = (m_run + log2f(l_tot)) * kLn2;
         tc_fence_before();
@@ -914,6 +949,8 @@ __global__ void __launch_bounds__(384, 1)
   }
 
   // ------------------------------------------------------------ teardown
+  // every tensor store issued must have completed before the CTA exits
+  if (L::OSTAGE && !TRANSPOSED && warp == 4 && lane == 0) bulk_wait_group0();
   tc_fence_before();
   __syncthreads();
   if (warp == 2) {
@@ -936,7 +973,7 @@ cudaError_t launch_fused(const FwdLaunch& L, cudaStream_t s) {
   if (L.p.n_items == 0) return cudaSuccess;
   const int grid = L.p.n_items < L.num_sms ? L.p.n_items : L.num_sms;
   trace_begin(s);
-  kern<<<grid, 384, S::ALLOC, s>>>(L.tm_q, L.tm_k, L.tm_v, L.p);
+  kern<<<grid, 384, S::ALLOC, s>>>(L.tm_q, L.tm_k, L.tm_v, L.tm_o, L.p);
   trace_end(s, TRANSPOSED ? "static_dv" : "hybrid_fwd");
   return cudaGetLastError();
 }

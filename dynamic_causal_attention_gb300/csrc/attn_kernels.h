@@ -47,6 +47,7 @@ struct FwdLaunch {
   // bf16 views [B*H*T, d_h] (Q) and [B*H_kv*T, d_h] (K, V); tm_v = dO
   // ([B*H*T, d_h]) when transposed
   CUtensorMap tm_q, tm_k, tm_v;
+  CUtensorMap tm_o;  // out [B*H*T, d_h] bf16 (forward, d_h = 64: tiled output stores)
   FwdParams p;
   int d_h;
   bool transposed;
