@@ -441,6 +441,11 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* v_empty = v_full + L::VST;
   constexpr int NB = TRANSPOSED ? L::NBUF_T : L::NBUF;
   constexpr uint32_t kTmemO = NB * 128;
+  // d_h <= 64, forward: the two compute halves take alternate key tiles of a
+  // dynamic item, each with its own running max, sum and O accumulator (O_0
+  // at kTmemO, O_1 after it), merged once per item
+  constexpr bool SPLIT = (D <= 64) && !TRANSPOSED;
+  static_assert(!SPLIT || kTmemO + 2 * D <= kTmemCols, "TMEM: two O accumulators");
   uint64_t* s_full = v_empty + L::VST;   // S ready (MMA -> compute)
   uint64_t* s_empty = s_full + NB;       // buffer free again: its P V MMAs done (MMA -> all)
   uint64_t* p_full = s_empty + NB;       // P / G written, O rescaled (compute -> MMA)
@@ -629,10 +634,19 @@ __global__ void __launch_bounds__(384, 1)
             tc_fence_after();
             const uint32_t vt = sV + vs * G::TILE_BYTES;
             const uint32_t pa = tmem + kTmemS + (u % NB) * 128;
+            if (SPLIT) {
+              // one half wrote all of P, packed, over the buffer's first 64 columns
+              const uint32_t oacc = tmem + kTmemO + (uint32_t)(j & 1) * D;
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_bf16_ts(tmem + kTmemO, pa + p_col(kk), G::mnmajor_desc(vt, kk), idesc_pv,
-                          (j > 0 || kk > 0));
+              for (int kk = 0; kk < 8; ++kk)
+                mma_bf16_ts(oacc, pa + 8 * kk, G::mnmajor_desc(vt, kk), idesc_pv,
+                            (j > 1 || kk > 0));
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                mma_bf16_ts(tmem + kTmemO, pa + p_col(kk), G::mnmajor_desc(vt, kk), idesc_pv,
+                            (j > 0 || kk > 0));
+            }
             mma_commit(v_empty + vs);
             mma_commit(s_empty + (u % NB));
             ++vc;
@@ -704,7 +718,176 @@ __global__ void __launch_bounds__(384, 1)
          it = snake_item(++kr, blockIdx.x, gridDim.x)) {
       const Item w = decode_item<TRANSPOSED>(p, it);
       const uint32_t sc0 = sc;
-      if (!w.is_static) {
+      if (!w.is_static && SPLIT) {
+        kc += w.nsteps;
+        // this half's key tiles: j = hf, hf + 2, ...; a thread holds a whole
+        // row of each of its tiles
+        float m_run = -INFINITY, l_run = 0.f;
+        for (int j = hf; j < w.nsteps; j += 2) {
+          const uint32_t u = sc0 + j;
+          const uint32_t sb = u % NB;
+          const uint32_t sbase = trow + kTmemS + sb * 128;
+          mbar_wait(s_full + sb, (u / NB) & 1, wc, kSiteCmpS);
+          tc_fence_after();
+          uint32_t sr[128];
+          {
+            uint32_t (&a0)[32] = *reinterpret_cast<uint32_t(*)[32]>(sr);
+            uint32_t (&a1)[32] = *reinterpret_cast<uint32_t(*)[32]>(sr + 32);
+            uint32_t (&a2)[32] = *reinterpret_cast<uint32_t(*)[32]>(sr + 64);
+            uint32_t (&a3)[32] = *reinterpret_cast<uint32_t(*)[32]>(sr + 96);
+            tmem_ld_x32(sbase, a0);
+            tmem_ld_x32(sbase + 32, a1);
+            tmem_ld_x32(sbase + 64, a2);
+            tmem_ld_x32(sbase + 96, a3);
+            tmem_wait_ld(a0);
+            tmem_wait_ld(a1);
+            tmem_wait_ld(a2);
+            tmem_wait_ld(a3);
+          }
+          // causal mask on the diagonal tile: key column c > row r
+          if (j == w.X) {
+#pragma unroll
+            for (int c = 0; c < 128; ++c)
+              if (c > r) sr[c] = 0xff800000u;  // -inf
+          }
+          float mx[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mx[k] = fmaxf(__uint_as_float(sr[k]), __uint_as_float(sr[k + 8]));
+#pragma unroll
+          for (int c = 16; c < 128; c += 16)
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              mx[k] = fmax3(mx[k], __uint_as_float(sr[c + k]), __uint_as_float(sr[c + 8 + k]));
+          const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                 fmaxf(mx[6], mx[7])) * p.scale_log2;
+          const float m_new = fmaxf(m_run, mt);
+          const bool need = m_new > m_run + 8.0f;
+          const float m_use = need ? m_new : m_run;
+          const float corr = need ? fast_exp2(m_run - m_new) : 1.0f;
+          const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
+          const uint64_t nm2 = f2_pack(-m_use, -m_use);
+          uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+          // P (packed bf16 pairs) over the buffer's first 64 columns, 16 at a
+          // time: those S columns are already in registers
+#pragma unroll
+          for (int q0 = 0; q0 < 64; q0 += 16) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int qq = 0; qq < 16; ++qq) {
+              const int q = q0 + qq;
+              float x0, x1;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * q]), __uint_as_float(sr[2 * q + 1])),
+                               sc2, nm2),
+                        x0, x1);
+              const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
+              acc[qq & 3] = f2_add(acc[qq & 3], f2_pack(e0, e1));
+              pk[qq] = pack_bf16x2(e0, e1);
+            }
+            tmem_st_x16(sbase + q0, pk);
+          }
+          float rs;
+          {
+            const uint64_t t = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
+            float lo, hi;
+            f2_unpack(t, lo, hi);
+            rs = lo + hi;
+          }
+          // Rescale this half's O when some row of the warp moved its max: the
+          // half's previous P V (two tiles back) must have finished first.
+          if (j > 1 && __any_sync(0xffffffffu, need)) {
+            const uint32_t up = u - 2;
+            mbar_wait(s_empty + (up % NB), (up / NB) & 1, wc, kSiteCmpPV);
+            tc_fence_after();
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 16) {
+              uint32_t o[16];
+              const uint32_t ta = trow + kTmemO + hf * D + c0;
+              tmem_ld_x16(ta, o);
+              tmem_wait_ld(o);
+#pragma unroll
+              for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+              tmem_st_x16(ta, o);
+            }
+          }
+          tmem_wait_st();
+          l_run = l_run * corr + rs;
+          m_run = m_use;
+          tc_fence_before();
+          mbar_arrive_cnt(p_full + sb, 2);  // the other half does not touch this tile
+        }
+        sc = sc0 + w.nsteps;
+        // merge the halves' (max, sum) of each row; a half without tiles (a
+        // one-tile item) has sum 0 and weight 0
+        xmax[hf * 128 + r] = m_run;
+        xsum[hf * 128 + r] = l_run;
+        named_bar_sync(pair_bar, 64);
+        const float m_oth = xmax[(1 - hf) * 128 + r], l_oth = xsum[(1 - hf) * 128 + r];
+        named_bar_sync(pair_bar, 64);  // xsum / xmax may be rewritten by the next item
+        const bool has1 = w.nsteps > 1;
+        const float m0 = hf == 0 ? m_run : m_oth, l0 = hf == 0 ? l_run : l_oth;
+        const float m1 = hf == 0 ? m_oth : m_run, l1 = hf == 0 ? l_oth : l_run;
+        const float mm = has1 ? fmaxf(m0, m1) : m0;
+        const float c0 = fast_exp2(m0 - mm);
+        const float c1 = has1 ? fast_exp2(m1 - mm) : 0.f;
+        const float l_tot = l0 * c0 + l1 * c1;
+        const float inv_l = 1.0f / l_tot;
+        const float w0 = c0 * inv_l, w1 = c1 * inv_l;
+        mbar_wait(o_full, oc & 1, wc, kSiteCmpO);
+        tc_fence_after();
+        // this half writes output columns hf * d_h / 2 .. + d_h / 2 - 1
+        uint32_t o[DH / 16][16];
+#pragma unroll
+        for (int c = 0; c < DH / 16; ++c) tmem_ld_x16(trow + kTmemO + hf * DH + 16 * c, o[c]);
+#pragma unroll
+        for (int c = 0; c < DH / 16; ++c) tmem_wait_ld(o[c]);
+#pragma unroll
+        for (int c = 0; c < DH / 16; ++c)
+#pragma unroll
+          for (int e = 0; e < 16; ++e) o[c][e] = __float_as_uint(__uint_as_float(o[c][e]) * w0);
+        if (has1) {
+#pragma unroll
+          for (int c = 0; c < DH / 16; ++c) {
+            uint32_t o1[16];
+            tmem_ld_x16(trow + kTmemO + D + hf * DH + 16 * c, o1);
+            tmem_wait_ld(o1);
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              o[c][e] = __float_as_uint(fmaf(__uint_as_float(o1[e]), w1, __uint_as_float(o[c][e])));
+          }
+        }
+        const size_t orow = ((size_t)(w.b * H + w.h) * T + (size_t)w.X * 128 + r);
+        if constexpr (L::OSTAGE) {
+          // bf16 into the staging tile, then one tensor store
+          if (warp == 4 && lane == 0) bulk_wait_group_read0();
+          named_bar_sync(1, 256);
+          const uint32_t stg = smem_u32(smem + L::OFF_OS);
+#pragma unroll
+          for (int c = 0; c < DH / 16; ++c) {
+            uint32_t v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              v[e] = pack_bf16x2(__uint_as_float(o[c][2 * e]), __uint_as_float(o[c][2 * e + 1]));
+            const uint32_t u = (uint32_t)(hf * (DH / 8) + 2 * c);
+            st_shared_v4(stg + sw128_offset(r, u), v[0], v[1], v[2], v[3]);
+            st_shared_v4(stg + sw128_offset(r, u + 1), v[4], v[5], v[6], v[7]);
+          }
+          fence_proxy_async_smem();
+          named_bar_sync(1, 256);
+          if (warp == 4 && lane == 0) {
+            tma_store_2d(&tm_o, smem + L::OFF_OS, 0, (w.b * H + w.h) * T + w.X * 128);
+            bulk_commit_group();
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < DH / 16; ++c)
+            store_row16(p.out + orow * D + hf * DH + 16 * c, o[c], 1.0f);
+        }
+        if (hf == 0 && p.lse) p.lse[orow] = (mm + log2f(l_tot)) * kLn2;
+        tc_fence_before();
+        mbar_arrive(o_empty);
+        ++oc;
+      } else if (!w.is_static) {
         kc += w.nsteps;
         float m_run = -INFINITY, l_run = 0.f;
         for (int j = 0; j < w.nsteps; ++j) {
