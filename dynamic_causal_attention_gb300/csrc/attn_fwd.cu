@@ -274,8 +274,11 @@ struct FwdSmem {
   // N = 128 operand (a tile is one 128-byte-swizzled chunk, so the slot
   // stride equals the chunk stride of a [128 x 128] MN-major operand).
   static constexpr bool PAIR_V = (D == 64) && (VST % 2 == 0);
+  // Q tiles: two slots for d_h <= 64 (the next item's Q lands while this
+  // item's score tiles are issued), one for d_h = 128 (shared memory budget)
+  static constexpr int QST = (D == 128) ? 1 : 2;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + G::TILE_BYTES;
+  static constexpr int OFF_K = OFF_Q + QST * G::TILE_BYTES;
   static constexpr int OFF_V = OFF_K + KST * G::TILE_BYTES;
   // d_h = 64: a dynamic item's output tile is staged here (128-byte swizzled,
   // as the tensor map expects) and written with one tensor store.
@@ -283,7 +286,7 @@ struct FwdSmem {
   static constexpr int OFF_OS = OFF_V + VST * G::TILE_BYTES;
   static constexpr int OFF_X = OFF_OS + (OSTAGE ? G::TILE_BYTES : 0);  // row max / sum exchange
   static constexpr int OFF_BAR = OFF_X + 3 * 2 * 128 * 4;
-  static constexpr int NBAR = 2 + 2 * KST + 2 * VST + 3 * NBUF + 2;  // NBUF >= NBUF_T
+  static constexpr int NBAR = 2 * QST + 2 * KST + 2 * VST + 3 * NBUF + 2 + 2;  // NBUF >= NBUF_T
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int ALLOC = BYTES + 1024;  // slack to align the base to 1024 B
@@ -346,12 +349,14 @@ __device__ __forceinline__ void gen_tile(uint32_t colv_s, uint32_t win_s, int rc
   }
 }
 
-// TMEM columns: NBUF 128-column buffers from 0 hold S (fp32).  Each compute
-// half (key columns 0..63 or 64..127 of the tile) writes its P, as packed
-// bf16, over the first 32 columns of its own S half, so P k-steps 0..3 sit at
-// buffer + 0.. and 4..7 at buffer + 64..; static items keep their generated
-// tiles in the same places.  The O accumulator follows the buffers (d_h
-// columns for a dynamic item, group * d_h for a static item).
+// TMEM columns (d_h = 128, and the transposed engine): NBUF 128-column
+// buffers from 0 hold S (fp32).  Each compute half (key columns 0..63 or
+// 64..127 of the tile) writes its P, as packed bf16, over the first 32
+// columns of its own S half, so P k-steps 0..3 sit at buffer + 0.. and 4..7
+// at buffer + 64..; static items keep their generated tiles in the same
+// places.  The O accumulator follows the buffers (d_h columns for a dynamic
+// item, group * d_h for a static item).  The forward at d_h <= 64 lays the
+// columns out differently (see SPLIT in the kernel).
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 0;
 __device__ __forceinline__ uint32_t p_col(int kk) {
@@ -417,9 +422,13 @@ __device__ __forceinline__ void store_row16(__nv_bfloat16* dst, const uint32_t (
   *reinterpret_cast<uint4*>(dst + 8) = v1;
 }
 
-// Threads: warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM owner, warps
-// 4..11 two compute halves (warps 4..7 key columns 0..63, warps 8..11 key
-// columns 64..127 of each tile; a row per thread, two threads per row).
+// Threads: warp 0 TMA producer (Q, K, static tables), warp 2 TMEM owner and V
+// producer, warps 1 and 3 MMA issuers, warps 4..11 two compute halves.
+// d_h = 128 and transposed: warp 1 issues S, warp 3 P V; warps 4..7 take key
+// columns 0..63 and warps 8..11 key columns 64..127 of each tile (a row per
+// thread, two threads per row).  Forward at d_h <= 64 (SPLIT): half g takes
+// the key tiles j = g, g + 2, ... of a dynamic item, whole rows, and warp 1
+// (g = 0) or 3 (g = 1) issues that half's S and P V.
 template <int D, bool TRANSPOSED>
 __global__ void __launch_bounds__(384, 1)
     hybrid_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -434,8 +443,8 @@ __global__ void __launch_bounds__(384, 1)
                                              ~(uintptr_t)1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
   uint64_t* q_full = bars + 0;
-  uint64_t* q_empty = bars + 1;
-  uint64_t* k_full = bars + 2;
+  uint64_t* q_empty = q_full + L::QST;
+  uint64_t* k_full = q_empty + L::QST;
   uint64_t* k_empty = k_full + L::KST;
   uint64_t* v_full = k_empty + L::KST;
   uint64_t* v_empty = v_full + L::VST;
@@ -445,12 +454,22 @@ __global__ void __launch_bounds__(384, 1)
   // dynamic item, each with its own running max, sum and O accumulator (O_0
   // at kTmemO, O_1 after it), merged once per item
   constexpr bool SPLIT = (D <= 64) && !TRANSPOSED;
+  // With SPLIT the TMEM holds two S buffers (columns 0..255), two P buffers
+  // of packed bf16 (256..383: a dynamic tile's P or a static step's
+  // generated tile) and O (384..511).  An S buffer is free once the softmax
+  // has read it, a P buffer once its P V products are done, so the next
+  // score tile never waits for a P V product.
+  constexpr uint32_t kTmemP = 256;
   static_assert(!SPLIT || kTmemO + 2 * D <= kTmemCols, "TMEM: two O accumulators");
+  static_assert(!SPLIT || kTmemP + 128 <= kTmemO, "TMEM: two P buffers");
   uint64_t* s_full = v_empty + L::VST;   // S ready (MMA -> compute)
-  uint64_t* s_empty = s_full + NB;       // buffer free again: its P V MMAs done (MMA -> all)
+  // buffer free again: its P V MMAs done (MMA -> all); with SPLIT: the
+  // softmax has read the S buffer (compute -> S issuer, 128 arrivals)
+  uint64_t* s_empty = s_full + NB;
   uint64_t* p_full = s_empty + NB;       // P / G written, O rescaled (compute -> MMA)
   uint64_t* o_full = p_full + NB;
   uint64_t* o_empty = o_full + 1;
+  uint64_t* p_empty = o_empty + 1;       // SPLIT: P buffer's P V products done (two)
   float* xmax = reinterpret_cast<float*>(smem + L::OFF_X);  // [2 parity][2 halves][128]
   float* xsum = xmax + 2 * 2 * 128;                         // [2 halves][128]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
@@ -459,16 +478,18 @@ __global__ void __launch_bounds__(384, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
+    // with SPLIT both MMA issuers release a Q slot and both complete O
+    for (int s = 0; s < L::QST; ++s) { mbar_init(q_full + s, 1); mbar_init(q_empty + s, SPLIT ? 2 : 1); }
     for (int s = 0; s < L::KST; ++s) { mbar_init(k_full + s, 1); mbar_init(k_empty + s, 1); }
     for (int s = 0; s < L::VST; ++s) { mbar_init(v_full + s, 1); mbar_init(v_empty + s, 1); }
     for (int s = 0; s < NB; ++s) {
       mbar_init(s_full + s, 1);
-      mbar_init(s_empty + s, 1);
+      mbar_init(s_empty + s, SPLIT ? 128 : 1);
       mbar_init(p_full + s, 256);
     }
-    mbar_init(o_full, 1);
+    mbar_init(p_empty, 1);
+    mbar_init(p_empty + 1, 1);
+    mbar_init(o_full, SPLIT ? 2 : 1);
     mbar_init(o_empty, 256);
     *abort_flag = 0;
     fence_barrier_init();
@@ -486,13 +507,15 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t sQ = smem_u32(smem + L::OFF_Q);
   const uint32_t sK = smem_u32(smem + L::OFF_K);
   const uint32_t sV = smem_u32(smem + L::OFF_V);
   const int H = p.H, T = p.T;
 
-  if (warp == 0) {
-    // ---------------------------------------------------------- producer
+  if (warp == 0 || warp == 2) {
+    // ---------------------------------------------------------- producers
+    // warp 0: Q, K (and a static step's tables); warp 2 (after the TMEM
+    // allocation): V, so that neither ring waits behind the other
+    const bool kprod = (warp == 0);
     if (lane == 0) {
       uint32_t qc = 0, kc = 0, vc = 0;
       for (int kr = 0, it = snake_item(0, blockIdx.x, gridDim.x); it < p.n_items;
@@ -501,31 +524,37 @@ __global__ void __launch_bounds__(384, 1)
         if (!w.is_static) {
           const int row0 = (w.b * H + w.h) * T;                           // Q rows
           const int kv0 = (w.b * p.H_kv + w.h / p.group_kv) * T;          // K/V rows
-          mbar_wait(q_empty, (qc & 1) ^ 1, wc, kSiteProdQ);
-          ++qc;
-          mbar_arrive_expect_tx(q_full, G::TILE_BYTES);
-          for (int c = 0; c < G::NCHUNK; ++c)
-            tma_load_2d(smem + L::OFF_Q + c * G::CHUNK_BYTES, &tm_q, q_full, c * G::CHUNK,
-                        row0 + w.X * 128);
-          for (int j = 0; j < w.nsteps; ++j) {
-            const int ks = kc % L::KST;
-            mbar_wait(k_empty + ks, ((kc / L::KST) & 1) ^ 1, wc, kSiteProdK);
-            ++kc;
-            mbar_arrive_expect_tx(k_full + ks, G::TILE_BYTES);
+          if (kprod) {
+            const int qs = qc % L::QST;
+            mbar_wait(q_empty + qs, ((qc / L::QST) & 1) ^ 1, wc, kSiteProdQ);
+            ++qc;
+            mbar_arrive_expect_tx(q_full + qs, G::TILE_BYTES);
             for (int c = 0; c < G::NCHUNK; ++c)
-              tma_load_2d(smem + L::OFF_K + ks * G::TILE_BYTES + c * G::CHUNK_BYTES, &tm_k,
-                          k_full + ks, c * G::CHUNK, kv0 + j * 128);
-            const int vs = vc % L::VST;
-            mbar_wait(v_empty + vs, ((vc / L::VST) & 1) ^ 1, wc, kSiteProdV);
-            ++vc;
-            mbar_arrive_expect_tx(v_full + vs, G::TILE_BYTES);
-            for (int c = 0; c < G::NCHUNK; ++c)
-              tma_load_2d(smem + L::OFF_V + vs * G::TILE_BYTES + c * G::CHUNK_BYTES, &tm_v,
-                          v_full + vs, c * G::CHUNK, kv0 + j * 128);
+              tma_load_2d(smem + L::OFF_Q + qs * G::TILE_BYTES + c * G::CHUNK_BYTES, &tm_q,
+                          q_full + qs, c * G::CHUNK, row0 + w.X * 128);
+            for (int j = 0; j < w.nsteps; ++j) {
+              const int ks = kc % L::KST;
+              mbar_wait(k_empty + ks, ((kc / L::KST) & 1) ^ 1, wc, kSiteProdK);
+              ++kc;
+              mbar_arrive_expect_tx(k_full + ks, G::TILE_BYTES);
+              for (int c = 0; c < G::NCHUNK; ++c)
+                tma_load_2d(smem + L::OFF_K + ks * G::TILE_BYTES + c * G::CHUNK_BYTES, &tm_k,
+                            k_full + ks, c * G::CHUNK, kv0 + j * 128);
+            }
+          } else {
+            for (int j = 0; j < w.nsteps; ++j) {
+              const int vs = vc % L::VST;
+              mbar_wait(v_empty + vs, ((vc / L::VST) & 1) ^ 1, wc, kSiteProdV);
+              ++vc;
+              mbar_arrive_expect_tx(v_full + vs, G::TILE_BYTES);
+              for (int c = 0; c < G::NCHUNK; ++c)
+                tma_load_2d(smem + L::OFF_V + vs * G::TILE_BYTES + c * G::CHUNK_BYTES, &tm_v,
+                            v_full + vs, c * G::CHUNK, kv0 + j * 128);
+            }
           }
         } else {
-          // The tables of a step go into the K ring one step ahead of its V
-          // tiles, so that the compute warps never wait behind a V slot.
+          // A static step's tables go into the K ring (warp 0), its V tiles
+          // into the V ring (warp 2).
           auto load_aux = [&](int step) {
             // inner tile Y: J (forward) or I (transposed)
             const int Y = TRANSPOSED ? (w.X + step) : step;
@@ -543,38 +572,171 @@ __global__ void __launch_bounds__(384, 1)
             bulk_load(aux + L::AUX_WIN, p.r_tab + (size_t)w.hs * (T + 128) + dist0 * 128, 1024,
                       k_full + ks);
           };
-          load_aux(0);
-          for (int step = 0; step < w.nsteps; ++step) {
-            const int Y = TRANSPOSED ? (w.X + step) : step;
-            if (step + 1 < w.nsteps) load_aux(step + 1);
-            if (L::PAIR_V && w.nb == 2 && (vc & 1)) {
-              // the pair must start at an even slot: one slot carries nothing
-              const int vs = vc % L::VST;
-              mbar_wait(v_empty + vs, ((vc / L::VST) & 1) ^ 1, wc, kSiteProdV);
-              ++vc;
-              mbar_arrive(v_full + vs);
-            }
-            for (int bb = 0; bb < w.nb; ++bb) {
-              const int vs = vc % L::VST;
-              mbar_wait(v_empty + vs, ((vc / L::VST) & 1) ^ 1, wc, kSiteProdV);
-              ++vc;
-              mbar_arrive_expect_tx(v_full + vs, G::TILE_BYTES);
-              // forward: V of the head's K/V group; transposed: dO of the head
-              const int row0 = TRANSPOSED ? ((w.b + bb) * H + w.h) * T
-                                          : ((w.b + bb) * p.H_kv + w.h / p.group_kv) * T;
-              for (int c = 0; c < G::NCHUNK; ++c)
-                tma_load_2d(smem + L::OFF_V + vs * G::TILE_BYTES + c * G::CHUNK_BYTES, &tm_v,
-                            v_full + vs, c * G::CHUNK, row0 + Y * 128);
+          if (kprod) {
+            for (int step = 0; step < w.nsteps; ++step) load_aux(step);
+          } else {
+            for (int step = 0; step < w.nsteps; ++step) {
+              const int Y = TRANSPOSED ? (w.X + step) : step;
+              if (L::PAIR_V && w.nb == 2 && (vc & 1)) {
+                // the pair must start at an even slot: one slot carries nothing
+                const int vs = vc % L::VST;
+                mbar_wait(v_empty + vs, ((vc / L::VST) & 1) ^ 1, wc, kSiteProdV);
+                ++vc;
+                mbar_arrive(v_full + vs);
+              }
+              for (int bb = 0; bb < w.nb; ++bb) {
+                const int vs = vc % L::VST;
+                mbar_wait(v_empty + vs, ((vc / L::VST) & 1) ^ 1, wc, kSiteProdV);
+                ++vc;
+                mbar_arrive_expect_tx(v_full + vs, G::TILE_BYTES);
+                // forward: V of the head's K/V group; transposed: dO of the head
+                const int row0 = TRANSPOSED ? ((w.b + bb) * H + w.h) * T
+                                            : ((w.b + bb) * p.H_kv + w.h / p.group_kv) * T;
+                for (int c = 0; c < G::NCHUNK; ++c)
+                  tma_load_2d(smem + L::OFF_V + vs * G::TILE_BYTES + c * G::CHUNK_BYTES, &tm_v,
+                              v_full + vs, c * G::CHUNK, row0 + Y * 128);
+              }
             }
           }
         }
       }
       // Drain: every copy issued must have landed before the CTA exits.
-      if (qc > 0) mbar_drain(q_full, (qc - 1) & 1);
+      for (int s = 0; s < L::QST; ++s)
+        if (qc > (uint32_t)s) mbar_drain(q_full + s, ((qc - 1 - s) / L::QST) & 1);
       for (int s = 0; s < L::KST; ++s)
         if (kc > (uint32_t)s) mbar_drain(k_full + s, ((kc - 1 - s) / L::KST) & 1);
       for (int s = 0; s < L::VST; ++s)
         if (vc > (uint32_t)s) mbar_drain(v_full + s, ((vc - 1 - s) / L::VST) & 1);
+    }
+  } else if (SPLIT && (warp == 1 || warp == 3)) {
+    // ---------------------------------------------------------- MMA issuers
+    // Issuer g (warp 1: g = 0, warp 3: g = 1) issues S and P V of the key
+    // tiles j = g, g + 2, ... of a dynamic item, i.e. of compute half g, so
+    // that one half's products never queue behind the other half's softmax.
+    // Static items: issuer 0 issues every step (one accumulation chain),
+    // issuer 1 only keeps its ring counts.
+    if (lane == 0) {
+      const int g = (warp == 1) ? 0 : 1;
+      constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16(128, D, false, true);
+      constexpr uint32_t idesc_pair = idesc_bf16(128, 2 * D, false, true);
+      uint32_t qc = 0, kc = 0, vc = 0, sc = 0, ss = 0, oc = 0;
+      for (int kr = 0, it = snake_item(0, blockIdx.x, gridDim.x); it < p.n_items;
+           it = snake_item(++kr, blockIdx.x, gridDim.x)) {
+        const Item w = decode_item<TRANSPOSED>(p, it);
+        // before the first product into O: the previous item's O has been
+        // read out (an issuer without products waits too, so that its
+        // o_full arrival falls into this item's phase)
+        bool o_ready = false;
+        auto wait_o = [&]() {
+          if (!o_ready) mbar_wait(o_empty, (oc & 1) ^ 1, wc, kSiteMmaO);
+          o_ready = true;
+        };
+        if (!w.is_static) {
+          const int qs = qc % L::QST;
+          const uint32_t sQ = smem_u32(smem + L::OFF_Q + qs * G::TILE_BYTES);
+          mbar_wait(q_full + qs, (qc / L::QST) & 1, wc, kSiteMmaQ);
+          ++qc;
+          auto issue_s = [&](int j) {
+            const uint32_t us = ss + j, b = us & 1;
+            const uint32_t kq = kc + j;
+            const int ks = kq % L::KST;
+            mbar_wait(k_full + ks, (kq / L::KST) & 1, wc, kSiteMmaK);
+            mbar_wait(s_empty + b, ((us >> 1) & 1) ^ 1, wc, kSiteMmaS);
+            tc_fence_after();
+            const uint32_t kt = sK + ks * G::TILE_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < G::KSTEPS; ++kk)
+              mma_bf16_ss(tmem + kTmemS + b * 128, G::kmajor_desc(sQ, kk), G::kmajor_desc(kt, kk),
+                          idesc_s, kk > 0);
+            mma_commit(k_empty + ks);
+            mma_commit(s_full + b);
+          };
+          auto issue_pv = [&](int j) {
+            const uint32_t u = sc + j, pb = u & 1;
+            const uint32_t vq = vc + j;
+            const int vs = vq % L::VST;
+            mbar_wait(v_full + vs, (vq / L::VST) & 1, wc, kSiteMmaV);
+            mbar_wait(p_full + pb, (u >> 1) & 1, wc, kSiteMmaP);
+            tc_fence_after();
+            const uint32_t vt = sV + vs * G::TILE_BYTES;
+            const uint32_t pa = tmem + kTmemP + pb * 64;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_bf16_ts(tmem + kTmemO + (uint32_t)g * D, pa + 8 * kk, G::mnmajor_desc(vt, kk),
+                          idesc_pv, (j > 1 || kk > 0));
+            mma_commit(v_empty + vs);
+            mma_commit(p_empty + pb);
+          };
+          // S of the half's next tile goes out as soon as the half has read
+          // the previous one; its P V once the P is written
+          if (g < w.nsteps) issue_s(g);
+          for (int j = g; j < w.nsteps; j += 2) {
+            if (j + 2 < w.nsteps) issue_s(j + 2);
+            wait_o();
+            issue_pv(j);
+          }
+          mma_commit(q_empty + qs);
+          kc += w.nsteps;
+          vc += w.nsteps;
+          ss += w.nsteps;
+        } else {
+          kc += w.nsteps;  // the aux entries of static steps are consumed by the compute warps
+          for (int step = 0; step < w.nsteps; ++step) {
+            const uint32_t u = sc + step, pb = u & 1;
+            if (g == 1) {
+              // the V ring positions issuer 0 consumes for this step
+              if (L::PAIR_V && w.nb == 2 && (vc & 1)) ++vc;
+              vc += w.nb;
+              continue;
+            }
+            mbar_wait(p_full + pb, (u >> 1) & 1, wc, kSiteMmaP);
+            wait_o();
+            const uint32_t ga = tmem + kTmemP + pb * 64;
+            if (L::PAIR_V && w.nb == 2) {
+              // Two sequences' V tiles in adjacent slots form one [128 x 2 d_h]
+              // MN-major operand (the slot stride is the chunk stride), so one
+              // N = 2 d_h product fills O_b0 | O_b1.
+              if (vc & 1) {
+                const int vs = vc % L::VST;
+                mbar_wait(v_full + vs, (vc / L::VST) & 1, wc, kSiteMmaV);
+                mma_commit(v_empty + vs);
+                ++vc;
+              }
+              const int vs = vc % L::VST;
+              mbar_wait(v_full + vs, (vc / L::VST) & 1, wc, kSiteMmaV);
+              mbar_wait(v_full + vs + 1, ((vc + 1) / L::VST) & 1, wc, kSiteMmaV);
+              tc_fence_after();
+              const uint32_t vt = sV + vs * G::TILE_BYTES;
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                mma_bf16_ts(tmem + kTmemO, ga + 8 * kk, G::mnmajor_desc(vt, kk), idesc_pair,
+                            (step > 0 || kk > 0));
+              mma_commit(v_empty + vs);
+              mma_commit(v_empty + vs + 1);
+              vc += 2;
+            } else {
+              for (int bb = 0; bb < w.nb; ++bb) {
+                const int vs = vc % L::VST;
+                mbar_wait(v_full + vs, (vc / L::VST) & 1, wc, kSiteMmaV);
+                tc_fence_after();
+                const uint32_t vt = sV + vs * G::TILE_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                  mma_bf16_ts(tmem + kTmemO + bb * D, ga + 8 * kk, G::mnmajor_desc(vt, kk),
+                              idesc_pv, (step > 0 || kk > 0));
+                mma_commit(v_empty + vs);
+                ++vc;
+              }
+            }
+            mma_commit(p_empty + pb);
+          }
+        }
+        sc += w.nsteps;
+        wait_o();
+        mma_commit(o_full);  // (with no products pending this arrives at once)
+        ++oc;
+      }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- S issuer
@@ -589,7 +751,9 @@ __global__ void __launch_bounds__(384, 1)
         const Item w = decode_item<TRANSPOSED>(p, it);
         const uint32_t sc0 = sc;
         if (!w.is_static) {
-          mbar_wait(q_full, qc & 1, wc, kSiteMmaQ);
+          const int qs = qc % L::QST;
+          const uint32_t sQ = smem_u32(smem + L::OFF_Q + qs * G::TILE_BYTES);
+          mbar_wait(q_full + qs, (qc / L::QST) & 1, wc, kSiteMmaQ);
           ++qc;
           for (int j = 0; j < w.nsteps; ++j) {
             const uint32_t u = sc0 + j;
@@ -605,7 +769,7 @@ __global__ void __launch_bounds__(384, 1)
                           idesc_s, kk > 0);
             mma_commit(k_empty + ks);
             mma_commit(s_full + b);
-            if (j == w.nsteps - 1) mma_commit(q_empty);
+            if (j == w.nsteps - 1) mma_commit(q_empty + qs);
             ++kc;
           }
         } else {
@@ -629,26 +793,18 @@ __global__ void __launch_bounds__(384, 1)
             const uint32_t u = sc0 + j;
             const int vs = vc % L::VST;
             mbar_wait(v_full + vs, (vc / L::VST) & 1, wc, kSiteMmaV);
-            mbar_wait(p_full + (u % NB), (u / NB) & 1, wc, kSiteMmaP);
+            const uint32_t pb = u % NB;
+            mbar_wait(p_full + pb, (u / NB) & 1, wc, kSiteMmaP);
             if (j == 0) mbar_wait(o_empty, (oc & 1) ^ 1, wc, kSiteMmaO);
             tc_fence_after();
             const uint32_t vt = sV + vs * G::TILE_BYTES;
-            const uint32_t pa = tmem + kTmemS + (u % NB) * 128;
-            if (SPLIT) {
-              // one half wrote all of P, packed, over the buffer's first 64 columns
-              const uint32_t oacc = tmem + kTmemO + (uint32_t)(j & 1) * D;
+            const uint32_t pa = tmem + kTmemS + pb * 128;
 #pragma unroll
-              for (int kk = 0; kk < 8; ++kk)
-                mma_bf16_ts(oacc, pa + 8 * kk, G::mnmajor_desc(vt, kk), idesc_pv,
-                            (j > 1 || kk > 0));
-            } else {
-#pragma unroll
-              for (int kk = 0; kk < 8; ++kk)
-                mma_bf16_ts(tmem + kTmemO, pa + p_col(kk), G::mnmajor_desc(vt, kk), idesc_pv,
-                            (j > 0 || kk > 0));
-            }
+            for (int kk = 0; kk < 8; ++kk)
+              mma_bf16_ts(tmem + kTmemO, pa + p_col(kk), G::mnmajor_desc(vt, kk), idesc_pv,
+                          (j > 0 || kk > 0));
             mma_commit(v_empty + vs);
-            mma_commit(s_empty + (u % NB));
+            mma_commit(s_empty + pb);
             ++vc;
           }
           mma_commit(o_full);
@@ -656,9 +812,10 @@ __global__ void __launch_bounds__(384, 1)
         } else {
           for (int step = 0; step < w.nsteps; ++step) {
             const uint32_t u = sc0 + step;
-            mbar_wait(p_full + (u % NB), (u / NB) & 1, wc, kSiteMmaP);
+            const uint32_t pb = u % NB;
+            mbar_wait(p_full + pb, (u / NB) & 1, wc, kSiteMmaP);
             if (step == 0) mbar_wait(o_empty, (oc & 1) ^ 1, wc, kSiteMmaO);
-            const uint32_t ga = tmem + kTmemS + (u % NB) * 128;
+            const uint32_t ga = tmem + kTmemS + pb * 128;
             if (L::PAIR_V && w.nb == 2) {
               // Two sequences' V tiles in adjacent slots form one [128 x 2 d_h]
               // MN-major operand (the slot stride is the chunk stride), so one
@@ -697,8 +854,8 @@ __global__ void __launch_bounds__(384, 1)
             }
             // every use of a TMEM buffer completes one phase of both of its
             // barriers, so that the compute warps can count uses uniformly
-            mma_commit(s_full + (u % NB));
-            mma_commit(s_empty + (u % NB));
+            mma_commit(s_full + pb);
+            mma_commit(s_empty + pb);
           }
           mma_commit(o_full);
           ++oc;
@@ -714,6 +871,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
     const int pair_bar = 2 + q4;                 // the two warps that share these rows
     uint32_t kc = 0, sc = 0, oc = 0;
+    uint32_t ss = 0;  // SPLIT: S ring uses (dynamic steps); sc counts P ring uses (all steps)
     for (int kr = 0, it = snake_item(0, blockIdx.x, gridDim.x); it < p.n_items;
          it = snake_item(++kr, blockIdx.x, gridDim.x)) {
       const Item w = decode_item<TRANSPOSED>(p, it);
@@ -724,10 +882,12 @@ __global__ void __launch_bounds__(384, 1)
         // row of each of its tiles
         float m_run = -INFINITY, l_run = 0.f;
         for (int j = hf; j < w.nsteps; j += 2) {
-          const uint32_t u = sc0 + j;
-          const uint32_t sb = u % NB;
+          const uint32_t us = ss + j;   // S ring use
+          const uint32_t u = sc0 + j;   // P ring use
+          const uint32_t sb = us & 1, pb = u & 1;
           const uint32_t sbase = trow + kTmemS + sb * 128;
-          mbar_wait(s_full + sb, (u / NB) & 1, wc, kSiteCmpS);
+          const uint32_t pbase = trow + kTmemP + pb * 64;
+          mbar_wait(s_full + sb, (us >> 1) & 1, wc, kSiteCmpS);
           tc_fence_after();
           uint32_t sr[128];
           {
@@ -744,6 +904,9 @@ __global__ void __launch_bounds__(384, 1)
             tmem_wait_ld(a2);
             tmem_wait_ld(a3);
           }
+          // the S buffer may take the next score tile
+          tc_fence_before();
+          mbar_arrive(s_empty + sb);
           // causal mask on the diagonal tile: key column c > row r
           if (j == w.X) {
 #pragma unroll
@@ -768,8 +931,12 @@ __global__ void __launch_bounds__(384, 1)
           const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
           const uint64_t nm2 = f2_pack(-m_use, -m_use);
           uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-          // P (packed bf16 pairs) over the buffer's first 64 columns, 16 at a
-          // time: those S columns are already in registers
+          // the P buffer is free once the P V products of two uses back are
+          // done (for j >= 2 those are this half's previous tile, so O_hf is
+          // also final for a rescale)
+          mbar_wait(p_empty + pb, ((u >> 1) & 1) ^ 1, wc, kSiteCmpPV);
+          tc_fence_after();
+          // P as packed bf16 pairs, 16 columns at a time
 #pragma unroll
           for (int q0 = 0; q0 < 64; q0 += 16) {
             uint32_t pk[16];
@@ -784,7 +951,7 @@ __global__ void __launch_bounds__(384, 1)
               acc[qq & 3] = f2_add(acc[qq & 3], f2_pack(e0, e1));
               pk[qq] = pack_bf16x2(e0, e1);
             }
-            tmem_st_x16(sbase + q0, pk);
+            tmem_st_x16(pbase + q0, pk);
           }
           float rs;
           {
@@ -793,12 +960,9 @@ __global__ void __launch_bounds__(384, 1)
             f2_unpack(t, lo, hi);
             rs = lo + hi;
           }
-          // Rescale this half's O when some row of the warp moved its max: the
-          // half's previous P V (two tiles back) must have finished first.
+          // Rescale this half's O when some row of the warp moved its max
+          // (its previous P V has finished: the P buffer wait above).
           if (j > 1 && __any_sync(0xffffffffu, need)) {
-            const uint32_t up = u - 2;
-            mbar_wait(s_empty + (up % NB), (up / NB) & 1, wc, kSiteCmpPV);
-            tc_fence_after();
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 16) {
               uint32_t o[16];
@@ -814,9 +978,10 @@ __global__ void __launch_bounds__(384, 1)
           l_run = l_run * corr + rs;
           m_run = m_use;
           tc_fence_before();
-          mbar_arrive_cnt(p_full + sb, 2);  // the other half does not touch this tile
+          mbar_arrive_cnt(p_full + pb, 2);  // the other half does not touch this tile
         }
         sc = sc0 + w.nsteps;
+        ss += w.nsteps;
         // merge the halves' (max, sum) of each row; a half without tiles (a
         // one-tile item) has sum 0 and weight 0
         xmax[hf * 128 + r] = m_run;
@@ -1057,9 +1222,14 @@ __global__ void __launch_bounds__(384, 1)
           const float* colv = aux + 64 * hf;       // this half's 64 column values
           const float* win = aux + L::AUX_WIN / 4; // window, centre at 127
           // the TMEM buffer must be free: the MMAs of two steps back are done
-          mbar_wait(s_empty + (u % NB), ((u / NB) & 1) ^ 1, wc, kSiteCmpP);
+          if (SPLIT)
+            mbar_wait(p_empty + (u & 1), ((u >> 1) & 1) ^ 1, wc, kSiteCmpP);
+          else
+            mbar_wait(s_empty + (u % NB), ((u / NB) & 1) ^ 1, wc, kSiteCmpP);
           tc_fence_after();
-          const uint32_t gdst = trow + kTmemS + (u % NB) * 128 + 64 * hf;
+          // this half's 64 keys as 32 packed columns
+          const uint32_t gdst = SPLIT ? trow + kTmemP + (u & 1) * 64 + 32 * hf
+                                      : trow + kTmemS + (u % NB) * 128 + 64 * hf;
           if (exact)
             gen_tile<TRANSPOSED, true, false>(smem_u32(colv), smem_u32(win), r - 64 * hf, row2,
                                               gdst, zpart, zround);
@@ -1072,7 +1242,7 @@ __global__ void __launch_bounds__(384, 1)
           ++kc;
           tmem_wait_st();
           tc_fence_before();
-          mbar_arrive(p_full + (u % NB));
+          mbar_arrive(p_full + (SPLIT ? (u & 1) : (u % NB)));
         }
         sc = sc0 + w.nsteps;
         // forward, factored: Z'(i) = both halves' sums.  out = O divided by
