@@ -268,7 +268,8 @@ struct FwdSmem {
   // engine at d_h = 128 keeps two buffers so that O holds two sequences.
   static constexpr int NBUF = 3;
   static constexpr int NBUF_T = (D == 128) ? 2 : 3;
-  static constexpr int KST = (D == 128) ? 2 : 4;  // K ring (also holds static aux)
+  // K ring; d_h <= 64 forward: two rings of two, one per MMA issuer
+  static constexpr int KST = (D == 128) ? 2 : 4;
   static constexpr int VST = (D == 128) ? 3 : 4;  // V ring (consumed a step after K)
   // d_h = 64: a static step's two V tiles in an even-aligned slot pair are one
   // N = 128 operand (a tile is one 128-byte-swizzled chunk, so the slot
@@ -285,14 +286,19 @@ struct FwdSmem {
   static constexpr bool OSTAGE = (D == 64);
   static constexpr int OFF_OS = OFF_V + VST * G::TILE_BYTES;
   static constexpr int OFF_X = OFF_OS + (OSTAGE ? G::TILE_BYTES : 0);  // row max / sum exchange
-  static constexpr int OFF_BAR = OFF_X + 3 * 2 * 128 * 4;
-  static constexpr int NBAR = 2 * QST + 2 * KST + 2 * VST + 3 * NBUF + 2 + 2;  // NBUF >= NBUF_T
+  // a static step's generator tables (a ring of its own, read only by the
+  // compute warps)
+  static constexpr int AST = 4;
+  static constexpr int AUX_SLOT = 2048;
+  static constexpr int OFF_AUX = OFF_X + 3 * 2 * 128 * 4;
+  static constexpr int OFF_BAR = OFF_AUX + AST * AUX_SLOT;
+  static constexpr int NBAR = 2 * QST + 2 * KST + 2 * VST + 3 * NBUF + 2 + 2 + 2 * AST;  // NBUF >= NBUF_T
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int ALLOC = BYTES + 1024;  // slack to align the base to 1024 B
   static_assert(ALLOC <= 232448, "shared memory budget exceeded");
-  // aux block (static items) inside a K-ring slot: 128 column values then a
-  // 256-entry distance window.
+  // a table slot (static items): 128 column values then a 256-entry distance
+  // window.
   static constexpr int AUX_COL = 0;
   static constexpr int AUX_WIN = 512;
   static constexpr int AUX_BYTES = 512 + 1024;
@@ -454,11 +460,13 @@ __global__ void __launch_bounds__(384, 1)
   // dynamic item, each with its own running max, sum and O accumulator (O_0
   // at kTmemO, O_1 after it), merged once per item
   constexpr bool SPLIT = (D <= 64) && !TRANSPOSED;
-  // With SPLIT the TMEM holds two S buffers (columns 0..255), two P buffers
-  // of packed bf16 (256..383: a dynamic tile's P or a static step's
-  // generated tile) and O (384..511).  An S buffer is free once the softmax
-  // has read it, a P buffer once its P V products are done, so the next
-  // score tile never waits for a P V product.
+  // With SPLIT the TMEM holds two S buffers (columns 0..255, buffer g for
+  // compute half g and its issuer, so each has one producer and one
+  // consumer), two P buffers of packed bf16 (256..383: a dynamic tile's P or
+  // a static step's generated tile) and O (384..511).  An S buffer is free
+  // once the softmax has read it, a P buffer once its P V products are done,
+  // so the next score tile never waits for a P V product.  K tiles likewise
+  // go to a ring per issuer (slots 2g, 2g + 1).
   constexpr uint32_t kTmemP = 256;
   static_assert(!SPLIT || kTmemO + 2 * D <= kTmemCols, "TMEM: two O accumulators");
   static_assert(!SPLIT || kTmemP + 128 <= kTmemO, "TMEM: two P buffers");
@@ -470,6 +478,8 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* o_full = p_full + NB;
   uint64_t* o_empty = o_full + 1;
   uint64_t* p_empty = o_empty + 1;       // SPLIT: P buffer's P V products done (two)
+  uint64_t* aux_full = p_empty + 2;      // static tables landed (TMA -> compute)
+  uint64_t* aux_empty = aux_full + L::AST;  // static tables read (compute -> producer)
   float* xmax = reinterpret_cast<float*>(smem + L::OFF_X);  // [2 parity][2 halves][128]
   float* xsum = xmax + 2 * 2 * 128;                         // [2 halves][128]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
@@ -489,6 +499,7 @@ __global__ void __launch_bounds__(384, 1)
     }
     mbar_init(p_empty, 1);
     mbar_init(p_empty + 1, 1);
+    for (int s = 0; s < L::AST; ++s) { mbar_init(aux_full + s, 1); mbar_init(aux_empty + s, 1); }
     mbar_init(o_full, SPLIT ? 2 : 1);
     mbar_init(o_empty, 256);
     *abort_flag = 0;
@@ -517,7 +528,8 @@ __global__ void __launch_bounds__(384, 1)
     // allocation): V, so that neither ring waits behind the other
     const bool kprod = (warp == 0);
     if (lane == 0) {
-      uint32_t qc = 0, kc = 0, vc = 0;
+      uint32_t qc = 0, kc = 0, vc = 0, ac = 0;
+      uint32_t kn0 = 0, kn1 = 0;  // SPLIT: uses of each issuer's K ring
       for (int kr = 0, it = snake_item(0, blockIdx.x, gridDim.x); it < p.n_items;
          it = snake_item(++kr, blockIdx.x, gridDim.x)) {
         const Item w = decode_item<TRANSPOSED>(p, it);
@@ -533,9 +545,18 @@ __global__ void __launch_bounds__(384, 1)
               tma_load_2d(smem + L::OFF_Q + qs * G::TILE_BYTES + c * G::CHUNK_BYTES, &tm_q,
                           q_full + qs, c * G::CHUNK, row0 + w.X * 128);
             for (int j = 0; j < w.nsteps; ++j) {
-              const int ks = kc % L::KST;
-              mbar_wait(k_empty + ks, ((kc / L::KST) & 1) ^ 1, wc, kSiteProdK);
-              ++kc;
+              int ks;
+              uint32_t kpar;
+              if (SPLIT) {
+                const uint32_t n = (j & 1) ? kn1++ : kn0++;
+                ks = 2 * (j & 1) + (int)(n & 1);
+                kpar = ((n >> 1) & 1) ^ 1;
+              } else {
+                ks = kc % L::KST;
+                kpar = ((kc / L::KST) & 1) ^ 1;
+                ++kc;
+              }
+              mbar_wait(k_empty + ks, kpar, wc, kSiteProdK);
               mbar_arrive_expect_tx(k_full + ks, G::TILE_BYTES);
               for (int c = 0; c < G::NCHUNK; ++c)
                 tma_load_2d(smem + L::OFF_K + ks * G::TILE_BYTES + c * G::CHUNK_BYTES, &tm_k,
@@ -553,24 +574,24 @@ __global__ void __launch_bounds__(384, 1)
             }
           }
         } else {
-          // A static step's tables go into the K ring (warp 0), its V tiles
-          // into the V ring (warp 2).
+          // A static step's tables go into the table ring (warp 0), its V
+          // tiles into the V ring (warp 2).
           auto load_aux = [&](int step) {
             // inner tile Y: J (forward) or I (transposed)
             const int Y = TRANSPOSED ? (w.X + step) : step;
             const int dist0 = TRANSPOSED ? (Y - w.X) : (w.X - Y);  // (I - J) in tiles
-            const int ks = kc % L::KST;
-            mbar_wait(k_empty + ks, ((kc / L::KST) & 1) ^ 1, wc, kSiteProdK);
-            ++kc;
-            mbar_arrive_expect_tx(k_full + ks, L::AUX_BYTES);
-            uint8_t* aux = smem + L::OFF_K + ks * G::TILE_BYTES;
+            const int as = ac % L::AST;
+            mbar_wait(aux_empty + as, ((ac / L::AST) & 1) ^ 1, wc, kSiteProdK);
+            ++ac;
+            mbar_arrive_expect_tx(aux_full + as, L::AUX_BYTES);
+            uint8_t* aux = smem + L::OFF_AUX + as * L::AUX_SLOT;
             // column values: a(j) for j in tile J (forward) or row values of
             // tile I (transposed)
             const float* col_src = TRANSPOSED ? (p.row_tab + (size_t)w.hs * T + Y * 128)
                                               : (p.a_tab + (size_t)w.hs * T + Y * 128);
-            bulk_load(aux + L::AUX_COL, col_src, 512, k_full + ks);
+            bulk_load(aux + L::AUX_COL, col_src, 512, aux_full + as);
             bulk_load(aux + L::AUX_WIN, p.r_tab + (size_t)w.hs * (T + 128) + dist0 * 128, 1024,
-                      k_full + ks);
+                      aux_full + as);
           };
           if (kprod) {
             for (int step = 0; step < w.nsteps; ++step) load_aux(step);
@@ -603,8 +624,21 @@ __global__ void __launch_bounds__(384, 1)
       // Drain: every copy issued must have landed before the CTA exits.
       for (int s = 0; s < L::QST; ++s)
         if (qc > (uint32_t)s) mbar_drain(q_full + s, ((qc - 1 - s) / L::QST) & 1);
-      for (int s = 0; s < L::KST; ++s)
-        if (kc > (uint32_t)s) mbar_drain(k_full + s, ((kc - 1 - s) / L::KST) & 1);
+      if (SPLIT) {
+        for (int g = 0; g < 2; ++g) {
+          const uint32_t n = g ? kn1 : kn0;
+          for (uint32_t i = 0; i < 2; ++i)
+            if (n > i) {
+              const uint32_t m = n - 1 - i;  // the last use of slot 2g + (m & 1)
+              mbar_drain(k_full + 2 * g + (int)(m & 1), (m >> 1) & 1);
+            }
+        }
+      } else {
+        for (int s = 0; s < L::KST; ++s)
+          if (kc > (uint32_t)s) mbar_drain(k_full + s, ((kc - 1 - s) / L::KST) & 1);
+      }
+      for (int s = 0; s < L::AST; ++s)
+        if (ac > (uint32_t)s) mbar_drain(aux_full + s, ((ac - 1 - s) / L::AST) & 1);
       for (int s = 0; s < L::VST; ++s)
         if (vc > (uint32_t)s) mbar_drain(v_full + s, ((vc - 1 - s) / L::VST) & 1);
     }
@@ -620,7 +654,8 @@ __global__ void __launch_bounds__(384, 1)
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16(128, D, false, true);
       constexpr uint32_t idesc_pair = idesc_bf16(128, 2 * D, false, true);
-      uint32_t qc = 0, kc = 0, vc = 0, sc = 0, ss = 0, oc = 0;
+      uint32_t qc = 0, vc = 0, sc = 0, oc = 0;
+      uint32_t kn = 0, sn = 0;  // uses of this issuer's K ring and of S buffer g
       for (int kr = 0, it = snake_item(0, blockIdx.x, gridDim.x); it < p.n_items;
            it = snake_item(++kr, blockIdx.x, gridDim.x)) {
         const Item w = decode_item<TRANSPOSED>(p, it);
@@ -637,20 +672,21 @@ __global__ void __launch_bounds__(384, 1)
           const uint32_t sQ = smem_u32(smem + L::OFF_Q + qs * G::TILE_BYTES);
           mbar_wait(q_full + qs, (qc / L::QST) & 1, wc, kSiteMmaQ);
           ++qc;
-          auto issue_s = [&](int j) {
-            const uint32_t us = ss + j, b = us & 1;
-            const uint32_t kq = kc + j;
-            const int ks = kq % L::KST;
-            mbar_wait(k_full + ks, (kq / L::KST) & 1, wc, kSiteMmaK);
-            mbar_wait(s_empty + b, ((us >> 1) & 1) ^ 1, wc, kSiteMmaS);
+          // S of this half's tiles, in order (j = g, g + 2, ...)
+          auto issue_s = [&]() {
+            const int ks = 2 * g + (int)(kn & 1);
+            mbar_wait(k_full + ks, (kn >> 1) & 1, wc, kSiteMmaK);
+            mbar_wait(s_empty + g, (sn & 1) ^ 1, wc, kSiteMmaS);
             tc_fence_after();
             const uint32_t kt = sK + ks * G::TILE_BYTES;
 #pragma unroll
             for (int kk = 0; kk < G::KSTEPS; ++kk)
-              mma_bf16_ss(tmem + kTmemS + b * 128, G::kmajor_desc(sQ, kk), G::kmajor_desc(kt, kk),
-                          idesc_s, kk > 0);
+              mma_bf16_ss(tmem + kTmemS + (uint32_t)g * 128, G::kmajor_desc(sQ, kk),
+                          G::kmajor_desc(kt, kk), idesc_s, kk > 0);
             mma_commit(k_empty + ks);
-            mma_commit(s_full + b);
+            mma_commit(s_full + g);
+            ++kn;
+            ++sn;
           };
           auto issue_pv = [&](int j) {
             const uint32_t u = sc + j, pb = u & 1;
@@ -670,18 +706,15 @@ __global__ void __launch_bounds__(384, 1)
           };
           // S of the half's next tile goes out as soon as the half has read
           // the previous one; its P V once the P is written
-          if (g < w.nsteps) issue_s(g);
+          if (g < w.nsteps) issue_s();
           for (int j = g; j < w.nsteps; j += 2) {
-            if (j + 2 < w.nsteps) issue_s(j + 2);
+            if (j + 2 < w.nsteps) issue_s();
             wait_o();
             issue_pv(j);
           }
           mma_commit(q_empty + qs);
-          kc += w.nsteps;
           vc += w.nsteps;
-          ss += w.nsteps;
         } else {
-          kc += w.nsteps;  // the aux entries of static steps are consumed by the compute warps
           for (int step = 0; step < w.nsteps; ++step) {
             const uint32_t u = sc + step, pb = u & 1;
             if (g == 1) {
@@ -772,8 +805,6 @@ __global__ void __launch_bounds__(384, 1)
             if (j == w.nsteps - 1) mma_commit(q_empty + qs);
             ++kc;
           }
-        } else {
-          kc += w.nsteps;  // the aux entries of static steps are consumed by the compute warps
         }
         sc = sc0 + w.nsteps;
       }
@@ -870,24 +901,23 @@ __global__ void __launch_bounds__(384, 1)
     const int r = q4 * 32 + lane;                // tile row == TMEM lane
     const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
     const int pair_bar = 2 + q4;                 // the two warps that share these rows
-    uint32_t kc = 0, sc = 0, oc = 0;
-    uint32_t ss = 0;  // SPLIT: S ring uses (dynamic steps); sc counts P ring uses (all steps)
+    uint32_t ac = 0, sc = 0, oc = 0;  // static tables, P ring uses (all steps), items
+    uint32_t sn = 0;  // SPLIT: this half's dynamic tiles (uses of S buffer hf)
     for (int kr = 0, it = snake_item(0, blockIdx.x, gridDim.x); it < p.n_items;
          it = snake_item(++kr, blockIdx.x, gridDim.x)) {
       const Item w = decode_item<TRANSPOSED>(p, it);
       const uint32_t sc0 = sc;
       if (!w.is_static && SPLIT) {
-        kc += w.nsteps;
         // this half's key tiles: j = hf, hf + 2, ...; a thread holds a whole
         // row of each of its tiles
         float m_run = -INFINITY, l_run = 0.f;
         for (int j = hf; j < w.nsteps; j += 2) {
-          const uint32_t us = ss + j;   // S ring use
           const uint32_t u = sc0 + j;   // P ring use
-          const uint32_t sb = us & 1, pb = u & 1;
+          const uint32_t sb = (uint32_t)hf, pb = u & 1;
           const uint32_t sbase = trow + kTmemS + sb * 128;
           const uint32_t pbase = trow + kTmemP + pb * 64;
-          mbar_wait(s_full + sb, (us >> 1) & 1, wc, kSiteCmpS);
+          mbar_wait(s_full + sb, sn & 1, wc, kSiteCmpS);
+          ++sn;
           tc_fence_after();
           uint32_t sr[128];
           {
@@ -930,32 +960,33 @@ __global__ void __launch_bounds__(384, 1)
           const float corr = need ? fast_exp2(m_run - m_new) : 1.0f;
           const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
           const uint64_t nm2 = f2_pack(-m_use, -m_use);
-          uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+          uint64_t acc[2] = {0ull, 0ull};
           // the P buffer is free once the P V products of two uses back are
           // done (for j >= 2 those are this half's previous tile, so O_hf is
           // also final for a rescale)
           mbar_wait(p_empty + pb, ((u >> 1) & 1) ^ 1, wc, kSiteCmpPV);
           tc_fence_after();
-          // P as packed bf16 pairs, 16 columns at a time
+          // P as packed bf16 pairs, 8 columns at a time (few registers live
+          // beside the row's 128 scores)
 #pragma unroll
-          for (int q0 = 0; q0 < 64; q0 += 16) {
-            uint32_t pk[16];
+          for (int q0 = 0; q0 < 64; q0 += 8) {
+            uint32_t pk[8];
 #pragma unroll
-            for (int qq = 0; qq < 16; ++qq) {
+            for (int qq = 0; qq < 8; ++qq) {
               const int q = q0 + qq;
               float x0, x1;
               f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * q]), __uint_as_float(sr[2 * q + 1])),
                                sc2, nm2),
                         x0, x1);
               const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
-              acc[qq & 3] = f2_add(acc[qq & 3], f2_pack(e0, e1));
+              acc[qq & 1] = f2_add(acc[qq & 1], f2_pack(e0, e1));
               pk[qq] = pack_bf16x2(e0, e1);
             }
-            tmem_st_x16(pbase + q0, pk);
+            tmem_st_x8(pbase + q0, pk);
           }
           float rs;
           {
-            const uint64_t t = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
+            const uint64_t t = f2_add(acc[0], acc[1]);
             float lo, hi;
             f2_unpack(t, lo, hi);
             rs = lo + hi;
@@ -981,7 +1012,6 @@ __global__ void __launch_bounds__(384, 1)
           mbar_arrive_cnt(p_full + pb, 2);  // the other half does not touch this tile
         }
         sc = sc0 + w.nsteps;
-        ss += w.nsteps;
         // merge the halves' (max, sum) of each row; a half without tiles (a
         // one-tile item) has sum 0 and weight 0
         xmax[hf * 128 + r] = m_run;
@@ -1053,7 +1083,6 @@ __global__ void __launch_bounds__(384, 1)
         mbar_arrive(o_empty);
         ++oc;
       } else if (!w.is_static) {
-        kc += w.nsteps;
         float m_run = -INFINITY, l_run = 0.f;
         for (int j = 0; j < w.nsteps; ++j) {
           const uint32_t u = sc0 + j;
@@ -1216,9 +1245,9 @@ __global__ void __launch_bounds__(384, 1)
         float zpart = 0.f, zround = 0.f;
         for (int step = 0; step < w.nsteps; ++step) {
           const uint32_t u = sc0 + step;
-          const int ks = kc % L::KST;
-          mbar_wait(k_full + ks, (kc / L::KST) & 1, wc, kSiteCmpAux);
-          const float* aux = reinterpret_cast<const float*>(smem + L::OFF_K + ks * G::TILE_BYTES);
+          const int as = ac % L::AST;
+          mbar_wait(aux_full + as, (ac / L::AST) & 1, wc, kSiteCmpAux);
+          const float* aux = reinterpret_cast<const float*>(smem + L::OFF_AUX + as * L::AUX_SLOT);
           const float* colv = aux + 64 * hf;       // this half's 64 column values
           const float* win = aux + L::AUX_WIN / 4; // window, centre at 127
           // the TMEM buffer must be free: the MMAs of two steps back are done
@@ -1238,8 +1267,8 @@ __global__ void __launch_bounds__(384, 1)
                                                      row2, gdst, zpart, zround);
           // all 256 compute threads have read the aux slot: release it once
           named_bar_sync(1, 256);
-          if (hf == 0 && r == 0) mbar_arrive(k_empty + ks);
-          ++kc;
+          if (hf == 0 && r == 0) mbar_arrive(aux_empty + as);
+          ++ac;
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(p_full + (SPLIT ? (u & 1) : (u % NB)));

@@ -81,6 +81,22 @@ def test_many_items_per_cta(api, d_h):
     compare(out, lse, ref_out, ref_lse, cfg.head_is_static, f"many d{d_h}")
 
 
+@pytest.mark.parametrize("static", [(), (1, 4, 6, 9, 10, 11)])
+@pytest.mark.parametrize("T", [640, 384])
+def test_many_short_odd_items(api, T, static):
+    # Tens of short items per persistent CTA, many of odd length (1, 3, 5
+    # key tiles), with and without frozen heads: the item boundaries, where
+    # the two compute halves and their MMA issuers hand the rings over,
+    # repeat hundreds of times in one launch.  Checked twice in a row, and
+    # the device status must show no abandoned wait.
+    cfg = AttnConfig("short", B=16, H=12, T=T, d_h=64, dtype="bf16", static_heads=static)
+    inp = attn_inputs(cfg, seed=43)
+    ref_out, ref_lse = oracle_fwd(inp, cfg.head_is_static)
+    for rep in range(2):
+        out, lse = gpu_fwd(api, inp, cfg.head_is_static)
+        compare(out, lse, ref_out, ref_lse, cfg.head_is_static, f"short T{T} rep{rep}")
+
+
 def test_identity_pattern_copies_v(api):
     B, H, T, d = 2, 1, 256, 64
     cfg = AttnConfig("id", B=B, H=H, T=T, d_h=d, dtype="bf16", static_heads=(0,))
