@@ -335,7 +335,8 @@ __device__ __forceinline__ void gen_tile(uint32_t colv_s, uint32_t win_s, int rc
         f2_unpack(f2_add(f2_add(cv, wv), row2), x0, x1);
         pk[qq] = pack_bf16x2(fast_exp2(x0), fast_exp2(x1));
       } else {
-        const uint64_t g = f2_mul(f2_mul(cv, wv), row2);
+        // the forward's factored row factor is 1 (Z' divides in the epilogue)
+        const uint64_t g = SUMS ? f2_mul(cv, wv) : f2_mul(f2_mul(cv, wv), row2);
         pk[qq] = pack_bf16x2_f2(g);
         if (SUMS) {
           sum2 = f2_add(sum2, g);
@@ -479,7 +480,7 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* o_empty = o_full + 1;
   uint64_t* p_empty = o_empty + 1;       // SPLIT: P buffer's P V products done (two)
   uint64_t* aux_full = p_empty + 2;      // static tables landed (TMA -> compute)
-  uint64_t* aux_empty = aux_full + L::AST;  // static tables read (compute -> producer)
+  uint64_t* aux_empty = aux_full + L::AST;  // static tables read (every compute thread -> producer)
   float* xmax = reinterpret_cast<float*>(smem + L::OFF_X);  // [2 parity][2 halves][128]
   float* xsum = xmax + 2 * 2 * 128;                         // [2 halves][128]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
@@ -499,7 +500,7 @@ __global__ void __launch_bounds__(384, 1)
     }
     mbar_init(p_empty, 1);
     mbar_init(p_empty + 1, 1);
-    for (int s = 0; s < L::AST; ++s) { mbar_init(aux_full + s, 1); mbar_init(aux_empty + s, 1); }
+    for (int s = 0; s < L::AST; ++s) { mbar_init(aux_full + s, 1); mbar_init(aux_empty + s, 256); }
     mbar_init(o_full, SPLIT ? 2 : 1);
     mbar_init(o_empty, 256);
     *abort_flag = 0;
@@ -1265,9 +1266,8 @@ __global__ void __launch_bounds__(384, 1)
           else
             gen_tile<TRANSPOSED, false, !TRANSPOSED>(smem_u32(colv), smem_u32(win), r - 64 * hf,
                                                      row2, gdst, zpart, zround);
-          // all 256 compute threads have read the aux slot: release it once
-          named_bar_sync(1, 256);
-          if (hf == 0 && r == 0) mbar_arrive(aux_empty + as);
+          // this thread has read the table slot
+          mbar_arrive(aux_empty + as);
           ++ac;
           tmem_wait_st();
           tc_fence_before();
