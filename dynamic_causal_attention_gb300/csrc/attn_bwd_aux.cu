@@ -19,49 +19,55 @@
 namespace saf {
 namespace {
 
-// One group of D/8 lanes per row; each lane reads 8 bf16 of dO and of out.
+// Blocks walk (b, h) slabs of T rows (blockIdx.y) so that the per-head
+// choices are uniform; one group of D/8 lanes per row, each lane reads 8 bf16
+// of dO and of out.  A frozen head's D is only formed when its batch sums
+// are wanted (alpha/rho gradients); its per-row table needs only the lse.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(BwdPre p) {
   constexpr int LPR = D / 8;  // lanes per row
-  const size_t rows = (size_t)p.B * p.H * p.T;
-  const int lane = threadIdx.x & 31;
-  const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const size_t row = tid / LPR;
-  const int sub = (int)(tid % LPR);
-  float acc = 0.f;
-  if (row < rows) {
-    const uint4 a = *reinterpret_cast<const uint4*>(p.out + row * D + sub * 8);
-    const uint4 b = *reinterpret_cast<const uint4*>(p.dout + row * D + sub * 8);
-    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+  const int n_bh = p.B * p.H;
+  for (int bh = blockIdx.y; bh < n_bh; bh += gridDim.y) {
+    const int h = bh % p.H;
+    const int hs = p.static_slot[h];
+    const bool need_d = (hs == 255) || (p.Dsum != nullptr);
+    for (uint32_t t = blockIdx.x * blockDim.x + threadIdx.x; t < (uint32_t)p.T * LPR;
+         t += gridDim.x * blockDim.x) {
+      const int i = (int)(t / LPR), sub = (int)(t % LPR);
+      const size_t row = (size_t)bh * p.T + i;
+      float acc = 0.f;
+      if (need_d) {
+        const uint4 a = *reinterpret_cast<const uint4*>(p.out + row * D + sub * 8);
+        const uint4 b = *reinterpret_cast<const uint4*>(p.dout + row * D + sub * 8);
+        const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+        const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float2 x = __bfloat1622float2(a2[k]), y = __bfloat1622float2(b2[k]);
-      acc = fmaf(x.x, y.x, acc);
-      acc = fmaf(x.y, y.y, acc);
-    }
-  }
+        for (int k = 0; k < 4; ++k) {
+          const float2 x = __bfloat1622float2(a2[k]), y = __bfloat1622float2(b2[k]);
+          acc = fmaf(x.x, y.x, acc);
+          acc = fmaf(x.y, y.y, acc);
+        }
 #pragma unroll
-  for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  (void)lane;
-  // the accumulator rows of frozen heads are never added to or read
-  if (row < rows && p.dq_acc && p.static_slot[(row / p.T) % p.H] == 255) {
-    float4* z = reinterpret_cast<float4*>(p.dq_acc + row * D + sub * 8);
-    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  if (row < rows && sub == 0) {
-    const float l = p.lse[row];
-    p.Dvec[row] = -acc;
-    p.lse2[row] = -l * 1.4426950408889634f;
-    if (p.row_tab && row < (size_t)p.H * p.T) {  // sequence 0: rows (h, i)
-      const int h = (int)(row / p.T), i = (int)(row - (size_t)h * p.T);
-      const int hs = p.static_slot[h];
-      if (hs != 255) {
-        float v;
-        if (p.mode[hs]) v = -l * 1.4426950408889634f;
-        else v = (l > -INFINITY) ? expf(p.shift[hs] - l) : 0.f;
-        p.row_tab[(size_t)hs * p.T + i] = v;
+        for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      }
+      // the accumulator rows of frozen heads are never added to or read
+      if (hs == 255 && p.dq_acc) {
+        float4* z = reinterpret_cast<float4*>(p.dq_acc + row * D + sub * 8);
+        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      if (sub == 0) {
+        const float l = p.lse[row];
+        if (need_d) {
+          p.Dvec[row] = -acc;
+          p.lse2[row] = -l * 1.4426950408889634f;
+        }
+        if (hs != 255 && p.row_tab && bh < p.H) {  // sequence 0: rows (h, i)
+          float v;
+          if (p.mode[hs]) v = -l * 1.4426950408889634f;
+          else v = (l > -INFINITY) ? expf(p.shift[hs] - l) : 0.f;
+          p.row_tab[(size_t)hs * p.T + i] = v;
+        }
       }
     }
   }
@@ -76,17 +82,20 @@ __global__ void dsum_kernel(BwdPre p) {
   p.Dsum[(size_t)hs * p.T + i] = s;
 }
 
+// Blocks walk (b, h) slabs (blockIdx.y), 16-byte units within a slab.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_post_kernel(BwdPost p, float scale) {
-  const size_t n8 = (size_t)p.B * p.H * p.T * D / 8;
-  for (size_t t = (size_t)blockIdx.x * blockDim.x + threadIdx.x; t < n8;
-       t += (size_t)gridDim.x * blockDim.x) {
-    const size_t e = t * 8;
-    const int h = (int)((e / ((size_t)p.T * D)) % p.H);
-    // the same element index in the [B, H_kv, T, d_h] tensors, while in range
-    if (e < (size_t)p.B * p.H_kv * p.T * D) {
-      const int kv = (int)((e / ((size_t)p.T * D)) % p.H_kv);
-      if (p.kv_no_dyn[kv]) {
+  const uint32_t units = (uint32_t)p.T * (D / 8);
+  const int n_bh = p.B * p.H, n_bkv = p.B * p.H_kv;
+  for (int bh = blockIdx.y; bh < n_bh; bh += gridDim.y) {
+    const bool st = p.is_static[bh % p.H];
+    // the [B, H_kv, T, d_h] tensors: slab bh is (b, kv) while in range
+    const bool kv_zero = bh < n_bkv && p.kv_no_dyn[bh % p.H_kv];
+    const size_t base = (size_t)bh * p.T * D;
+    for (uint32_t u = blockIdx.x * blockDim.x + threadIdx.x; u < units;
+         u += gridDim.x * blockDim.x) {
+      const size_t e = base + (size_t)u * 8;
+      if (kv_zero) {
         *reinterpret_cast<uint4*>(p.dK + e) = make_uint4(0u, 0u, 0u, 0u);
         if (p.dv_acc) {
           const float4 a = *reinterpret_cast<const float4*>(p.dv_acc + e);
@@ -99,34 +108,34 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(BwdPost p, float scale) {
           *reinterpret_cast<uint4*>(p.dV + e) = v;
         }
       }
+      uint4 q;
+      if (st) {
+        q = make_uint4(0u, 0u, 0u, 0u);
+      } else {
+        const float4 a = *reinterpret_cast<const float4*>(p.dq_acc + e);
+        const float4 b = *reinterpret_cast<const float4*>(p.dq_acc + e + 4);
+        q.x = pack_bf16x2(a.x * scale, a.y * scale);
+        q.y = pack_bf16x2(a.z * scale, a.w * scale);
+        q.z = pack_bf16x2(b.x * scale, b.y * scale);
+        q.w = pack_bf16x2(b.z * scale, b.w * scale);
+      }
+      *reinterpret_cast<uint4*>(p.dQ + e) = q;
     }
-    uint4 q;
-    if (p.is_static[h]) {
-      q = make_uint4(0u, 0u, 0u, 0u);
-    } else {
-      const float4 a = *reinterpret_cast<const float4*>(p.dq_acc + e);
-      const float4 b = *reinterpret_cast<const float4*>(p.dq_acc + e + 4);
-      q.x = pack_bf16x2(a.x * scale, a.y * scale);
-      q.y = pack_bf16x2(a.z * scale, a.w * scale);
-      q.z = pack_bf16x2(b.x * scale, b.y * scale);
-      q.w = pack_bf16x2(b.z * scale, b.w * scale);
-    }
-    *reinterpret_cast<uint4*>(p.dQ + e) = q;
   }
 }
 
-int grid_for(size_t threads) {
-  size_t b = (threads + 255) / 256;
-  if (b < 1) b = 1;
-  if (b > 8192) b = 8192;
-  return (int)b;
+// Grid over (b, h) slabs: x covers one slab's threads in about four rounds.
+dim3 slab_grid(size_t slab_threads, int n_bh) {
+  size_t gx = (slab_threads + 1023) / 1024;
+  if (gx < 1) gx = 1;
+  if (gx > 1024) gx = 1024;
+  return dim3((unsigned)gx, (unsigned)(n_bh < 65535 ? n_bh : 65535));
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_pre(const BwdPre& p, cudaStream_t s) {
-  const size_t threads = (size_t)p.B * p.H * p.T * (p.d_h / 8);
-  const int blocks = (int)((threads + 255) / 256);
+  const dim3 blocks = slab_grid((size_t)p.T * (p.d_h / 8), p.B * p.H);
   trace_begin(s);
   switch (p.d_h) {
     case 32: bwd_pre_kernel<32><<<blocks, 256, 0, s>>>(p); break;
@@ -145,7 +154,7 @@ cudaError_t launch_bwd_pre(const BwdPre& p, cudaStream_t s) {
 
 cudaError_t launch_bwd_post(const BwdPost& p, cudaStream_t s) {
   const float scale = 1.0f / sqrtf((float)p.d_h);
-  const int blocks = grid_for((size_t)p.B * p.H * p.T * p.d_h / 8);
+  const dim3 blocks = slab_grid((size_t)p.T * p.d_h / 8, p.B * p.H);
   trace_begin(s);
   switch (p.d_h) {
     case 32: bwd_post_kernel<32><<<blocks, 256, 0, s>>>(p, scale); break;
