@@ -91,6 +91,19 @@ def test_many_items_per_cta(api, d_h, grads):
             f"many d{d_h}", grads)
 
 
+@pytest.mark.parametrize("d_h,static,grads", [(64, (), False), (64, (1, 4, 6, 9, 10, 11), False),
+                                             (128, (1, 4, 6, 9, 10, 11), True)])
+def test_many_short_odd_items(api, d_h, static, grads):
+    # Tens of short items per persistent CTA in every kernel (T = 640: key
+    # tiles of 1..5 query tiles each, many of odd length), with and without
+    # frozen heads, so every item-boundary hand-over repeats many times.
+    cfg = AttnConfig("short", B=16, H=12, T=640, d_h=d_h, dtype="bf16", static_heads=static)
+    inp = attn_inputs(cfg, seed=47)
+    got = gpu_fwd_bwd(api, inp, cfg.head_is_static, grads)
+    compare(got, oracle_bwd(inp, cfg.head_is_static, grads), cfg.head_is_static,
+            f"short d{d_h}", grads)
+
+
 def test_identity_pattern_backward(api):
     B, H, T, d = 2, 1, 256, 64
     cfg = AttnConfig("id", B=B, H=H, T=T, d_h=d, dtype="bf16", static_heads=(0,))
