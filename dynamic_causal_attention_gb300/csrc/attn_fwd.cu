@@ -724,8 +724,10 @@ __global__ void __launch_bounds__(384, 1)
               vc += w.nb;
               continue;
             }
-            mbar_wait(p_full + pb, (u >> 1) & 1, wc, kSiteMmaP);
+            // the previous item's P buffers are all written and read once its
+            // O has been read out, so this parity wait cannot match an older use
             wait_o();
+            mbar_wait(p_full + pb, (u >> 1) & 1, wc, kSiteMmaP);
             const uint32_t ga = tmem + kTmemP + pb * 64;
             if (L::PAIR_V && w.nb == 2) {
               // Two sequences' V tiles in adjacent slots form one [128 x 2 d_h]
