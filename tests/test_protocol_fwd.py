@@ -1,0 +1,389 @@
+"""Model check of the forward kernel's mbarrier protocol at d_h <= 64.
+
+The fused forward at d_h <= 64 runs seven roles over shared rings: a Q/K and
+table producer, a V producer, two MMA issuers, two compute halves and the
+asynchronous engines (TMA loads that land in any order, tensor-core products
+that complete in issue order per issuing thread, their commits arriving after
+every earlier product of that thread).  This file restates, role by role, the
+waits, arrivals and commits the kernel performs (attn_fwd.cu, hybrid_fwd_kernel
+with SPLIT) and runs them under random interleavings.
+
+An mbarrier parity wait passes when the barrier's current phase parity differs
+from the awaited one.  Such a wait is only right if, when it passes, exactly
+the awaited phase has completed: one phase fewer (the waiter ran two phases
+ahead) passes spuriously, one more (the waiter fell two behind) would block
+on the wrong phase.  The checker asserts this at every wait, forbids arrivals
+beyond a barrier's count, and requires every role to finish (no deadlock).
+
+Two planted mistakes, both once in the kernel, must be caught: the S buffers
+shared by both halves and chosen by the parity of a global tile count, and
+the issuer of static products waiting on a P buffer before the previous
+item's O.  Host logic only: no GPU.
+"""
+
+import random
+
+import pytest
+
+QST, KST, VST, AST = 2, 4, 4, 4
+
+
+class Violation(Exception):
+    pass
+
+
+class Barrier:
+    def __init__(self, name, count):
+        self.name, self.count = name, count
+        self.done = 0      # completed phases
+        self.pending = 0   # arrivals in the current phase
+
+    def arrive(self, k=1):
+        self.pending += k
+        if self.pending > self.count:
+            raise Violation(f"{self.name}: {self.pending} arrivals for a count of {self.count}")
+        if self.pending == self.count:
+            self.done += 1
+            self.pending = 0
+
+    def try_wait(self, m):
+        """Wait for phase m (m = -1: nothing to wait for).  Hardware rule:
+        pass when the current phase parity differs from m's parity."""
+        parity = m & 1
+        passes = (self.done & 1) != parity
+        if passes and self.done != m + 1:
+            raise Violation(f"{self.name}: wait for phase {m} passed with {self.done} completed")
+        if not passes and self.done > m + 1:
+            raise Violation(f"{self.name}: wait for phase {m} overtaken ({self.done} completed)")
+        return passes
+
+
+def make_barriers(shared_s):
+    b = {}
+    def add(name, count):
+        b[name] = Barrier(name, count)
+    for s in range(QST):
+        add(f"q_full{s}", 1); add(f"q_empty{s}", 2)
+    for s in range(KST):
+        add(f"k_full{s}", 1); add(f"k_empty{s}", 1)
+    for s in range(VST):
+        add(f"v_full{s}", 1); add(f"v_empty{s}", 1)
+    for s in range(2):
+        add(f"s_full{s}", 1); add(f"s_empty{s}", 1)   # one unit = a half's 128 threads
+        add(f"p_full{s}", 2); add(f"p_empty{s}", 1)   # two units = 256 threads
+    for s in range(AST):
+        add(f"aux_full{s}", 1); add(f"aux_empty{s}", 2)
+    add("o_full", 2); add("o_empty", 2)
+    return b
+
+
+# --------------------------------------------------------------- the roles
+# Each role is a generator of actions:
+#   ("wait", barrier, phase) ("arrive", barrier, units) ("tma", barrier)
+#   ("mma",) ("commit", barrier) ("pair", item index)
+
+def producer_qk(items):
+    qc = ac = 0
+    kn = [0, 0]
+    for it in items:
+        if it["dyn"]:
+            qs = qc % QST
+            yield ("wait", f"q_empty{qs}", qc // QST - 1)
+            qc += 1
+            yield ("tma", f"q_full{qs}")
+            for j in range(it["n"]):
+                r = j & 1
+                n = kn[r]
+                kn[r] += 1
+                slot = 2 * r + (n & 1)
+                yield ("wait", f"k_empty{slot}", (n >> 1) - 1)
+                yield ("tma", f"k_full{slot}")
+        else:
+            for _ in range(it["n"]):
+                a = ac % AST
+                yield ("wait", f"aux_empty{a}", ac // AST - 1)
+                ac += 1
+                yield ("tma", f"aux_full{a}")
+
+
+def producer_v(items):
+    vc = 0
+    for it in items:
+        if it["dyn"]:
+            for _ in range(it["n"]):
+                vs = vc % VST
+                yield ("wait", f"v_empty{vs}", vc // VST - 1)
+                vc += 1
+                yield ("tma", f"v_full{vs}")
+        else:
+            for _ in range(it["n"]):
+                if it["nb"] == 2 and (vc & 1):
+                    vs = vc % VST
+                    yield ("wait", f"v_empty{vs}", vc // VST - 1)
+                    vc += 1
+                    yield ("arrive", f"v_full{vs}", 1)
+                for _ in range(it["nb"]):
+                    vs = vc % VST
+                    yield ("wait", f"v_empty{vs}", vc // VST - 1)
+                    vc += 1
+                    yield ("tma", f"v_full{vs}")
+
+
+def issuer(g, items, shared_s, late_o=False):
+    qc = vc = sc = oc = kn = sn = ss = 0
+    for it in items:
+        o_ready = [False]
+
+        def wait_o():
+            if not o_ready[0]:
+                o_ready[0] = True
+                yield ("wait", "o_empty", oc - 1)
+
+        if it["dyn"]:
+            n = it["n"]
+            qs = qc % QST
+            yield ("wait", f"q_full{qs}", qc // QST)
+            qc += 1
+
+            def issue_s(j):
+                nonlocal kn, sn
+                slot = 2 * g + (kn & 1)
+                yield ("wait", f"k_full{slot}", kn >> 1)
+                if shared_s:   # planted mistake: buffer by the parity of a global count
+                    us = ss + j
+                    yield ("wait", f"s_empty{us & 1}", (us >> 1) - 1)
+                    buf = us & 1
+                else:
+                    yield ("wait", f"s_empty{g}", sn - 1)
+                    buf = g
+                yield ("mma",)
+                yield ("commit", f"k_empty{slot}")
+                yield ("commit", f"s_full{buf}")
+                kn += 1
+                sn += 1
+
+            def issue_pv(j):
+                u = sc + j
+                vq = vc + j
+                yield ("wait", f"v_full{vq % VST}", vq // VST)
+                yield ("wait", f"p_full{u & 1}", u >> 1)
+                yield ("mma",)
+                yield ("commit", f"v_empty{vq % VST}")
+                yield ("commit", f"p_empty{u & 1}")
+
+            if g < n:
+                yield from issue_s(g)
+            for j in range(g, n, 2):
+                if j + 2 < n:
+                    yield from issue_s(j + 2)
+                yield from wait_o()
+                yield from issue_pv(j)
+            yield ("commit", f"q_empty{qs}")
+            vc += n
+            ss += n
+        else:
+            for step in range(it["n"]):
+                u = sc + step
+                if g == 1:
+                    if it["nb"] == 2 and (vc & 1):
+                        vc += 1
+                    vc += it["nb"]
+                    continue
+                if late_o:   # planted mistake: the static P wait before the O wait
+                    yield ("wait", f"p_full{u & 1}", u >> 1)
+                    yield from wait_o()
+                else:
+                    yield from wait_o()
+                    yield ("wait", f"p_full{u & 1}", u >> 1)
+                if it["nb"] == 2:
+                    if vc & 1:
+                        yield ("wait", f"v_full{vc % VST}", vc // VST)
+                        yield ("commit", f"v_empty{vc % VST}")
+                        vc += 1
+                    yield ("wait", f"v_full{vc % VST}", vc // VST)
+                    yield ("wait", f"v_full{(vc + 1) % VST}", (vc + 1) // VST)
+                    yield ("mma",)
+                    yield ("commit", f"v_empty{vc % VST}")
+                    yield ("commit", f"v_empty{(vc + 1) % VST}")
+                    vc += 2
+                else:
+                    yield ("wait", f"v_full{vc % VST}", vc // VST)
+                    yield ("mma",)
+                    yield ("commit", f"v_empty{vc % VST}")
+                    vc += 1
+                yield ("commit", f"p_empty{u & 1}")
+        sc += it["n"]
+        yield from wait_o()
+        yield ("commit", "o_full")
+        oc += 1
+
+
+def compute(hf, items, shared_s):
+    ac = sc = oc = sn = ss = 0
+    for idx, it in enumerate(items):
+        sc0 = sc
+        if it["dyn"]:
+            for j in range(hf, it["n"], 2):
+                u = sc0 + j
+                if shared_s:
+                    us = ss + j
+                    sb, ph = us & 1, us >> 1
+                else:
+                    sb, ph = hf, sn
+                yield ("wait", f"s_full{sb}", ph)
+                sn += 1
+                yield ("arrive", f"s_empty{sb}", 1)
+                yield ("wait", f"p_empty{u & 1}", (u >> 1) - 1)
+                yield ("arrive", f"p_full{u & 1}", 2)
+            ss += it["n"]
+        else:
+            for step in range(it["n"]):
+                u = sc0 + step
+                a = ac % AST
+                yield ("wait", f"aux_full{a}", ac // AST)
+                yield ("wait", f"p_empty{u & 1}", (u >> 1) - 1)
+                yield ("arrive", f"aux_empty{a}", 1)
+                ac += 1
+                yield ("arrive", f"p_full{u & 1}", 1)
+        sc = sc0 + it["n"]
+        yield ("pair", idx)   # the halves' max/sum exchange (named barriers)
+        yield ("wait", "o_full", oc)
+        yield ("arrive", "o_empty", 1)
+        oc += 1
+
+
+# --------------------------------------------------------------- the engine
+
+def run_model(items, rng, shared_s=False, late_o=False, max_events=200000):
+    bars = make_barriers(shared_s)
+    roles = {
+        "qk": producer_qk(items), "v": producer_v(items),
+        "i0": issuer(0, items, shared_s, late_o), "i1": issuer(1, items, shared_s, late_o),
+        "c0": compute(0, items, shared_s), "c1": compute(1, items, shared_s),
+    }
+    nxt = {k: None for k in roles}
+    finished = set()
+    tma = []                            # barriers of copies in flight (land in any order)
+    fifo = {"i0": [], "i1": []}         # per issuer: products and commits in issue order
+    pair_seen = {}
+
+    def step_role(k):
+        if nxt[k] is None:
+            try:
+                nxt[k] = next(roles[k])
+            except StopIteration:
+                finished.add(k)
+                return True
+        act = nxt[k]
+        kind = act[0]
+        if kind == "wait":
+            if not bars[act[1]].try_wait(act[2]):
+                return False
+        elif kind == "arrive":
+            bars[act[1]].arrive(act[2])
+        elif kind == "tma":
+            tma.append(act[1])
+        elif kind in ("mma", "commit"):
+            fifo[k].append(act)
+        elif kind == "pair":
+            pair_seen.setdefault(act[1], set()).add(k)
+            if len(pair_seen[act[1]]) < 2:
+                nxt[k] = ("pairwait", act[1])
+                return True
+        elif kind == "pairwait":
+            if len(pair_seen[act[1]]) < 2:
+                return False
+        nxt[k] = None
+        return True
+
+    # per-run speeds: some roles and engines run much slower than others, so
+    # that one half can fall several tiles behind the other
+    speed = {k: rng.choice([0.05, 0.2, 1.0, 1.0]) for k in roles}
+    speed["tma"] = rng.choice([0.05, 0.3, 1.0])
+    speed["i0_mma"] = rng.choice([0.05, 0.3, 1.0])
+    speed["i1_mma"] = rng.choice([0.05, 0.3, 1.0])
+
+    def fire(ev):
+        if ev == "tma":
+            bars[tma.pop(rng.randrange(len(tma)))].arrive(1)
+            return True
+        if ev.endswith("_mma"):
+            act = fifo[ev[:2]].pop(0)
+            if act[0] == "commit":
+                bars[act[1]].arrive(1)
+            return True
+        return step_role(ev)
+
+    for _ in range(max_events):
+        if len(finished) == len(roles) and not tma and not fifo["i0"] and not fifo["i1"]:
+            return
+        cands = [k for k in roles if k not in finished]
+        if tma:
+            cands.append("tma")
+        cands += [f"{k}_mma" for k in fifo if fifo[k]]
+        while cands:
+            ev = rng.choices(cands, weights=[speed[c] for c in cands])[0]
+            if fire(ev):
+                break
+            cands.remove(ev)
+        else:
+            stuck = {k: nxt[k] for k in roles if k not in finished}
+            raise Violation(f"deadlock: {stuck}")
+    raise Violation("did not finish")
+
+
+def random_items(rng, n_items):
+    items = []
+    for _ in range(n_items):
+        if rng.random() < 0.3:
+            items.append({"dyn": False, "n": rng.randint(1, 6), "nb": rng.choice([1, 2, 2])})
+        else:
+            items.append({"dyn": True, "n": rng.randint(1, 7)})
+    return items
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_forward_protocol_holds(seed):
+    rng = random.Random(seed)
+    for _ in range(5):
+        run_model(random_items(rng, rng.randint(1, 14)), rng)
+
+
+def test_planted_shared_s_buffers_are_caught():
+    # The earlier protocol: both halves share the two S buffers, picked by the
+    # parity of a global tile count, so the halves swap buffers after an
+    # odd-length item.  Some interleaving must make a wait pass early.
+    rng = random.Random(1234)
+    caught = 0
+    for _ in range(200):
+        try:
+            run_model(random_items(rng, rng.randint(2, 10)), rng, shared_s=True)
+        except Violation:
+            caught += 1
+    assert caught >= 10
+
+
+def test_planted_late_o_wait_is_caught():
+    # Issuer 0 waits on a static step's P buffer before the previous item's O
+    # has been read: the buffer's older use may belong to the other half's
+    # last tile of a dynamic item that is not written yet.
+    rng = random.Random(99)
+    caught = 0
+    for _ in range(200):
+        try:
+            run_model(random_items(rng, rng.randint(2, 12)), rng, late_o=True)
+        except Violation:
+            caught += 1
+    assert caught >= 10
+
+
+def test_long_odd_item_runs():
+    # the prefill shape: runs of one- and three-tile items, static groups between
+    rng = random.Random(7)
+    for _ in range(20):
+        items = []
+        for _ in range(12):
+            items.append({"dyn": True, "n": rng.choice([1, 3, 5])})
+            if rng.random() < 0.3:
+                items.append({"dyn": False, "n": rng.choice([1, 2, 3]), "nb": 2})
+        run_model(items, rng)
