@@ -25,37 +25,9 @@ import random
 
 import pytest
 
+from protocol_model import Barrier, Violation, run_roles
+
 QST, KST, VST, AST = 2, 4, 4, 4
-
-
-class Violation(Exception):
-    pass
-
-
-class Barrier:
-    def __init__(self, name, count):
-        self.name, self.count = name, count
-        self.done = 0      # completed phases
-        self.pending = 0   # arrivals in the current phase
-
-    def arrive(self, k=1):
-        self.pending += k
-        if self.pending > self.count:
-            raise Violation(f"{self.name}: {self.pending} arrivals for a count of {self.count}")
-        if self.pending == self.count:
-            self.done += 1
-            self.pending = 0
-
-    def try_wait(self, m):
-        """Wait for phase m (m = -1: nothing to wait for).  Hardware rule:
-        pass when the current phase parity differs from m's parity."""
-        parity = m & 1
-        passes = (self.done & 1) != parity
-        if passes and self.done != m + 1:
-            raise Violation(f"{self.name}: wait for phase {m} passed with {self.done} completed")
-        if not passes and self.done > m + 1:
-            raise Violation(f"{self.name}: wait for phase {m} overtaken ({self.done} completed)")
-        return passes
 
 
 def make_barriers(shared_s):
@@ -252,84 +224,13 @@ def compute(hf, items, shared_s):
         oc += 1
 
 
-# --------------------------------------------------------------- the engine
-
-def run_model(items, rng, shared_s=False, late_o=False, max_events=200000):
-    bars = make_barriers(shared_s)
+def run_model(items, rng, shared_s=False, late_o=False):
     roles = {
         "qk": producer_qk(items), "v": producer_v(items),
         "i0": issuer(0, items, shared_s, late_o), "i1": issuer(1, items, shared_s, late_o),
         "c0": compute(0, items, shared_s), "c1": compute(1, items, shared_s),
     }
-    nxt = {k: None for k in roles}
-    finished = set()
-    tma = []                            # barriers of copies in flight (land in any order)
-    fifo = {"i0": [], "i1": []}         # per issuer: products and commits in issue order
-    pair_seen = {}
-
-    def step_role(k):
-        if nxt[k] is None:
-            try:
-                nxt[k] = next(roles[k])
-            except StopIteration:
-                finished.add(k)
-                return True
-        act = nxt[k]
-        kind = act[0]
-        if kind == "wait":
-            if not bars[act[1]].try_wait(act[2]):
-                return False
-        elif kind == "arrive":
-            bars[act[1]].arrive(act[2])
-        elif kind == "tma":
-            tma.append(act[1])
-        elif kind in ("mma", "commit"):
-            fifo[k].append(act)
-        elif kind == "pair":
-            pair_seen.setdefault(act[1], set()).add(k)
-            if len(pair_seen[act[1]]) < 2:
-                nxt[k] = ("pairwait", act[1])
-                return True
-        elif kind == "pairwait":
-            if len(pair_seen[act[1]]) < 2:
-                return False
-        nxt[k] = None
-        return True
-
-    # per-run speeds: some roles and engines run much slower than others, so
-    # that one half can fall several tiles behind the other
-    speed = {k: rng.choice([0.05, 0.2, 1.0, 1.0]) for k in roles}
-    speed["tma"] = rng.choice([0.05, 0.3, 1.0])
-    speed["i0_mma"] = rng.choice([0.05, 0.3, 1.0])
-    speed["i1_mma"] = rng.choice([0.05, 0.3, 1.0])
-
-    def fire(ev):
-        if ev == "tma":
-            bars[tma.pop(rng.randrange(len(tma)))].arrive(1)
-            return True
-        if ev.endswith("_mma"):
-            act = fifo[ev[:2]].pop(0)
-            if act[0] == "commit":
-                bars[act[1]].arrive(1)
-            return True
-        return step_role(ev)
-
-    for _ in range(max_events):
-        if len(finished) == len(roles) and not tma and not fifo["i0"] and not fifo["i1"]:
-            return
-        cands = [k for k in roles if k not in finished]
-        if tma:
-            cands.append("tma")
-        cands += [f"{k}_mma" for k in fifo if fifo[k]]
-        while cands:
-            ev = rng.choices(cands, weights=[speed[c] for c in cands])[0]
-            if fire(ev):
-                break
-            cands.remove(ev)
-        else:
-            stuck = {k: nxt[k] for k in roles if k not in finished}
-            raise Violation(f"deadlock: {stuck}")
-    raise Violation("did not finish")
+    run_roles(roles, make_barriers(shared_s), ("i0", "i1"), rng)
 
 
 def random_items(rng, n_items):
