@@ -419,9 +419,145 @@ def calib_secondary(peaks):
         "selected_first": [int(x) for x in sel[:8].cpu()],
     }
     cal.close()
+
+    # forward-KL selector: the same samples, with the entropy sums tracked
+    cal_kl = api.Calibration(c.num_heads, c.T, track_kl=True)
+
+    def once_kl():
+        cal_kl.reset()
+        for l, a in enumerate(layers):
+            cal_kl.accumulate(a, head_begin=l * c.H)
+        return cal_kl.finalize_kl(k)
+
+    once_kl()
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(3):
+        s_kl, sel_kl = once_kl()
+    e1.record()
+    torch.cuda.synchronize()
+    kl_ms = e0.elapsed_time(e1) / 3
+    out["kl_selector"] = {
+        "ms": round(kl_ms, 3),
+        "GB_per_s": round(read_bytes / (kl_ms / 1e3) / 1e9, 1),
+        "frac_of_hbm": round(read_bytes / (kl_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 3),
+        "note": "accumulate with the entropy sums + finalize_kl; GB/s counts the samples read",
+        "selected_first": [int(x) for x in sel_kl[:8].cpu()],
+    }
+    cal_kl.close()
+
+    # compact fit of alpha/rho to the mean pattern, candidates in variance order
+    order = torch.argsort(s_var).to(torch.int32)
+    api.fit_compact(A_hat, order, k)
+    torch.cuda.synchronize()
+    e0.record()
+    alpha, rho, kl, fsel = api.fit_compact(A_hat, order, k)
+    e1.record()
+    torch.cuda.synchronize()
+    fit_ms = e0.elapsed_time(e1)
+    kl_h = kl.cpu()
+    out["compact_fit"] = {
+        "ms": round(fit_ms, 3),
+        "workload": f"alpha/rho fit, 400 Adam steps per candidate, T={c.T}, "
+                    f"{c.num_heads} candidates in variance order, k={k}, KL gate 0.2 nat",
+        "selected": int(fsel.numel()),
+        "kl_of_first_candidates": [round(float(x), 4) for x in kl_h[:8]],
+    }
     del layers, A_hat
     torch.cuda.empty_cache()
     return out
+
+
+def sharp_secondary(peaks):
+    """The sharp-mean pattern: calibration fed logits (N=16 sequences x 144
+    heads x T = 1024, generated on the device outside timing), then the
+    causal softmax of each row of their mean."""
+    import torch
+    from dynamic_causal_attention_gb300 import api
+    from dynamic_causal_attention_gb300.synthetic import calib_probabilities
+    c = CALIB_CONFIG
+    N = 16
+    X = calib_probabilities(N, c.num_heads, c.T, d_h=c.d_h, device="cuda", want_logits=True)
+    layers = [X[:, l * c.H:(l + 1) * c.H].contiguous() for l in range(c.L)]
+    del X
+    torch.cuda.empty_cache()
+    cal = api.Calibration(c.num_heads, c.T)
+
+    def once():
+        cal.reset()
+        for l, a in enumerate(layers):
+            cal.accumulate(a, head_begin=l * c.H)
+        return cal.finalize_sharp()
+
+    once()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(3):
+        pat = once()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / 3
+    tri = c.T * (c.T + 1) // 2
+    alg = N * c.num_heads * tri * 4 + c.num_heads * c.T * c.T * 4
+    out = {"workload": f"sharp mean: N={N} logit samples, {c.num_heads} heads, T={c.T} "
+                       "(12 per-layer accumulate calls + finalize_sharp)",
+           "ms": round(ms, 3),
+           "GB_per_s": round(alg / (ms / 1e3) / 1e9, 1),
+           "frac_of_hbm": round(alg / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 3),
+           "row_sum_max_err": float((pat.sum(-1) - 1).abs().max())}
+    cal.close()
+    del layers, pat
+    torch.cuda.empty_cache()
+    return out
+
+
+def gqa_secondary(peaks, steps=20, warmup=3):
+    """The 124M-shaped layer with grouped K/V: 12 query heads over 4 K/V heads
+    (3 frozen query heads), forward + backward through the C ABI."""
+    import torch
+    from dynamic_causal_attention_gb300 import api
+    cfg = ATTN_CONFIGS["124m"]
+    B, H, T, d, Hkv = cfg.B, cfg.H, cfg.T, cfg.d_h, 4
+    g = torch.Generator(device="cuda")
+    g.manual_seed(11)
+    bf = torch.bfloat16
+    rnd = lambda *shp: torch.randn(shp, generator=g, device="cuda").to(bf)
+    q, do = rnd(B, H, T, d), rnd(B, H, T, d)
+    k, v = rnd(B, Hkv, T, d), rnd(B, Hkv, T, d)
+    inp = attn_inputs(cfg, B=1, H=H, T=T, d_h=8)  # alpha, rho only
+    alpha = torch.from_numpy(inp["alpha"]).cuda()
+    rho = torch.from_numpy(inp["rho"]).cuda()
+    layer = api.HybridAttention(B, H, T, d, cfg.head_is_static, H_kv=Hkv)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, T), dtype=torch.float32, device="cuda")
+    grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), None, None)
+
+    def step():
+        layer.forward(q, k, v, alpha, rho, out=out, lse=lse)
+        layer.backward(q, k, v, out, lse, do, alpha, rho, grads=grads)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    st, site = layer.device_status()
+    per = e0.elapsed_time(e1) / steps
+    f, b = useful_flops(cfg)
+    tf = (f + b) / (per / 1e3) / 1e12
+    res = {"workload": f"124m with grouped K/V: B={B} H={H} H_kv={Hkv} T={T} d_h={d} "
+                       f"static={list(cfg.static_heads)}",
+           "ms_per_step": round(per, 4), "TFLOP_per_s": round(tf, 1),
+           "frac_of_bf16_peak": round(tf / peaks["bf16_tflops_sustained"], 3),
+           "device_status": int(st)}
+    del layer, q, k, v, do, out, lse, grads
+    torch.cuda.empty_cache()
+    return res
 
 
 def layer_secondary(cfg, steps, warmup, peaks):
@@ -625,6 +761,8 @@ def run_saf(args):
     if rank == 0 and not args.quick:
         secondary["1b"] = layer_secondary(ATTN_CONFIGS["1b"], 30, 3, peaks)
         secondary["calibration"] = calib_secondary(peaks)
+        secondary["sharp_mean"] = sharp_secondary(peaks)
+        secondary["gqa_124m"] = gqa_secondary(peaks)
         sweep = {}
         for r in (0.0, 0.125, 0.25, 0.5, 1.0):
             s = layer_secondary(sweep_config(r), 20, 3, peaks)
