@@ -135,8 +135,9 @@ __global__ void __launch_bounds__(128) calib_kl_rows_kernel(CalibFinalize p) {
     const int col0 = c4 * 4;
     const float4 mu = masked(*reinterpret_cast<const float4*>(p.mean + base + col0), row, col0);
     const float4 e = masked(*reinterpret_cast<const float4*>(p.ent + base + col0), row, col0);
-    acc += (double)(e.x - N * xlogx(mu.x)) + (double)(e.y - N * xlogx(mu.y)) +
-           (double)(e.z - N * xlogx(mu.z)) + (double)(e.w - N * xlogx(mu.w));
+    // four terms in fp32, the running sum in fp64
+    acc += (double)(((e.x - N * xlogx(mu.x)) + (e.y - N * xlogx(mu.y))) +
+                    ((e.z - N * xlogx(mu.z)) + (e.w - N * xlogx(mu.w))));
   }
   __shared__ double red[128];
   red[threadIdx.x] = acc;
@@ -175,36 +176,56 @@ __global__ void __launch_bounds__(128) calib_rows_kernel(CalibFinalize p) {
   if (threadIdx.x == 0) p.row_partials[(size_t)h * T + row] = red[0];
 }
 
-// Sharp-mean pattern: one block per (row, head) applies a causal softmax to
-// the row of the running mean of the accumulated logits: maximum, then the
-// sum of exponentials in fp64 (fixed-order block reduction), then the
-// normalised row with exact zeros above the diagonal.
-__global__ void __launch_bounds__(128) calib_sharp_rows_kernel(const float* __restrict__ mean,
-                                                               int T, float* __restrict__ out) {
-  const int row = blockIdx.x, h = blockIdx.y;
+// Sharp-mean pattern: one warp per (row, head) applies a causal softmax to
+// the row of the running mean of the accumulated logits, in three passes
+// over the row (16-byte loads; the row stays in L1 between passes): the
+// maximum, the sum of exponentials (fp32 per 4 columns, fp64 across them and
+// across the warp, in a fixed order), then the normalised row with exact
+// zeros above the diagonal.
+constexpr int kSharpRows = 8;  // rows (warps) per block
+
+__device__ __forceinline__ float4 causal_row4(const float4* src, int c4, int row) {
+  float4 a = src[c4];
+  const int c = 4 * c4;
+  if (c + 1 > row) a.y = -INFINITY;
+  if (c + 2 > row) a.z = -INFINITY;
+  if (c + 3 > row) a.w = -INFINITY;
+  return a;
+}
+
+__global__ void __launch_bounds__(32 * kSharpRows) calib_sharp_rows_kernel(
+    const float* __restrict__ mean, int T, float* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kSharpRows + (threadIdx.x >> 5), h = blockIdx.y;
+  if (row >= T) return;  // a whole warp
   const size_t base = ((size_t)h * T + row) * (size_t)T;
-  __shared__ float fred[128];
-  __shared__ double dred[128];
+  const float4* src = reinterpret_cast<const float4*>(mean + base);
+  const int n4 = T / 4, last4 = row / 4;
   float mx = -INFINITY;
-  for (int j = threadIdx.x; j <= row; j += blockDim.x) mx = fmaxf(mx, mean[base + j]);
-  fred[threadIdx.x] = mx;
-  __syncthreads();
-  for (int s = 64; s > 0; s >>= 1) {
-    if (threadIdx.x < s) fred[threadIdx.x] = fmaxf(fred[threadIdx.x], fred[threadIdx.x + s]);
-    __syncthreads();
+  for (int c4 = lane; c4 <= last4; c4 += 32) {
+    const float4 a = causal_row4(src, c4, row);
+    mx = fmaxf(mx, fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w)));
   }
-  mx = fred[0];
-  double acc = 0.0;
-  for (int j = threadIdx.x; j <= row; j += blockDim.x) acc += (double)expf(mean[base + j] - mx);
-  dred[threadIdx.x] = acc;
-  __syncthreads();
-  for (int s = 64; s > 0; s >>= 1) {
-    if (threadIdx.x < s) dred[threadIdx.x] += dred[threadIdx.x + s];
-    __syncthreads();
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  double sum = 0.0;
+  for (int c4 = lane; c4 <= last4; c4 += 32) {
+    const float4 a = causal_row4(src, c4, row);
+    sum += (double)((expf(a.x - mx) + expf(a.y - mx)) + (expf(a.z - mx) + expf(a.w - mx)));
   }
-  const float inv = (float)(1.0 / dred[0]);
-  for (int j = threadIdx.x; j < T; j += blockDim.x)
-    out[base + j] = (j <= row) ? expf(mean[base + j] - mx) * inv : 0.f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  const float inv = (float)(1.0 / sum);
+  float4* dst = reinterpret_cast<float4*>(out + base);
+  for (int c4 = lane; c4 < n4; c4 += 32) {
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (c4 <= last4) {
+      const float4 a = causal_row4(src, c4, row);
+      o = make_float4(expf(a.x - mx) * inv, expf(a.y - mx) * inv, expf(a.z - mx) * inv,
+                      expf(a.w - mx) * inv);
+    }
+    __stcs(dst + c4, o);
+  }
 }
 
 // One block: s_var per head (one warp per head, fixed-order sums) and the
@@ -281,7 +302,9 @@ cudaError_t launch_calib_finalize_kl(const CalibFinalize& p, cudaStream_t s) {
 cudaError_t launch_calib_sharp(const float* mean, int num_heads, int T, float* out,
                                cudaStream_t s) {
   trace_begin(s);
-  calib_sharp_rows_kernel<<<dim3(T, num_heads), 128, 0, s>>>(mean, T, out);
+  if (T % 4 != 0) return cudaErrorInvalidValue;
+  calib_sharp_rows_kernel<<<dim3((T + kSharpRows - 1) / kSharpRows, num_heads), 32 * kSharpRows, 0,
+                            s>>>(mean, T, out);
   trace_end(s, "calib_sharp_rows");
   return cudaGetLastError();
 }

@@ -180,12 +180,13 @@ def test_forward_kl_selector_matches_oracle(api):
     cal.close()
 
 
-def test_sharp_mean_pattern_matches_oracle(api):
-    N, nh, T = 7, 5, 96
+@pytest.mark.parametrize("N,nh,T", [(7, 5, 96), (3, 2, 1028), (2, 1, 4100)])
+def test_sharp_mean_pattern_matches_oracle(api, N, nh, T):
+    # T = 1028 and 4100: rows longer than one 4-column unit per thread
     L = calib_probabilities(N, nh, T, d_h=16, seed=33, want_logits=True)
     cal = api.Calibration(nh, T)
-    cal.accumulate(L[:3].cuda())
-    cal.accumulate(L[3:].cuda())
+    cal.accumulate(L[:N // 2].cuda())
+    cal.accumulate(L[N // 2:].cuda())
     P = cal.finalize_sharp()
     torch.cuda.synchronize()
     P = P.cpu().numpy()
