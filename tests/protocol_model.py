@@ -15,6 +15,12 @@ actions:
                               in issue order; a commit arrives after all of
                               the role's earlier products
   ("pair", key)               meet the other role that yields the same key
+Data versions (optional): ("mma", reads, writes) with lists of (region, tag)
+checks at issue and again at completion that each region it reads holds that
+tag, and stores its tags at completion; ("tma", barrier, region, tag) stores
+its tag when it lands; ("read", region, tag) and ("write", region, tag) are a
+role's own accesses.  A read that meets another tag is a stale read or an
+overwrite of data still in use.
 Host logic only.
 """
 
@@ -55,6 +61,12 @@ def run_roles(roles, bars, issuers, rng, max_events=200000):
     """Run role generators to the end under a random interleaving.  `issuers`
     names the roles whose products and commits complete in issue order."""
     nxt = {k: None for k in roles}
+    regions = {}
+
+    def check_reads(reads, when):
+        for r, tag in reads:
+            if regions.get(r) != tag:
+                raise Violation(f"{r}: {when} expects {tag}, holds {regions.get(r)}")
     finished = set()
     tma = []                            # barriers of copies in flight (land in any order)
     fifo = {k: [] for k in issuers}     # per issuer: products and commits in issue order
@@ -75,9 +87,17 @@ def run_roles(roles, bars, issuers, rng, max_events=200000):
         elif kind == "arrive":
             bars[act[1]].arrive(act[2])
         elif kind == "tma":
-            tma.append(act[1])
-        elif kind in ("mma", "commit"):
+            tma.append(act)
+        elif kind == "mma":
+            if len(act) > 1:
+                check_reads(act[1], "a product at issue")
             fifo[k].append(act)
+        elif kind == "commit":
+            fifo[k].append(act)
+        elif kind == "read":
+            check_reads([(act[1], act[2])], "a read")
+        elif kind == "write":
+            regions[act[1]] = act[2]
         elif kind == "pair":
             pair_seen.setdefault(act[1], set()).add(k)
             if len(pair_seen[act[1]]) < 2:
@@ -96,14 +116,23 @@ def run_roles(roles, bars, issuers, rng, max_events=200000):
     for k in issuers:
         speed[k + "_mma"] = rng.choice([0.05, 0.3, 1.0])
 
+    def land(act):
+        if len(act) > 2:
+            regions[act[2]] = act[3]
+        bars[act[1]].arrive(1)
+
     def fire(ev):
         if ev == "tma":
-            bars[tma.pop(rng.randrange(len(tma)))].arrive(1)
+            land(tma.pop(rng.randrange(len(tma))))
             return True
         if ev.endswith("_mma"):
             act = fifo[ev[:-4]].pop(0)
             if act[0] == "commit":
                 bars[act[1]].arrive(1)
+            elif len(act) > 1:
+                check_reads(act[1], "a product at completion")
+                for r, tag in act[2]:
+                    regions[r] = tag
             return True
         return step_role(ev)
 

@@ -1,4 +1,4 @@
-"""Model check of the dynamic backward's mbarrier protocol at d_h <= 64.
+"""Model check of the dynamic backward's mbarrier protocols (d_h <= 64 and 128).
 
 The dynamic backward kernel (attn_bwd.cu, bwd_dynamic_kernel, the path that
 keeps P^T in TMEM and alternates two dS^T tiles in shared memory) runs a
@@ -9,7 +9,12 @@ file restates each role's waits, arrivals and commits and runs them under
 random interleavings with the checker of protocol_model: every parity wait
 must pass on exactly the awaited phase, no barrier may see more arrivals
 than its count, and every role must finish.  A planted mistake (both dS^T
-tiles released through one barrier) must be caught.  Host logic only.
+tiles released through one barrier) must be caught.
+
+At d_h = 128 the kernel has no TMEM to spare: one warp issues every product,
+P^T and dS^T overwrite the S^T and dP^T columns, dQ accumulates over the dP^T
+columns and is staged through the dS^T tile.  The second model restates that
+path (QST = 2, dv_done / dk_done / dp_full / dqs_free).  Host logic only.
 """
 
 import random
@@ -158,6 +163,182 @@ def test_planted_shared_tile_barrier_is_caught():
     for _ in range(200):
         try:
             run_model(random_items(rng, rng.randint(2, 10)), rng, one_tile=True)
+        except Violation:
+            caught += 1
+    assert caught >= 10
+
+
+# ------------------------------------------------------------ d_h = 128 path
+QST128 = 2
+
+
+def make_barriers_128():
+    b = {}
+    def add(name, count):
+        b[name] = Barrier(name, count)
+    add("kv_full", 1); add("kv_empty", 1)
+    for s in range(QST128):
+        add(f"q_full{s}", 1); add(f"q_empty{s}", 1)
+    add("s_full", 1); add("dp_full", 1)
+    add("p_full", 2)
+    add("p_empty", 1)
+    add("dq_full", 1); add("dq_empty", 1)
+    add("kd_full", 1); add("kd_empty", 2)
+    add("dv_done", 1); add("dk_done", 1)
+    add("dqs_free", 1)
+    return b
+
+
+def producer_128(items):
+    kvc = qc = 0
+    for i, n in enumerate(items):
+        yield ("wait", "kv_empty", kvc - 1)
+        kvc += 1
+        yield ("tma", "kv_full", "KV", f"kv{i}")
+        for _ in range(n):
+            qs = qc % QST128
+            yield ("wait", f"q_empty{qs}", qc // QST128 - 1)
+            yield ("tma", f"q_full{qs}", f"Q{qs}", f"q{qc}")
+            qc += 1
+
+
+# TMEM regions: TS (S^T, then P^T), TDP (dP^T, then dS^T, then dQ), TDV, TDK;
+# the halves' columns of TS, TDP and of the shared dS^T tile DST are separate
+# regions for the compute warps (h0, h1).  Tags name the step u (global) or
+# the item i and step t.
+def both(region, tag):
+    return [(region + "h0", tag), (region + "h1", tag)]
+
+
+def issuer_128(items, skip_dq_drain=False):
+    kvc = qc = pc = dqc = kdc = dvc = dkc = 0
+
+    def issue_st(q, i):
+        yield ("wait", f"q_full{q % QST128}", q // QST128)
+        yield ("mma", [("KV", f"kv{i}"), (f"Q{q % QST128}", f"q{q}")], both("TS", f"S{q}"))
+        yield ("commit", "s_full")
+
+    def issue_dpt(q, i):
+        yield ("wait", f"q_full{q % QST128}", q // QST128)
+        yield ("mma", [("KV", f"kv{i}"), (f"Q{q % QST128}", f"q{q}")], both("TDP", f"dP{q}"))
+        yield ("commit", "dp_full")
+
+    for i, n in enumerate(items):
+        yield ("wait", "kv_full", kvc)
+        kvc += 1
+        if dvc > 0:
+            yield ("wait", "dv_done", dvc - 1)
+        yield from issue_st(qc, i)
+        yield ("wait", "dq_empty", dqc - 1)
+        yield from issue_dpt(qc, i)
+        for t in range(n):
+            qs = qc % QST128
+            u = qc
+            yield ("wait", "p_full", pc)
+            if t == 0:
+                yield ("wait", "kd_empty", kdc - 1)
+            acc_v = [("TDV", f"dv{i}.{t - 1}")] if t > 0 else []
+            yield ("mma", both("TS", f"P{u}") + [(f"Q{qs}", f"q{u}")] + acc_v,
+                   [("TDV", f"dv{i}.{t}")])                     # dV
+            yield ("commit", "dv_done")
+            dvc += 1
+            acc_k = [("TDK", f"dk{i}.{t - 1}")] if t > 0 else []
+            yield ("mma", both("TDP", f"dS{u}") + [(f"Q{qs}", f"q{u}")] + acc_k,
+                   [("TDK", f"dk{i}.{t}")])                     # dK
+            yield ("commit", "dk_done")
+            dkc += 1
+            yield ("commit", f"q_empty{qs}")
+            qc += 1
+            pc += 1
+            yield ("wait", "dk_done", dkc - 1)
+            yield ("mma", both("DST", f"dS{u}") + [("KV", f"kv{i}")],
+                   both("TDP", f"dQ{u}"))                        # dQ over the dP^T columns
+            yield ("commit", "p_empty")
+            yield ("commit", "dq_full")
+            dqc += 1
+            if t + 1 < n:
+                yield ("wait", "dv_done", dvc - 1)
+                yield from issue_st(qc, i)
+                if not skip_dq_drain:
+                    yield ("wait", "dq_empty", dqc - 1)
+                yield from issue_dpt(qc, i)
+        yield ("commit", "kd_full")
+        yield ("commit", "kv_empty")
+        kdc += 1
+
+
+def compute_128(hf, items):
+    qc = sc = pc = kdc = 0
+    h = f"h{hf}"
+    for i, n in enumerate(items):
+        for _ in range(n):
+            qs = qc % QST128
+            u = qc
+            yield ("wait", f"q_full{qs}", qc // QST128)
+            yield ("read", f"Q{qs}", f"q{u}")           # -lse, -D of the stage
+            yield ("wait", "s_full", sc)
+            yield ("read", "TS" + h, f"S{u}")
+            yield ("write", "TS" + h, f"P{u}")
+            yield ("wait", "dp_full", sc)
+            yield ("read", "TDP" + h, f"dP{u}")
+            yield ("write", "TDP" + h, f"dS{u}")
+            yield ("wait", "p_empty", pc - 1)
+            yield ("wait", "dqs_free", pc - 1)
+            yield ("write", "DST" + h, f"dS{u}")
+            yield ("arrive", "p_full", 1)
+            qc += 1
+            sc += 1
+            pc += 1
+        yield ("wait", "kd_full", kdc)
+        yield ("read", "TDV" if hf == 0 else "TDK", f"{'dv' if hf == 0 else 'dk'}{i}.{n - 1}")
+        yield ("arrive", "kd_empty", 1)
+        kdc += 1
+
+
+def dq_warps_128(items):
+    dqc = 0
+    u = 0
+    for n in items:
+        for _ in range(n):
+            yield ("wait", "dq_full", dqc)
+            yield ("read", "TDPh0", f"dQ{u}")
+            yield ("read", "TDPh1", f"dQ{u}")
+            yield ("arrive", "dq_empty", 1)    # every dQ column in registers
+            # staged through the dS^T tile (its dQ product has completed), then
+            # read by the tensor reduce-adds
+            yield ("write", "DSTh0", f"dQs{u}")
+            yield ("write", "DSTh1", f"dQs{u}")
+            yield ("read", "DSTh0", f"dQs{u}")
+            yield ("read", "DSTh1", f"dQs{u}")
+            yield ("arrive", "dqs_free", 1)
+            dqc += 1
+            u += 1
+
+
+def run_model_128(items, rng, skip_dq_drain=False):
+    roles = {
+        "prod": producer_128(items), "g": issuer_128(items, skip_dq_drain),
+        "c0": compute_128(0, items), "c1": compute_128(1, items), "dq": dq_warps_128(items),
+    }
+    run_roles(roles, make_barriers_128(), ("g",), rng)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_backward_128_protocol_holds(seed):
+    rng = random.Random(1000 + seed)
+    for _ in range(5):
+        run_model_128(random_items(rng, rng.randint(1, 14)), rng)
+
+
+def test_planted_skipped_dq_drain_is_caught():
+    # The next step's dP^T issued without waiting for the dQ warps to drain
+    # the columns it overwrites: the later dq_empty wait then meets a barrier
+    # two phases on, or the phases of dq_empty run ahead of their waiter.
+    rng = random.Random(17)
+    caught = 0
+    for _ in range(200):
+        try:
+            run_model_128(random_items(rng, rng.randint(2, 10)), rng, skip_dq_drain=True)
         except Violation:
             caught += 1
     assert caught >= 10
