@@ -17,7 +17,10 @@ actions:
   ("pair", key)               meet the other role that yields the same key
 Data versions (optional): ("mma", reads, writes) with lists of (region, tag)
 checks at issue and again at completion that each region it reads holds that
-tag, and stores its tags at completion; ("tma", barrier, region, tag) stores
+tag, and stores its tags at completion (a third list, ("mma", reads, writes,
+chained), names accumulator inputs written by the same role's earlier
+products: products of one role execute in order, so those are checked at
+completion only); ("tma", barrier, region, tag) stores
 its tag when it lands; ("read", region, tag) and ("write", region, tag) are a
 role's own accesses.  A read that meets another tag is a stale read or an
 overwrite of data still in use.
@@ -131,6 +134,8 @@ def run_roles(roles, bars, issuers, rng, max_events=200000):
                 bars[act[1]].arrive(1)
             elif len(act) > 1:
                 check_reads(act[1], "a product at completion")
+                if len(act) > 3:
+                    check_reads(act[3], "a chained product at completion")
                 for r, tag in act[2]:
                     regions[r] = tag
             return True

@@ -45,15 +45,22 @@ def make_barriers():
 
 def producer(items):
     kvc = qc = 0
-    for n in items:
+    for i, n in enumerate(items):
         yield ("wait", "kv_empty", kvc - 1)
         kvc += 1
-        yield ("tma", "kv_full")
+        yield ("tma", "kv_full", "KV", f"kv{i}")
         for _ in range(n):
             qs = qc % QST
             yield ("wait", f"q_empty{qs}", qc // QST - 1)
+            yield ("tma", f"q_full{qs}", f"Q{qs}", f"q{qc}")
             qc += 1
-            yield ("tma", f"q_full{qs}")
+
+
+# Data regions (d_h <= 64): KV, Q{stage} in shared memory, DST{tile}h0/h1 (the
+# halves' columns of a dS^T tile); in TMEM TS and TDP (S^T, dP^T, per half),
+# TPT (P^T, per half), TDV, TDK, TDQ.
+def halves(region, tag):
+    return [(region + "h0", tag), (region + "h1", tag)]
 
 
 def s_issuer(items):
@@ -70,29 +77,37 @@ def s_issuer(items):
                 sfc += 1
             qs = qc % QST
             yield ("wait", f"q_full{qs}", qc // QST)
-            yield ("mma",)            # S^T, dP^T
+            yield ("mma", [("KV", f"kv{idx}"), (f"Q{qs}", f"q{qc}")],
+                   halves("TS", f"S{qc}") + halves("TDP", f"dP{qc}"))   # S^T, dP^T
             yield ("commit", "s_full")
             qc += 1
 
 
 def grad_issuer(items, one_tile=False):
     kvc = qc = pc = dqc = kdc = 0
-    for n in items:
+    for i, n in enumerate(items):
         yield ("wait", "kv_full", kvc)
         kvc += 1
         for t in range(n):
             qs = qc % QST
+            u = qc
+            tile = 0 if one_tile else (pc & 1)
             yield ("wait", "p_full", pc)
             if t == 0:
                 yield ("wait", "kd_empty", kdc - 1)
-            yield ("mma",)            # dV from P^T in TMEM
+            yield ("mma", halves("TPT", f"P{u}") + [(f"Q{qs}", f"q{u}")],
+                   [("TDV", f"dv{i}.{t}")],
+                   [("TDV", f"dv{i}.{t - 1}")] if t > 0 else [])     # dV from P^T in TMEM
             yield ("commit", "pt_empty")
-            yield ("mma",)            # dK from the dS^T tile
+            yield ("mma", halves(f"DST{pc & 1}", f"dS{u}") + [(f"Q{qs}", f"q{u}")],
+                   [("TDK", f"dk{i}.{t}")],
+                   [("TDK", f"dk{i}.{t - 1}")] if t > 0 else [])     # dK from the dS^T tile
             yield ("commit", f"q_empty{qs}")
             qc += 1
             yield ("wait", "dq_empty", dqc - 1)
-            yield ("mma",)            # dQ from the dS^T tile
-            yield ("commit", "p_empty0" if one_tile or not (pc & 1) else "p_empty1")
+            yield ("mma", halves(f"DST{pc & 1}", f"dS{u}") + [("KV", f"kv{i}")],
+                   [("TDQ", f"dQ{u}")])                               # dQ
+            yield ("commit", f"p_empty{tile}")
             pc += 1
             yield ("commit", "dq_full")
             dqc += 1
@@ -103,23 +118,31 @@ def grad_issuer(items, one_tile=False):
 
 def compute(hf, items, one_tile=False):
     qc = sc = pc = kdc = 0
-    for idx, n in enumerate(items):
+    h = f"h{hf}"
+    for i, n in enumerate(items):
         for t in range(n):
             qs = qc % QST
+            u = qc
             yield ("wait", f"q_full{qs}", qc // QST)
+            yield ("read", f"Q{qs}", f"q{u}")           # -lse, -D of the stage
             yield ("wait", "s_full", sc)
+            yield ("read", "TS" + h, f"S{u}")
+            yield ("read", "TDP" + h, f"dP{u}")
             # first chunk: P^T and the dS^T tile must be free
             yield ("wait", "pt_empty", pc - 1)
             # (planted: both tiles' releases land on one barrier, while the
             # wait keeps the per-tile phase count)
             tile = 0 if one_tile else (pc & 1)
             yield ("wait", f"p_empty{tile}", (pc >> 1) - 1)
+            yield ("write", "TPT" + h, f"P{u}")
+            yield ("write", f"DST{pc & 1}" + h, f"dS{u}")
             yield ("arrive", "s_free", 1)   # after the last chunk's loads
             yield ("arrive", "p_full", 1)
             qc += 1
             sc += 1
             pc += 1
         yield ("wait", "kd_full", kdc)
+        yield ("read", "TDV" if hf == 0 else "TDK", f"{'dv' if hf == 0 else 'dk'}{i}.{n - 1}")
         yield ("arrive", "kd_empty", 1)
         kdc += 1
 
@@ -129,6 +152,7 @@ def dq_warps(items):
     for n in items:
         for _ in range(n):
             yield ("wait", "dq_full", dqc)
+            yield ("read", "TDQ", f"dQ{dqc}")
             yield ("arrive", "dq_empty", 1)
             dqc += 1
 

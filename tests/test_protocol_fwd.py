@@ -50,60 +50,65 @@ def make_barriers(shared_s):
 
 
 # --------------------------------------------------------------- the roles
-# Each role is a generator of actions:
-#   ("wait", barrier, phase) ("arrive", barrier, units) ("tma", barrier)
-#   ("mma",) ("commit", barrier) ("pair", item index)
+# Each role is a generator of actions (see protocol_model).  Data regions:
+# Q{slot}, K{slot}, V{slot}, A{slot} (tables) in shared memory; S{g} (a half's
+# S buffer), P{b}h0 / P{b}h1 (the two halves' columns of a P buffer), O0, O1
+# in TMEM.  Tags name the item i and its key tile j (or static step).
 
 def producer_qk(items):
     qc = ac = 0
     kn = [0, 0]
-    for it in items:
+    for i, it in enumerate(items):
         if it["dyn"]:
             qs = qc % QST
             yield ("wait", f"q_empty{qs}", qc // QST - 1)
             qc += 1
-            yield ("tma", f"q_full{qs}")
+            yield ("tma", f"q_full{qs}", f"Q{qs}", f"q{i}")
             for j in range(it["n"]):
                 r = j & 1
                 n = kn[r]
                 kn[r] += 1
                 slot = 2 * r + (n & 1)
                 yield ("wait", f"k_empty{slot}", (n >> 1) - 1)
-                yield ("tma", f"k_full{slot}")
+                yield ("tma", f"k_full{slot}", f"K{slot}", f"k{i}.{j}")
         else:
-            for _ in range(it["n"]):
+            for step in range(it["n"]):
                 a = ac % AST
                 yield ("wait", f"aux_empty{a}", ac // AST - 1)
                 ac += 1
-                yield ("tma", f"aux_full{a}")
+                yield ("tma", f"aux_full{a}", f"A{a}", f"a{i}.{step}")
 
 
 def producer_v(items):
     vc = 0
-    for it in items:
+    for i, it in enumerate(items):
         if it["dyn"]:
-            for _ in range(it["n"]):
+            for j in range(it["n"]):
                 vs = vc % VST
                 yield ("wait", f"v_empty{vs}", vc // VST - 1)
                 vc += 1
-                yield ("tma", f"v_full{vs}")
+                yield ("tma", f"v_full{vs}", f"V{vs}", f"v{i}.{j}")
         else:
-            for _ in range(it["n"]):
+            for step in range(it["n"]):
                 if it["nb"] == 2 and (vc & 1):
                     vs = vc % VST
                     yield ("wait", f"v_empty{vs}", vc // VST - 1)
                     vc += 1
                     yield ("arrive", f"v_full{vs}", 1)
-                for _ in range(it["nb"]):
+                for bb in range(it["nb"]):
                     vs = vc % VST
                     yield ("wait", f"v_empty{vs}", vc // VST - 1)
                     vc += 1
-                    yield ("tma", f"v_full{vs}")
+                    yield ("tma", f"v_full{vs}", f"V{vs}", f"v{i}.{step}.{bb}")
+
+
+def pbuf(b, tag):
+    return [(f"P{b}h0", tag), (f"P{b}h1", tag)]
 
 
 def issuer(g, items, shared_s, late_o=False):
     qc = vc = sc = oc = kn = sn = ss = 0
-    for it in items:
+    for i, it in enumerate(items):
         o_ready = [False]
 
         def wait_o():
@@ -128,7 +133,8 @@ def issuer(g, items, shared_s, late_o=False):
                 else:
                     yield ("wait", f"s_empty{g}", sn - 1)
                     buf = g
-                yield ("mma",)
+                yield ("mma", [(f"Q{qs}", f"q{i}"), (f"K{slot}", f"k{i}.{j}")],
+                       [(f"S{buf}", f"s{i}.{j}")])
                 yield ("commit", f"k_empty{slot}")
                 yield ("commit", f"s_full{buf}")
                 kn += 1
@@ -139,7 +145,9 @@ def issuer(g, items, shared_s, late_o=False):
                 vq = vc + j
                 yield ("wait", f"v_full{vq % VST}", vq // VST)
                 yield ("wait", f"p_full{u & 1}", u >> 1)
-                yield ("mma",)
+                acc = [(f"O{g}", f"o{i}.{j - 2}r")] if j > 1 else []
+                yield ("mma", pbuf(u & 1, f"p{i}.{j}") + [(f"V{vq % VST}", f"v{i}.{j}")] + acc,
+                       [(f"O{g}", f"o{i}.{j}")])
                 yield ("commit", f"v_empty{vq % VST}")
                 yield ("commit", f"p_empty{u & 1}")
 
@@ -154,6 +162,7 @@ def issuer(g, items, shared_s, late_o=False):
             vc += n
             ss += n
         else:
+            outs = ["O0", "O1"][: it["nb"]]
             for step in range(it["n"]):
                 u = sc + step
                 if g == 1:
@@ -167,6 +176,9 @@ def issuer(g, items, shared_s, late_o=False):
                 else:
                     yield from wait_o()
                     yield ("wait", f"p_full{u & 1}", u >> 1)
+                # the group's O chain: products of this issuer, in order
+                acc = [(o, f"st{i}.{step - 1}") for o in outs] if step > 0 else []
+                writes = [(o, f"st{i}.{step}") for o in outs]
                 if it["nb"] == 2:
                     if vc & 1:
                         yield ("wait", f"v_full{vc % VST}", vc // VST)
@@ -174,13 +186,16 @@ def issuer(g, items, shared_s, late_o=False):
                         vc += 1
                     yield ("wait", f"v_full{vc % VST}", vc // VST)
                     yield ("wait", f"v_full{(vc + 1) % VST}", (vc + 1) // VST)
-                    yield ("mma",)
+                    yield ("mma", pbuf(u & 1, f"g{i}.{step}") +
+                           [(f"V{vc % VST}", f"v{i}.{step}.0"),
+                            (f"V{(vc + 1) % VST}", f"v{i}.{step}.1")], writes, acc)
                     yield ("commit", f"v_empty{vc % VST}")
                     yield ("commit", f"v_empty{(vc + 1) % VST}")
                     vc += 2
                 else:
                     yield ("wait", f"v_full{vc % VST}", vc // VST)
-                    yield ("mma",)
+                    yield ("mma", pbuf(u & 1, f"g{i}.{step}") +
+                           [(f"V{vc % VST}", f"v{i}.{step}.0")], writes, acc)
                     yield ("commit", f"v_empty{vc % VST}")
                     vc += 1
                 yield ("commit", f"p_empty{u & 1}")
@@ -192,10 +207,11 @@ def issuer(g, items, shared_s, late_o=False):
 
 def compute(hf, items, shared_s):
     ac = sc = oc = sn = ss = 0
-    for idx, it in enumerate(items):
+    for i, it in enumerate(items):
         sc0 = sc
+        n = it["n"]
         if it["dyn"]:
-            for j in range(hf, it["n"], 2):
+            for j in range(hf, n, 2):
                 u = sc0 + j
                 if shared_s:
                     us = ss + j
@@ -204,22 +220,36 @@ def compute(hf, items, shared_s):
                     sb, ph = hf, sn
                 yield ("wait", f"s_full{sb}", ph)
                 sn += 1
+                yield ("read", f"S{sb}", f"s{i}.{j}")
                 yield ("arrive", f"s_empty{sb}", 1)
                 yield ("wait", f"p_empty{u & 1}", (u >> 1) - 1)
+                yield ("write", f"P{u & 1}h0", f"p{i}.{j}")
+                yield ("write", f"P{u & 1}h1", f"p{i}.{j}")
+                if j > 1:   # a rescale of this half's O, in place
+                    yield ("read", f"O{hf}", f"o{i}.{j - 2}")
+                    yield ("write", f"O{hf}", f"o{i}.{j - 2}r")
                 yield ("arrive", f"p_full{u & 1}", 2)
-            ss += it["n"]
+            ss += n
+            reads = [("O0", f"o{i}.{(n - 1) // 2 * 2}")]
+            if n > 1:
+                reads.append(("O1", f"o{i}.{(n - 2) // 2 * 2 + 1}"))
         else:
-            for step in range(it["n"]):
+            for step in range(n):
                 u = sc0 + step
                 a = ac % AST
                 yield ("wait", f"aux_full{a}", ac // AST)
+                yield ("read", f"A{a}", f"a{i}.{step}")
                 yield ("wait", f"p_empty{u & 1}", (u >> 1) - 1)
+                yield ("write", f"P{u & 1}h{hf}", f"g{i}.{step}")
                 yield ("arrive", f"aux_empty{a}", 1)
                 ac += 1
                 yield ("arrive", f"p_full{u & 1}", 1)
-        sc = sc0 + it["n"]
-        yield ("pair", idx)   # the halves' max/sum exchange (named barriers)
+            reads = [(o, f"st{i}.{n - 1}") for o in ["O0", "O1"][: it["nb"]]]
+        sc = sc0 + n
+        yield ("pair", i)   # the halves' max/sum exchange (named barriers)
         yield ("wait", "o_full", oc)
+        for r, tag in reads:
+            yield ("read", r, tag)
         yield ("arrive", "o_empty", 1)
         oc += 1
 
