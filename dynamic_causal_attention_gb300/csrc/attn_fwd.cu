@@ -471,7 +471,9 @@ __global__ void __launch_bounds__(384, 1)
   constexpr uint32_t kTmemP = 256;
   static_assert(!SPLIT || kTmemO + 2 * D <= kTmemCols, "TMEM: two O accumulators");
   static_assert(!SPLIT || kTmemP + 128 <= kTmemO, "TMEM: two P buffers");
-  uint64_t* s_full = v_empty + L::VST;   // S ready (MMA -> compute)
+  // S ready (MMA -> compute); without SPLIT also a static use of the buffer
+  // granted (warp 1 -> compute)
+  uint64_t* s_full = v_empty + L::VST;
   // buffer free again: its P V MMAs done (MMA -> all); with SPLIT: the
   // softmax has read the S buffer (compute -> S issuer, 128 arrivals)
   uint64_t* s_empty = s_full + NB;
@@ -808,6 +810,15 @@ __global__ void __launch_bounds__(384, 1)
             if (j == w.nsteps - 1) mma_commit(q_empty + qs);
             ++kc;
           }
+        } else {
+          // A static step's buffer is granted here too, once its previous
+          // use is done: this warp takes part in every use of every buffer,
+          // so its parity waits never meet a phase two uses away.
+          for (int step = 0; step < w.nsteps; ++step) {
+            const uint32_t u = sc0 + step, b = u % NB;
+            mbar_wait(s_empty + b, ((u / NB) & 1) ^ 1, wc, kSiteMmaS);
+            mbar_arrive(s_full + b);
+          }
         }
         sc = sc0 + w.nsteps;
       }
@@ -886,9 +897,7 @@ __global__ void __launch_bounds__(384, 1)
                 ++vc;
               }
             }
-            // every use of a TMEM buffer completes one phase of both of its
-            // barriers, so that the compute warps can count uses uniformly
-            mma_commit(s_full + pb);
+            // the use ends here (warp 1 granted it through s_full)
             mma_commit(s_empty + pb);
           }
           mma_commit(o_full);
@@ -1253,11 +1262,12 @@ __global__ void __launch_bounds__(384, 1)
           const float* aux = reinterpret_cast<const float*>(smem + L::OFF_AUX + as * L::AUX_SLOT);
           const float* colv = aux + 64 * hf;       // this half's 64 column values
           const float* win = aux + L::AUX_WIN / 4; // window, centre at 127
-          // the TMEM buffer must be free: the MMAs of two steps back are done
+          // the buffer must be free: SPLIT, the P V products of two uses back
+          // are done; otherwise warp 1 has granted it
           if (SPLIT)
             mbar_wait(p_empty + (u & 1), ((u >> 1) & 1) ^ 1, wc, kSiteCmpP);
           else
-            mbar_wait(s_empty + (u % NB), ((u / NB) & 1) ^ 1, wc, kSiteCmpP);
+            mbar_wait(s_full + (u % NB), (u / NB) & 1, wc, kSiteCmpP);  // warp 1's grant
           tc_fence_after();
           // this half's 64 keys as 32 packed columns
           const uint32_t gdst = SPLIT ? trow + kTmemP + (u & 1) * 64 + 32 * hf
