@@ -72,20 +72,20 @@ __device__ __forceinline__ void block_minmax(float& mx, float& mn, float* red) {
   }
 }
 
-// grid (T / 64, n_static), 256 threads (8 warps), dynamic smem 2 * T + 8
+// grid (T / kPrepRows, n_static), 256 threads (8 warps), dynamic smem 2 * T + 8
 // floats.  Each block scans alpha/rho for their finite ranges and picks the
-// mode.  Factored heads: the block writes its 64 entries of the tables and,
+// mode.  Factored heads: the block writes its kPrepRows entries of the tables and,
 // block 0, the head's shift max alpha + max rho.  Exact heads: each warp
-// also forms log Z of 8 rows by an online log-sum-exp, its 32 lanes
+// also forms log Z of kPrepRows / 8 rows by an online log-sum-exp, its 32 lanes
 // splitting the causal sum, merged across lanes in a fixed order.
-constexpr int kPrepRows = 64;
+constexpr int kPrepRows = 128;  // rows of a head per block (T is a multiple of 128)
 
 __global__ void __launch_bounds__(256) static_prep_kernel(StaticPrep p) {
   extern __shared__ float sh[];
   __shared__ float red[64];
   const int T = p.T, hs = blockIdx.y, h = p.heads[hs];
   const int row0 = blockIdx.x * kPrepRows;
-  const int nload = row0 + kPrepRows;  // entries 0 .. row0 + 63 are needed
+  const int nload = row0 + kPrepRows;  // entries 0 .. row0 + kPrepRows - 1 are needed
   float* sa = sh;
   float* sr = sh + T + 8;  // sr[-8 .. -1] = 0: the last stride reads past d = 0
   const float* alpha = p.alpha + (size_t)h * T;
@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(256) static_prep_kernel(StaticPrep p) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
   if (!exact) {
-    // a = exp(alpha - max), r = exp(rho - max) for this block's 64 entries.
+    // a = exp(alpha - max), r = exp(rho - max) for this block's kPrepRows entries.
     // Z'(i) is not formed here: the forward sums it from its own tiles and
     // the backward reads it back from the forward's lse.
     __syncthreads();
