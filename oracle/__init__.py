@@ -49,6 +49,7 @@ from .fit import (
     fit_loss,
     fit_gradient,
     mean_row_kl,
+    adam_step,
     compact_fit,
     select_fitted,
 )
@@ -91,6 +92,7 @@ __all__ = [
     "fit_loss",
     "fit_gradient",
     "mean_row_kl",
+    "adam_step",
     "compact_fit",
     "select_fitted",
 ]

@@ -34,6 +34,7 @@ __all__ = [
     "fit_loss",
     "fit_gradient",
     "mean_row_kl",
+    "adam_step",
     "compact_fit",
     "select_fitted",
 ]
@@ -71,6 +72,17 @@ def mean_row_kl(A_hat, P) -> float:
     return float((A[m] * (np.log(A[m]) - np.log(P[m]))).sum() / A.shape[0])
 
 
+def adam_step(theta, g, m, v, t, lr, beta1, beta2, eps):
+    """One Adam update (Kingma & Ba, Algorithm 1) of step number t >= 1:
+    moments m, v; bias-corrected mhat, vhat; theta - lr mhat / (sqrt(vhat) + eps).
+    Returns (theta, m, v)."""
+    m = beta1 * m + (1 - beta1) * g
+    v = beta2 * v + (1 - beta2) * g * g
+    mhat = m / (1 - beta1 ** t)
+    vhat = v / (1 - beta2 ** t)
+    return theta - lr * mhat / (np.sqrt(vhat) + eps), m, v
+
+
 def compact_fit(A_hat, steps=400, lr=1e-2, beta1=0.9, beta2=0.999, eps=1e-8):
     """Fit (alpha, rho) to one head's A_hat.  Returns (alpha, rho, mean row KL)."""
     A = np.asarray(A_hat, dtype=np.float64)
@@ -84,14 +96,8 @@ def compact_fit(A_hat, steps=400, lr=1e-2, beta1=0.9, beta2=0.999, eps=1e-8):
     v_r = np.zeros(T)
     for t in range(1, steps + 1):
         g_a, g_r = fit_gradient(alpha, rho, (col_t, diag_t))
-        m_a = beta1 * m_a + (1 - beta1) * g_a
-        v_a = beta2 * v_a + (1 - beta2) * g_a * g_a
-        m_r = beta1 * m_r + (1 - beta1) * g_r
-        v_r = beta2 * v_r + (1 - beta2) * g_r * g_r
-        c1 = 1 - beta1 ** t
-        c2 = 1 - beta2 ** t
-        alpha = alpha - lr * (m_a / c1) / (np.sqrt(v_a / c2) + eps)
-        rho = rho - lr * (m_r / c1) / (np.sqrt(v_r / c2) + eps)
+        alpha, m_a, v_a = adam_step(alpha, g_a, m_a, v_a, t, lr, beta1, beta2, eps)
+        rho, m_r, v_r = adam_step(rho, g_r, m_r, v_r, t, lr, beta1, beta2, eps)
     return alpha, rho, mean_row_kl(A, static_pattern(alpha, rho))
 
 

@@ -75,3 +75,56 @@ def test_select_fitted_skips_heads_over_the_gate():
     assert list(oracle.select_fitted(order, kls, 3)) == [5, 9, 1]
     assert list(oracle.select_fitted(order, kls, 10)) == [5, 9, 1, 7]
     assert list(oracle.select_fitted(order, kls, 0)) == []
+
+
+def test_mean_row_kl_golden(golden):
+    # Hand-worked T = 3 case: the direction KL(A_hat || P_hat) and the 1/T row
+    # average are both visible in the value.
+    g = golden("fit_row_kl_T3.txt")
+    want = float(np.sum(g["kl_terms"]))
+    assert abs(oracle.mean_row_kl(g["A"], g["P"]) - want) < 1e-14
+    # the other direction is a different number (1/4 ln(3/2))
+    assert abs(oracle.mean_row_kl(g["P"], g["A"]) - 0.25 * np.log(1.5)) < 1e-14
+
+
+def test_mean_row_kl_is_cross_entropy_minus_entropy():
+    # The gate and the fitted objective are tied: for any causal target A and
+    # any (alpha, rho), mean row KL(A || P_hat) = fit_loss - (row entropy of A) / T.
+    T = 11
+    A = _random_causal_rows(T)
+    alpha, rho = RNG.normal(size=T), RNG.normal(size=T)
+    m = A > 0
+    entropy = -(A[m] * np.log(A[m])).sum()
+    kl = oracle.mean_row_kl(A, oracle.static_pattern(alpha, rho))
+    assert abs(kl - (oracle.fit_loss(alpha, rho, A) - entropy / T)) < 1e-12
+
+
+def test_adam_two_steps_golden(golden):
+    g = golden("adam_two_steps.txt")
+    lr, b1, b2, eps = (float(g[k][0]) for k in ("lr", "b1", "b2", "eps"))
+    theta, m, v = np.array([g["theta0"][0]]), np.zeros(1), np.zeros(1)
+    for t in (1, 2):
+        theta, m, v = oracle.adam_step(theta, np.array([g["g"][t - 1]]), m, v, t, lr, b1, b2, eps)
+        assert abs(m[0] - g["m"][t - 1]) < 1e-15
+        assert abs(v[0] - g["v"][t - 1]) < 1e-18
+        assert abs(theta[0] - g["theta"][t - 1]) < 1e-13
+    # a gradient as small as eps: the step is lr / 2 only with eps outside the
+    # square root and with the bias correction
+    theta, _, _ = oracle.adam_step(np.zeros(1), np.array([g["g_small"][0]]), np.zeros(1),
+                                   np.zeros(1), 1, lr, b1, b2, eps)
+    assert abs(theta[0] - g["theta_small"][0]) < 1e-12
+
+
+def test_compact_fit_runs_adam_from_the_log_marginals():
+    # One step of compact_fit is one adam_step from the stated initial point.
+    T = 7
+    A = _random_causal_rows(T)
+    col, diag = oracle.marginals(A)
+    a0 = np.log(np.maximum(col / (T - np.arange(T)), 1e-30))
+    r0 = np.log(np.maximum(diag / (T - np.arange(T)), 1e-30))
+    ga, gr = oracle.fit_gradient(a0, r0, (col, diag))
+    a1, _, _ = oracle.adam_step(a0, ga, np.zeros(T), np.zeros(T), 1, 1e-2, 0.9, 0.999, 1e-8)
+    r1, _, _ = oracle.adam_step(r0, gr, np.zeros(T), np.zeros(T), 1, 1e-2, 0.9, 0.999, 1e-8)
+    alpha, rho, kl = oracle.compact_fit(A, steps=1)
+    np.testing.assert_allclose(alpha, a1, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(rho, r1, rtol=0, atol=1e-15)
