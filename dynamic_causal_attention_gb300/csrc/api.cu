@@ -10,6 +10,7 @@
 
 #include "../../include/saf.h"
 #include "attn_kernels.h"
+#include "host_common.h"
 #include "internal.h"
 
 namespace saf {
@@ -56,9 +57,25 @@ void trace_end(cudaStream_t s, const char* kernel) {
   g_pending = nullptr;
 }
 
-namespace {
+void launch_count_reset() { g_launches = 0; }
 
-constexpr int kMaxT = 16384;
+cudaError_t set_max_dynamic_smem(const void* kernel, int bytes) {
+  struct Done {
+    const void* kernel;
+    int device, bytes;
+  };
+  static std::mutex mu;
+  static std::vector<Done> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const Done& d : done)
+    if (d.kernel == kernel && d.device == dev && d.bytes == bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.push_back(Done{kernel, dev, bytes});
+  return e;
+}
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -83,6 +100,7 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+namespace {
 EncodeTiledFn encode_fn() {
   static EncodeTiledFn fn = nullptr;
   static std::once_flag once;
@@ -96,6 +114,7 @@ EncodeTiledFn encode_fn() {
   });
   return fn;
 }
+}  // namespace
 
 // 2-D view [rows, d] of a bf16 tensor, box of 128 rows x one swizzle chunk.
 bool encode_rows(CUtensorMap* m, const void* base, uint64_t rows, int d) {
@@ -113,6 +132,7 @@ bool encode_rows(CUtensorMap* m, const void* base, uint64_t rows, int d) {
   return r == CUDA_SUCCESS;
 }
 
+namespace {
 // 2-D view [rows, d] of an fp32 tensor, box of 128 rows x 32 columns (128 B,
 // 128-byte swizzle): the staging layout of the backward's dQ reduction.
 bool encode_rows_f32(CUtensorMap* m, const void* base, uint64_t rows, int d) {
@@ -137,8 +157,11 @@ struct WsLayout {
   size_t total;
 };
 
+}  // namespace
+
 int kv_heads(const saf_attn_dims& d) { return d.H_kv > 0 ? d.H_kv : d.H; }
 
+namespace {
 WsLayout ws_layout(const saf_attn_dims& d) {
   WsLayout L;
   const size_t B = d.B, H = d.H, T = d.T, D = d.d_h;
@@ -178,6 +201,20 @@ WsLayout ws_layout(const saf_attn_dims& d) {
   return L;
 }
 
+// The static tables of the workspace (every head has a slot).
+StaticTables ws_tables(uint8_t* ws, const WsLayout& L, int H) {
+  StaticTables t;
+  t.a_tab = reinterpret_cast<float*>(ws + L.a_tab);
+  t.r_tab = reinterpret_cast<float*>(ws + L.r_tab);
+  t.row_tab = reinterpret_cast<float*>(ws + L.row_tab);
+  t.logZ = reinterpret_cast<float*>(ws + L.logZ);
+  t.mode = reinterpret_cast<int*>(ws + L.mode);
+  t.shift = reinterpret_cast<float*>(ws + L.mode) + H;
+  t.status = reinterpret_cast<int*>(ws + L.status);
+  return t;
+}
+}  // namespace
+
 saf_status check_dims(const saf_attn_dims* d) {
   if (!d) return SAF_ERR_INVALID_ARG;
   if (d->B < 1 || d->H < 1 || d->T < 1 || d->d_h < 1) return SAF_ERR_INVALID_ARG;
@@ -189,11 +226,6 @@ saf_status check_dims(const saf_attn_dims* d) {
   if ((uint64_t)d->B * d->H * d->T >= (1ull << 31)) return SAF_ERR_UNSUPPORTED;
   return SAF_OK;
 }
-
-struct HeadSplit {
-  int n_static = 0, n_dynamic = 0;
-  uint8_t st[kMaxHeads], dy[kMaxHeads], is_static[kMaxHeads];
-};
 
 HeadSplit split_heads(const uint8_t* head_is_static, int H) {
   HeadSplit s;
@@ -209,7 +241,9 @@ HeadSplit split_heads(const uint8_t* head_is_static, int H) {
   return s;
 }
 
+namespace {
 saf_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SAF_OK : SAF_ERR_CUDA; }
+}  // namespace
 
 #define SAF_TRY(expr)                           \
   do {                                          \
@@ -218,7 +252,7 @@ saf_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SAF_OK : SAF_E
   } while (0)
 
 StaticPrep make_prep(const saf_attn_dims& d, const HeadSplit& hs, const float* alpha,
-                     const float* rho, uint8_t* ws, const WsLayout& L) {
+                     const float* rho, const StaticTables& t) {
   StaticPrep sp;
   memset(&sp, 0, sizeof(sp));
   sp.T = d.T;
@@ -226,17 +260,17 @@ StaticPrep make_prep(const saf_attn_dims& d, const HeadSplit& hs, const float* a
   memcpy(sp.heads, hs.st, sizeof(sp.heads));
   sp.alpha = alpha;
   sp.rho = rho;
-  sp.a_tab = reinterpret_cast<float*>(ws + L.a_tab);
-  sp.r_tab = reinterpret_cast<float*>(ws + L.r_tab);
-  sp.row_tab = reinterpret_cast<float*>(ws + L.row_tab);
-  sp.logZ = reinterpret_cast<float*>(ws + L.logZ);
-  sp.mode = reinterpret_cast<int*>(ws + L.mode);
-  sp.shift = reinterpret_cast<float*>(ws + L.mode) + d.H;
+  sp.a_tab = t.a_tab;
+  sp.r_tab = t.r_tab;
+  sp.row_tab = t.row_tab;
+  sp.logZ = t.logZ;
+  sp.mode = t.mode;
+  sp.shift = t.shift;
   return sp;
 }
 
-void fill_fwd_params(FwdParams& p, const saf_attn_dims& d, const HeadSplit& hs, uint8_t* ws,
-                     const WsLayout& L, bool transposed) {
+void fill_fwd_params(FwdParams& p, const saf_attn_dims& d, const HeadSplit& hs,
+                     const StaticTables& t, bool transposed) {
   memset(&p, 0, sizeof(p));
   p.B = d.B;
   p.H = d.H;
@@ -252,16 +286,15 @@ void fill_fwd_params(FwdParams& p, const saf_attn_dims& d, const HeadSplit& hs, 
   p.scale_log2 = 1.4426950408889634f / sqrtf((float)d.d_h);
   memcpy(p.static_heads, hs.st, sizeof(p.static_heads));
   memcpy(p.dynamic_heads, hs.dy, sizeof(p.dynamic_heads));
-  p.a_tab = reinterpret_cast<const float*>(ws + L.a_tab);
-  p.r_tab = reinterpret_cast<const float*>(ws + L.r_tab);
-  p.row_tab = reinterpret_cast<const float*>(ws + L.row_tab);
-  p.logZ = reinterpret_cast<const float*>(ws + L.logZ);
-  p.mode = reinterpret_cast<const int*>(ws + L.mode);
-  p.shift = reinterpret_cast<const float*>(ws + L.mode) + d.H;
-  p.status = reinterpret_cast<int*>(ws + L.status);
+  p.a_tab = t.a_tab;
+  p.r_tab = t.r_tab;
+  p.row_tab = t.row_tab;
+  p.logZ = t.logZ;
+  p.mode = t.mode;
+  p.shift = t.shift;
+  p.status = t.status;
 }
 
-}  // namespace
 }  // namespace saf
 
 using namespace saf;
@@ -343,11 +376,12 @@ saf_status saf_hybrid_attn_fwd(const saf_attn_dims* dims, const void* Q, const v
     v16 = ws + L.v16;
     o16 = ws + L.o16;
   }
-  if (hs.n_static > 0) SAF_TRY(launch_static_prep(make_prep(d, hs, alpha, rho, ws, L), s));
+  if (hs.n_static > 0)
+    SAF_TRY(launch_static_prep(make_prep(d, hs, alpha, rho, ws_tables(ws, L, d.H)), s));
 
   FwdLaunch fl;
   memset(&fl, 0, sizeof(fl));
-  fill_fwd_params(fl.p, d, hs, ws, L, false);
+  fill_fwd_params(fl.p, d, hs, ws_tables(ws, L, d.H), false);
   fl.p.out = static_cast<__nv_bfloat16*>(o16);
   fl.p.lse = lse;
   const uint64_t rows = (uint64_t)d.B * d.H * d.T;
@@ -426,7 +460,8 @@ saf_status saf_hybrid_attn_bwd(const saf_attn_dims* dims, const void* Q, const v
     dk16 = ws + L.dk16;
     dv16 = ws + L.dv16;
   }
-  if (hs.n_static > 0) SAF_TRY(launch_static_prep(make_prep(d, hs, alpha, rho, ws, L), s));
+  if (hs.n_static > 0)
+    SAF_TRY(launch_static_prep(make_prep(d, hs, alpha, rho, ws_tables(ws, L, d.H)), s));
 
   // pre-pass: D, lse2, per-head batch sums of D for static heads
   BwdPre pre;
@@ -458,7 +493,7 @@ saf_status saf_hybrid_attn_bwd(const saf_attn_dims* dims, const void* Q, const v
     if (dv_acc) SAF_TRY(cudaMemsetAsync(dv_acc, 0, elems_kv * sizeof(float), s));
     FwdLaunch fl;
     memset(&fl, 0, sizeof(fl));
-    fill_fwd_params(fl.p, d, hs, ws, L, true);
+    fill_fwd_params(fl.p, d, hs, ws_tables(ws, L, d.H), true);
     fl.p.out = static_cast<__nv_bfloat16*>(dv16);
     fl.p.out_acc = dv_acc;
     fl.p.lse = nullptr;

@@ -17,13 +17,15 @@
 //     dV_J += P^T dO_I,  dK_J += dS^T Q_I           (tcgen05, A operand in TMEM)
 //     dQ_I  = dS K_J                                (tcgen05, dS^T tile in smem
 //                                                    read as an MN-major A)
-// The compute warps write P^T and dS^T as packed bf16 over the TMEM columns
-// of S^T and dP^T they have just read, so the dV/dK products read only dO and
-// Q from shared memory.  dQ_I is read from TMEM by a second warpgroup and
-// added into an fp32 accumulator (zeroed by the pre-pass): for d_h <= 64 the
-// tile is staged in shared memory and added with one TMA tensor reduce per 32
-// columns, for d_h = 128 with vector atomics.  A post-pass scales it by
-// 1/sqrt(d) and converts it.
+// d_h <= 64: P^T goes, as packed bf16, to spare TMEM columns (dV is a TS MMA)
+// and dS^T to one of two swizzled shared-memory tiles (dK and dQ are SS MMAs).
+// d_h = 128: TMEM has no spare columns, so P^T and dS^T are written over the
+// S^T and dP^T columns just read (dV and dK are TS MMAs) and dS^T also goes to
+// shared memory for dQ.  dQ_I is read from TMEM by a second warpgroup and
+// added into an fp32 accumulator (zeroed by the pre-pass) with one TMA tensor
+// reduce-add per 32 columns: staged in a tile of its own for d_h <= 64, in the
+// two halves of the dS^T tile (once its dQ product has read it) for
+// d_h = 128.  A post-pass scales it by 1/sqrt(d) and converts it.
 //
 // param_grad_kernel (K5): items (h_static, J), handed out in snake order.
 // For I = J..nI-1 the batch-summed dP^T(j, i) = sum_b V_b(j) . dO_b(i) is one
@@ -54,10 +56,11 @@ struct BwdSmem {
   // d_h = 128 leaves no free TMEM columns: dQ reuses the S^T/P^T columns once
   // the dV MMAs that read P^T have completed.
   static constexpr bool DQ_ALIAS = (256 + 3 * D > 512);
-  // d_h <= 64: P^T and dS^T go to shared memory (SS MMAs for dV, dK), so the
-  // S^T/dP^T columns are free as soon as the compute warps have loaded them
-  // and the next step's scores overlap this step's softmax.  d_h = 128 keeps
-  // P^T and dS^T in TMEM (TS MMAs): shared memory has no room for the tile.
+  // d_h <= 64: P^T goes to spare TMEM columns (TS MMA for dV) and dS^T to
+  // shared memory (SS MMAs for dK, dQ), so the S^T/dP^T columns are free as
+  // soon as the compute warps have loaded them and the next step's scores
+  // overlap this step's softmax.  d_h = 128 writes P^T and dS^T over the
+  // S^T/dP^T columns (TS MMAs for dV, dK); dS^T also goes to shared memory.
   static constexpr bool PS = !DQ_ALIAS;
   // Q_I, dO_I stages; d_h = 128 keeps two stages by dropping the alignment
   // slack (the dynamic shared base is checked at run time instead).
@@ -69,7 +72,7 @@ struct BwdSmem {
   static constexpr int OFF_DST = OFF_Q + QST * STAGE;
   // dQ staging for the tensor reduce-add (d_h <= 64): one [128 rows x 128 B]
   // chunk (32 fp32 columns), 128-byte swizzled, reused for each chunk of the
-  // row.  d_h = 128 adds with atomics.
+  // row.  d_h = 128 stages through the dS^T tile (below).
   static constexpr bool DQ_TMA = (D <= 64);
   // d_h = 128 has no room for a staging tile: dQ is staged through the dS^T
   // tile (its two 16 KB halves alternate) once the dQ MMA has read it.
@@ -995,18 +998,10 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <typename K>
-cudaError_t set_smem(K kern, int bytes, bool& done) {
-  if (done) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess) done = true;
-  return e;
-}
-
 template <int D>
 cudaError_t launch_dyn(const BwdLaunch& L, cudaStream_t s) {
-  static bool done = false;
-  cudaError_t e = set_smem(bwd_dynamic_kernel<D>, BwdSmem<D>::ALLOC, done);
+  cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(bwd_dynamic_kernel<D>),
+                                       BwdSmem<D>::ALLOC);
   if (e != cudaSuccess) return e;
   if (L.p.n_items == 0) return cudaSuccess;
   const int grid = L.p.n_items < L.num_sms ? L.p.n_items : L.num_sms;
@@ -1019,8 +1014,8 @@ cudaError_t launch_dyn(const BwdLaunch& L, cudaStream_t s) {
 
 template <int D>
 cudaError_t launch_pg(const ParamGradLaunch& L, cudaStream_t s) {
-  static bool done = false;
-  cudaError_t e = set_smem(param_grad_kernel<D>, PgSmem<D>::ALLOC, done);
+  cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(param_grad_kernel<D>),
+                                       PgSmem<D>::ALLOC);
   if (e != cudaSuccess) return e;
   if (L.p.n_items == 0) return cudaSuccess;
   const int grid = L.p.n_items < L.num_sms ? L.p.n_items : L.num_sms;

@@ -218,13 +218,9 @@ int elementwise_blocks(size_t n) {
 cudaError_t launch_static_prep(const StaticPrep& p, cudaStream_t s) {
   if (p.n_static == 0) return cudaSuccess;
   const size_t smem = (2 * (size_t)p.T + 8) * sizeof(float);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(static_prep_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(static_prep_kernel),
+                                       160 * 1024);
+  if (e != cudaSuccess) return e;
   trace_begin(s);
   static_prep_kernel<<<dim3(p.T / kPrepRows, p.n_static), 256, smem, s>>>(p);
   trace_end(s, "static_prep");
@@ -1357,13 +1353,8 @@ template <int D, bool TRANSPOSED>
 cudaError_t launch_fused(const FwdLaunch& L, cudaStream_t s) {
   using S = FwdSmem<D>;
   auto kern = hybrid_fwd_kernel<D, TRANSPOSED>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::ALLOC);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(kern), S::ALLOC);
+  if (e != cudaSuccess) return e;
   if (L.p.n_items == 0) return cudaSuccess;
   const int grid = L.p.n_items < L.num_sms ? L.p.n_items : L.num_sms;
   trace_begin(s);

@@ -162,17 +162,12 @@ size_t fit_smem_bytes(int T) { return (size_t)11 * T * sizeof(float); }
 
 cudaError_t launch_fit(const FitParams& p, cudaStream_t s) {
   const size_t smem = fit_smem_bytes(p.T);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(fit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(fit_kernel), 200 * 1024);
+  if (e != cudaSuccess) return e;
   trace_begin(s);
   fit_kernel<<<p.n_candidates, kFitThreads, smem, s>>>(p);
   trace_end(s, "fit");
-  cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   trace_begin(s);
   fit_select_kernel<<<1, 32, 0, s>>>(p);

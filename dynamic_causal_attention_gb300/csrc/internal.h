@@ -16,6 +16,13 @@ namespace saf {
 // records two CUDA events on the launch stream around the kernel.
 void trace_begin(cudaStream_t s);
 void trace_end(cudaStream_t s, const char* kernel);
+// Start counting launches for a new entry-point call.
+void launch_count_reset();
+
+// Raise `kernel`'s dynamic shared-memory limit to `bytes` on the current
+// device.  cudaFuncSetAttribute applies to the current device only, so this
+// is done once per (kernel, device); safe to call from several host threads.
+cudaError_t set_max_dynamic_smem(const void* kernel, int bytes);
 
 // ------------------------------------------------------------ calibration
 struct CalibLaunch {

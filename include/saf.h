@@ -158,8 +158,10 @@ SAF_API saf_status saf_hybrid_attn_bwd(const saf_attn_dims* dims,
  * file-scope device array of 4 MiB that every GPU which loads the library
  * holds until the process exits; a shape whose tables need more,
  * n_static * (4 T + 130) * 4 bytes plus at most 1.5 KiB of status word and
- * alignment, is rejected with SAF_ERR_UNSUPPORTED before anything is launched.  Nothing is allocated:
- * no cudaMalloc, no cudaFree, no allocating library routine.
+ * alignment, is rejected with SAF_ERR_UNSUPPORTED before anything is launched
+ * (15 frozen heads fit at T = 16384, 16 fit at T = 16256, 16 at T = 16384 do
+ * not).  Nothing is allocated: no cudaMalloc, no cudaFree, no allocating
+ * library routine.
  *
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
