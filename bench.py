@@ -27,6 +27,7 @@ time.  ``--impl reference`` times the float64 CPU oracle on this host instead
 from __future__ import annotations
 
 import argparse
+from dataclasses import replace
 import hashlib
 import json
 import os
@@ -85,6 +86,35 @@ def load_peaks():
     except Exception:
         return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0,
                 "source": "fallback"}
+
+
+def bf16_peak(peaks, region_s):
+    """The bf16 denominator for a kernel timed inside a region of region_s
+    seconds: the burst figure (a GEMM timed alone) for regions under a
+    second, the sustained one (a seconds-long GEMM loop under the power cap)
+    for longer ones.  Returns (TFLOP/s, description)."""
+    if region_s < 1.0:
+        return peaks["bf16_tflops"], (f"{peaks['source']} burst bf16 (timed region "
+                                      f"{region_s:.3f} s < 1 s)")
+    return peaks["bf16_tflops_sustained"], (f"{peaks['source']} sustained bf16 (timed region "
+                                            f"{region_s:.1f} s)")
+
+
+def roofline_of(cfg, kernels, region_s, peaks, sm_mhz=None):
+    """The roofline object of the dominant kernel of a traced step loop."""
+    dom = max(kernels, key=lambda n: kernels[n]["ms_total"]) if kernels else None
+    if not dom or not kernel_flops(cfg, dom):
+        return None
+    avg_ms = kernels[dom]["ms_total"] / kernels[dom]["launches"]
+    ach = kernel_flops(cfg, dom) / (avg_ms / 1e3) / 1e12
+    peak, kind = bf16_peak(peaks, region_s)
+    return {"kernel": dom, "bound": "tensor", "achieved": round(ach, 1), "peak": peak,
+            "unit": "TFLOP/s", "frac": round(ach / peak, 4), "peak_kind": kind,
+            "frac_of_burst_peak": round(ach / peaks["bf16_tflops"], 4),
+            "frac_of_sustained_peak": round(ach / peaks["bf16_tflops_sustained"], 4),
+            "sm_mhz_median": sm_mhz, "timed_region_s": round(region_s, 4),
+            "flop_per_launch": kernel_flops(cfg, dom),
+            "traffic": ncu_traffic(dom, cfg.name)}
 
 
 # Source files that define each timed kernel: a recorded DRAM-traffic figure
@@ -356,14 +386,17 @@ def e2e_steps(run, steps):
     return (time.perf_counter() - t0) * 1e3 / steps, h2d, d2h
 
 
-def calib_secondary(peaks):
+def calib_secondary(peaks, n_samples=None):
     """The calibration reduction at its full size: 64 sequences x 144 heads x
     T = 1024 fp32 probabilities (38.65 GB, generated on the device outside
-    timing), accumulated in 12 per-layer calls, then finalized."""
+    timing), accumulated in 12 per-layer calls, then finalized.  n_samples
+    replaces the 64 sequences (a smaller case for profiling)."""
     import torch
     from dynamic_causal_attention_gb300 import api
     from dynamic_causal_attention_gb300.synthetic import calib_probabilities
     c = CALIB_CONFIG
+    if n_samples:
+        c = replace(c, N=int(n_samples))
     A = calib_probabilities(c.N, c.num_heads, c.T, d_h=c.d_h, device="cuda")
     layers = [A[:, l * c.H:(l + 1) * c.H].contiguous() for l in range(c.L)]
     del A
@@ -409,7 +442,8 @@ def calib_secondary(peaks):
     alg_bytes = read_bytes + c.num_heads * c.T * c.T * 4
     acc_gbs = (read_bytes + state_bytes) / (acc_ms / n_acc * c.L / 1e3) / 1e9 if n_acc else None
     out = {
-        "workload": "calibration N=64, 144 heads, T=1024, k=36 (12 per-layer accumulate calls + finalize)",
+        "workload": f"calibration N={c.N}, {c.num_heads} heads, T={c.T}, k={k} (12 per-layer "
+                    "accumulate calls + finalize)",
         "ms": round(ms, 3),
         "algorithmic_bytes": alg_bytes,
         "GB_per_s": round(alg_bytes / (ms / 1e3) / 1e9, 1),
@@ -553,14 +587,14 @@ def gqa_secondary(peaks, steps=20, warmup=3):
     res = {"workload": f"124m with grouped K/V: B={B} H={H} H_kv={Hkv} T={T} d_h={d} "
                        f"static={list(cfg.static_heads)}",
            "ms_per_step": round(per, 4), "TFLOP_per_s": round(tf, 1),
-           "frac_of_bf16_peak": round(tf / peaks["bf16_tflops_sustained"], 3),
+           "frac_of_bf16_peak": round(tf / bf16_peak(peaks, per * steps / 1e3)[0], 3),
            "device_status": int(st)}
     del layer, q, k, v, do, out, lse, grads
     torch.cuda.empty_cache()
     return res
 
 
-def layer_secondary(cfg, steps, warmup, peaks):
+def layer_secondary(cfg, steps, warmup, peaks, roofline=False, cpu_s=0.0):
     run = LayerRun(cfg)
     ms, _, kernels = time_steps(run, steps, warmup, 1, trace=True)
     f, b = useful_flops(cfg)
@@ -570,9 +604,13 @@ def layer_secondary(cfg, steps, warmup, peaks):
                        f"static={list(cfg.static_heads)} grads={cfg.want_param_grads}",
            "ms_per_step": round(per, 4), "TFLOP_per_s": round(tf, 1),
            "tokens_per_s": round(cfg.B * cfg.T / (per / 1e3)),
-           "frac_of_bf16_peak": round(tf / peaks["bf16_tflops_sustained"], 3),
+           "frac_of_bf16_peak": round(tf / bf16_peak(peaks, ms / 1e3)[0], 3),
            "kernels_ms_per_step": {k: round(v["ms_total"] / steps, 4) for k, v in kernels.items()}}
+    if roofline:
+        res["roofline"] = roofline_of(cfg, kernels, ms / 1e3, peaks)
     del run
+    if cpu_s > 0:
+        res["cpu_baseline"] = cpu_baseline(cfg, budget_s=cpu_s)
     return res
 
 
@@ -712,6 +750,34 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------- main arm
+def sweep_secondary(peaks, args=None):
+    sweep = {}
+    for r in (0.0, 0.125, 0.25, 0.5, 1.0):
+        s = layer_secondary(sweep_config(r), 20, 3, peaks)
+        sweep[f"r={r:g}"] = {k: s[k] for k in ("ms_per_step", "TFLOP_per_s", "tokens_per_s",
+                                              "frac_of_bf16_peak")}
+    return sweep
+
+
+SECONDARY = {
+    "prefill": lambda peaks, args: prefill_secondary(peaks),
+    "static_ratio_sweep_124m": lambda peaks, args: sweep_secondary(peaks),
+    "gqa_124m": lambda peaks, args: gqa_secondary(peaks),
+    "sharp_mean": lambda peaks, args: sharp_secondary(peaks),
+    "calibration": lambda peaks, args: calib_secondary(peaks, args.calib_samples),
+    "1b": lambda peaks, args: layer_secondary(ATTN_CONFIGS["1b"], 30, 3, peaks, roofline=True,
+                                              cpu_s=0.0 if args.no_cpu else 8.0),
+}
+
+
+def run_only(args):
+    """One secondary workload alone (for profiling it): prints its JSON."""
+    import torch
+    torch.cuda.set_device(0)
+    peaks = load_peaks()
+    print(json.dumps({args.only: SECONDARY[args.only](peaks, args)}))
+
+
 def run_saf(args):
     import torch
     world, rank, local = dist_setup(args.gpus)
@@ -725,24 +791,16 @@ def run_saf(args):
     value, per = job_throughput(ms, args.steps, f + b, world)
     launches = run.launches
 
-    # dominant kernel of the timed region
+    # dominant kernel of the timed region, against the bf16 peak that fits
+    # the length of the timed region (burst under a second)
+    region_s = max_over_ranks(ms, world) / 1e3
+    roofline = roofline_of(cfg, kernels, region_s, peaks,
+                           clocks.get("sm_mhz") if clocks else None)
     total = sum(k["ms_total"] for k in kernels.values()) or 1.0
     for k in kernels.values():
         k["share"] = round(k["ms_total"] / total, 4)
         k["ms_total"] = round(k["ms_total"], 3)
-    dom = max(kernels, key=lambda n: kernels[n]["ms_total"]) if kernels else None
-    roofline = None
-    if dom and kernel_flops(cfg, dom):
-        avg_ms = kernels[dom]["ms_total"] / kernels[dom]["launches"]
-        ach = kernel_flops(cfg, dom) / (avg_ms / 1e3) / 1e12
-        peak = peaks["bf16_tflops_sustained"]
-        roofline = {"kernel": dom, "bound": "tensor", "achieved": round(ach, 1), "peak": peak,
-                    "unit": "TFLOP/s", "frac": round(ach / peak, 4),
-                    "peak_kind": f"{peaks['source']} sustained bf16 (kernel timed inside a "
-                                 f"seconds-long step loop)",
-                    "frac_of_burst_peak": round(ach / peaks["bf16_tflops"], 4),
-                    "flop_per_launch": kernel_flops(cfg, dom),
-                    "traffic": ncu_traffic(dom, cfg.name)}
+    peak, _ = bf16_peak(peaks, region_s)
 
     e2e = None
     if rank == 0:
@@ -757,19 +815,12 @@ def run_saf(args):
     del run
     torch.cuda.empty_cache()
 
+    # Secondary workloads, in the order they appear in the line: the long
+    # prefill table first, the calibration reduction and the 1B layer last,
+    # so that the end of the output holds them.
     secondary = {}
     if rank == 0 and not args.quick:
-        secondary["1b"] = layer_secondary(ATTN_CONFIGS["1b"], 30, 3, peaks)
-        secondary["calibration"] = calib_secondary(peaks)
-        secondary["sharp_mean"] = sharp_secondary(peaks)
-        secondary["gqa_124m"] = gqa_secondary(peaks)
-        sweep = {}
-        for r in (0.0, 0.125, 0.25, 0.5, 1.0):
-            s = layer_secondary(sweep_config(r), 20, 3, peaks)
-            sweep[f"r={r:g}"] = {k: s[k] for k in ("ms_per_step", "TFLOP_per_s", "tokens_per_s",
-                                                  "frac_of_bf16_peak")}
-        secondary["static_ratio_sweep_124m"] = sweep
-        secondary["prefill"] = prefill_secondary(peaks)
+        secondary = {name: SECONDARY[name](peaks, args) for name in SECONDARY}
     barrier(world)
     if rank != 0:
         return
@@ -797,7 +848,8 @@ def run_saf(args):
                   f"exceed the 129 MB L2",
         },
         "tokens_per_s": round(world * cfg.B * cfg.T / (per / 1e3)),
-        "frac_of_bf16_peak": round(value / world / peaks["bf16_tflops_sustained"], 4),
+        "frac_of_bf16_peak": round(value / world / peak, 4),
+        "frac_of_bf16_peak_sustained": round(value / world / peaks["bf16_tflops_sustained"], 4),
         "peaks": peaks,
         "roofline": roofline,
         "kernels": kernels,
@@ -819,11 +871,17 @@ def main():
     ap.add_argument("--workload", default="124m", choices=["124m", "1b"])
     ap.add_argument("--quick", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline")
+    ap.add_argument("--calib-samples", type=int, default=None,
+                    help="sequences of the calibration workload (default 64; fewer to profile)")
+    ap.add_argument("--only", choices=sorted(SECONDARY),
+                    help="run one secondary workload alone and print its figures")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.only:
+        run_only(args)
     else:
         run_saf(args)
 
