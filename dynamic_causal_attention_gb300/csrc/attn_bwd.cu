@@ -120,13 +120,31 @@ struct BItem {
   int b, kv, J, span, db, nsteps;  // span = nI - J query tiles per head
 };
 
+// Items come in groups of p.pairs_per_group (sequence, K/V head) pairs, the
+// groups one after another and, inside a group, key tile by key tile
+// (longest first).  The CTAs running at any time then add into the dQ rows of
+// a few groups only, a working set that stays in L2 (the TMA reduce-adds run
+// at about half speed once their target falls out of L2); across the whole
+// list the item lengths still cycle from long to short for the snake order.
 __device__ __forceinline__ BItem decode_bwd(const BwdParams& p, int it) {
   BItem r;
-  const int per = p.B * p.n_kv;
-  r.J = it / per;
-  const int rem = it - r.J * per;
-  r.b = rem / p.n_kv;
-  r.kv = p.kv_list[rem - r.b * p.n_kv];
+  const int n_pairs = p.B * p.n_kv;
+  const int G = p.pairs_per_group;
+  const int full = n_pairs / G;                          // complete groups
+  const int per_full = G * p.nI;
+  int pair;
+  if (it < full * per_full) {
+    const int g = it / per_full, w = it - g * per_full;
+    r.J = w / G;
+    pair = g * G + (w - r.J * G);
+  } else {
+    const int gs = n_pairs - full * G;                   // the last, smaller group
+    const int w = it - full * per_full;
+    r.J = w / gs;
+    pair = full * G + (w - r.J * gs);
+  }
+  r.b = pair / p.n_kv;
+  r.kv = p.kv_list[pair - r.b * p.n_kv];
   r.span = p.nI - r.J;
   r.db = p.dyn_begin[r.kv];
   r.nsteps = p.dyn_count[r.kv] * r.span;

@@ -82,6 +82,7 @@ struct BwdParams {
   int B, H, T, nI;
   int H_kv;                   // K/V heads (H: one per query head)
   int n_kv, n_items;          // K/V heads that serve a dynamic query head; items
+  int pairs_per_group;        // (sequence, K/V head) pairs per group of items
   float scale_log2;           // log2(e) / sqrt(d_h)
   float scale;                // 1 / sqrt(d_h)
   // The dynamic query heads grouped by K/V head: K/V head kv_list[i] serves
