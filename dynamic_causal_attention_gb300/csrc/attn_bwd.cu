@@ -74,36 +74,36 @@ struct BwdSmem {
   // chunk (32 fp32 columns), 128-byte swizzled, reused for each chunk of the
   // row.  d_h = 128 stages through the dS^T tile (below).
   static constexpr bool DQ_TMA = (D <= 64);
-  // d_h = 128 has no room for a staging tile: dQ is staged through the dS^T
-  // tile (its two 16 KB halves alternate) once the dQ MMA has read it.
-  static constexpr bool DQ_DST = !DQ_TMA;
   static constexpr int DQS_BYTES = DQ_TMA ? 128 * 32 * 4 : 0;
   // PS: two dS^T tiles, used by alternate steps
   static constexpr int DST_BUFS = PS ? 2 : 1;
   static constexpr int OFF_DQS = OFF_DST + DST_BUFS * SqTile::BYTES;
   static constexpr int OFF_BAR = OFF_DQS + DQS_BYTES;
-  static constexpr int NBAR = 2 + 2 * QST + 15;
+  static constexpr int NBAR = 2 + 2 * QST + 16;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int SLACK = (BYTES + 1024 <= 232448) ? 1024 : 0;
   static constexpr int ALLOC = BYTES + SLACK;
   static_assert(ALLOC <= 232448, "shared memory budget exceeded");
-  // TMEM columns.  S^T (fp32) at 0, dP^T at 128.  Each compute half (64 of
-  // the 128 query columns) writes its P^T, packed bf16, over the first 32
-  // columns of its own S^T half, and its dS^T over the first 32 of its dP^T
-  // half: P^T k-steps 0..3 sit at 0.., 4..7 at 64.. (dS^T likewise + 128).
+  // TMEM columns.  S^T (fp32) at 0, dP^T at 128, then dV and dK.
+  // d_h = 128: compute half hf reads query columns 32hf..32hf+31 and
+  // 64+32hf..64+32hf+31 of S^T and dP^T and writes its packed P^T (dS^T) over
+  // the first 32 of them, so P^T fills columns 0..63 and dS^T 128..191; the
+  // two 64-column halves of dQ then go to the columns both halves have read
+  // and nothing else uses until the next step: 64..127 and 192..255.
   static constexpr uint32_t T_S = 0, T_DP = 128;
   static constexpr uint32_t T_DV = 256, T_DK = 256 + D;
-  // d_h = 128: dQ reuses the dP^T/dS^T columns once dK has read dS^T, so
-  // that the next step's S^T (over P^T, free once dV has read it) need not
-  // wait for dQ to be drained.
-  static constexpr uint32_t T_DQ = DQ_ALIAS ? 128 : 256 + 2 * D;
+  static constexpr uint32_t T_DQ = 256 + 2 * D;                // d_h <= 64
+  static constexpr uint32_t T_DQ_LO = 64, T_DQ_HI = 192;       // d_h = 128
   // PS: P^T as packed bf16 (query columns 2c, 2c+1 in column T_PT + c), the
   // TMEM A operand of dV; 64 columns, free for d_h <= 64.
   static constexpr uint32_t T_PT = 256 + 3 * D;
   static_assert(!PS || T_PT + 64 <= 512, "P^T does not fit in TMEM");
+  // d_h = 128: packed column of the P^T / dS^T k-step kk (query columns
+  // 16kk..16kk+15): written by half (kk >> 1) & 1, in its first (kk < 4) or
+  // second group of 32 query columns.
   __device__ static __forceinline__ uint32_t a_col(int kk) {
-    return (uint32_t)((kk < 4) ? kk * 8 : 64 + (kk - 4) * 8);
+    return (uint32_t)(32 * ((kk >> 1) & 1) + 16 * (kk >> 2) + 8 * (kk & 1));
   }
 };
 
@@ -199,6 +199,9 @@ __global__ void __launch_bounds__(512, 1)
   uint64_t* dp_full = dqs_free + 1;      // DQ_ALIAS: dP^T ready (s_full: S^T ready)
   uint64_t* dv_done = dp_full + 1;       // DQ_ALIAS: the step's dV has read P^T
   uint64_t* dk_done = dv_done + 1;       // DQ_ALIAS: the step's dK has read dS^T
+  // DQ_ALIAS: dq_empty is dQ's low 64 columns taken into the dQ warps'
+  // registers, dqhi_empty its high 64 columns
+  uint64_t* dqhi_empty = dk_done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
   const WaitCtl wc{abort_flag, p.status};
@@ -222,6 +225,7 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(dp_full, 1);
     mbar_init(dv_done, 1);
     mbar_init(dk_done, 1);
+    mbar_init(dqhi_empty, 128);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -288,7 +292,6 @@ __global__ void __launch_bounds__(512, 1)
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);
       constexpr uint32_t id_acc = idesc_bf16(128, D, false, true);
-      constexpr uint32_t id_dq = idesc_bf16(128, D, true, true);
       uint32_t kvc = 0, qc = 0, pc = 0, dqc = 0, kdc = 0;
       // S^T and dP^T of the step whose Q/dO sit in stage `qs_of`.
       auto issue_s = [&](uint32_t qcount) {
@@ -354,17 +357,24 @@ __global__ void __launch_bounds__(512, 1)
           }
         }
       }
+      // d_h = 128: per step dQ (two N = 64 halves into the columns the
+      // compute left free), then dV and dK.  The next step's S^T goes out
+      // once dV has read P^T and the dQ warps hold dQ's low half, its dP^T
+      // once dK has read dS^T and they hold the high half; the reduce-adds
+      // of dQ then run while the next step computes.
+      constexpr uint32_t id_dq64 = idesc_bf16(128, 64, true, true);
       uint32_t dvc = 0, dkc = 0;
       for (int kr = 0, it = snake_item(0, blockIdx.x, gridDim.x); !L::PS && it < p.n_items;
            it = snake_item(++kr, blockIdx.x, gridDim.x)) {
         const BItem w = decode_bwd(p, it);
         mbar_wait(kv_full, kvc & 1, wc, kSiteBMmaKV);
         ++kvc;
-        // S^T over the previous step's P^T: its dV must have completed.
-        // dP^T over the previous step's dQ: it must have been drained.
+        // the previous step's dV / dK done and its dQ halves in the dQ warps
         if (dvc > 0) mbar_wait(dv_done, (dvc - 1) & 1, wc, kSiteBMmaTS);
+        if (dqc > 0) mbar_wait(dq_empty, (dqc - 1) & 1, wc, kSiteBMmaDQ);
         issue_st(qc);
-        mbar_wait(dq_empty, (dqc & 1) ^ 1, wc, kSiteBMmaDQ);
+        if (dkc > 0) mbar_wait(dk_done, (dkc - 1) & 1, wc, kSiteBMmaTS);
+        if (dqc > 0) mbar_wait(dqhi_empty, (dqc - 1) & 1, wc, kSiteBMmaDQ);
         issue_dpt(qc);
         for (int t = 0; t < w.nsteps; ++t) {
           const int qs = qc % L::QST;
@@ -373,6 +383,19 @@ __global__ void __launch_bounds__(512, 1)
           mbar_wait(p_full, pc & 1, wc, kSiteBMmaP);
           if (t == 0) mbar_wait(kd_empty, (kdc & 1) ^ 1, wc, kSiteBMmaKD);
           tc_fence_after();
+          // dQ_I = dS K_J: A the dS^T tile (MN-major), B the two 64-column
+          // halves of K_J
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tmem + L::T_DQ_LO, SqTile::mnmajor_desc(sDST, kk), G::mnmajor_desc(sK, kk),
+                        id_dq64, kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tmem + L::T_DQ_HI, SqTile::mnmajor_desc(sDST, kk),
+                        G::mnmajor_desc(sK + G::CHUNK_BYTES, kk), id_dq64, kk > 0);
+          mma_commit(p_empty);  // the dS^T tile has been read
+          mma_commit(dq_full);
+          ++dqc;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_bf16_ts(tmem + L::T_DV, tmem + L::T_S + L::a_col(kk), G::mnmajor_desc(sDO, kk),
@@ -388,20 +411,12 @@ __global__ void __launch_bounds__(512, 1)
           mma_commit(q_empty + qs);
           ++qc;
           ++pc;
-          // dQ first, so that its drain overlaps the next step's S^T
-          mbar_wait(dk_done, (dkc - 1) & 1, wc, kSiteBMmaTS);    // dS^T read: columns free
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ss(tmem + L::T_DQ, SqTile::mnmajor_desc(sDST, kk), G::mnmajor_desc(sK, kk),
-                        id_dq, kk > 0);
-          mma_commit(p_empty);
-          mma_commit(dq_full);
-          ++dqc;
           if (t + 1 < w.nsteps) {
-            mbar_wait(dv_done, (dvc - 1) & 1, wc, kSiteBMmaTS);  // P^T read: S^T columns free
+            mbar_wait(dv_done, (dvc - 1) & 1, wc, kSiteBMmaTS);      // P^T read
+            mbar_wait(dq_empty, (dqc - 1) & 1, wc, kSiteBMmaDQ);     // dQ low half held
             issue_st(qc);
-            mbar_wait(dq_empty, (dqc & 1) ^ 1, wc, kSiteBMmaDQ);  // dQ drained
+            mbar_wait(dk_done, (dkc - 1) & 1, wc, kSiteBMmaTS);      // dS^T read
+            mbar_wait(dqhi_empty, (dqc - 1) & 1, wc, kSiteBMmaDQ);   // dQ high half held
             issue_dpt(qc);
           }
         }
@@ -471,7 +486,6 @@ __global__ void __launch_bounds__(512, 1)
         mbar_wait(q_full + qs, (qc / L::QST) & 1, wc, kSiteBCmpQ);
         const float* nl_s = reinterpret_cast<const float*>(smem + L::OFF_Q + qs * L::STAGE +
                                                            2 * G::TILE_BYTES) + 64 * hf;
-        const float* nd_s = nl_s + 128;
         const uint32_t nl_a = smem_u32(nl_s);  // -lse2 at +0, -D at +512 bytes
         mbar_wait(s_full, sc & 1, wc, kSiteBCmpS);
         tc_fence_after();
@@ -544,14 +558,17 @@ __global__ void __launch_bounds__(512, 1)
         }
 #pragma unroll 1
         for (int c0 = 0; !L::PS && c0 < 64; c0 += 32) {
-          const int col = 64 * hf + c0;      // first query column of this chunk
+          // this half's query columns: 32hf..32hf+31, then 64+32hf..64+32hf+31
+          const int col = 32 * hf + 2 * c0;  // first query column of this chunk
+          const float* nlc = nl_s - 64 * hf + col;   // -lse2 of these columns
+          const float* ndc = nlc + 128;               // -D of these columns
           // P from S^T first (dP^T may still be on its way), then dS
           uint32_t sv[32], pk[16], dk[16];
           tmem_ld_x32(trow + L::T_S + col, sv);
           tmem_wait_ld(sv);
 #pragma unroll
           for (int k4 = 0; k4 < 32; k4 += 4) {
-            const float4 nl = *reinterpret_cast<const float4*>(nl_s + c0 + k4);
+            const float4 nl = *reinterpret_cast<const float4*>(nlc + k4);
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
               const int k = k4 + 2 * h2;
@@ -570,8 +587,9 @@ __global__ void __launch_bounds__(512, 1)
               pk[k >> 1] = pack_bf16x2(p0, p1);
             }
           }
-          // P^T over this half's S^T columns just read (TMEM A operand of dV)
-          tmem_st_x16(trow + L::T_S + 64 * hf + (c0 >> 1), pk);
+          // P^T over this half's first S^T columns, already read (TMEM A
+          // operand of dV)
+          tmem_st_x16(trow + L::T_S + 32 * hf + (c0 >> 1), pk);
           if (c0 == 0 && L::DQ_ALIAS) {
             mbar_wait(dp_full, sc & 1, wc, kSiteBCmpS);
             tc_fence_after();
@@ -581,7 +599,7 @@ __global__ void __launch_bounds__(512, 1)
           tmem_wait_ld(dv);
 #pragma unroll
           for (int k4 = 0; k4 < 32; k4 += 4) {
-            const float4 nd = *reinterpret_cast<const float4*>(nd_s + c0 + k4);
+            const float4 nd = *reinterpret_cast<const float4*>(ndc + k4);
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
               const int k = k4 + 2 * h2;
@@ -593,14 +611,14 @@ __global__ void __launch_bounds__(512, 1)
               dk[k >> 1] = pack_bf16x2_f2(g2);
             }
           }
-          // dS^T over this half's dP^T columns just read (A operand of dK),
-          // and into shared memory for dQ
-          tmem_st_x16(trow + L::T_DP + 64 * hf + (c0 >> 1), dk);
+          // dS^T over this half's first dP^T columns, already read (A
+          // operand of dK), and into shared memory for dQ
+          tmem_st_x16(trow + L::T_DP + 32 * hf + (c0 >> 1), dk);
           // the dS^T tile in shared memory is read by the previous step's dQ
           // (and, staged there, by its reductions)
           if (c0 == 0) {
             mbar_wait(p_empty, (pc & 1) ^ 1, wc, kSiteBCmpP);
-            if (L::DQ_DST) mbar_wait(dqs_free, (pc & 1) ^ 1, wc, kSiteBCmpP);
+            mbar_wait(dqs_free, (pc & 1) ^ 1, wc, kSiteBCmpP);
           }
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
@@ -702,30 +720,42 @@ __global__ void __launch_bounds__(512, 1)
             }
           }
         } else {
-          // d_h = 128: 32 columns at a time through the two halves of the
-          // dS^T tile (its dQ MMA has completed), one tensor reduce-add each
+          // d_h = 128: each 64-column half of dQ is loaded and its TMEM
+          // columns released (the next step's S^T or dP^T goes there), then
+          // staged 32 columns at a time through the two 16 KB halves of the
+          // dS^T tile (both dQ products have read it) and added with one
+          // tensor reduce-add per chunk.
           const int row = (w.b * H + hq) * T + I * 128;
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld_x32(tmem + lane_base + L::T_DQ + 32 * c, o);
-            tmem_wait_ld(o);
-            if (c == D / 32 - 1) {
-              tc_fence_before();
-              mbar_arrive(dq_empty);  // every dQ column is in registers
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t o[64];
+            {
+              uint32_t (&o0)[32] = *reinterpret_cast<uint32_t(*)[32]>(o);
+              uint32_t (&o1)[32] = *reinterpret_cast<uint32_t(*)[32]>(o + 32);
+              const uint32_t src = tmem + lane_base + (hh ? L::T_DQ_HI : L::T_DQ_LO);
+              tmem_ld_x32(src, o0);
+              tmem_ld_x32(src + 32, o1);
+              tmem_wait_ld(o0);
+              tmem_wait_ld(o1);
             }
-            const uint32_t slot = (uint32_t)(c & 1) * 16384u;
-            if (r == 0 && c >= 2) bulk_wait_group_read1();  // chunk c - 2 has left the slot
-            named_bar_sync(6, 128);
+            tc_fence_before();
+            mbar_arrive(hh ? dqhi_empty : dq_empty);  // this half is in registers
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-              st_shared_v4(sDST + slot + sw128_offset(r, (uint32_t)u), o[4 * u], o[4 * u + 1],
-                           o[4 * u + 2], o[4 * u + 3]);
-            fence_proxy_async_smem();
-            named_bar_sync(6, 128);
-            if (r == 0) {
-              tma_reduce_add_2d(&tm_dq, smem + L::OFF_DST + slot, c * 32, row);
-              bulk_commit_group();
+            for (int c = 0; c < 2; ++c) {
+              const int cc = 2 * hh + c;  // dQ columns 32cc .. 32cc + 31
+              const uint32_t slot = (uint32_t)(cc & 1) * 16384u;
+              if (r == 0 && cc >= 2) bulk_wait_group_read1();  // chunk cc - 2 has left the slot
+              named_bar_sync(6, 128);
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+                st_shared_v4(sDST + slot + sw128_offset(r, (uint32_t)u), o[32 * c + 4 * u],
+                             o[32 * c + 4 * u + 1], o[32 * c + 4 * u + 2], o[32 * c + 4 * u + 3]);
+              fence_proxy_async_smem();
+              named_bar_sync(6, 128);
+              if (r == 0) {
+                tma_reduce_add_2d(&tm_dq, smem + L::OFF_DST + slot, cc * 32, row);
+                bulk_commit_group();
+              }
             }
           }
           if (r == 0) {

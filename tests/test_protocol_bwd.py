@@ -12,9 +12,10 @@ than its count, and every role must finish.  A planted mistake (both dS^T
 tiles released through one barrier) must be caught.
 
 At d_h = 128 the kernel has no TMEM to spare: one warp issues every product,
-P^T and dS^T overwrite the S^T and dP^T columns, dQ accumulates over the dP^T
-columns and is staged through the dS^T tile.  The second model restates that
-path (QST = 2, dv_done / dk_done / dp_full / dqs_free).  Host logic only.
+P^T and dS^T overwrite half of the S^T and dP^T columns, dQ's two 64-column
+halves go over the other halves, and dQ is staged through the dS^T tile.  The
+second model restates that path (QST = 2, dv_done / dk_done / dp_full /
+dq_empty / dqhi_empty / dqs_free).  Host logic only.
 """
 
 import random
@@ -206,7 +207,8 @@ def make_barriers_128():
     add("s_full", 1); add("dp_full", 1)
     add("p_full", 2)
     add("p_empty", 1)
-    add("dq_full", 1); add("dq_empty", 1)
+    add("dq_full", 1)
+    add("dq_empty", 1); add("dqhi_empty", 1)   # dQ low / high half in the dQ warps' registers
     add("kd_full", 1); add("kd_empty", 2)
     add("dv_done", 1); add("dk_done", 1)
     add("dqs_free", 1)
@@ -226,12 +228,14 @@ def producer_128(items):
             qc += 1
 
 
-# TMEM regions: TS (S^T, then P^T), TDP (dP^T, then dS^T, then dQ), TDV, TDK;
-# the halves' columns of TS, TDP and of the shared dS^T tile DST are separate
-# regions for the compute warps (h0, h1).  Tags name the step u (global) or
-# the item i and step t.
+# TMEM regions.  Compute half h reads two groups of 32 query columns of S^T
+# (TSa{h}: the group it then overwrites with its packed P^T; TSb{h}: the other
+# one) and of dP^T (TDPa{h}, then dS^T; TDPb{h}).  dQ's low half goes over
+# TSb0 + TSb1, its high half over TDPb0 + TDPb1.  DST{h} are the halves'
+# columns of the shared dS^T tile, which also stages dQ for the reduce-adds.
+# Tags name the global step u.
 def both(region, tag):
-    return [(region + "h0", tag), (region + "h1", tag)]
+    return [(region + "0", tag), (region + "1", tag)]
 
 
 def issuer_128(items, skip_dq_drain=False):
@@ -239,12 +243,14 @@ def issuer_128(items, skip_dq_drain=False):
 
     def issue_st(q, i):
         yield ("wait", f"q_full{q % QST128}", q // QST128)
-        yield ("mma", [("KV", f"kv{i}"), (f"Q{q % QST128}", f"q{q}")], both("TS", f"S{q}"))
+        yield ("mma", [("KV", f"kv{i}"), (f"Q{q % QST128}", f"q{q}")],
+               both("TSa", f"S{q}") + both("TSb", f"S{q}"))
         yield ("commit", "s_full")
 
     def issue_dpt(q, i):
         yield ("wait", f"q_full{q % QST128}", q // QST128)
-        yield ("mma", [("KV", f"kv{i}"), (f"Q{q % QST128}", f"q{q}")], both("TDP", f"dP{q}"))
+        yield ("mma", [("KV", f"kv{i}"), (f"Q{q % QST128}", f"q{q}")],
+               both("TDPa", f"dP{q}") + both("TDPb", f"dP{q}"))
         yield ("commit", "dp_full")
 
     for i, n in enumerate(items):
@@ -252,8 +258,13 @@ def issuer_128(items, skip_dq_drain=False):
         kvc += 1
         if dvc > 0:
             yield ("wait", "dv_done", dvc - 1)
+        if dqc > 0 and not skip_dq_drain:
+            yield ("wait", "dq_empty", dqc - 1)
         yield from issue_st(qc, i)
-        yield ("wait", "dq_empty", dqc - 1)
+        if dkc > 0:
+            yield ("wait", "dk_done", dkc - 1)
+        if dqc > 0:
+            yield ("wait", "dqhi_empty", dqc - 1)
         yield from issue_dpt(qc, i)
         for t in range(n):
             qs = qc % QST128
@@ -261,30 +272,33 @@ def issuer_128(items, skip_dq_drain=False):
             yield ("wait", "p_full", pc)
             if t == 0:
                 yield ("wait", "kd_empty", kdc - 1)
+            yield ("mma", both("DST", f"dS{u}") + [("KV", f"kv{i}")],
+                   both("TSb", f"dQlo{u}"))                     # dQ, low half
+            yield ("mma", both("DST", f"dS{u}") + [("KV", f"kv{i}")],
+                   both("TDPb", f"dQhi{u}"))                    # dQ, high half
+            yield ("commit", "p_empty")
+            yield ("commit", "dq_full")
+            dqc += 1
             acc_v = [("TDV", f"dv{i}.{t - 1}")] if t > 0 else []
-            yield ("mma", both("TS", f"P{u}") + [(f"Q{qs}", f"q{u}")] + acc_v,
+            yield ("mma", both("TSa", f"P{u}") + [(f"Q{qs}", f"q{u}")] + acc_v,
                    [("TDV", f"dv{i}.{t}")])                     # dV
             yield ("commit", "dv_done")
             dvc += 1
             acc_k = [("TDK", f"dk{i}.{t - 1}")] if t > 0 else []
-            yield ("mma", both("TDP", f"dS{u}") + [(f"Q{qs}", f"q{u}")] + acc_k,
+            yield ("mma", both("TDPa", f"dS{u}") + [(f"Q{qs}", f"q{u}")] + acc_k,
                    [("TDK", f"dk{i}.{t}")])                     # dK
             yield ("commit", "dk_done")
             dkc += 1
             yield ("commit", f"q_empty{qs}")
             qc += 1
             pc += 1
-            yield ("wait", "dk_done", dkc - 1)
-            yield ("mma", both("DST", f"dS{u}") + [("KV", f"kv{i}")],
-                   both("TDP", f"dQ{u}"))                        # dQ over the dP^T columns
-            yield ("commit", "p_empty")
-            yield ("commit", "dq_full")
-            dqc += 1
             if t + 1 < n:
                 yield ("wait", "dv_done", dvc - 1)
-                yield from issue_st(qc, i)
                 if not skip_dq_drain:
                     yield ("wait", "dq_empty", dqc - 1)
+                yield from issue_st(qc, i)
+                yield ("wait", "dk_done", dkc - 1)
+                yield ("wait", "dqhi_empty", dqc - 1)
                 yield from issue_dpt(qc, i)
         yield ("commit", "kd_full")
         yield ("commit", "kv_empty")
@@ -293,21 +307,29 @@ def issuer_128(items, skip_dq_drain=False):
 
 def compute_128(hf, items):
     qc = sc = pc = kdc = 0
-    h = f"h{hf}"
+    h = f"{hf}"
     for i, n in enumerate(items):
         for _ in range(n):
             qs = qc % QST128
             u = qc
             yield ("wait", f"q_full{qs}", qc // QST128)
             yield ("read", f"Q{qs}", f"q{u}")           # -lse, -D of the stage
+            # first group of query columns (chunk 0), then the second
+            # (chunk 32); the packed P^T / dS^T of both go over the first
+            # group's columns, read in chunk 0
             yield ("wait", "s_full", sc)
-            yield ("read", "TS" + h, f"S{u}")
-            yield ("write", "TS" + h, f"P{u}")
+            yield ("read", "TSa" + h, f"S{u}")
+            yield ("write", "TSa" + h, f"P{u}")
             yield ("wait", "dp_full", sc)
-            yield ("read", "TDP" + h, f"dP{u}")
-            yield ("write", "TDP" + h, f"dS{u}")
+            yield ("read", "TDPa" + h, f"dP{u}")
+            yield ("write", "TDPa" + h, f"dS{u}")
             yield ("wait", "p_empty", pc - 1)
             yield ("wait", "dqs_free", pc - 1)
+            yield ("write", "DST" + h, f"dS{u}")
+            yield ("read", "TSb" + h, f"S{u}")
+            yield ("write", "TSa" + h, f"P{u}")
+            yield ("read", "TDPb" + h, f"dP{u}")
+            yield ("write", "TDPa" + h, f"dS{u}")
             yield ("write", "DST" + h, f"dS{u}")
             yield ("arrive", "p_full", 1)
             qc += 1
@@ -325,15 +347,16 @@ def dq_warps_128(items):
     for n in items:
         for _ in range(n):
             yield ("wait", "dq_full", dqc)
-            yield ("read", "TDPh0", f"dQ{u}")
-            yield ("read", "TDPh1", f"dQ{u}")
-            yield ("arrive", "dq_empty", 1)    # every dQ column in registers
-            # staged through the dS^T tile (its dQ product has completed), then
-            # read by the tensor reduce-adds
-            yield ("write", "DSTh0", f"dQs{u}")
-            yield ("write", "DSTh1", f"dQs{u}")
-            yield ("read", "DSTh0", f"dQs{u}")
-            yield ("read", "DSTh1", f"dQs{u}")
+            for half, region, bar in (("lo", "TSb", "dq_empty"), ("hi", "TDPb", "dqhi_empty")):
+                yield ("read", region + "0", f"dQ{half}{u}")
+                yield ("read", region + "1", f"dQ{half}{u}")
+                yield ("arrive", bar, 1)           # this half is in registers
+                # staged through the dS^T tile (both dQ products have read it),
+                # then read by the tensor reduce-adds
+                yield ("write", "DST0", f"dQs{half}{u}")
+                yield ("write", "DST1", f"dQs{half}{u}")
+                yield ("read", "DST0", f"dQs{half}{u}")
+                yield ("read", "DST1", f"dQs{half}{u}")
             yield ("arrive", "dqs_free", 1)
             dqc += 1
             u += 1
@@ -355,9 +378,9 @@ def test_backward_128_protocol_holds(seed):
 
 
 def test_planted_skipped_dq_drain_is_caught():
-    # The next step's dP^T issued without waiting for the dQ warps to drain
-    # the columns it overwrites: the later dq_empty wait then meets a barrier
-    # two phases on, or the phases of dq_empty run ahead of their waiter.
+    # The next step's S^T issued without waiting for the dQ warps to hold
+    # dQ's low half, whose columns it overwrites: a dQ read then finds S^T
+    # there, or the phases of dq_empty run ahead of their waiter.
     rng = random.Random(17)
     caught = 0
     for _ in range(200):
