@@ -48,6 +48,7 @@ EXPORTED = (
     "saf_trace_enable",
     "saf_trace_count",
     "saf_trace_get",
+    "saf_debug_forward_hold",
 )
 
 
@@ -120,6 +121,8 @@ _lib.saf_trace_count.argtypes = []
 _lib.saf_trace_count.restype = _i
 _lib.saf_trace_get.argtypes = [_i, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float)]
 _lib.saf_trace_get.restype = _i
+_lib.saf_debug_forward_hold.argtypes = [_i]
+_lib.saf_debug_forward_hold.restype = _i
 
 
 def lib():
@@ -144,6 +147,10 @@ def saf_trace_enable(enable: int) -> int:
 
 def saf_trace_count() -> int:
     return _lib.saf_trace_count()
+
+
+def saf_debug_forward_hold(hold: int) -> int:
+    return _lib.saf_debug_forward_hold(int(hold))
 
 
 def saf_trace_get(index: int):

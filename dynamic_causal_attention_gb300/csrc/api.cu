@@ -5,6 +5,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -58,6 +59,9 @@ void trace_end(cudaStream_t s, const char* kernel) {
 }
 
 void launch_count_reset() { g_launches = 0; }
+
+// Failure-path testing (saf_debug_forward_hold): read by every forward launch.
+static std::atomic<int> g_dbg_hold{0};
 
 cudaError_t set_max_dynamic_smem(const void* kernel, int bytes) {
   struct Done {
@@ -293,6 +297,7 @@ void fill_fwd_params(FwdParams& p, const saf_attn_dims& d, const HeadSplit& hs,
   p.mode = t.mode;
   p.shift = t.shift;
   p.status = t.status;
+  if (!transposed) p.hold_first_q = g_dbg_hold.load();
 }
 
 }  // namespace saf
@@ -314,6 +319,11 @@ const char* saf_status_string(saf_status s) {
 }
 
 int saf_last_launch_count(void) { return g_launches; }
+
+saf_status saf_debug_forward_hold(int hold) {
+  g_dbg_hold.store(hold != 0);
+  return SAF_OK;
+}
 
 saf_status saf_trace_enable(int enable) {
   g_trace.on = enable != 0;

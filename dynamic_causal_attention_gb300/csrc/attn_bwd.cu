@@ -79,7 +79,7 @@ struct BwdSmem {
   static constexpr int DST_BUFS = PS ? 2 : 1;
   static constexpr int OFF_DQS = OFF_DST + DST_BUFS * SqTile::BYTES;
   static constexpr int OFF_BAR = OFF_DQS + DQS_BYTES;
-  static constexpr int NBAR = 2 + 2 * QST + 16;
+  static constexpr int NBAR = 2 + 2 * QST + 18;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int SLACK = (BYTES + 1024 <= 232448) ? 1024 : 0;
@@ -202,6 +202,8 @@ __global__ void __launch_bounds__(512, 1)
   // DQ_ALIAS: dq_empty is dQ's low 64 columns taken into the dQ warps'
   // registers, dqhi_empty its high 64 columns
   uint64_t* dqhi_empty = dk_done + 1;
+  // per MMA-issuing warp (1, 3): all its products done, before TMEM is freed
+  uint64_t* mma_drained = dqhi_empty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
   const WaitCtl wc{abort_flag, p.status};
@@ -226,6 +228,8 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(dv_done, 1);
     mbar_init(dk_done, 1);
     mbar_init(dqhi_empty, 128);
+    mbar_init(mma_drained, 1);
+    mbar_init(mma_drained + 1, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -424,6 +428,10 @@ __global__ void __launch_bounds__(512, 1)
         mma_commit(kv_empty);
         ++kdc;
       }
+      // every product of this warp has completed before TMEM is freed (after
+      // an abort no later wait guarantees it)
+      mma_commit(mma_drained);
+      mbar_drain(mma_drained, 0);
     }
   } else if (warp == 3) {
     // ---------------------------------------------------------- dV/dK/dQ issuer (PS)
@@ -470,6 +478,8 @@ __global__ void __launch_bounds__(512, 1)
         mma_commit(kv_empty);  // the item's S^T/dP^T all completed before its last p_full
         ++kdc;
       }
+      mma_commit(mma_drained + 1);  // every product of this warp done before TMEM is freed
+      mbar_drain(mma_drained + 1, 0);
     }
   } else if (warp >= 4 && warp < 12) {
     // ---------------------------------------------------------- compute halves
@@ -795,7 +805,7 @@ struct PgSmem {
   static constexpr int OFF_SKW = OFF_AUX + 2 * AUX;
   static constexpr int OFF_CW = OFF_SKW + 8 * SKW;
   static constexpr int OFF_BAR = OFF_CW + 2 * CW;
-  static constexpr int NBAR = 2 * ST + 4 + 4;
+  static constexpr int NBAR = 2 * ST + 4 + 4 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int ALLOC = OFF_MISC + 16 + 1024;
   static_assert(ALLOC <= 232448, "shared memory budget exceeded");
@@ -820,6 +830,7 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* aux_empty = aux_full + 2;
   uint64_t* acc_full = aux_empty + 2;
   uint64_t* acc_empty = acc_full + 2;
+  uint64_t* mma_drained = acc_empty + 2;  // the issuer's products all done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
   const WaitCtl wc{abort_flag, p.status};
@@ -833,6 +844,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(acc_full + s, 1);
       mbar_init(acc_empty + s, 256);
     }
+    mbar_init(mma_drained, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -920,6 +932,10 @@ __global__ void __launch_bounds__(384, 1)
           ++cc;
         }
       }
+      // every product has completed before TMEM is freed (after an abort no
+      // later wait guarantees it)
+      mma_commit(mma_drained);
+      mbar_drain(mma_drained, 0);
     }
   } else if (warp >= 4) {
     // Warp (rg, hf): key rows r = 32 rg + lane of tile J, query columns

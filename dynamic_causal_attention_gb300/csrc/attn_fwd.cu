@@ -288,7 +288,7 @@ struct FwdSmem {
   static constexpr int AUX_SLOT = 2048;
   static constexpr int OFF_AUX = OFF_X + 3 * 2 * 128 * 4;
   static constexpr int OFF_BAR = OFF_AUX + AST * AUX_SLOT;
-  static constexpr int NBAR = 2 * QST + 2 * KST + 2 * VST + 3 * NBUF + 2 + 2 + 2 * AST;  // NBUF >= NBUF_T
+  static constexpr int NBAR = 2 * QST + 2 * KST + 2 * VST + 3 * NBUF + 2 + 2 + 2 * AST + 2;  // NBUF >= NBUF_T
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int ALLOC = BYTES + 1024;  // slack to align the base to 1024 B
@@ -479,6 +479,8 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* p_empty = o_empty + 1;       // SPLIT: P buffer's P V products done (two)
   uint64_t* aux_full = p_empty + 2;      // static tables landed (TMA -> compute)
   uint64_t* aux_empty = aux_full + L::AST;  // static tables read (every compute thread -> producer)
+  // per MMA-issuing warp (1, 3): all its products done, before TMEM is freed
+  uint64_t* mma_drained = aux_empty + L::AST;
   float* xmax = reinterpret_cast<float*>(smem + L::OFF_X);  // [2 parity][2 halves][128]
   float* xsum = xmax + 2 * 2 * 128;                         // [2 halves][128]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
@@ -500,6 +502,8 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(p_empty + 1, 1);
     for (int s = 0; s < L::AST; ++s) { mbar_init(aux_full + s, 1); mbar_init(aux_empty + s, 256); }
     mbar_init(o_full, SPLIT ? 2 : 1);
+    mbar_init(mma_drained, 1);
+    mbar_init(mma_drained + 1, 1);
     mbar_init(o_empty, 256);
     *abort_flag = 0;
     fence_barrier_init();
@@ -529,6 +533,7 @@ __global__ void __launch_bounds__(384, 1)
     if (lane == 0) {
       uint32_t qc = 0, kc = 0, vc = 0, ac = 0;
       uint32_t kn0 = 0, kn1 = 0;  // SPLIT: uses of each issuer's K ring
+      bool held_q = false;        // the first Q tile was withheld (testing)
       for (int kr = 0, it = snake_item(0, blockIdx.x, gridDim.x); it < p.n_items;
          it = snake_item(++kr, blockIdx.x, gridDim.x)) {
         const Item w = decode_item<TRANSPOSED>(p, it);
@@ -538,11 +543,17 @@ __global__ void __launch_bounds__(384, 1)
           if (kprod) {
             const int qs = qc % L::QST;
             mbar_wait(q_empty + qs, ((qc / L::QST) & 1) ^ 1, wc, kSiteProdQ);
+            // failure-path testing: CTA 0 withholds its first Q tile, so that
+            // the waits on it run out (it is then not drained either)
+            const bool hold = p.hold_first_q && blockIdx.x == 0 && qc == 0;
+            held_q |= hold;
             ++qc;
-            mbar_arrive_expect_tx(q_full + qs, G::TILE_BYTES);
-            for (int c = 0; c < G::NCHUNK; ++c)
-              tma_load_2d(smem + L::OFF_Q + qs * G::TILE_BYTES + c * G::CHUNK_BYTES, &tm_q,
-                          q_full + qs, c * G::CHUNK, row0 + w.X * 128);
+            if (!hold) {
+              mbar_arrive_expect_tx(q_full + qs, G::TILE_BYTES);
+              for (int c = 0; c < G::NCHUNK; ++c)
+                tma_load_2d(smem + L::OFF_Q + qs * G::TILE_BYTES + c * G::CHUNK_BYTES, &tm_q,
+                            q_full + qs, c * G::CHUNK, row0 + w.X * 128);
+            }
             for (int j = 0; j < w.nsteps; ++j) {
               int ks;
               uint32_t kpar;
@@ -620,9 +631,11 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
       }
-      // Drain: every copy issued must have landed before the CTA exits.
+      // Drain: every copy issued must have landed before the CTA exits (a
+      // withheld Q tile, use 0 of slot 0, was never issued).
       for (int s = 0; s < L::QST; ++s)
-        if (qc > (uint32_t)s) mbar_drain(q_full + s, ((qc - 1 - s) / L::QST) & 1);
+        if (qc > (uint32_t)s && !(held_q && s == 0 && (qc - 1) / L::QST == 0))
+          mbar_drain(q_full + s, ((qc - 1 - s) / L::QST) & 1);
       if (SPLIT) {
         for (int g = 0; g < 2; ++g) {
           const uint32_t n = g ? kn1 : kn0;
@@ -771,6 +784,10 @@ __global__ void __launch_bounds__(384, 1)
         mma_commit(o_full);  // (with no products pending this arrives at once)
         ++oc;
       }
+      // every product of this warp has completed before TMEM is freed (after
+      // an abort no later wait guarantees it)
+      mma_commit(mma_drained + g);
+      mbar_drain(mma_drained + g, 0);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- S issuer
@@ -818,6 +835,8 @@ __global__ void __launch_bounds__(384, 1)
         }
         sc = sc0 + w.nsteps;
       }
+      mma_commit(mma_drained);  // every product of this warp done before TMEM is freed
+      mbar_drain(mma_drained, 0);
     }
   } else if (warp == 3) {
     // ---------------------------------------------------------- P V issuer
@@ -901,6 +920,8 @@ __global__ void __launch_bounds__(384, 1)
         }
         sc = sc0 + w.nsteps;
       }
+      mma_commit(mma_drained + 1);  // every product of this warp done before TMEM is freed
+      mbar_drain(mma_drained + 1, 0);
     }
   } else if (warp >= 4) {
     // ---------------------------------------------------------- compute halves

@@ -32,6 +32,9 @@ struct FwdParams {
                               // added to with atomics (out is then unused)
   float* lse;                 // forward only (nullable)
   int* status;                // device status word
+  // Failure-path testing only (0 otherwise): CTA 0 withholds its first Q tile
+  // so that the waits on it run out and the CTA takes the abort path.
+  int hold_first_q;
 };
 
 // Sequences per static work item: the TMEM columns left for the O

@@ -297,6 +297,17 @@ SAF_API saf_status saf_trace_enable(int enable);
 SAF_API int saf_trace_count(void);
 SAF_API saf_status saf_trace_get(int index, const char** kernel, float* ms);
 
+/* Failure-path testing (off by default; the paper has no counterpart).  With
+ * hold != 0, the forward launches that follow on any host thread withhold the
+ * first Q tile of their first CTA, so that the kernel's bounded waits on it
+ * run out (after 2 s): that CTA records SAF_ERR_TIMEOUT and a site in the
+ * workspace's status word, abandons its remaining waits, lets its copies and
+ * tensor-core products finish, frees its tensor memory and returns; its
+ * outputs are then undefined and the next call on the context runs normally.
+ * hold = 0 restores normal operation.  Nothing faults, traps or hangs: the
+ * forward only takes its own abort path. */
+SAF_API saf_status saf_debug_forward_hold(int hold);
+
 #ifdef __cplusplus
 }  /* extern "C" */
 #endif
