@@ -29,6 +29,9 @@ namespace saf {
 namespace {
 
 constexpr int kBatch = 8;
+// 128-thread blocks: at the accumulate kernel's ~90 registers a thread, five
+// of them fit an SM (20 warps), against two of 256 threads (16 warps).
+constexpr int kAccThreads = 128;
 
 // Lower-triangle float4 units of a T x T matrix (T % 4 == 0): rows 4q..4q+3
 // each have q + 1 units; the group of rows 4q..4q+3 starts at unit 2 q (q+1).
@@ -50,11 +53,15 @@ __device__ __forceinline__ float4 masked(float4 v, int row, int col0) {
   return v;
 }
 
-// x log x with the limit 0 at x = 0.
-__device__ __forceinline__ float xlogx(float x) { return x > 0.f ? x * __logf(x) : 0.f; }
+// x log2 x with the limit 0 at x = 0: the argument is clamped to 1e-30 (for
+// x below it the term is under 1e-28, far below what the sums resolve), so
+// no branch is needed.  The entropy sums are kept in log2 units; the score
+// rows convert to nats once per row.
+constexpr float kLn2f = 0.6931471805599453f;
+__device__ __forceinline__ float xlog2x(float x) { return x * __log2f(fmaxf(x, 1e-30f)); }
 
 template <bool KL>
-__global__ void __launch_bounds__(256) calib_accumulate_kernel(CalibLaunch p) {
+__global__ void __launch_bounds__(kAccThreads) calib_accumulate_kernel(CalibLaunch p) {
   const int T = p.T;
   const uint32_t units_per_head = 2u * (uint32_t)(T / 4) * (uint32_t)(T / 4 + 1);
   const uint64_t total = (uint64_t)units_per_head * (uint64_t)p.head_count;
@@ -90,8 +97,10 @@ __global__ void __launch_bounds__(256) calib_accumulate_kernel(CalibLaunch p) {
           x[k] = masked(x[k], row, col0);
           mb.x += x[k].x; mb.y += x[k].y; mb.z += x[k].z; mb.w += x[k].w;
           if (KL) {
-            ent.x += xlogx(x[k].x); ent.y += xlogx(x[k].y);
-            ent.z += xlogx(x[k].z); ent.w += xlogx(x[k].w);
+            ent.x = fmaf(x[k].x, __log2f(fmaxf(x[k].x, 1e-30f)), ent.x);
+            ent.y = fmaf(x[k].y, __log2f(fmaxf(x[k].y, 1e-30f)), ent.y);
+            ent.z = fmaf(x[k].z, __log2f(fmaxf(x[k].z, 1e-30f)), ent.z);
+            ent.w = fmaf(x[k].w, __log2f(fmaxf(x[k].w, 1e-30f)), ent.w);
           }
         }
       mb.x *= inv_m; mb.y *= inv_m; mb.z *= inv_m; mb.w *= inv_m;
@@ -123,65 +132,85 @@ __global__ void __launch_bounds__(256) calib_accumulate_kernel(CalibLaunch p) {
   }
 }
 
-// KL score rows: sum_j (sum_n x log x - N A_hat log A_hat) over the lower
-// part of one row, in fp64 (sum_n KL(A_n,i || A_hat_i) = that difference,
+// Row kernels: one warp per (row, head), kRowsPerBlock rows per block, 16-byte
+// loads.  Each lane sums its terms in fp32; the lanes' sums are combined by a
+// fixed-order shuffle tree (deterministic) and the row's total leaves as one
+// double.  (Per-element fp64 additions would run on this GPU's few fp64
+// units and bound the kernels; fp32 partial sums of non-negative M2 terms, or
+// of the score's per-element terms, carry no cancellation at this length.)
+constexpr int kRowsPerBlock = 8;
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// KL score rows: sum_j (sum_n x log2 x - N A_hat log2 A_hat) over the lower
+// part of one row, times ln 2 (sum_n KL(A_n,i || A_hat_i) = that difference,
 // because sum_n A_n = N A_hat).
-__global__ void __launch_bounds__(128) calib_kl_rows_kernel(CalibFinalize p) {
-  const int row = blockIdx.x, h = blockIdx.y, T = p.T;
+__global__ void __launch_bounds__(32 * kRowsPerBlock) calib_kl_rows_kernel(CalibFinalize p) {
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5), h = blockIdx.y, T = p.T;
+  if (row >= T) return;  // a whole warp
   const size_t base = ((size_t)h * T + row) * (size_t)T;
   const float N = (float)p.N;
-  double acc = 0.0;
-  for (int c4 = threadIdx.x; c4 * 4 <= row; c4 += blockDim.x) {
+  float acc = 0.f;
+  for (int c4 = lane; c4 * 4 <= row; c4 += 32) {
     const int col0 = c4 * 4;
     const float4 mu = masked(*reinterpret_cast<const float4*>(p.mean + base + col0), row, col0);
     const float4 e = masked(*reinterpret_cast<const float4*>(p.ent + base + col0), row, col0);
-    // four terms in fp32, the running sum in fp64
-    acc += (double)(((e.x - N * xlogx(mu.x)) + (e.y - N * xlogx(mu.y))) +
-                    ((e.z - N * xlogx(mu.z)) + (e.w - N * xlogx(mu.w))));
+    acc += ((e.x - N * xlog2x(mu.x)) + (e.y - N * xlog2x(mu.y))) +
+           ((e.z - N * xlog2x(mu.z)) + (e.w - N * xlog2x(mu.w)));
   }
-  __shared__ double red[128];
-  red[threadIdx.x] = acc;
-  __syncthreads();
-  for (int s = 64; s > 0; s >>= 1) {
-    if (threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) p.row_partials[(size_t)h * T + row] = red[0];
+  acc = warp_sum(acc);
+  if (lane == 0) p.row_partials[(size_t)h * T + row] = (double)acc * (double)kLn2f;
 }
 
-// One block per (row, head): writes the full row of A_hat (zeros above the
-// diagonal) and the row's sum of M2 over its lower part, in fp64.
-__global__ void __launch_bounds__(128) calib_rows_kernel(CalibFinalize p) {
-  const int row = blockIdx.x, h = blockIdx.y, T = p.T;
+// Writes the full row of A_hat (zeros above the diagonal) and the row's sum
+// of M2 over its lower part.
+__global__ void __launch_bounds__(32 * kRowsPerBlock) calib_rows_kernel(CalibFinalize p) {
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5), h = blockIdx.y, T = p.T;
+  if (row >= T) return;  // a whole warp
   const size_t base = ((size_t)h * T + row) * (size_t)T;
-  double acc = 0.0;
-  for (int c4 = threadIdx.x; c4 < T / 4; c4 += blockDim.x) {
+  float acc = 0.f;
+  for (int c4 = lane; c4 < T / 4; c4 += 32) {
     const int col0 = c4 * 4;
     float4 mu = make_float4(0.f, 0.f, 0.f, 0.f);
     if (col0 <= row) {
       mu = masked(*reinterpret_cast<const float4*>(p.mean + base + col0), row, col0);
       const float4 q = masked(*reinterpret_cast<const float4*>(p.m2 + base + col0), row, col0);
-      acc += (double)((q.x + q.y) + (q.z + q.w));
+      acc += (q.x + q.y) + (q.z + q.w);
     }
     if (p.A_hat) __stcs(reinterpret_cast<float4*>(p.A_hat + base + col0), mu);
   }
-  // fixed-order block reduction
-  __shared__ double red[128];
-  red[threadIdx.x] = acc;
-  __syncthreads();
-  for (int s = 64; s > 0; s >>= 1) {
-    if (threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) p.row_partials[(size_t)h * T + row] = red[0];
+  acc = warp_sum(acc);
+  if (lane == 0) p.row_partials[(size_t)h * T + row] = (double)acc;
+}
+
+// Per head: the sum of its T row totals (fp64, one warp per head, fixed
+// order), divided by `denom`.
+__global__ void __launch_bounds__(256) calib_head_sums_kernel(CalibFinalize p, double denom) {
+  const int lane = threadIdx.x & 31;
+  const int h = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (h >= p.num_heads) return;
+  double acc = 0.0;
+  for (int r = lane; r < p.T; r += 32) acc += p.row_partials[(size_t)h * p.T + r];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) p.s_var[h] = (float)(acc / denom);
 }
 
 // Sharp-mean pattern: one warp per (row, head) applies a causal softmax to
-// the row of the running mean of the accumulated logits, in three passes
-// over the row (16-byte loads; the row stays in L1 between passes): the
-// maximum, the sum of exponentials (fp32 per 4 columns, fp64 across them and
-// across the warp, in a fixed order), then the normalised row with exact
-// zeros above the diagonal.
+// the row of the running mean of the accumulated logits and writes the
+// normalised row with exact zeros above the diagonal.  Rows of up to
+// 128 * NC columns are held in registers (NC float4 per lane): one read of
+// the row, one exponential per entry, fp32 lane sums and a fixed-order
+// shuffle tree.  Longer rows take three passes over the row (the row stays
+// in L1 between them): the maximum, the sum of exponentials (fp32 per 4
+// columns, fp64 across them and across the warp, in a fixed order), then the
+// normalised row.
 constexpr int kSharpRows = 8;  // rows (warps) per block
 
 __device__ __forceinline__ float4 causal_row4(const float4* src, int c4, int row) {
@@ -191,6 +220,42 @@ __device__ __forceinline__ float4 causal_row4(const float4* src, int c4, int row
   if (c + 2 > row) a.z = -INFINITY;
   if (c + 3 > row) a.w = -INFINITY;
   return a;
+}
+
+template <int NC>
+__global__ void __launch_bounds__(32 * kSharpRows) calib_sharp_rows_reg_kernel(
+    const float* __restrict__ mean, int T, float* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kSharpRows + (threadIdx.x >> 5), h = blockIdx.y;
+  if (row >= T) return;  // a whole warp
+  const size_t base = ((size_t)h * T + row) * (size_t)T;
+  const float4* src = reinterpret_cast<const float4*>(mean + base);
+  const int n4 = T / 4, last4 = row / 4;
+  float4 a[NC];
+  float mx = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < NC; ++j) {
+    const int c4 = lane + 32 * j;
+    a[j] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    if (c4 <= last4) a[j] = causal_row4(src, c4, row);
+    mx = fmaxf(mx, fmaxf(fmaxf(a[j].x, a[j].y), fmaxf(a[j].z, a[j].w)));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  // column 0 is in every row, so mx is finite; exp(-inf - mx) is an exact 0
+  float sum = 0.f;
+#pragma unroll
+  for (int j = 0; j < NC; ++j) {
+    a[j] = make_float4(expf(a[j].x - mx), expf(a[j].y - mx), expf(a[j].z - mx), expf(a[j].w - mx));
+    sum += (a[j].x + a[j].y) + (a[j].z + a[j].w);
+  }
+  const float inv = 1.0f / warp_sum(sum);
+  float4* dst = reinterpret_cast<float4*>(out + base);
+#pragma unroll
+  for (int j = 0; j < NC; ++j) {
+    const int c4 = lane + 32 * j;
+    if (c4 < n4) __stcs(dst + c4, make_float4(a[j].x * inv, a[j].y * inv, a[j].z * inv, a[j].w * inv));
+  }
 }
 
 __global__ void __launch_bounds__(32 * kSharpRows) calib_sharp_rows_kernel(
@@ -228,24 +293,13 @@ __global__ void __launch_bounds__(32 * kSharpRows) calib_sharp_rows_kernel(
   }
 }
 
-// One block: s_var per head (one warp per head, fixed-order sums) and the
-// exact top-k by rank over the unique 64-bit keys (bits(s_var) << 32 | index).
+// One block: the exact top-k of the per-head scores by rank over the unique
+// 64-bit keys (bits(score) << 32 | index).
 constexpr int kMaxCalibHeads = 8192;
 
-__global__ void __launch_bounds__(1024) calib_select_kernel(CalibFinalize p, double denom) {
+__global__ void __launch_bounds__(1024) calib_select_kernel(CalibFinalize p) {
   __shared__ float sv[kMaxCalibHeads];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-  for (int h = warp; h < p.num_heads; h += nwarps) {
-    double acc = 0.0;
-    for (int r = lane; r < p.T; r += 32) acc += p.row_partials[(size_t)h * p.T + r];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) {
-      const float v = (float)(acc / denom);
-      sv[h] = v;
-      p.s_var[h] = v;
-    }
-  }
+  for (int h = threadIdx.x; h < p.num_heads; h += blockDim.x) sv[h] = p.s_var[h];
   __syncthreads();
   for (int h = threadIdx.x; h < p.num_heads; h += blockDim.x) {
     const uint64_t kh = ((uint64_t)__float_as_uint(sv[h]) << 32) | (uint32_t)h;
@@ -262,49 +316,65 @@ __global__ void __launch_bounds__(1024) calib_select_kernel(CalibFinalize p, dou
 
 cudaError_t launch_calib_accumulate(const CalibLaunch& p, cudaStream_t s) {
   const uint64_t units = 2ull * (uint64_t)(p.T / 4) * (uint64_t)(p.T / 4 + 1) * (uint64_t)p.head_count;
-  const uint64_t want = (units + 255) / 256;
+  const uint64_t want = (units + kAccThreads - 1) / kAccThreads;
   const int blocks = (int)(want < (1u << 30) ? want : (1u << 30));
   trace_begin(s);
   if (p.ent)
-    calib_accumulate_kernel<true><<<blocks, 256, 0, s>>>(p);
+    calib_accumulate_kernel<true><<<blocks, kAccThreads, 0, s>>>(p);
   else
-    calib_accumulate_kernel<false><<<blocks, 256, 0, s>>>(p);
+    calib_accumulate_kernel<false><<<blocks, kAccThreads, 0, s>>>(p);
   trace_end(s, "calib_accumulate");
+  return cudaGetLastError();
+}
+
+cudaError_t launch_head_sums_and_select(const CalibFinalize& p, double denom, cudaStream_t s) {
+  trace_begin(s);
+  calib_head_sums_kernel<<<(p.num_heads + 7) / 8, 256, 0, s>>>(p, denom);
+  trace_end(s, "calib_head_sums");
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || p.k == 0) return e;
+  trace_begin(s);
+  calib_select_kernel<<<1, 1024, 0, s>>>(p);
+  trace_end(s, "calib_select");
   return cudaGetLastError();
 }
 
 cudaError_t launch_calib_finalize(const CalibFinalize& p, cudaStream_t s) {
   if (p.num_heads > kMaxCalibHeads) return cudaErrorInvalidValue;
   trace_begin(s);
-  calib_rows_kernel<<<dim3(p.T, p.num_heads), 128, 0, s>>>(p);
+  calib_rows_kernel<<<dim3((p.T + kRowsPerBlock - 1) / kRowsPerBlock, p.num_heads),
+                      32 * kRowsPerBlock, 0, s>>>(p);
   trace_end(s, "calib_rows");
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  trace_begin(s);
-  calib_select_kernel<<<1, 1024, 0, s>>>(p, (double)(p.N - 1) * (double)p.T * (double)p.T);
-  trace_end(s, "calib_select");
-  return cudaGetLastError();
+  return launch_head_sums_and_select(p, (double)(p.N - 1) * (double)p.T * (double)p.T, s);
 }
 
 cudaError_t launch_calib_finalize_kl(const CalibFinalize& p, cudaStream_t s) {
   if (p.num_heads > kMaxCalibHeads || p.ent == nullptr) return cudaErrorInvalidValue;
   trace_begin(s);
-  calib_kl_rows_kernel<<<dim3(p.T, p.num_heads), 128, 0, s>>>(p);
+  calib_kl_rows_kernel<<<dim3((p.T + kRowsPerBlock - 1) / kRowsPerBlock, p.num_heads),
+                         32 * kRowsPerBlock, 0, s>>>(p);
   trace_end(s, "calib_kl_rows");
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  trace_begin(s);
-  calib_select_kernel<<<1, 1024, 0, s>>>(p, (double)p.N * (double)p.T);
-  trace_end(s, "calib_select");
-  return cudaGetLastError();
+  return launch_head_sums_and_select(p, (double)p.N * (double)p.T, s);
 }
 
 cudaError_t launch_calib_sharp(const float* mean, int num_heads, int T, float* out,
                                cudaStream_t s) {
-  trace_begin(s);
   if (T % 4 != 0) return cudaErrorInvalidValue;
-  calib_sharp_rows_kernel<<<dim3((T + kSharpRows - 1) / kSharpRows, num_heads), 32 * kSharpRows, 0,
-                            s>>>(mean, T, out);
+  trace_begin(s);
+  const dim3 grid((T + kSharpRows - 1) / kSharpRows, num_heads);
+  const int n4 = T / 4;
+  if (n4 <= 32 * 2)
+    calib_sharp_rows_reg_kernel<2><<<grid, 32 * kSharpRows, 0, s>>>(mean, T, out);
+  else if (n4 <= 32 * 4)
+    calib_sharp_rows_reg_kernel<4><<<grid, 32 * kSharpRows, 0, s>>>(mean, T, out);
+  else if (n4 <= 32 * 8)
+    calib_sharp_rows_reg_kernel<8><<<grid, 32 * kSharpRows, 0, s>>>(mean, T, out);
+  else
+    calib_sharp_rows_kernel<<<grid, 32 * kSharpRows, 0, s>>>(mean, T, out);
   trace_end(s, "calib_sharp_rows");
   return cudaGetLastError();
 }

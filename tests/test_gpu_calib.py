@@ -180,9 +180,11 @@ def test_forward_kl_selector_matches_oracle(api):
     cal.close()
 
 
-@pytest.mark.parametrize("N,nh,T", [(7, 5, 96), (3, 2, 1028), (2, 1, 4100)])
+@pytest.mark.parametrize("N,nh,T", [(7, 5, 96), (4, 3, 500), (2, 2, 1024), (3, 2, 1028),
+                                     (2, 1, 4100)])
 def test_sharp_mean_pattern_matches_oracle(api, N, nh, T):
-    # T = 1028 and 4100: rows longer than one 4-column unit per thread
+    # T up to 1024: rows held in registers (T = 500 with a partial last block
+    # of rows); T = 1028 and 4100: rows longer than that, three passes
     L = calib_probabilities(N, nh, T, d_h=16, seed=33, want_logits=True)
     cal = api.Calibration(nh, T)
     cal.accumulate(L[:N // 2].cuda())
