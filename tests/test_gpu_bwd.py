@@ -104,6 +104,31 @@ def test_many_short_odd_items(api, d_h, static, grads):
             f"short d{d_h}", grads)
 
 
+@pytest.mark.parametrize("d_h", [64, 128])
+def test_backward_run_to_run(api, d_h):
+    # Two backward passes on the same inputs.  dK and dV accumulate in tensor
+    # memory in a fixed order (and the frozen heads' dV comes from the
+    # transposed forward engine, which has no atomics): bit for bit equal.
+    # dQ is summed over key tiles by fp32 reduce-adds in whatever order the
+    # CTAs arrive, and dalpha/drho by fp32 atomics: the two runs may differ
+    # by the rounding of a reordered fp32 sum, which after the bf16
+    # conversion of dQ is at most one bf16 unit in the last place.
+    cfg = AttnConfig("rep", B=16, H=12, T=640, d_h=d_h, dtype="bf16",
+                     static_heads=(1, 4, 6, 9, 10, 11))
+    inp = attn_inputs(cfg, seed=49)
+    a = gpu_fwd_bwd(api, inp, cfg.head_is_static, True)
+    b = gpu_fwd_bwd(api, inp, cfg.head_is_static, True)
+    np.testing.assert_array_equal(a[1], b[1])   # dK
+    np.testing.assert_array_equal(a[2], b[2])   # dV
+    dq1, dq2 = a[0], b[0]
+    one_ulp = 2.0 ** -7 * np.maximum(np.abs(dq1), np.abs(dq2))
+    spread = np.abs(dq1 - dq2)
+    assert np.all(spread <= one_ulp + 1e-6 * np.abs(dq1).max()), spread.max()
+    for name, x, y in (("dalpha", a[3], b[3]), ("drho", a[4], b[4])):
+        st = np.asarray(cfg.head_is_static, bool)
+        assert np.abs(x[st] - y[st]).max() <= 1e-5 * np.abs(x[st]).max(), name
+
+
 def test_identity_pattern_backward(api):
     B, H, T, d = 2, 1, 256, 64
     cfg = AttnConfig("id", B=B, H=H, T=T, d_h=d, dtype="bf16", static_heads=(0,))
