@@ -295,12 +295,31 @@ class LayerRun:
         return sum(t.numel() * t.element_size() for t in (self.q, self.k, self.v, self.do))
 
 
-def time_steps(run, steps, warmup, world, trace=False, sampler=None):
+def time_steps(run, steps, warmup, world, trace=False, sampler=None, graph=False):
+    """Time `steps` steps on the device (CUDA events on the launching stream,
+    synchronised on both sides).  With `graph`, one step (the same C-ABI
+    calls on the same resident buffers) is captured once in a CUDA graph
+    after the warm-up and the timed loop replays it, as a training loop that
+    keeps its buffers would; run.launches then counts the captured step's
+    launches once per replay."""
     import torch
     from dynamic_causal_attention_gb300 import _binding as B
     for _ in range(warmup):
         run.step()
     torch.cuda.synchronize()
+    g = None
+    if graph:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            before = run.launches
+            with torch.cuda.graph(g, stream=side):
+                run.step()
+            per_step = run.launches - before
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
     barrier(world)
     if sampler:
         sampler.start()
@@ -313,8 +332,13 @@ def time_steps(run, steps, warmup, world, trace=False, sampler=None):
     torch.cuda.synchronize()
     barrier(world)
     e0.record(stream)
-    for _ in range(steps):
-        run.step()
+    if g is not None:
+        for _ in range(steps):
+            g.replay()
+        run.launches = per_step * steps
+    else:
+        for _ in range(steps):
+            run.step()
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -596,13 +620,14 @@ def gqa_secondary(peaks, steps=20, warmup=3):
 
 def layer_secondary(cfg, steps, warmup, peaks, roofline=False, cpu_s=0.0):
     run = LayerRun(cfg)
-    ms, _, _ = time_steps(run, steps, warmup, 1, trace=False)
+    ms, _, _ = time_steps(run, steps, warmup, 1, trace=False, graph=True)
     ms_traced, _, kernels = time_steps(run, steps, 3, 1, trace=True)
     f, b = useful_flops(cfg)
     per = ms / steps
     tf = (f + b) / (per / 1e3) / 1e12
     res = {"workload": f"{cfg.name}: B={cfg.B} H={cfg.H} T={cfg.T} d_h={cfg.d_h} "
                        f"static={list(cfg.static_heads)} grads={cfg.want_param_grads}",
+           "launch": "one step captured in a CUDA graph, replayed",
            "ms_per_step": round(per, 4), "TFLOP_per_s": round(tf, 1),
            "tokens_per_s": round(cfg.B * cfg.T / (per / 1e3)),
            "frac_of_bf16_peak": round(tf / bf16_peak(peaks, ms / 1e3)[0], 3),
@@ -634,18 +659,29 @@ def prefill_secondary(peaks):
         lse = torch.empty((B, H, T), dtype=torch.float32, device="cuda")
         for _ in range(2):
             layer.forward(q, k, v, alpha, rho, out=out, lse=lse)
+        torch.cuda.synchronize()
+        # one forward (the frozen-head pre-pass and the fused kernel) captured
+        # in a CUDA graph and replayed
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                layer.forward(q, k, v, alpha, rho, out=out, lse=lse)
+        torch.cuda.synchronize()
+        g.replay()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         e0.record()
         for _ in range(reps):
-            layer.forward(q, k, v, alpha, rho, out=out, lse=lse)
+            g.replay()
         e1.record()
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / reps
         u = d * T * T / 2.0
         hs = int(mask.sum())
         flop = B * (4 * u * (H - hs) + 2 * u * hs)
-        del q, k, v, out, lse, layer
+        del q, k, v, out, lse, layer, g
         torch.cuda.empty_cache()
         return ms, flop / (ms / 1e3) / 1e12
 
@@ -666,7 +702,8 @@ def prefill_secondary(peaks):
         base = ms if r == 0.0 else base
         b1[f"r={r:g}"] = {"ms": round(ms, 4), "speedup_vs_r0": round(base / ms, 3)}
     res[f"batch1_T={P['batch1_T']}"] = b1
-    return {"workload": f"causal prefill, forward only, B={P['B']} H={H} d_h={d}", "sweep": res}
+    return {"workload": f"causal prefill, forward only, B={P['B']} H={H} d_h={d}",
+            "launch": "one forward captured in a CUDA graph, replayed", "sweep": res}
 
 
 # ---------------------------------------------------------------- oracle leg
@@ -786,11 +823,12 @@ def run_saf(args):
     cfg = ATTN_CONFIGS[args.workload]
     run = LayerRun(cfg)
     sampler = ClockSampler(local) if rank == 0 else None
-    # The headline loop runs without the kernel trace (its two events per
-    # launch cost about 4% of a 124M step); a second timed loop of the same
-    # K steps, traced, gives each kernel's time for the roofline.
+    # The headline loop replays one step captured in a CUDA graph, without
+    # the kernel trace (its two events per launch cost about 4% of a 124M
+    # step); a second timed loop of the same K steps, eager and traced, gives
+    # each kernel's time for the roofline.
     ms, clocks, _ = time_steps(run, args.steps, args.warmup, world, trace=False,
-                               sampler=sampler)
+                               sampler=sampler, graph=True)
     f, b = useful_flops(cfg)
     value, per = job_throughput(ms, args.steps, f + b, world)
     launches = run.launches
@@ -851,6 +889,7 @@ def run_saf(args):
             "parallelism": f"replicas x{world}",
             "l2": f"no flush: the step's bf16 Q/K/V/dO inputs ({in_bytes / 2**20:.0f} MiB) "
                   f"exceed the 129 MB L2",
+            "launch": "one step captured in a CUDA graph, replayed K times",
         },
         "tokens_per_s": round(world * cfg.B * cfg.T / (per / 1e3)),
         "frac_of_bf16_peak": round(value / world / peak, 4),
