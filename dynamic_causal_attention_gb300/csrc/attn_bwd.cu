@@ -33,9 +33,9 @@
 // half each) form dl = P(i,j) (dP - sum_b D_b(i)) with P(i,j) rebuilt from the
 // static tables and keep the row sums (alpha) in registers.  For the diagonal
 // sums (rho) each warp writes its 32 x 32 block of dl to shared memory by
-// diagonal, so that lane q adds up diagonals q and q + 32 with vector loads;
-// the per-warp sums of a tile are combined in a fixed order and added to
-// global with one atomic per distance.
+// diagonal, so that lane q adds up diagonals q and q + 32 with vector loads,
+// and adds its three distance sums of the tile to global with atomics (no
+// barrier across the warps per tile).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -799,12 +799,10 @@ struct PgSmem {
   // e = k - rr + 32 (k column, rr row of the block), 36 floats a row.
   static constexpr int SKW_ROW = 36;
   static constexpr int SKW = 64 * SKW_ROW * 4;
-  static constexpr int CW = 8 * 96 * 4;                // per-warp diagonal sums, x2
   static constexpr int OFF_ST = 0;
   static constexpr int OFF_AUX = OFF_ST + ST * STAGE;
   static constexpr int OFF_SKW = OFF_AUX + 2 * AUX;
-  static constexpr int OFF_CW = OFF_SKW + 8 * SKW;
-  static constexpr int OFF_BAR = OFF_CW + 2 * CW;
+  static constexpr int OFF_BAR = OFF_SKW + 8 * SKW;
   static constexpr int NBAR = 2 * ST + 4 + 4 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int ALLOC = OFF_MISC + 16 + 1024;
@@ -840,7 +838,7 @@ __global__ void __launch_bounds__(384, 1)
     for (int s = 0; s < L::ST; ++s) { mbar_init(st_full + s, 1); mbar_init(st_empty + s, 1); }
     for (int s = 0; s < 2; ++s) {
       mbar_init(aux_full + s, 1);
-      mbar_init(aux_empty + s, 1);
+      mbar_init(aux_empty + s, 8);  // every compute warp has read the slot
       mbar_init(acc_full + s, 1);
       mbar_init(acc_empty + s, 256);
     }
@@ -1025,25 +1023,22 @@ __global__ void __launch_bounds__(384, 1)
         tc_fence_before();
         mbar_arrive(acc_empty + ab);
         ++cc;
-        float* cw = reinterpret_cast<float*>(smem + L::OFF_CW + (ac & 1) * L::CW);
-        cw[w8 * 96 + lane] = dg0;
-        cw[w8 * 96 + 32 + lane] = dg1;
-        cw[w8 * 96 + 64 + lane] = dg2;
-        named_bar_sync(1, 256);
-        if (threadIdx.x == 128) mbar_arrive(aux_empty + as);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(aux_empty + as);  // this warp has read the table slot
         ++ac;
-        // tile diagonal t = c - r + 127, global distance (I - J) * 128 - 127 + t;
-        // the per-warp sums are added in a fixed order
-        const int t = threadIdx.x - 128;
-        if (t < 255) {
-          float vs = 0.f;
+        // This warp's diagonal sums go straight to drho (no step-wide barrier
+        // to combine the eight warps first): lane's sums dg0..dg2 are the
+        // block diagonals o = lane, lane + 32, lane + 64, i.e. tile diagonal
+        // t = c - r + 127 = o + 95 + 64 hf - 32 rg, global distance
+        // (I - J) * 128 - 127 + t.
+        const int t0 = lane + 95 + 64 * hf - 32 * rg;
+        const int d0 = (I - J) * 128 - 127 + t0;
+        const float dgs[3] = {dg0, dg1, dg2};
 #pragma unroll
-          for (int w = 0; w < 8; ++w) {
-            const int o = t - (95 + 64 * (w >> 2) - 32 * (w & 3));
-            if (o >= 0 && o < 96) vs += cw[w * 96 + o];
-          }
-          const int delta = (I - J) * 128 - 127 + t;
-          if (delta >= 0 && delta < T && vs != 0.f) atomicAdd(&p.drho[(size_t)h * T + delta], vs);
+        for (int m = 0; m < 3; ++m) {
+          const int delta = d0 + 32 * m;
+          if (delta >= 0 && delta < T && dgs[m] != 0.f)
+            atomicAdd(&p.drho[(size_t)h * T + delta], dgs[m]);
         }
       }
       float da0, da1;
