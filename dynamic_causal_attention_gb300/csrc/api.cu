@@ -158,6 +158,7 @@ struct WsLayout {
   size_t status, a_tab, r_tab, row_tab, logZ, mode;
   size_t q16, k16, v16, o16, do16, dq16, dk16, dv16;
   size_t Dvec, lse2, Dsum, dq_acc, dv_acc;
+  size_t lse_p, ap, rp, dap, drp;  // padded copies (sequence length not a multiple of 128)
   size_t total;
 };
 
@@ -165,9 +166,22 @@ struct WsLayout {
 
 int kv_heads(const saf_attn_dims& d) { return d.H_kv > 0 ? d.H_kv : d.H; }
 
+// The kernels work on whole 128-row tiles: a sequence length that is not a
+// multiple of 128 runs on copies padded to the next multiple (zero rows of Q,
+// K, V, dO; -inf entries of alpha and rho), cropped afterwards.  Padded keys
+// lie above the causal diagonal of every real row, and padded rows carry
+// dO = 0, so they change no output or gradient of the real rows.
+saf_attn_dims padded_dims(const saf_attn_dims& d) {
+  saf_attn_dims p = d;
+  p.T = (d.T + 127) / 128 * 128;
+  return p;
+}
+
 namespace {
-WsLayout ws_layout(const saf_attn_dims& d) {
+WsLayout ws_layout(const saf_attn_dims& du) {
   WsLayout L;
+  const saf_attn_dims d = padded_dims(du);
+  const bool ragged = d.T != du.T;
   const size_t B = d.B, H = d.H, T = d.T, D = d.d_h;
   const size_t Hkv = (size_t)kv_heads(d);
   const size_t elems = B * H * T * D;
@@ -184,9 +198,9 @@ WsLayout ws_layout(const saf_attn_dims& d) {
   L.row_tab = take(H * T * 4);
   L.logZ = take(H * T * 4);
   L.mode = take(H * 8);  // H ints of mode, then H floats of shift
-  const bool f32 = d.dtype == SAF_F32;
-  const size_t stage = f32 ? elems * 2 : 0;
-  const size_t stage_kv = f32 ? elems_kv * 2 : 0;
+  const bool staged = d.dtype == SAF_F32 || ragged;
+  const size_t stage = staged ? elems * 2 : 0;
+  const size_t stage_kv = staged ? elems_kv * 2 : 0;
   L.q16 = take(stage);
   L.k16 = take(stage_kv);
   L.v16 = take(stage_kv);
@@ -201,6 +215,11 @@ WsLayout ws_layout(const saf_attn_dims& d) {
   L.dq_acc = take(elems * 4);
   // grouped K/V: the frozen query heads' dV, summed per K/V head in fp32
   L.dv_acc = take(Hkv < H ? elems_kv * 4 : 0);
+  L.lse_p = take(ragged ? B * H * T * 4 : 0);
+  L.ap = take(ragged ? H * T * 4 : 0);
+  L.rp = take(ragged ? H * T * 4 : 0);
+  L.dap = take(ragged ? H * T * 4 : 0);
+  L.drp = take(ragged ? H * T * 4 : 0);
   L.total = off;
   return L;
 }
@@ -225,9 +244,10 @@ saf_status check_dims(const saf_attn_dims* d) {
   if (d->dtype != SAF_BF16 && d->dtype != SAF_F32) return SAF_ERR_INVALID_ARG;
   if (d->H_kv < 0 || (d->H_kv > 0 && d->H % d->H_kv != 0)) return SAF_ERR_INVALID_ARG;
   if (d->H > kMaxHeads) return SAF_ERR_UNSUPPORTED;
-  if (d->T % 128 != 0 || d->T > kMaxT) return SAF_ERR_UNSUPPORTED;
+  if (d->T > kMaxT) return SAF_ERR_UNSUPPORTED;
   if (d->d_h != 32 && d->d_h != 64 && d->d_h != 128) return SAF_ERR_UNSUPPORTED;
-  if ((uint64_t)d->B * d->H * d->T >= (1ull << 31)) return SAF_ERR_UNSUPPORTED;
+  const uint64_t t_pad = ((uint64_t)d->T + 127) / 128 * 128;
+  if ((uint64_t)d->B * d->H * t_pad >= (1ull << 31)) return SAF_ERR_UNSUPPORTED;
   return SAF_OK;
 }
 
@@ -356,7 +376,9 @@ saf_status saf_hybrid_attn_fwd(const saf_attn_dims* dims, const void* Q, const v
   g_launches = 0;
   const saf_status ds = check_dims(dims);
   if (ds != SAF_OK) return ds;
-  const saf_attn_dims d = *dims;
+  const saf_attn_dims du = *dims;                 // the caller's shape
+  const saf_attn_dims d = padded_dims(du);       // the kernels' shape
+  const bool ragged = d.T != du.T;
   if (!head_is_static || !V || !out || !workspace) return SAF_ERR_INVALID_ARG;
   const HeadSplit hs = split_heads(head_is_static, d.H);
   if (hs.n_dynamic > 0 && (!Q || !K)) return SAF_ERR_INVALID_ARG;
@@ -365,35 +387,47 @@ saf_status saf_hybrid_attn_fwd(const saf_attn_dims* dims, const void* Q, const v
       (lse && !aligned16(lse)) || (alpha && !aligned16(alpha)) || (rho && !aligned16(rho)))
     return SAF_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SAF_ERR_INVALID_ARG;
-  const WsLayout L = ws_layout(d);
+  const WsLayout L = ws_layout(du);
   if (ws_bytes < L.total) return SAF_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  const size_t elems = (size_t)d.B * d.H * d.T * d.d_h;
-  const size_t elems_kv = (size_t)d.B * kv_heads(d) * d.T * d.d_h;
+  const size_t slabs = (size_t)d.B * d.H, slabs_kv = (size_t)d.B * kv_heads(d);
   SAF_TRY(cudaMemsetAsync(ws + L.status, 0, sizeof(int), s));
 
+  // fp32 I/O and ragged lengths run on bf16 copies of whole tiles
+  const bool f32 = d.dtype == SAF_F32;
+  const bool staged = f32 || ragged;
   const void *q16 = Q, *k16 = K, *v16 = V;
   void* o16 = out;
-  if (d.dtype == SAF_F32) {
+  if (staged) {
     if (hs.n_dynamic > 0) {
-      SAF_TRY(launch_f32_to_bf16(static_cast<const float*>(Q), ws + L.q16, elems, s));
-      SAF_TRY(launch_f32_to_bf16(static_cast<const float*>(K), ws + L.k16, elems_kv, s));
+      SAF_TRY(launch_restage_rows(Q, f32, ws + L.q16, false, slabs, du.T, d.T, d.d_h, s));
+      SAF_TRY(launch_restage_rows(K, f32, ws + L.k16, false, slabs_kv, du.T, d.T, d.d_h, s));
     }
-    SAF_TRY(launch_f32_to_bf16(static_cast<const float*>(V), ws + L.v16, elems_kv, s));
+    SAF_TRY(launch_restage_rows(V, f32, ws + L.v16, false, slabs_kv, du.T, d.T, d.d_h, s));
     q16 = ws + L.q16;
     k16 = ws + L.k16;
     v16 = ws + L.v16;
     o16 = ws + L.o16;
   }
+  const float *alpha_k = alpha, *rho_k = rho;
+  if (ragged && hs.n_static > 0) {
+    float* ap = reinterpret_cast<float*>(ws + L.ap);
+    float* rp = reinterpret_cast<float*>(ws + L.rp);
+    SAF_TRY(launch_restage_vec(alpha, ap, d.H, du.T, d.T, -INFINITY, s));
+    SAF_TRY(launch_restage_vec(rho, rp, d.H, du.T, d.T, -INFINITY, s));
+    alpha_k = ap;
+    rho_k = rp;
+  }
+  float* lse_k = (ragged && lse) ? reinterpret_cast<float*>(ws + L.lse_p) : lse;
   if (hs.n_static > 0)
-    SAF_TRY(launch_static_prep(make_prep(d, hs, alpha, rho, ws_tables(ws, L, d.H)), s));
+    SAF_TRY(launch_static_prep(make_prep(d, hs, alpha_k, rho_k, ws_tables(ws, L, d.H)), s));
 
   FwdLaunch fl;
   memset(&fl, 0, sizeof(fl));
   fill_fwd_params(fl.p, d, hs, ws_tables(ws, L, d.H), false);
   fl.p.out = static_cast<__nv_bfloat16*>(o16);
-  fl.p.lse = lse;
+  fl.p.lse = lse_k;
   const uint64_t rows = (uint64_t)d.B * d.H * d.T;
   const uint64_t rows_kv = (uint64_t)d.B * kv_heads(d) * d.T;
   // Q/K maps must be valid descriptors even when only static heads exist.
@@ -406,7 +440,8 @@ saf_status saf_hybrid_attn_fwd(const saf_attn_dims* dims, const void* Q, const v
   fl.transposed = false;
   fl.num_sms = sm_count();
   SAF_TRY(launch_hybrid_fwd(fl, s));
-  if (d.dtype == SAF_F32) SAF_TRY(launch_bf16_to_f32(o16, static_cast<float*>(out), elems, s));
+  if (staged) SAF_TRY(launch_restage_rows(o16, false, out, f32, slabs, d.T, du.T, d.d_h, s));
+  if (ragged && lse) SAF_TRY(launch_restage_vec(lse_k, lse, slabs, d.T, du.T, 0.f, s));
   return SAF_OK;
 }
 
@@ -419,7 +454,9 @@ saf_status saf_hybrid_attn_bwd(const saf_attn_dims* dims, const void* Q, const v
   g_launches = 0;
   const saf_status ds = check_dims(dims);
   if (ds != SAF_OK) return ds;
-  const saf_attn_dims d = *dims;
+  const saf_attn_dims du = *dims;                 // the caller's shape
+  const saf_attn_dims d = padded_dims(du);       // the kernels' shape
+  const bool ragged = d.T != du.T;
   if (!head_is_static || !V || !out || !lse || !dout || !dQ || !dK || !dV || !workspace)
     return SAF_ERR_INVALID_ARG;
   if ((dalpha == nullptr) != (drho == nullptr)) return SAF_ERR_INVALID_ARG;
@@ -433,13 +470,13 @@ saf_status saf_hybrid_attn_bwd(const saf_attn_dims* dims, const void* Q, const v
       (rho && !aligned16(rho)) || (dalpha && !aligned16(dalpha)) || (drho && !aligned16(drho)))
     return SAF_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SAF_ERR_INVALID_ARG;
-  const WsLayout L = ws_layout(d);
+  const WsLayout L = ws_layout(du);
   if (ws_bytes < L.total) return SAF_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const int Hkv = kv_heads(d), gkv = d.H / Hkv;
-  const size_t elems = (size_t)d.B * d.H * d.T * d.d_h;
   const size_t elems_kv = (size_t)d.B * Hkv * d.T * d.d_h;
+  const size_t slabs = (size_t)d.B * d.H, slabs_kv = (size_t)d.B * Hkv;
   const uint64_t rows = (uint64_t)d.B * d.H * d.T;
   const uint64_t rows_kv = (uint64_t)d.B * Hkv * d.T;
   SAF_TRY(cudaMemsetAsync(ws + L.status, 0, sizeof(int), s));
@@ -451,16 +488,19 @@ saf_status saf_hybrid_attn_bwd(const saf_attn_dims* dims, const void* Q, const v
   for (int h = 0; h < d.H; ++h) (hs.is_static[h] ? kv_has_static : kv_has_dyn)[h / gkv] = 1;
   float* dv_acc = (gkv > 1 && hs.n_static > 0) ? reinterpret_cast<float*>(ws + L.dv_acc) : nullptr;
 
+  // fp32 I/O and ragged lengths run on bf16 copies of whole tiles
+  const bool f32 = d.dtype == SAF_F32;
+  const bool staged = f32 || ragged;
   const void *q16 = Q, *k16 = K, *v16 = V, *o16 = out, *do16 = dout;
   void *dq16 = dQ, *dk16 = dK, *dv16 = dV;
-  if (d.dtype == SAF_F32) {
+  if (staged) {
     if (hs.n_dynamic > 0) {
-      SAF_TRY(launch_f32_to_bf16(static_cast<const float*>(Q), ws + L.q16, elems, s));
-      SAF_TRY(launch_f32_to_bf16(static_cast<const float*>(K), ws + L.k16, elems_kv, s));
+      SAF_TRY(launch_restage_rows(Q, f32, ws + L.q16, false, slabs, du.T, d.T, d.d_h, s));
+      SAF_TRY(launch_restage_rows(K, f32, ws + L.k16, false, slabs_kv, du.T, d.T, d.d_h, s));
     }
-    SAF_TRY(launch_f32_to_bf16(static_cast<const float*>(V), ws + L.v16, elems_kv, s));
-    SAF_TRY(launch_f32_to_bf16(static_cast<const float*>(out), ws + L.o16, elems, s));
-    SAF_TRY(launch_f32_to_bf16(static_cast<const float*>(dout), ws + L.do16, elems, s));
+    SAF_TRY(launch_restage_rows(V, f32, ws + L.v16, false, slabs_kv, du.T, d.T, d.d_h, s));
+    SAF_TRY(launch_restage_rows(out, f32, ws + L.o16, false, slabs, du.T, d.T, d.d_h, s));
+    SAF_TRY(launch_restage_rows(dout, f32, ws + L.do16, false, slabs, du.T, d.T, d.d_h, s));
     q16 = ws + L.q16;
     k16 = ws + L.k16;
     v16 = ws + L.v16;
@@ -470,8 +510,30 @@ saf_status saf_hybrid_attn_bwd(const saf_attn_dims* dims, const void* Q, const v
     dk16 = ws + L.dk16;
     dv16 = ws + L.dv16;
   }
+  // ragged lengths: lse of the padded rows 0 (their dO is 0, so P there
+  // is finite and contributes nothing), alpha/rho padded with -inf, and
+  // dalpha/drho formed over the padded length, then cropped
+  const float *alpha_k = alpha, *rho_k = rho, *lse_k = lse;
+  float *dalpha_k = dalpha, *drho_k = drho;
+  if (ragged) {
+    float* lp = reinterpret_cast<float*>(ws + L.lse_p);
+    SAF_TRY(launch_restage_vec(lse, lp, slabs, du.T, d.T, 0.f, s));
+    lse_k = lp;
+    if (hs.n_static > 0) {
+      float* ap = reinterpret_cast<float*>(ws + L.ap);
+      float* rp = reinterpret_cast<float*>(ws + L.rp);
+      SAF_TRY(launch_restage_vec(alpha, ap, d.H, du.T, d.T, -INFINITY, s));
+      SAF_TRY(launch_restage_vec(rho, rp, d.H, du.T, d.T, -INFINITY, s));
+      alpha_k = ap;
+      rho_k = rp;
+    }
+    if (dalpha) {
+      dalpha_k = reinterpret_cast<float*>(ws + L.dap);
+      drho_k = reinterpret_cast<float*>(ws + L.drp);
+    }
+  }
   if (hs.n_static > 0)
-    SAF_TRY(launch_static_prep(make_prep(d, hs, alpha, rho, ws_tables(ws, L, d.H)), s));
+    SAF_TRY(launch_static_prep(make_prep(d, hs, alpha_k, rho_k, ws_tables(ws, L, d.H)), s));
 
   // pre-pass: D, lse2, per-head batch sums of D for static heads
   BwdPre pre;
@@ -479,10 +541,10 @@ saf_status saf_hybrid_attn_bwd(const saf_attn_dims* dims, const void* Q, const v
   pre.B = d.B; pre.H = d.H; pre.T = d.T; pre.d_h = d.d_h;
   pre.out = static_cast<const __nv_bfloat16*>(o16);
   pre.dout = static_cast<const __nv_bfloat16*>(do16);
-  pre.lse = lse;
+  pre.lse = lse_k;
   pre.Dvec = reinterpret_cast<float*>(ws + L.Dvec);
   pre.lse2 = reinterpret_cast<float*>(ws + L.lse2);
-  pre.Dsum = dalpha ? reinterpret_cast<float*>(ws + L.Dsum) : nullptr;
+  pre.Dsum = dalpha_k ? reinterpret_cast<float*>(ws + L.Dsum) : nullptr;
   pre.n_static = hs.n_static;
   memset(pre.static_slot, 255, sizeof(pre.static_slot));
   for (int i = 0; i < hs.n_static; ++i) pre.static_slot[hs.st[i]] = (uint8_t)i;
@@ -564,9 +626,9 @@ saf_status saf_hybrid_attn_bwd(const saf_attn_dims* dims, const void* Q, const v
     bl.num_sms = sm_count();
     SAF_TRY(launch_bwd_dynamic(bl, s));
   }
-  if (dalpha) {
-    SAF_TRY(launch_zero_u32(dalpha, (size_t)d.H * d.T, s));
-    SAF_TRY(launch_zero_u32(drho, (size_t)d.H * d.T, s));
+  if (dalpha_k) {
+    SAF_TRY(launch_zero_u32(dalpha_k, (size_t)d.H * d.T, s));
+    SAF_TRY(launch_zero_u32(drho_k, (size_t)d.H * d.T, s));
     if (hs.n_static > 0) {
       ParamGradLaunch gl;
       memset(&gl, 0, sizeof(gl));
@@ -582,8 +644,8 @@ saf_status saf_hybrid_attn_bwd(const saf_attn_dims* dims, const void* Q, const v
       p.row_tab = reinterpret_cast<const float*>(ws + L.row_tab);
       p.mode = reinterpret_cast<const int*>(ws + L.mode);
       p.Dsum = pre.Dsum;
-      p.dalpha = dalpha;
-      p.drho = drho;
+      p.dalpha = dalpha_k;
+      p.drho = drho_k;
       p.status = reinterpret_cast<int*>(ws + L.status);
       if (!encode_rows(&gl.tm_v, v16, rows_kv, d.d_h) || !encode_rows(&gl.tm_do, do16, rows, d.d_h))
         return SAF_ERR_CUDA;
@@ -603,10 +665,14 @@ saf_status saf_hybrid_attn_bwd(const saf_attn_dims* dims, const void* Q, const v
   memcpy(post.is_static, hs.is_static, sizeof(post.is_static));
   for (int kv = 0; kv < Hkv; ++kv) post.kv_no_dyn[kv] = kv_has_dyn[kv] ? 0 : 1;
   SAF_TRY(launch_bwd_post(post, s));
-  if (d.dtype == SAF_F32) {
-    SAF_TRY(launch_bf16_to_f32(dq16, static_cast<float*>(dQ), elems, s));
-    SAF_TRY(launch_bf16_to_f32(dk16, static_cast<float*>(dK), elems_kv, s));
-    SAF_TRY(launch_bf16_to_f32(dv16, static_cast<float*>(dV), elems_kv, s));
+  if (staged) {
+    SAF_TRY(launch_restage_rows(dq16, false, dQ, f32, slabs, d.T, du.T, d.d_h, s));
+    SAF_TRY(launch_restage_rows(dk16, false, dK, f32, slabs_kv, d.T, du.T, d.d_h, s));
+    SAF_TRY(launch_restage_rows(dv16, false, dV, f32, slabs_kv, d.T, du.T, d.d_h, s));
+  }
+  if (ragged && dalpha) {
+    SAF_TRY(launch_restage_vec(dalpha_k, dalpha, d.H, d.T, du.T, 0.f, s));
+    SAF_TRY(launch_restage_vec(drho_k, drho, d.H, d.T, du.T, 0.f, s));
   }
   return SAF_OK;
 }

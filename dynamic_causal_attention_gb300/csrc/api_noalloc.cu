@@ -104,7 +104,8 @@ extern "C" saf_status saf_hybrid_attn_fwd_noalloc(const saf_attn_dims* dims, con
   const saf_status ds = check_dims(dims);
   if (ds != SAF_OK) return ds;
   const saf_attn_dims d = *dims;
-  if (d.dtype != SAF_BF16) return SAF_ERR_UNSUPPORTED;  // fp32 I/O needs staging buffers
+  // fp32 I/O and lengths that are not a multiple of 128 need staging buffers
+  if (d.dtype != SAF_BF16 || d.T % 128 != 0) return SAF_ERR_UNSUPPORTED;
   if (!head_is_static || !V || !out) return SAF_ERR_INVALID_ARG;
   const HeadSplit hs = split_heads(head_is_static, d.H);
   if (hs.n_dynamic > 0 && (!Q || !K)) return SAF_ERR_INVALID_ARG;

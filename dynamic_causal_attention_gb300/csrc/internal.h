@@ -101,5 +101,13 @@ cudaError_t launch_static_prep(const StaticPrep& p, cudaStream_t s);
 cudaError_t launch_f32_to_bf16(const float* src, void* dst, size_t n, cudaStream_t s);
 cudaError_t launch_bf16_to_f32(const void* src, float* dst, size_t n, cudaStream_t s);
 cudaError_t launch_zero_u32(void* dst, size_t n_words, cudaStream_t s);
+// [n_slabs, T_src, d] rows (bf16 or fp32) into [n_slabs, T_dst, d] (bf16 or
+// fp32): rows t >= T_src of the destination are zero (padding), rows of the
+// source past T_dst are dropped (cropping).  d % 4 == 0.
+cudaError_t launch_restage_rows(const void* src, bool src_f32, void* dst, bool dst_f32,
+                                size_t n_slabs, int T_src, int T_dst, int d, cudaStream_t s);
+// [n_rows, T_src] fp32 into [n_rows, T_dst], entries t >= T_src set to `fill`.
+cudaError_t launch_restage_vec(const float* src, float* dst, size_t n_rows, int T_src, int T_dst,
+                               float fill, cudaStream_t s);
 
 }  // namespace saf

@@ -55,7 +55,7 @@ extern "C" {
 typedef enum saf_status {
   SAF_OK = 0,
   SAF_ERR_INVALID_ARG = 1,  /* null or misaligned pointer, bad size, k out of range   */
-  SAF_ERR_UNSUPPORTED = 2,  /* valid but not implemented: d_h, T % 128, H > 256, ...    */
+  SAF_ERR_UNSUPPORTED = 2,  /* valid but not implemented: d_h, T > 16384, H > 256, ...  */
   SAF_ERR_CUDA = 3,         /* a CUDA runtime/driver call or a launch failed            */
   SAF_ERR_STATE = 4,        /* calibration state misuse (e.g. finalize with N < 2)      */
   SAF_ERR_TIMEOUT = 5       /* a bounded device wait ran out (read with get_device_status) */
@@ -77,11 +77,19 @@ typedef enum saf_dtype {
  * h / (H / H_kv).  A frozen query head still mixes its group's V (only its
  * query path is gone); dK and dV of a K/V head sum the gradients of every
  * query head it serves, and dK of a K/V head that serves no dynamic head is
- * zero.  H_kv = 0 means H_kv = H (one K/V head per query head). */
+ * zero.  H_kv = 0 means H_kv = H (one K/V head per query head).
+ *
+ * The kernels work on whole tiles of 128 rows.  A length T that is not a
+ * multiple of 128 runs on copies padded to the next multiple, held in the
+ * workspace (zero rows of Q, K, V, dout; alpha and rho padded with -inf;
+ * lse of the padded rows 0), and the results are cropped back to T: padded
+ * keys lie above the causal diagonal of every real row and padded rows carry
+ * dout = 0, so the real rows' outputs and gradients are those of length T.
+ * The workspace then holds the padded copies too. */
 typedef struct saf_attn_dims {
   int B;        /* batch size, >= 1                                    */
   int H;        /* query heads in the layer, 1..256                    */
-  int T;        /* sequence length, a positive multiple of 128         */
+  int T;        /* sequence length, >= 1 (see below for T % 128 != 0)  */
   int d_h;      /* head dimension: 32, 64 or 128                       */
   saf_dtype dtype;
   int H_kv;     /* K/V heads: 0 (= H) or a divisor of H                */
@@ -153,7 +161,8 @@ SAF_API saf_status saf_hybrid_attn_bwd(const saf_attn_dims* dims,
  * call; it is an interface convenience.
  *
  * Arguments and results are those of saf_hybrid_attn_fwd with dims->dtype ==
- * SAF_BF16 (fp32 I/O would need staging buffers: SAF_ERR_UNSUPPORTED).  The
+ * SAF_BF16 and dims->T a multiple of 128 (fp32 I/O and other lengths would
+ * need staging buffers: SAF_ERR_UNSUPPORTED).  The
  * scratch (the frozen heads' tables, log Z and the status word) lives in one
  * file-scope device array of 4 MiB that every GPU which loads the library
  * holds until the process exits; a shape whose tables need more,

@@ -58,7 +58,11 @@ def test_workspace_size_and_unsupported_shapes(binding):
     d = binding._dims
     assert binding.saf_hybrid_attn_workspace_size(d(8, 12, 4096, 64, 0), 0) > 0
     assert binding.saf_hybrid_attn_workspace_size(d(1, 4, 128, 32, 1), 1) > 0
-    assert binding.saf_hybrid_attn_workspace_size(d(1, 4, 100, 32, 0), 0) == 0   # T % 128
+    # a length that is not a multiple of 128 runs on padded copies: the
+    # workspace holds them (and more than the padded length's own workspace)
+    ws_ragged = binding.saf_hybrid_attn_workspace_size(d(1, 4, 100, 32, 0), 0)
+    assert ws_ragged > binding.saf_hybrid_attn_workspace_size(d(1, 4, 128, 32, 0), 0)
+    assert binding.saf_hybrid_attn_workspace_size(d(1, 4, 16385, 32, 0), 0) == 0   # T
     assert binding.saf_hybrid_attn_workspace_size(d(1, 4, 128, 48, 0), 0) == 0   # d_h
     assert binding.saf_hybrid_attn_workspace_size(d(1, 300, 128, 64, 0), 0) == 0  # H
     assert binding.saf_hybrid_attn_workspace_size(d(0, 4, 128, 64, 0), 0) == 0   # B
@@ -121,8 +125,11 @@ def test_noalloc_forward_rejects_what_its_scratch_cannot_hold(binding):
     st = binding.saf_hybrid_attn_fwd_noalloc(d(1, 64, 16384, 64, 0), 16, 16, 16, 16, 16, hs,
                                              16, 16, None)
     assert st == binding.SAF_ERR_UNSUPPORTED
-    # fp32 I/O would need staging buffers
+    # fp32 I/O and lengths that are not a multiple of 128 would need staging buffers
     st = binding.saf_hybrid_attn_fwd_noalloc(d(1, 4, 128, 32, 1), 16, 16, 16, 16, 16,
+                                             bytes([1, 0, 0, 0]), 16, 16, None)
+    assert st == binding.SAF_ERR_UNSUPPORTED
+    st = binding.saf_hybrid_attn_fwd_noalloc(d(1, 4, 200, 32, 0), 16, 16, 16, 16, 16,
                                              bytes([1, 0, 0, 0]), 16, 16, None)
     assert st == binding.SAF_ERR_UNSUPPORTED
     st = binding.saf_hybrid_attn_fwd_noalloc(d(1, 4, 128, 32, 0), 16, 16, None, 16, 16,
