@@ -176,30 +176,6 @@ __global__ void __launch_bounds__(256) static_prep_kernel(StaticPrep p) {
   }
 }
 
-__global__ void f32_to_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst,
-                                   size_t n) {
-  for (size_t i = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 4; i < n;
-       i += (size_t)gridDim.x * blockDim.x * 4) {
-    const float4 v = *reinterpret_cast<const float4*>(src + i);
-    uint2 o;
-    o.x = pack_bf16x2(v.x, v.y);
-    o.y = pack_bf16x2(v.z, v.w);
-    *reinterpret_cast<uint2*>(dst + i) = o;
-  }
-}
-
-__global__ void bf16_to_f32_kernel(const __nv_bfloat16* __restrict__ src, float* __restrict__ dst,
-                                   size_t n) {
-  for (size_t i = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 4; i < n;
-       i += (size_t)gridDim.x * blockDim.x * 4) {
-    const uint2 v = *reinterpret_cast<const uint2*>(src + i);
-    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&v.x);
-    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&v.y);
-    *reinterpret_cast<float4*>(dst + i) =
-        make_float4(__low2float(a), __high2float(a), __low2float(b), __high2float(b));
-  }
-}
-
 __global__ void zero_u32_kernel(uint32_t* dst, size_t n) {
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (size_t)gridDim.x * blockDim.x)
@@ -224,22 +200,6 @@ cudaError_t launch_static_prep(const StaticPrep& p, cudaStream_t s) {
   trace_begin(s);
   static_prep_kernel<<<dim3(p.T / kPrepRows, p.n_static), 256, smem, s>>>(p);
   trace_end(s, "static_prep");
-  return cudaGetLastError();
-}
-
-cudaError_t launch_f32_to_bf16(const float* src, void* dst, size_t n, cudaStream_t s) {
-  trace_begin(s);
-  f32_to_bf16_kernel<<<elementwise_blocks(n / 4), 256, 0, s>>>(
-      src, static_cast<__nv_bfloat16*>(dst), n);
-  trace_end(s, "f32_to_bf16");
-  return cudaGetLastError();
-}
-
-cudaError_t launch_bf16_to_f32(const void* src, float* dst, size_t n, cudaStream_t s) {
-  trace_begin(s);
-  bf16_to_f32_kernel<<<elementwise_blocks(n / 4), 256, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(src), dst, n);
-  trace_end(s, "bf16_to_f32");
   return cudaGetLastError();
 }
 

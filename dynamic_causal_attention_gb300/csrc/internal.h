@@ -98,8 +98,6 @@ struct StaticPrep {
 cudaError_t launch_static_prep(const StaticPrep& p, cudaStream_t s);
 
 // Elementwise helpers.
-cudaError_t launch_f32_to_bf16(const float* src, void* dst, size_t n, cudaStream_t s);
-cudaError_t launch_bf16_to_f32(const void* src, float* dst, size_t n, cudaStream_t s);
 cudaError_t launch_zero_u32(void* dst, size_t n_words, cudaStream_t s);
 // [n_slabs, T_src, d] rows (bf16 or fp32) into [n_slabs, T_dst, d] (bf16 or
 // fp32): rows t >= T_src of the destination are zero (padding), rows of the
