@@ -240,7 +240,7 @@ StaticTables ws_tables(uint8_t* ws, const WsLayout& L, int H) {
 
 saf_status check_dims(const saf_attn_dims* d) {
   if (!d) return SAF_ERR_INVALID_ARG;
-  if (d->B < 1 || d->H < 1 || d->T < 1 || d->d_h < 1) return SAF_ERR_INVALID_ARG;
+  if (d->B < 0 || d->H < 0 || d->T < 0 || d->d_h < 1) return SAF_ERR_INVALID_ARG;
   if (d->dtype != SAF_BF16 && d->dtype != SAF_F32) return SAF_ERR_INVALID_ARG;
   if (d->H_kv < 0 || (d->H_kv > 0 && d->H % d->H_kv != 0)) return SAF_ERR_INVALID_ARG;
   if (d->H > kMaxHeads) return SAF_ERR_UNSUPPORTED;
@@ -365,7 +365,7 @@ saf_status saf_trace_get(int index, const char** kernel, float* ms) {
 
 size_t saf_hybrid_attn_workspace_size(const saf_attn_dims* dims, int want_param_grads) {
   (void)want_param_grads;  // the parameter-gradient pass needs no extra scratch
-  if (check_dims(dims) != SAF_OK) return 0;
+  if (check_dims(dims) != SAF_OK || empty_dims(*dims)) return 0;
   return ws_layout(*dims).total;
 }
 
@@ -376,6 +376,7 @@ saf_status saf_hybrid_attn_fwd(const saf_attn_dims* dims, const void* Q, const v
   g_launches = 0;
   const saf_status ds = check_dims(dims);
   if (ds != SAF_OK) return ds;
+  if (empty_dims(*dims)) return SAF_OK;  // nothing to compute
   const saf_attn_dims du = *dims;                 // the caller's shape
   const saf_attn_dims d = padded_dims(du);       // the kernels' shape
   const bool ragged = d.T != du.T;
@@ -454,6 +455,7 @@ saf_status saf_hybrid_attn_bwd(const saf_attn_dims* dims, const void* Q, const v
   g_launches = 0;
   const saf_status ds = check_dims(dims);
   if (ds != SAF_OK) return ds;
+  if (empty_dims(*dims)) return SAF_OK;  // nothing to compute
   const saf_attn_dims du = *dims;                 // the caller's shape
   const saf_attn_dims d = padded_dims(du);       // the kernels' shape
   const bool ragged = d.T != du.T;
@@ -727,9 +729,10 @@ saf_status saf_calib_accumulate(void* handle, const float* A, int n, int head_be
                                 int head_count, void* stream) {
   g_launches = 0;
   CalibHandle* h = static_cast<CalibHandle*>(handle);
-  if (!h || !A || !aligned16(A) || n < 1 || head_count < 1 || head_begin < 0 ||
-      head_begin + head_count > h->num_heads)
+  if (!h || n < 0 || head_count < 0 || head_begin < 0 || head_begin + head_count > h->num_heads)
     return SAF_ERR_INVALID_ARG;
+  if (n == 0 || head_count == 0) return SAF_OK;  // no samples: nothing changes
+  if (!A || !aligned16(A)) return SAF_ERR_INVALID_ARG;
   const int c0 = h->counts[head_begin];
   for (int i = head_begin; i < head_begin + head_count; ++i)
     if (h->counts[i] != c0) return SAF_ERR_STATE;

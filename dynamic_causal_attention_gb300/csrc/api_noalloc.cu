@@ -103,6 +103,7 @@ extern "C" saf_status saf_hybrid_attn_fwd_noalloc(const saf_attn_dims* dims, con
   launch_count_reset();
   const saf_status ds = check_dims(dims);
   if (ds != SAF_OK) return ds;
+  if (empty_dims(*dims)) return SAF_OK;  // nothing to compute
   const saf_attn_dims d = *dims;
   // fp32 I/O and lengths that are not a multiple of 128 need staging buffers
   if (d.dtype != SAF_BF16 || d.T % 128 != 0) return SAF_ERR_UNSUPPORTED;

@@ -22,6 +22,9 @@ int kv_heads(const saf_attn_dims& d);
 
 // SAF_OK, or the status an attention call returns for these dimensions.
 saf_status check_dims(const saf_attn_dims* d);
+// B, H or T zero: a layer with nothing to compute (valid; the calls return
+// SAF_OK at once, touching no pointer).
+inline bool empty_dims(const saf_attn_dims& d) { return d.B == 0 || d.H == 0 || d.T == 0; }
 
 struct HeadSplit {
   int n_static = 0, n_dynamic = 0;

@@ -85,11 +85,15 @@ typedef enum saf_dtype {
  * lse of the padded rows 0), and the results are cropped back to T: padded
  * keys lie above the causal diagonal of every real row and padded rows carry
  * dout = 0, so the real rows' outputs and gradients are those of length T.
- * The workspace then holds the padded copies too. */
+ * The workspace then holds the padded copies too.
+ *
+ * B, H or T zero is an empty layer: the attention calls return SAF_OK at once
+ * without reading any pointer or launching anything, and the workspace query
+ * returns 0. */
 typedef struct saf_attn_dims {
-  int B;        /* batch size, >= 1                                    */
-  int H;        /* query heads in the layer, 1..256                    */
-  int T;        /* sequence length, >= 1 (see below for T % 128 != 0)  */
+  int B;        /* batch size, >= 0                                    */
+  int H;        /* query heads in the layer, 0..256                    */
+  int T;        /* sequence length, 0..16384 (below: T % 128 != 0)     */
   int d_h;      /* head dimension: 32, 64 or 128                       */
   saf_dtype dtype;
   int H_kv;     /* K/V heads: 0 (= H) or a divisor of H                */
@@ -203,7 +207,8 @@ SAF_API saf_status saf_calib_create_ex(void** handle, int num_heads, int T, unsi
  *      lower triangle j <= i is read; entries above the diagonal are treated
  *      as zero.
  * All heads in the range must have seen the same number of samples so far
- * (SAF_ERR_STATE otherwise).  Per element the kernel keeps a count, a mean
+ * (SAF_ERR_STATE otherwise).  n = 0 or head_count = 0 changes nothing and
+ * returns SAF_OK (A is then not read).  Per element the kernel keeps a count, a mean
  * and a sum of squared deviations (Welford's update, merged with Chan et
  * al.'s pairwise formula), so chunked calls match a one-shot call. */
 SAF_API saf_status saf_calib_accumulate(void* handle, const float* A, int n,

@@ -65,7 +65,8 @@ def test_workspace_size_and_unsupported_shapes(binding):
     assert binding.saf_hybrid_attn_workspace_size(d(1, 4, 16385, 32, 0), 0) == 0   # T
     assert binding.saf_hybrid_attn_workspace_size(d(1, 4, 128, 48, 0), 0) == 0   # d_h
     assert binding.saf_hybrid_attn_workspace_size(d(1, 300, 128, 64, 0), 0) == 0  # H
-    assert binding.saf_hybrid_attn_workspace_size(d(0, 4, 128, 64, 0), 0) == 0   # B
+    assert binding.saf_hybrid_attn_workspace_size(d(0, 4, 128, 64, 0), 0) == 0   # empty
+    assert binding.saf_hybrid_attn_workspace_size(d(-1, 4, 128, 64, 0), 0) == 0  # B
     # grouped K/V: H_kv must divide H; the grouped layout needs the extra dV sum
     ws_mha = binding.saf_hybrid_attn_workspace_size(d(2, 8, 256, 64, 0), 0)
     ws_gqa = binding.saf_hybrid_attn_workspace_size(d(2, 8, 256, 64, 0, 2), 0)
@@ -135,3 +136,27 @@ def test_noalloc_forward_rejects_what_its_scratch_cannot_hold(binding):
     st = binding.saf_hybrid_attn_fwd_noalloc(d(1, 4, 128, 32, 0), 16, 16, None, 16, 16,
                                              bytes([1, 0, 0, 0]), 16, 16, None)
     assert st == binding.SAF_ERR_INVALID_ARG
+
+
+def test_empty_layers_are_no_ops(binding):
+    # B, H or T zero: SAF_OK at once, no pointer read (all None here), nothing
+    # launched.  Invalid fields are still rejected.
+    d = binding._dims
+    for dims in (d(0, 4, 128, 64, 0), d(2, 0, 128, 64, 0), d(2, 4, 0, 64, 0)):
+        st = binding.saf_hybrid_attn_fwd(dims, None, None, None, None, None, b"", None, None,
+                                         None, 0, None)
+        assert st == binding.SAF_OK, binding.saf_status_string(st)
+        assert binding.saf_last_launch_count() == 0
+        st = binding.saf_hybrid_attn_bwd(dims, None, None, None, None, None, None, None, None,
+                                         b"", None, None, None, None, None, None, 0, None)
+        assert st == binding.SAF_OK, binding.saf_status_string(st)
+        assert binding.saf_last_launch_count() == 0
+        st = binding.saf_hybrid_attn_fwd_noalloc(dims, None, None, None, None, None, b"",
+                                                 None, None, None)
+        assert st == binding.SAF_OK, binding.saf_status_string(st)
+    bad = d(0, 4, 128, 48, 0)   # d_h is still checked
+    assert binding.saf_hybrid_attn_fwd(bad, None, None, None, None, None, b"", None, None,
+                                       None, 0, None) == binding.SAF_ERR_UNSUPPORTED
+    neg = d(-2, 4, 128, 64, 0)
+    assert binding.saf_hybrid_attn_fwd(neg, None, None, None, None, None, b"", None, None,
+                                       None, 0, None) == binding.SAF_ERR_INVALID_ARG

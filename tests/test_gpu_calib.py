@@ -129,6 +129,26 @@ def test_state_errors(api):
     cal.close()
 
 
+def test_zero_samples_change_nothing(api):
+    # n = 0 (an empty batch) is a no-op: the statistics equal, bit for bit,
+    # those of the same batches without it
+    N, nh, T = 5, 3, 64
+    A = calib_probabilities(N, nh, T, d_h=16, seed=41)
+    a = api.Calibration(nh, T)
+    a.accumulate(A[:2].cuda())
+    a.accumulate(torch.empty((0, nh, T, T), device="cuda"))
+    a.accumulate(A[2:].cuda())
+    b = api.Calibration(nh, T)
+    b.accumulate(A[:2].cuda())
+    b.accumulate(A[2:].cuda())
+    ra, rb = a.finalize(1), b.finalize(1)
+    torch.cuda.synchronize()
+    for x, y in zip(ra, rb):
+        np.testing.assert_array_equal(x.cpu().numpy(), y.cpu().numpy())
+    a.close()
+    b.close()
+
+
 def test_full_size_calibration(api):
     c = CALIB_CONFIG
     k = oracle.num_select(c.r, c.num_heads)
