@@ -1,4 +1,5 @@
-"""Parity at sequence lengths that are not a multiple of 128.
+"""Parity at sequence lengths that are not a multiple of 128, and at the most
+heads a call takes.
 
 The kernels work on whole 128-row tiles; the C ABI runs such a length on
 zero-padded copies in the workspace (alpha and rho padded with -inf, the
@@ -94,3 +95,13 @@ def test_ragged_length_grouped_kv():
     cfg = AttnConfig("ragged_g", B=2, H=4, T=170, d_h=64, dtype="bf16", static_heads=(1,))
     inp = attn_inputs(cfg, seed=313)
     check(cfg, inp, run(inp, cfg.head_is_static, True, H_kv=2), True, H_kv=2)
+
+
+def test_most_heads_at_once():
+    # H = 256, the most heads a call takes (one item per head and sequence),
+    # a third of them frozen, with the head index stored in 8 bits everywhere
+    H = 256
+    static = tuple(range(0, H, 3))
+    cfg = AttnConfig("many_heads", B=1, H=H, T=128, d_h=32, dtype="bf16", static_heads=static)
+    inp = attn_inputs(cfg, seed=317)
+    check(cfg, inp, run(inp, cfg.head_is_static, True), True)
