@@ -72,14 +72,15 @@ struct BwdSmem {
   static constexpr int OFF_DST = OFF_Q + QST * STAGE;
   // dQ staging for the tensor reduce-add (d_h <= 64): one [128 rows x 128 B]
   // chunk (32 fp32 columns), 128-byte swizzled, reused for each chunk of the
-  // row.  d_h = 128 stages through the dS^T tile (below).
+  // row.  d_h = 128 stages dQ (64 KB) in its step's own Q_I/dO_I stage, whose
+  // 64 KB of tiles are free once dK and dV have read them.
   static constexpr bool DQ_TMA = (D <= 64);
   static constexpr int DQS_BYTES = DQ_TMA ? 128 * 32 * 4 : 0;
   // PS: two dS^T tiles, used by alternate steps
   static constexpr int DST_BUFS = PS ? 2 : 1;
   static constexpr int OFF_DQS = OFF_DST + DST_BUFS * SqTile::BYTES;
   static constexpr int OFF_BAR = OFF_DQS + DQS_BYTES;
-  static constexpr int NBAR = 2 + 2 * QST + 18;
+  static constexpr int NBAR = 2 + 2 * QST + 16;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int SLACK = (BYTES + 1024 <= 232448) ? 1024 : 0;
@@ -195,10 +196,10 @@ __global__ void __launch_bounds__(512, 1)
   uint64_t* s_free = kd_empty + 1;       // S^T, dP^T loaded by the compute warps (PS)
   uint64_t* pt_empty = s_free + 1;       // the P^T columns are free again (PS)
   uint64_t* p_empty2 = pt_empty + 1;     // PS: dS^T tile 1 free again (tile 0: p_empty)
-  uint64_t* dqs_free = p_empty2 + 1;     // DQ_DST: the dQ reductions have read the tile
-  uint64_t* dp_full = dqs_free + 1;      // DQ_ALIAS: dP^T ready (s_full: S^T ready)
-  uint64_t* dv_done = dp_full + 1;       // DQ_ALIAS: the step's dV has read P^T
-  uint64_t* dk_done = dv_done + 1;       // DQ_ALIAS: the step's dK has read dS^T
+  uint64_t* dp_full = p_empty2 + 1;      // DQ_ALIAS: dP^T ready (s_full: S^T ready)
+  // DQ_ALIAS: the step's dV has read P^T and dO (dk_done: dK, dS^T and Q)
+  uint64_t* dv_done = dp_full + 1;
+  uint64_t* dk_done = dv_done + 1;
   // DQ_ALIAS: dq_empty is dQ's low 64 columns taken into the dQ warps'
   // registers, dqhi_empty its high 64 columns
   uint64_t* dqhi_empty = dk_done + 1;
@@ -223,7 +224,6 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(s_free, 256);
     mbar_init(pt_empty, 1);
     mbar_init(p_empty2, 1);
-    mbar_init(dqs_free, 1);
     mbar_init(dp_full, 1);
     mbar_init(dv_done, 1);
     mbar_init(dk_done, 1);
@@ -412,7 +412,7 @@ __global__ void __launch_bounds__(512, 1)
                         id_acc, (t > 0 || kk > 0));
           mma_commit(dk_done);
           ++dkc;
-          mma_commit(q_empty + qs);
+          // (the dQ warps stage dQ in this stage and then release it)
           ++qc;
           ++pc;
           if (t + 1 < w.nsteps) {
@@ -625,11 +625,7 @@ __global__ void __launch_bounds__(512, 1)
           // operand of dK), and into shared memory for dQ
           tmem_st_x16(trow + L::T_DP + 32 * hf + (c0 >> 1), dk);
           // the dS^T tile in shared memory is read by the previous step's dQ
-          // (and, staged there, by its reductions)
-          if (c0 == 0) {
-            mbar_wait(p_empty, (pc & 1) ^ 1, wc, kSiteBCmpP);
-            mbar_wait(dqs_free, (pc & 1) ^ 1, wc, kSiteBCmpP);
-          }
+          if (c0 == 0) mbar_wait(p_empty, (pc & 1) ^ 1, wc, kSiteBCmpP);
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const uint32_t unit = (uint32_t)(col >> 3) + u;
@@ -732,10 +728,16 @@ __global__ void __launch_bounds__(512, 1)
         } else {
           // d_h = 128: each 64-column half of dQ is loaded and its TMEM
           // columns released (the next step's S^T or dP^T goes there), then
-          // staged 32 columns at a time through the two 16 KB halves of the
-          // dS^T tile (both dQ products have read it) and added with one
-          // tensor reduce-add per chunk.
+          // staged in this step's Q_I/dO_I stage, the low half over dO_I once
+          // dV has read it and the high half over Q_I once dK has, and added
+          // with one tensor reduce-add per 32-column chunk.  Waiting for dV
+          // (dK) before releasing the half also keeps dv_done (dk_done) from
+          // running two phases ahead of this wait: the next step's S^T (dP^T)
+          // waits for the release.  The stage goes back to the producer once
+          // the reduce-adds have read it.
+          const int qs = (int)(dqc % (uint32_t)L::QST);
           const int row = (w.b * H + hq) * T + I * 128;
+          const int stage_off = L::OFF_Q + qs * L::STAGE;
 #pragma unroll 1
           for (int hh = 0; hh < 2; ++hh) {
             uint32_t o[64];
@@ -749,28 +751,29 @@ __global__ void __launch_bounds__(512, 1)
               tmem_wait_ld(o1);
             }
             tc_fence_before();
+            mbar_wait(hh ? dk_done : dv_done, dqc & 1, wc, kSiteBDq);
             mbar_arrive(hh ? dqhi_empty : dq_empty);  // this half is in registers
+            // low half: dO_I's two 16 KB chunks; high half: Q_I's
+            const int half_off = stage_off + (hh ? 0 : G::TILE_BYTES);
+            const uint32_t sh = smem_u32(smem + half_off);
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              const int cc = 2 * hh + c;  // dQ columns 32cc .. 32cc + 31
-              const uint32_t slot = (uint32_t)(cc & 1) * 16384u;
-              if (r == 0 && cc >= 2) bulk_wait_group_read1();  // chunk cc - 2 has left the slot
-              named_bar_sync(6, 128);
+            for (int c = 0; c < 2; ++c)
 #pragma unroll
               for (int u = 0; u < 8; ++u)
-                st_shared_v4(sDST + slot + sw128_offset(r, (uint32_t)u), o[32 * c + 4 * u],
-                             o[32 * c + 4 * u + 1], o[32 * c + 4 * u + 2], o[32 * c + 4 * u + 3]);
-              fence_proxy_async_smem();
-              named_bar_sync(6, 128);
-              if (r == 0) {
-                tma_reduce_add_2d(&tm_dq, smem + L::OFF_DST + slot, cc * 32, row);
-                bulk_commit_group();
-              }
+                st_shared_v4(sh + (uint32_t)c * 16384u + sw128_offset(r, (uint32_t)u),
+                             o[32 * c + 4 * u], o[32 * c + 4 * u + 1], o[32 * c + 4 * u + 2],
+                             o[32 * c + 4 * u + 3]);
+            fence_proxy_async_smem();
+            named_bar_sync(6, 128);
+            if (r == 0) {
+              tma_reduce_add_2d(&tm_dq, smem + half_off, 64 * hh, row);
+              tma_reduce_add_2d(&tm_dq, smem + half_off + 16384, 64 * hh + 32, row);
+              bulk_commit_group();
             }
           }
           if (r == 0) {
-            bulk_wait_group_read0();  // the tile may be rewritten with dS^T
-            mbar_arrive(dqs_free);
+            bulk_wait_group_read0();  // the producer may load the stage again
+            mbar_arrive(q_empty + qs);
           }
         }
         ++dqc;

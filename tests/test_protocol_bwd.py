@@ -12,10 +12,14 @@ than its count, and every role must finish.  A planted mistake (both dS^T
 tiles released through one barrier) must be caught.
 
 At d_h = 128 the kernel has no TMEM to spare: one warp issues every product,
-P^T and dS^T overwrite half of the S^T and dP^T columns, dQ's two 64-column
-halves go over the other halves, and dQ is staged through the dS^T tile.  The
-second model restates that path (QST = 2, dv_done / dk_done / dp_full /
-dq_empty / dqhi_empty / dqs_free).  Host logic only.
+P^T and dS^T overwrite half of the S^T and dP^T columns, and dQ's two
+64-column halves go over the other halves.  dQ is staged for its reduce-adds
+in the step's own Q/dO stage, once dV and dK have read it, and the dQ warps
+(not the issuer) release the stage to the producer when the reduce-adds have
+read it; the next step's dS^T stores then need only the dQ products to have
+read the dS^T tile.  The second model restates that path (QST = 2, dv_done /
+dk_done / dp_full / dq_empty / dqhi_empty), and a planted mistake (the dQ
+warps staging before dV has read dO) must be caught.  Host logic only.
 """
 
 import random
@@ -203,7 +207,7 @@ def make_barriers_128():
         b[name] = Barrier(name, count)
     add("kv_full", 1); add("kv_empty", 1)
     for s in range(QST128):
-        add(f"q_full{s}", 1); add(f"q_empty{s}", 1)
+        add(f"q_full{s}", 3); add(f"q_empty{s}", 1)   # Q, dO and -lse/-D land
     add("s_full", 1); add("dp_full", 1)
     add("p_full", 2)
     add("p_empty", 1)
@@ -211,7 +215,6 @@ def make_barriers_128():
     add("dq_empty", 1); add("dqhi_empty", 1)   # dQ low / high half in the dQ warps' registers
     add("kd_full", 1); add("kd_empty", 2)
     add("dv_done", 1); add("dk_done", 1)
-    add("dqs_free", 1)
     return b
 
 
@@ -224,16 +227,17 @@ def producer_128(items):
         for _ in range(n):
             qs = qc % QST128
             yield ("wait", f"q_empty{qs}", qc // QST128 - 1)
-            yield ("tma", f"q_full{qs}", f"Q{qs}", f"q{qc}")
+            for part in ("Q", "O", "L"):
+                yield ("tma", f"q_full{qs}", f"{part}{qs}", f"q{qc}")
             qc += 1
 
 
+# A stage holds Q (region Q{s}), dO (O{s}) and the -lse/-D vectors (L{s}).
 # TMEM regions.  Compute half h reads two groups of 32 query columns of S^T
 # (TSa{h}: the group it then overwrites with its packed P^T; TSb{h}: the other
 # one) and of dP^T (TDPa{h}, then dS^T; TDPb{h}).  dQ's low half goes over
 # TSb0 + TSb1, its high half over TDPb0 + TDPb1.  DST{h} are the halves'
-# columns of the shared dS^T tile, which also stages dQ for the reduce-adds.
-# Tags name the global step u.
+# columns of the shared dS^T tile.  Tags name the global step u.
 def both(region, tag):
     return [(region + "0", tag), (region + "1", tag)]
 
@@ -249,7 +253,7 @@ def issuer_128(items, skip_dq_drain=False):
 
     def issue_dpt(q, i):
         yield ("wait", f"q_full{q % QST128}", q // QST128)
-        yield ("mma", [("KV", f"kv{i}"), (f"Q{q % QST128}", f"q{q}")],
+        yield ("mma", [("KV", f"kv{i}"), (f"O{q % QST128}", f"q{q}")],
                both("TDPa", f"dP{q}") + both("TDPb", f"dP{q}"))
         yield ("commit", "dp_full")
 
@@ -280,7 +284,7 @@ def issuer_128(items, skip_dq_drain=False):
             yield ("commit", "dq_full")
             dqc += 1
             acc_v = [("TDV", f"dv{i}.{t - 1}")] if t > 0 else []
-            yield ("mma", both("TSa", f"P{u}") + [(f"Q{qs}", f"q{u}")] + acc_v,
+            yield ("mma", both("TSa", f"P{u}") + [(f"O{qs}", f"q{u}")] + acc_v,
                    [("TDV", f"dv{i}.{t}")])                     # dV
             yield ("commit", "dv_done")
             dvc += 1
@@ -289,7 +293,7 @@ def issuer_128(items, skip_dq_drain=False):
                    [("TDK", f"dk{i}.{t}")])                     # dK
             yield ("commit", "dk_done")
             dkc += 1
-            yield ("commit", f"q_empty{qs}")
+            # (the stage goes back to the producer from the dQ warps)
             qc += 1
             pc += 1
             if t + 1 < n:
@@ -313,7 +317,7 @@ def compute_128(hf, items):
             qs = qc % QST128
             u = qc
             yield ("wait", f"q_full{qs}", qc // QST128)
-            yield ("read", f"Q{qs}", f"q{u}")           # -lse, -D of the stage
+            yield ("read", f"L{qs}", f"q{u}")           # -lse, -D of the stage
             # first group of query columns (chunk 0), then the second
             # (chunk 32); the packed P^T / dS^T of both go over the first
             # group's columns, read in chunk 0
@@ -324,7 +328,6 @@ def compute_128(hf, items):
             yield ("read", "TDPa" + h, f"dP{u}")
             yield ("write", "TDPa" + h, f"dS{u}")
             yield ("wait", "p_empty", pc - 1)
-            yield ("wait", "dqs_free", pc - 1)
             yield ("write", "DST" + h, f"dS{u}")
             yield ("read", "TSb" + h, f"S{u}")
             yield ("write", "TSa" + h, f"P{u}")
@@ -341,31 +344,41 @@ def compute_128(hf, items):
         kdc += 1
 
 
-def dq_warps_128(items):
+def dq_warps_128(items, early_stage=False):
     dqc = 0
     u = 0
     for n in items:
         for _ in range(n):
+            qs = u % QST128
             yield ("wait", "dq_full", dqc)
-            for half, region, bar in (("lo", "TSb", "dq_empty"), ("hi", "TDPb", "dqhi_empty")):
-                yield ("read", region + "0", f"dQ{half}{u}")
-                yield ("read", region + "1", f"dQ{half}{u}")
-                yield ("arrive", bar, 1)           # this half is in registers
-                # staged through the dS^T tile (both dQ products have read it),
-                # then read by the tensor reduce-adds
-                yield ("write", "DST0", f"dQs{half}{u}")
-                yield ("write", "DST1", f"dQs{half}{u}")
-                yield ("read", "DST0", f"dQs{half}{u}")
-                yield ("read", "DST1", f"dQs{half}{u}")
-            yield ("arrive", "dqs_free", 1)
+            # low half into registers; its staging goes where dO was, so dV
+            # must have read the stage first (planted: not waited for)
+            yield ("read", "TSb0", f"dQlo{u}")
+            yield ("read", "TSb1", f"dQlo{u}")
+            if not early_stage:
+                yield ("wait", "dv_done", dqc)
+            yield ("arrive", "dq_empty", 1)
+            yield ("write", f"O{qs}", f"dQs{u}")
+            # high half; its staging goes where Q was, after dK has read it
+            yield ("read", "TDPb0", f"dQhi{u}")
+            yield ("read", "TDPb1", f"dQhi{u}")
+            yield ("wait", "dk_done", dqc)
+            yield ("arrive", "dqhi_empty", 1)
+            yield ("write", f"Q{qs}", f"dQs{u}")
+            # the tensor reduce-adds read the staged rows; then the stage
+            # goes back to the producer
+            yield ("read", f"O{qs}", f"dQs{u}")
+            yield ("read", f"Q{qs}", f"dQs{u}")
+            yield ("arrive", f"q_empty{qs}", 1)
             dqc += 1
             u += 1
 
 
-def run_model_128(items, rng, skip_dq_drain=False):
+def run_model_128(items, rng, skip_dq_drain=False, early_stage=False):
     roles = {
         "prod": producer_128(items), "g": issuer_128(items, skip_dq_drain),
-        "c0": compute_128(0, items), "c1": compute_128(1, items), "dq": dq_warps_128(items),
+        "c0": compute_128(0, items), "c1": compute_128(1, items),
+        "dq": dq_warps_128(items, early_stage),
     }
     run_roles(roles, make_barriers_128(), ("g",), rng)
 
@@ -386,6 +399,19 @@ def test_planted_skipped_dq_drain_is_caught():
     for _ in range(200):
         try:
             run_model_128(random_items(rng, rng.randint(2, 10)), rng, skip_dq_drain=True)
+        except Violation:
+            caught += 1
+    assert caught >= 10
+
+
+def test_planted_staging_before_dv_read_is_caught():
+    # The dQ warps staging dQ over the stage before dV has read dO: a dV
+    # product then reads staged dQ where it expects dO.
+    rng = random.Random(23)
+    caught = 0
+    for _ in range(200):
+        try:
+            run_model_128(random_items(rng, rng.randint(2, 10)), rng, early_stage=True)
         except Violation:
             caught += 1
     assert caught >= 10
