@@ -59,8 +59,8 @@ struct BwdSmem {
   // d_h <= 64: P^T goes to spare TMEM columns (TS MMA for dV) and dS^T to
   // shared memory (SS MMAs for dK, dQ), so the S^T/dP^T columns are free as
   // soon as the compute warps have loaded them and the next step's scores
-  // overlap this step's softmax.  d_h = 128 writes P^T and dS^T over the
-  // S^T/dP^T columns (TS MMAs for dV, dK); dS^T also goes to shared memory.
+  // overlap this step's softmax.  d_h = 128 writes P^T and dS^T packed over
+  // the S^T columns (TS MMAs for dV, dK); dS^T also goes to shared memory.
   static constexpr bool PS = !DQ_ALIAS;
   // Q_I, dO_I stages; d_h = 128 keeps two stages by dropping the alignment
   // slack (the dynamic shared base is checked at run time instead).
@@ -80,32 +80,32 @@ struct BwdSmem {
   static constexpr int DST_BUFS = PS ? 2 : 1;
   static constexpr int OFF_DQS = OFF_DST + DST_BUFS * SqTile::BYTES;
   static constexpr int OFF_BAR = OFF_DQS + DQS_BYTES;
-  static constexpr int NBAR = 2 + 2 * QST + 16;
+  static constexpr int NBAR = 2 + 2 * QST + 15;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int SLACK = (BYTES + 1024 <= 232448) ? 1024 : 0;
   static constexpr int ALLOC = BYTES + SLACK;
   static_assert(ALLOC <= 232448, "shared memory budget exceeded");
   // TMEM columns.  S^T (fp32) at 0, dP^T at 128, then dV and dK.
-  // d_h = 128: compute half hf reads query columns 32hf..32hf+31 and
-  // 64+32hf..64+32hf+31 of S^T and dP^T and writes its packed P^T (dS^T) over
-  // the first 32 of them, so P^T fills columns 0..63 and dS^T 128..191; the
-  // two 64-column halves of dQ then go to the columns both halves have read
-  // and nothing else uses until the next step: 64..127 and 192..255.
+  // d_h = 128: compute half hf reads the groups of 32 query columns
+  // 32hf..32hf+31 and 64+32hf..64+32hf+31 of S^T and dP^T; into each S^T
+  // group, once read, it writes the group's P^T packed as bf16 pairs (16
+  // columns) and then its dS^T (the other 16).  The whole dP^T region is then
+  // free, and dQ (one N = 128 product) goes there.
   static constexpr uint32_t T_S = 0, T_DP = 128;
   static constexpr uint32_t T_DV = 256, T_DK = 256 + D;
-  static constexpr uint32_t T_DQ = 256 + 2 * D;                // d_h <= 64
-  static constexpr uint32_t T_DQ_LO = 64, T_DQ_HI = 192;       // d_h = 128
+  static constexpr uint32_t T_DQ = (D == 128) ? T_DP : 256 + 2 * D;
   // PS: P^T as packed bf16 (query columns 2c, 2c+1 in column T_PT + c), the
   // TMEM A operand of dV; 64 columns, free for d_h <= 64.
   static constexpr uint32_t T_PT = 256 + 3 * D;
   static_assert(!PS || T_PT + 64 <= 512, "P^T does not fit in TMEM");
-  // d_h = 128: packed column of the P^T / dS^T k-step kk (query columns
-  // 16kk..16kk+15): written by half (kk >> 1) & 1, in its first (kk < 4) or
-  // second group of 32 query columns.
+  // d_h = 128: packed P^T column of the k-step kk (query columns
+  // 16kk..16kk+15), in the S^T group of 32 columns that holds them (half
+  // (kk >> 1) & 1, group kk >> 2); dS^T of the same k-step 16 columns on.
   __device__ static __forceinline__ uint32_t a_col(int kk) {
-    return (uint32_t)(32 * ((kk >> 1) & 1) + 16 * (kk >> 2) + 8 * (kk & 1));
+    return (uint32_t)(32 * ((kk >> 1) & 1) + 64 * (kk >> 2) + 8 * (kk & 1));
   }
+  static constexpr uint32_t DS_OFF = 16;
 };
 
 enum : int {
@@ -200,11 +200,8 @@ __global__ void __launch_bounds__(512, 1)
   // DQ_ALIAS: the step's dV has read P^T and dO (dk_done: dK, dS^T and Q)
   uint64_t* dv_done = dp_full + 1;
   uint64_t* dk_done = dv_done + 1;
-  // DQ_ALIAS: dq_empty is dQ's low 64 columns taken into the dQ warps'
-  // registers, dqhi_empty its high 64 columns
-  uint64_t* dqhi_empty = dk_done + 1;
   // per MMA-issuing warp (1, 3): all its products done, before TMEM is freed
-  uint64_t* mma_drained = dqhi_empty + 1;
+  uint64_t* mma_drained = dk_done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
   const WaitCtl wc{abort_flag, p.status};
@@ -227,7 +224,6 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(dp_full, 1);
     mbar_init(dv_done, 1);
     mbar_init(dk_done, 1);
-    mbar_init(dqhi_empty, 128);
     mbar_init(mma_drained, 1);
     mbar_init(mma_drained + 1, 1);
     *abort_flag = 0;
@@ -361,24 +357,22 @@ __global__ void __launch_bounds__(512, 1)
           }
         }
       }
-      // d_h = 128: per step dQ (two N = 64 halves into the columns the
-      // compute left free), then dV and dK.  The next step's S^T goes out
-      // once dV has read P^T and the dQ warps hold dQ's low half, its dP^T
-      // once dK has read dS^T and they hold the high half; the reduce-adds
-      // of dQ then run while the next step computes.
-      constexpr uint32_t id_dq64 = idesc_bf16(128, 64, true, true);
-      uint32_t dvc = 0, dkc = 0;
+      // d_h = 128: per step dQ (one N = 128 product into the dP^T columns the
+      // compute has read), then dV and dK.  The next step's S^T goes out once
+      // dK has completed (dV and dK read P^T and dS^T from the S^T columns;
+      // this warp's products complete in issue order, so the wait only makes
+      // the order explicit), its dP^T once the dQ warps have taken dQ out of
+      // TMEM; the reduce-adds of dQ then run while the next step computes.
+      constexpr uint32_t id_dq = idesc_bf16(128, 128, true, true);
+      uint32_t dkc = 0;
       for (int kr = 0, it = snake_item(0, blockIdx.x, gridDim.x); !L::PS && it < p.n_items;
            it = snake_item(++kr, blockIdx.x, gridDim.x)) {
         const BItem w = decode_bwd(p, it);
         mbar_wait(kv_full, kvc & 1, wc, kSiteBMmaKV);
         ++kvc;
-        // the previous step's dV / dK done and its dQ halves in the dQ warps
-        if (dvc > 0) mbar_wait(dv_done, (dvc - 1) & 1, wc, kSiteBMmaTS);
-        if (dqc > 0) mbar_wait(dq_empty, (dqc - 1) & 1, wc, kSiteBMmaDQ);
-        issue_st(qc);
         if (dkc > 0) mbar_wait(dk_done, (dkc - 1) & 1, wc, kSiteBMmaTS);
-        if (dqc > 0) mbar_wait(dqhi_empty, (dqc - 1) & 1, wc, kSiteBMmaDQ);
+        issue_st(qc);
+        if (dqc > 0) mbar_wait(dq_empty, (dqc - 1) & 1, wc, kSiteBMmaDQ);
         issue_dpt(qc);
         for (int t = 0; t < w.nsteps; ++t) {
           const int qs = qc % L::QST;
@@ -387,16 +381,11 @@ __global__ void __launch_bounds__(512, 1)
           mbar_wait(p_full, pc & 1, wc, kSiteBMmaP);
           if (t == 0) mbar_wait(kd_empty, (kdc & 1) ^ 1, wc, kSiteBMmaKD);
           tc_fence_after();
-          // dQ_I = dS K_J: A the dS^T tile (MN-major), B the two 64-column
-          // halves of K_J
+          // dQ_I = dS K_J: A the dS^T tile (MN-major), B K_J (MN-major)
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ss(tmem + L::T_DQ_LO, SqTile::mnmajor_desc(sDST, kk), G::mnmajor_desc(sK, kk),
-                        id_dq64, kk > 0);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ss(tmem + L::T_DQ_HI, SqTile::mnmajor_desc(sDST, kk),
-                        G::mnmajor_desc(sK + G::CHUNK_BYTES, kk), id_dq64, kk > 0);
+            mma_bf16_ss(tmem + L::T_DQ, SqTile::mnmajor_desc(sDST, kk), G::mnmajor_desc(sK, kk),
+                        id_dq, kk > 0);
           mma_commit(p_empty);  // the dS^T tile has been read
           mma_commit(dq_full);
           ++dqc;
@@ -405,22 +394,19 @@ __global__ void __launch_bounds__(512, 1)
             mma_bf16_ts(tmem + L::T_DV, tmem + L::T_S + L::a_col(kk), G::mnmajor_desc(sDO, kk),
                         id_acc, (t > 0 || kk > 0));
           mma_commit(dv_done);
-          ++dvc;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ts(tmem + L::T_DK, tmem + L::T_DP + L::a_col(kk), G::mnmajor_desc(sQ, kk),
-                        id_acc, (t > 0 || kk > 0));
+            mma_bf16_ts(tmem + L::T_DK, tmem + L::T_S + L::a_col(kk) + L::DS_OFF,
+                        G::mnmajor_desc(sQ, kk), id_acc, (t > 0 || kk > 0));
           mma_commit(dk_done);
           ++dkc;
           // (the dQ warps stage dQ in this stage and then release it)
           ++qc;
           ++pc;
           if (t + 1 < w.nsteps) {
-            mbar_wait(dv_done, (dvc - 1) & 1, wc, kSiteBMmaTS);      // P^T read
-            mbar_wait(dq_empty, (dqc - 1) & 1, wc, kSiteBMmaDQ);     // dQ low half held
+            mbar_wait(dk_done, (dkc - 1) & 1, wc, kSiteBMmaTS);      // P^T, dS^T read
             issue_st(qc);
-            mbar_wait(dk_done, (dkc - 1) & 1, wc, kSiteBMmaTS);      // dS^T read
-            mbar_wait(dqhi_empty, (dqc - 1) & 1, wc, kSiteBMmaDQ);   // dQ high half held
+            mbar_wait(dq_empty, (dqc - 1) & 1, wc, kSiteBMmaDQ);     // dQ out of TMEM
             issue_dpt(qc);
           }
         }
@@ -597,9 +583,9 @@ __global__ void __launch_bounds__(512, 1)
               pk[k >> 1] = pack_bf16x2(p0, p1);
             }
           }
-          // P^T over this half's first S^T columns, already read (TMEM A
+          // P^T over the first 16 of the S^T columns just read (TMEM A
           // operand of dV)
-          tmem_st_x16(trow + L::T_S + 32 * hf + (c0 >> 1), pk);
+          tmem_st_x16(trow + L::T_S + col, pk);
           if (c0 == 0 && L::DQ_ALIAS) {
             mbar_wait(dp_full, sc & 1, wc, kSiteBCmpS);
             tc_fence_after();
@@ -621,9 +607,9 @@ __global__ void __launch_bounds__(512, 1)
               dk[k >> 1] = pack_bf16x2_f2(g2);
             }
           }
-          // dS^T over this half's first dP^T columns, already read (A
-          // operand of dK), and into shared memory for dQ
-          tmem_st_x16(trow + L::T_DP + 32 * hf + (c0 >> 1), dk);
+          // dS^T over the other 16 of them (A operand of dK), and into
+          // shared memory for dQ
+          tmem_st_x16(trow + L::T_S + col + L::DS_OFF, dk);
           // the dS^T tile in shared memory is read by the previous step's dQ
           if (c0 == 0) mbar_wait(p_empty, (pc & 1) ^ 1, wc, kSiteBCmpP);
 #pragma unroll
@@ -726,15 +712,15 @@ __global__ void __launch_bounds__(512, 1)
             }
           }
         } else {
-          // d_h = 128: each 64-column half of dQ is loaded and its TMEM
-          // columns released (the next step's S^T or dP^T goes there), then
-          // staged in this step's Q_I/dO_I stage, the low half over dO_I once
-          // dV has read it and the high half over Q_I once dK has, and added
-          // with one tensor reduce-add per 32-column chunk.  Waiting for dV
-          // (dK) before releasing the half also keeps dv_done (dk_done) from
-          // running two phases ahead of this wait: the next step's S^T (dP^T)
-          // waits for the release.  The stage goes back to the producer once
-          // the reduce-adds have read it.
+          // d_h = 128: dQ is loaded 64 columns at a time and staged in this
+          // step's Q_I/dO_I stage, the low half over dO_I once dV has read it
+          // and the high half over Q_I once dK has, with one tensor
+          // reduce-add per 32-column chunk.  The TMEM columns (the next
+          // step's dP^T goes there) are released once both halves are out;
+          // waiting for dK first also keeps dk_done (and dv_done) from
+          // running two phases ahead of these waits, since the next step's
+          // dP^T waits for the release.  The stage goes back to the producer
+          // once the reduce-adds have read it.
           const int qs = (int)(dqc % (uint32_t)L::QST);
           const int row = (w.b * H + hq) * T + I * 128;
           const int stage_off = L::OFF_Q + qs * L::STAGE;
@@ -744,15 +730,17 @@ __global__ void __launch_bounds__(512, 1)
             {
               uint32_t (&o0)[32] = *reinterpret_cast<uint32_t(*)[32]>(o);
               uint32_t (&o1)[32] = *reinterpret_cast<uint32_t(*)[32]>(o + 32);
-              const uint32_t src = tmem + lane_base + (hh ? L::T_DQ_HI : L::T_DQ_LO);
+              const uint32_t src = tmem + lane_base + L::T_DQ + 64u * (uint32_t)hh;
               tmem_ld_x32(src, o0);
               tmem_ld_x32(src + 32, o1);
               tmem_wait_ld(o0);
               tmem_wait_ld(o1);
             }
-            tc_fence_before();
             mbar_wait(hh ? dk_done : dv_done, dqc & 1, wc, kSiteBDq);
-            mbar_arrive(hh ? dqhi_empty : dq_empty);  // this half is in registers
+            if (hh) {
+              tc_fence_before();
+              mbar_arrive(dq_empty);  // all of dQ is out of TMEM
+            }
             // low half: dO_I's two 16 KB chunks; high half: Q_I's
             const int half_off = stage_off + (hh ? 0 : G::TILE_BYTES);
             const uint32_t sh = smem_u32(smem + half_off);

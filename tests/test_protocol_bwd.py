@@ -12,14 +12,14 @@ than its count, and every role must finish.  A planted mistake (both dS^T
 tiles released through one barrier) must be caught.
 
 At d_h = 128 the kernel has no TMEM to spare: one warp issues every product,
-P^T and dS^T overwrite half of the S^T and dP^T columns, and dQ's two
-64-column halves go over the other halves.  dQ is staged for its reduce-adds
-in the step's own Q/dO stage, once dV and dK have read it, and the dQ warps
-(not the issuer) release the stage to the producer when the reduce-adds have
-read it; the next step's dS^T stores then need only the dQ products to have
-read the dS^T tile.  The second model restates that path (QST = 2, dv_done /
-dk_done / dp_full / dq_empty / dqhi_empty), and a planted mistake (the dQ
-warps staging before dV has read dO) must be caught.  Host logic only.
+P^T and dS^T go packed over the S^T columns the compute has read, and dQ
+over the whole dP^T region.  dQ is staged for its reduce-adds in the step's
+own Q/dO stage, once dV and dK have read it, and the dQ warps (not the
+issuer) release the stage to the producer when the reduce-adds have read it.
+The second model restates that path (QST = 2, dv_done / dk_done / dp_full /
+dq_empty), and two planted mistakes (the next dP^T issued before dQ has left
+its columns; the dQ warps staging before dV has read dO) must be caught.
+Host logic only.
 """
 
 import random
@@ -212,7 +212,7 @@ def make_barriers_128():
     add("p_full", 2)
     add("p_empty", 1)
     add("dq_full", 1)
-    add("dq_empty", 1); add("dqhi_empty", 1)   # dQ low / high half in the dQ warps' registers
+    add("dq_empty", 1)                 # all of dQ taken from TMEM by the dQ warps
     add("kd_full", 1); add("kd_empty", 2)
     add("dv_done", 1); add("dk_done", 1)
     return b
@@ -233,13 +233,18 @@ def producer_128(items):
 
 
 # A stage holds Q (region Q{s}), dO (O{s}) and the -lse/-D vectors (L{s}).
-# TMEM regions.  Compute half h reads two groups of 32 query columns of S^T
-# (TSa{h}: the group it then overwrites with its packed P^T; TSb{h}: the other
-# one) and of dP^T (TDPa{h}, then dS^T; TDPb{h}).  dQ's low half goes over
-# TSb0 + TSb1, its high half over TDPb0 + TDPb1.  DST{h} are the halves'
-# columns of the shared dS^T tile.  Tags name the global step u.
-def both(region, tag):
-    return [(region + "0", tag), (region + "1", tag)]
+# TMEM regions.  Compute half h reads two groups of 32 query columns of S^T,
+# g = a then b (TS{g}{h}), and the same groups of dP^T (TDP{g}{h}); into each
+# S^T group it has read it writes its packed P^T (TS{g}{h}P, the group's first
+# 16 columns) and dS^T (TS{g}{h}D, the other 16).  dQ then goes over the whole
+# dP^T region.  DST{h} are the halves' columns of the shared dS^T tile.  Tags
+# name the global step u.
+def s_cols(tag):
+    return [(f"TS{g}{h}{x}", tag) for g in "ab" for h in "01" for x in "PD"]
+
+
+def dp_cols(tag):
+    return [(f"TDP{g}{h}", tag) for g in "ab" for h in "01"]
 
 
 def issuer_128(items, skip_dq_drain=False):
@@ -247,28 +252,25 @@ def issuer_128(items, skip_dq_drain=False):
 
     def issue_st(q, i):
         yield ("wait", f"q_full{q % QST128}", q // QST128)
-        yield ("mma", [("KV", f"kv{i}"), (f"Q{q % QST128}", f"q{q}")],
-               both("TSa", f"S{q}") + both("TSb", f"S{q}"))
+        yield ("mma", [("KV", f"kv{i}"), (f"Q{q % QST128}", f"q{q}")], s_cols(f"S{q}"))
         yield ("commit", "s_full")
 
     def issue_dpt(q, i):
         yield ("wait", f"q_full{q % QST128}", q // QST128)
-        yield ("mma", [("KV", f"kv{i}"), (f"O{q % QST128}", f"q{q}")],
-               both("TDPa", f"dP{q}") + both("TDPb", f"dP{q}"))
+        yield ("mma", [("KV", f"kv{i}"), (f"O{q % QST128}", f"q{q}")], dp_cols(f"dP{q}"))
         yield ("commit", "dp_full")
 
     for i, n in enumerate(items):
         yield ("wait", "kv_full", kvc)
         kvc += 1
-        if dvc > 0:
-            yield ("wait", "dv_done", dvc - 1)
-        if dqc > 0 and not skip_dq_drain:
-            yield ("wait", "dq_empty", dqc - 1)
-        yield from issue_st(qc, i)
+        # the previous step's dV and dK have read P^T and dS^T (products of
+        # this warp complete in issue order, so the wait is kept only to make
+        # the order explicit), and dQ has left the dP^T columns
         if dkc > 0:
             yield ("wait", "dk_done", dkc - 1)
-        if dqc > 0:
-            yield ("wait", "dqhi_empty", dqc - 1)
+        yield from issue_st(qc, i)
+        if dqc > 0 and not skip_dq_drain:
+            yield ("wait", "dq_empty", dqc - 1)
         yield from issue_dpt(qc, i)
         for t in range(n):
             qs = qc % QST128
@@ -276,33 +278,29 @@ def issuer_128(items, skip_dq_drain=False):
             yield ("wait", "p_full", pc)
             if t == 0:
                 yield ("wait", "kd_empty", kdc - 1)
-            yield ("mma", both("DST", f"dS{u}") + [("KV", f"kv{i}")],
-                   both("TSb", f"dQlo{u}"))                     # dQ, low half
-            yield ("mma", both("DST", f"dS{u}") + [("KV", f"kv{i}")],
-                   both("TDPb", f"dQhi{u}"))                    # dQ, high half
+            yield ("mma", [("DST0", f"dS{u}"), ("DST1", f"dS{u}"), ("KV", f"kv{i}")],
+                   dp_cols(f"dQ{u}"))                           # dQ
             yield ("commit", "p_empty")
             yield ("commit", "dq_full")
             dqc += 1
             acc_v = [("TDV", f"dv{i}.{t - 1}")] if t > 0 else []
-            yield ("mma", both("TSa", f"P{u}") + [(f"O{qs}", f"q{u}")] + acc_v,
-                   [("TDV", f"dv{i}.{t}")])                     # dV
+            pt = [(f"TS{g}{h}P", f"P{u}") for g in "ab" for h in "01"]
+            yield ("mma", pt + [(f"O{qs}", f"q{u}")] + acc_v, [("TDV", f"dv{i}.{t}")])   # dV
             yield ("commit", "dv_done")
             dvc += 1
             acc_k = [("TDK", f"dk{i}.{t - 1}")] if t > 0 else []
-            yield ("mma", both("TDPa", f"dS{u}") + [(f"Q{qs}", f"q{u}")] + acc_k,
-                   [("TDK", f"dk{i}.{t}")])                     # dK
+            dst = [(f"TS{g}{h}D", f"dS{u}") for g in "ab" for h in "01"]
+            yield ("mma", dst + [(f"Q{qs}", f"q{u}")] + acc_k, [("TDK", f"dk{i}.{t}")])  # dK
             yield ("commit", "dk_done")
             dkc += 1
             # (the stage goes back to the producer from the dQ warps)
             qc += 1
             pc += 1
             if t + 1 < n:
-                yield ("wait", "dv_done", dvc - 1)
+                yield ("wait", "dk_done", dkc - 1)
+                yield from issue_st(qc, i)
                 if not skip_dq_drain:
                     yield ("wait", "dq_empty", dqc - 1)
-                yield from issue_st(qc, i)
-                yield ("wait", "dk_done", dkc - 1)
-                yield ("wait", "dqhi_empty", dqc - 1)
                 yield from issue_dpt(qc, i)
         yield ("commit", "kd_full")
         yield ("commit", "kv_empty")
@@ -318,22 +316,20 @@ def compute_128(hf, items):
             u = qc
             yield ("wait", f"q_full{qs}", qc // QST128)
             yield ("read", f"L{qs}", f"q{u}")           # -lse, -D of the stage
-            # first group of query columns (chunk 0), then the second
-            # (chunk 32); the packed P^T / dS^T of both go over the first
-            # group's columns, read in chunk 0
             yield ("wait", "s_full", sc)
-            yield ("read", "TSa" + h, f"S{u}")
-            yield ("write", "TSa" + h, f"P{u}")
-            yield ("wait", "dp_full", sc)
-            yield ("read", "TDPa" + h, f"dP{u}")
-            yield ("write", "TDPa" + h, f"dS{u}")
-            yield ("wait", "p_empty", pc - 1)
-            yield ("write", "DST" + h, f"dS{u}")
-            yield ("read", "TSb" + h, f"S{u}")
-            yield ("write", "TSa" + h, f"P{u}")
-            yield ("read", "TDPb" + h, f"dP{u}")
-            yield ("write", "TDPa" + h, f"dS{u}")
-            yield ("write", "DST" + h, f"dS{u}")
+            for g in "ab":
+                # P from this group of S^T, then dS from the same group of
+                # dP^T; both packed over the S^T group just read
+                yield ("read", f"TS{g}{h}P", f"S{u}")
+                yield ("read", f"TS{g}{h}D", f"S{u}")
+                yield ("write", f"TS{g}{h}P", f"P{u}")
+                if g == "a":
+                    yield ("wait", "dp_full", sc)
+                yield ("read", f"TDP{g}{h}", f"dP{u}")
+                yield ("write", f"TS{g}{h}D", f"dS{u}")
+                if g == "a":
+                    yield ("wait", "p_empty", pc - 1)
+                yield ("write", "DST" + h, f"dS{u}")
             yield ("arrive", "p_full", 1)
             qc += 1
             sc += 1
@@ -351,19 +347,19 @@ def dq_warps_128(items, early_stage=False):
         for _ in range(n):
             qs = u % QST128
             yield ("wait", "dq_full", dqc)
-            # low half into registers; its staging goes where dO was, so dV
-            # must have read the stage first (planted: not waited for)
-            yield ("read", "TSb0", f"dQlo{u}")
-            yield ("read", "TSb1", f"dQlo{u}")
+            # low 64 columns into registers, staged where dO was once dV
+            # has read it (planted: not waited for)
+            for g in "ab":
+                yield ("read", f"TDP{g}0", f"dQ{u}")
             if not early_stage:
                 yield ("wait", "dv_done", dqc)
-            yield ("arrive", "dq_empty", 1)
             yield ("write", f"O{qs}", f"dQs{u}")
-            # high half; its staging goes where Q was, after dK has read it
-            yield ("read", "TDPb0", f"dQhi{u}")
-            yield ("read", "TDPb1", f"dQhi{u}")
+            # high 64 columns; all of dQ has then left TMEM.  Waiting for dK
+            # first keeps dk_done from running two phases ahead of this wait.
+            for g in "ab":
+                yield ("read", f"TDP{g}1", f"dQ{u}")
             yield ("wait", "dk_done", dqc)
-            yield ("arrive", "dqhi_empty", 1)
+            yield ("arrive", "dq_empty", 1)
             yield ("write", f"Q{qs}", f"dQs{u}")
             # the tensor reduce-adds read the staged rows; then the stage
             # goes back to the producer
@@ -391,9 +387,9 @@ def test_backward_128_protocol_holds(seed):
 
 
 def test_planted_skipped_dq_drain_is_caught():
-    # The next step's S^T issued without waiting for the dQ warps to hold
-    # dQ's low half, whose columns it overwrites: a dQ read then finds S^T
-    # there, or the phases of dq_empty run ahead of their waiter.
+    # The next step's dP^T issued without waiting for the dQ warps to take dQ
+    # out of the dP^T columns: a dQ read then finds dP^T there, or the phases
+    # of dq_empty run ahead of their waiter.
     rng = random.Random(17)
     caught = 0
     for _ in range(200):
