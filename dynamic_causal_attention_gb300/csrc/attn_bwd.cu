@@ -386,7 +386,6 @@ __global__ void __launch_bounds__(512, 1)
           for (int kk = 0; kk < 8; ++kk)
             mma_bf16_ss(tmem + L::T_DQ, SqTile::mnmajor_desc(sDST, kk), G::mnmajor_desc(sK, kk),
                         id_dq, kk > 0);
-          mma_commit(p_empty);  // the dS^T tile has been read
           mma_commit(dq_full);
           ++dqc;
 #pragma unroll
@@ -610,8 +609,9 @@ __global__ void __launch_bounds__(512, 1)
           // dS^T over the other 16 of them (A operand of dK), and into
           // shared memory for dQ
           tmem_st_x16(trow + L::T_S + col + L::DS_OFF, dk);
-          // the dS^T tile in shared memory is read by the previous step's dQ
-          if (c0 == 0) mbar_wait(p_empty, (pc & 1) ^ 1, wc, kSiteBCmpP);
+          // the dS^T tile in shared memory was read by the previous step's
+          // dQ, which completed before this step's S^T (one issuing thread,
+          // so s_full's commit covers it)
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const uint32_t unit = (uint32_t)(col >> 3) + u;

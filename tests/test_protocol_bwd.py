@@ -210,7 +210,6 @@ def make_barriers_128():
         add(f"q_full{s}", 3); add(f"q_empty{s}", 1)   # Q, dO and -lse/-D land
     add("s_full", 1); add("dp_full", 1)
     add("p_full", 2)
-    add("p_empty", 1)
     add("dq_full", 1)
     add("dq_empty", 1)                 # all of dQ taken from TMEM by the dQ warps
     add("kd_full", 1); add("kd_empty", 2)
@@ -280,7 +279,6 @@ def issuer_128(items, skip_dq_drain=False):
                 yield ("wait", "kd_empty", kdc - 1)
             yield ("mma", [("DST0", f"dS{u}"), ("DST1", f"dS{u}"), ("KV", f"kv{i}")],
                    dp_cols(f"dQ{u}"))                           # dQ
-            yield ("commit", "p_empty")
             yield ("commit", "dq_full")
             dqc += 1
             acc_v = [("TDV", f"dv{i}.{t - 1}")] if t > 0 else []
@@ -327,8 +325,8 @@ def compute_128(hf, items):
                     yield ("wait", "dp_full", sc)
                 yield ("read", f"TDP{g}{h}", f"dP{u}")
                 yield ("write", f"TS{g}{h}D", f"dS{u}")
-                if g == "a":
-                    yield ("wait", "p_empty", pc - 1)
+                # the previous step's dQ has read the dS^T tile: its commit
+                # precedes this step's s_full, waited for above
                 yield ("write", "DST" + h, f"dS{u}")
             yield ("arrive", "p_full", 1)
             qc += 1
