@@ -80,7 +80,7 @@ struct BwdSmem {
   static constexpr int DST_BUFS = PS ? 2 : 1;
   static constexpr int OFF_DQS = OFF_DST + DST_BUFS * SqTile::BYTES;
   static constexpr int OFF_BAR = OFF_DQS + DQS_BYTES;
-  static constexpr int NBAR = 2 + 2 * QST + 15;
+  static constexpr int NBAR = 2 + 2 * QST + 16;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int SLACK = (BYTES + 1024 <= 232448) ? 1024 : 0;
@@ -200,8 +200,11 @@ __global__ void __launch_bounds__(512, 1)
   // DQ_ALIAS: the step's dV has read P^T and dO (dk_done: dK, dS^T and Q)
   uint64_t* dv_done = dp_full + 1;
   uint64_t* dk_done = dv_done + 1;
+  // DQ_ALIAS: p_full is the first group of query columns of both compute
+  // halves done (P^T and dS^T in TMEM), p_full1 the second (and the dS^T tile)
+  uint64_t* p_full1 = dk_done + 1;
   // per MMA-issuing warp (1, 3): all its products done, before TMEM is freed
-  uint64_t* mma_drained = dk_done + 1;
+  uint64_t* mma_drained = p_full1 + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
   const WaitCtl wc{abort_flag, p.status};
@@ -224,6 +227,7 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(dp_full, 1);
     mbar_init(dv_done, 1);
     mbar_init(dk_done, 1);
+    mbar_init(p_full1, 256);
     mbar_init(mma_drained, 1);
     mbar_init(mma_drained + 1, 1);
     *abort_flag = 0;
@@ -378,8 +382,20 @@ __global__ void __launch_bounds__(512, 1)
           const int qs = qc % L::QST;
           const uint32_t sQ = smem_u32(smem + L::OFF_Q + qs * L::STAGE);
           const uint32_t sDO = sQ + G::TILE_BYTES;
+          // dV and dK over the k-steps of the first group of query columns
+          // (0..63) while the compute works on the second
           mbar_wait(p_full, pc & 1, wc, kSiteBMmaP);
           if (t == 0) mbar_wait(kd_empty, (kdc & 1) ^ 1, wc, kSiteBMmaKD);
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ts(tmem + L::T_DV, tmem + L::T_S + L::a_col(kk), G::mnmajor_desc(sDO, kk),
+                        id_acc, (t > 0 || kk > 0));
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ts(tmem + L::T_DK, tmem + L::T_S + L::a_col(kk) + L::DS_OFF,
+                        G::mnmajor_desc(sQ, kk), id_acc, (t > 0 || kk > 0));
+          mbar_wait(p_full1, pc & 1, wc, kSiteBMmaP);
           tc_fence_after();
           // dQ_I = dS K_J: A the dS^T tile (MN-major), B K_J (MN-major)
 #pragma unroll
@@ -389,14 +405,14 @@ __global__ void __launch_bounds__(512, 1)
           mma_commit(dq_full);
           ++dqc;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
+          for (int kk = 4; kk < 8; ++kk)
             mma_bf16_ts(tmem + L::T_DV, tmem + L::T_S + L::a_col(kk), G::mnmajor_desc(sDO, kk),
-                        id_acc, (t > 0 || kk > 0));
+                        id_acc, true);
           mma_commit(dv_done);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
+          for (int kk = 4; kk < 8; ++kk)
             mma_bf16_ts(tmem + L::T_DK, tmem + L::T_S + L::a_col(kk) + L::DS_OFF,
-                        G::mnmajor_desc(sQ, kk), id_acc, (t > 0 || kk > 0));
+                        G::mnmajor_desc(sQ, kk), id_acc, true);
           mma_commit(dk_done);
           ++dkc;
           // (the dQ warps stage dQ in this stage and then release it)
@@ -618,11 +634,18 @@ __global__ void __launch_bounds__(512, 1)
             st_shared_v4(SqTile::unit_addr(sDST, r, unit), dk[4 * u], dk[4 * u + 1],
                          dk[4 * u + 2], dk[4 * u + 3]);
           }
+          if (c0 == 0) {
+            // the first group's P^T and dS^T are in TMEM: dV and dK take
+            // their k-steps 0..3 while this thread does the second group
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(p_full);
+          }
         }
         if constexpr (!L::PS) tmem_wait_st();
         tc_fence_before();
         fence_proxy_async_smem();
-        mbar_arrive(p_full);
+        mbar_arrive(L::PS ? p_full : p_full1);
         ++qc;
         ++sc;
         ++pc;

@@ -16,9 +16,13 @@ P^T and dS^T go packed over the S^T columns the compute has read, and dQ
 over the whole dP^T region.  dQ is staged for its reduce-adds in the step's
 own Q/dO stage, once dV and dK have read it, and the dQ warps (not the
 issuer) release the stage to the producer when the reduce-adds have read it.
-The second model restates that path (QST = 2, dv_done / dk_done / dp_full /
-dq_empty), and two planted mistakes (the next dP^T issued before dQ has left
-its columns; the dQ warps staging before dV has read dO) must be caught.
+The compute signals each of its two groups of query columns (p_full0,
+p_full1): dV and dK take the first group's k-steps while the compute works on
+the second.  The second model restates that path (QST = 2, dv_done / dk_done
+/ dp_full / dq_empty), and three planted mistakes (the next dP^T issued
+before dQ has left its columns; the dQ warps staging before dV has read dO;
+the second group's products issued after the first group only) must be
+caught.
 Host logic only.
 """
 
@@ -209,7 +213,7 @@ def make_barriers_128():
     for s in range(QST128):
         add(f"q_full{s}", 3); add(f"q_empty{s}", 1)   # Q, dO and -lse/-D land
     add("s_full", 1); add("dp_full", 1)
-    add("p_full", 2)
+    add("p_full0", 2); add("p_full1", 2)   # first / second group of each half done
     add("dq_full", 1)
     add("dq_empty", 1)                 # all of dQ taken from TMEM by the dQ warps
     add("kd_full", 1); add("kd_empty", 2)
@@ -246,7 +250,7 @@ def dp_cols(tag):
     return [(f"TDP{g}{h}", tag) for g in "ab" for h in "01"]
 
 
-def issuer_128(items, skip_dq_drain=False):
+def issuer_128(items, skip_dq_drain=False, skip_second_wait=False):
     kvc = qc = pc = dqc = kdc = dvc = dkc = 0
 
     def issue_st(q, i):
@@ -274,21 +278,29 @@ def issuer_128(items, skip_dq_drain=False):
         for t in range(n):
             qs = qc % QST128
             u = qc
-            yield ("wait", "p_full", pc)
+            # the k-steps of the first group of both halves (query columns
+            # 0..63) while the compute works on the second
+            yield ("wait", "p_full0", pc)
             if t == 0:
                 yield ("wait", "kd_empty", kdc - 1)
+            acc_v = [("TDV", f"dv{i}.{t - 1}")] if t > 0 else []
+            acc_k = [("TDK", f"dk{i}.{t - 1}")] if t > 0 else []
+            yield ("mma", [(f"TSa{h}P", f"P{u}") for h in "01"] + [(f"O{qs}", f"q{u}")],
+                   [("TDV", f"dv{i}.{t}a")], acc_v)                      # dV, k-steps 0..3
+            yield ("mma", [(f"TSa{h}D", f"dS{u}") for h in "01"] + [(f"Q{qs}", f"q{u}")],
+                   [("TDK", f"dk{i}.{t}a")], acc_k)                      # dK, k-steps 0..3
+            if not skip_second_wait:
+                yield ("wait", "p_full1", pc)
             yield ("mma", [("DST0", f"dS{u}"), ("DST1", f"dS{u}"), ("KV", f"kv{i}")],
                    dp_cols(f"dQ{u}"))                           # dQ
             yield ("commit", "dq_full")
             dqc += 1
-            acc_v = [("TDV", f"dv{i}.{t - 1}")] if t > 0 else []
-            pt = [(f"TS{g}{h}P", f"P{u}") for g in "ab" for h in "01"]
-            yield ("mma", pt + [(f"O{qs}", f"q{u}")] + acc_v, [("TDV", f"dv{i}.{t}")])   # dV
+            yield ("mma", [(f"TSb{h}P", f"P{u}") for h in "01"] + [(f"O{qs}", f"q{u}")],
+                   [("TDV", f"dv{i}.{t}")], [("TDV", f"dv{i}.{t}a")])   # dV, k-steps 4..7
             yield ("commit", "dv_done")
             dvc += 1
-            acc_k = [("TDK", f"dk{i}.{t - 1}")] if t > 0 else []
-            dst = [(f"TS{g}{h}D", f"dS{u}") for g in "ab" for h in "01"]
-            yield ("mma", dst + [(f"Q{qs}", f"q{u}")] + acc_k, [("TDK", f"dk{i}.{t}")])  # dK
+            yield ("mma", [(f"TSb{h}D", f"dS{u}") for h in "01"] + [(f"Q{qs}", f"q{u}")],
+                   [("TDK", f"dk{i}.{t}")], [("TDK", f"dk{i}.{t}a")])   # dK, k-steps 4..7
             yield ("commit", "dk_done")
             dkc += 1
             # (the stage goes back to the producer from the dQ warps)
@@ -328,7 +340,7 @@ def compute_128(hf, items):
                 # the previous step's dQ has read the dS^T tile: its commit
                 # precedes this step's s_full, waited for above
                 yield ("write", "DST" + h, f"dS{u}")
-            yield ("arrive", "p_full", 1)
+                yield ("arrive", f"p_full{0 if g == 'a' else 1}", 1)
             qc += 1
             sc += 1
             pc += 1
@@ -368,9 +380,9 @@ def dq_warps_128(items, early_stage=False):
             u += 1
 
 
-def run_model_128(items, rng, skip_dq_drain=False, early_stage=False):
+def run_model_128(items, rng, skip_dq_drain=False, early_stage=False, skip_second_wait=False):
     roles = {
-        "prod": producer_128(items), "g": issuer_128(items, skip_dq_drain),
+        "prod": producer_128(items), "g": issuer_128(items, skip_dq_drain, skip_second_wait),
         "c0": compute_128(0, items), "c1": compute_128(1, items),
         "dq": dq_warps_128(items, early_stage),
     }
@@ -406,6 +418,19 @@ def test_planted_staging_before_dv_read_is_caught():
     for _ in range(200):
         try:
             run_model_128(random_items(rng, rng.randint(2, 10)), rng, early_stage=True)
+        except Violation:
+            caught += 1
+    assert caught >= 10
+
+
+def test_planted_second_group_before_written_is_caught():
+    # dQ and the second half of dV / dK issued after the first group only:
+    # they read P^T / dS^T columns that still hold S^T.
+    rng = random.Random(29)
+    caught = 0
+    for _ in range(200):
+        try:
+            run_model_128(random_items(rng, rng.randint(2, 10)), rng, skip_second_wait=True)
         except Violation:
             caught += 1
     assert caught >= 10
