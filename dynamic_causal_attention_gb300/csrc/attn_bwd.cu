@@ -254,39 +254,57 @@ __global__ void __launch_bounds__(512, 1)
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer
-    if (lane == 0) {
-      uint32_t kvc = 0, qc = 0;
-      for (int kr = 0, it = snake_item(0, blockIdx.x, gridDim.x); it < p.n_items;
+    // Lane 0 waits for the buffer and posts the expected bytes; then one lane
+    // per tile chunk issues its copy (one issuing thread moves about 29 bytes
+    // per clock from L2, four about 74) and two more the -lse/-D vectors.
+    uint32_t kvc = 0, qc = 0;
+    for (int kr = 0, it = snake_item(0, blockIdx.x, gridDim.x); it < p.n_items;
          it = snake_item(++kr, blockIdx.x, gridDim.x)) {
-        const BItem w = decode_bwd(p, it);
-        const int kvrow0 = (w.b * p.H_kv + w.kv) * T;
+      const BItem w = decode_bwd(p, it);
+      const int kvrow0 = (w.b * p.H_kv + w.kv) * T;
+      if (lane == 0) {
         mbar_wait(kv_empty, (kvc & 1) ^ 1, wc, kSiteBProdKV);
-        ++kvc;
         mbar_arrive_expect_tx(kv_full, 2 * G::TILE_BYTES);
-        for (int c = 0; c < G::NCHUNK; ++c) {
-          tma_load_2d(smem + L::OFF_K + c * G::CHUNK_BYTES, &tm_k, kv_full, c * G::CHUNK,
-                      kvrow0 + w.J * 128);
+      }
+      __syncwarp();
+      ++kvc;
+      if (lane < 2 * G::NCHUNK) {
+        const int c = lane >> 1;
+        if (lane & 1)
           tma_load_2d(smem + L::OFF_V + c * G::CHUNK_BYTES, &tm_v, kv_full, c * G::CHUNK,
                       kvrow0 + w.J * 128);
-        }
-        for (int t = 0; t < w.nsteps; ++t) {
-          int hq, I;
-          step_of(p, w, t, hq, I);
-          const int row0 = (w.b * H + hq) * T;
-          const int qs = qc % L::QST;
+        else
+          tma_load_2d(smem + L::OFF_K + c * G::CHUNK_BYTES, &tm_k, kv_full, c * G::CHUNK,
+                      kvrow0 + w.J * 128);
+      }
+      for (int t = 0; t < w.nsteps; ++t) {
+        int hq, I;
+        step_of(p, w, t, hq, I);
+        const int row0 = (w.b * H + hq) * T;
+        const int qs = qc % L::QST;
+        if (lane == 0) {
           mbar_wait(q_empty + qs, ((qc / L::QST) & 1) ^ 1, wc, kSiteBProdQ);
-          ++qc;
-          uint8_t* st = smem + L::OFF_Q + qs * L::STAGE;
           mbar_arrive_expect_tx(q_full + qs, 2 * G::TILE_BYTES + 1024);
-          for (int c = 0; c < G::NCHUNK; ++c) {
-            tma_load_2d(st + c * G::CHUNK_BYTES, &tm_q, q_full + qs, c * G::CHUNK, row0 + I * 128);
-            tma_load_2d(st + G::TILE_BYTES + c * G::CHUNK_BYTES, &tm_do, q_full + qs, c * G::CHUNK,
+        }
+        __syncwarp();
+        ++qc;
+        uint8_t* st = smem + L::OFF_Q + qs * L::STAGE;
+        if (lane < 2 * G::NCHUNK) {
+          const int c = lane >> 1;
+          if (lane & 1)
+            tma_load_2d(st + G::TILE_BYTES + c * G::CHUNK_BYTES, &tm_do, q_full + qs,
+                        c * G::CHUNK, row0 + I * 128);
+          else
+            tma_load_2d(st + c * G::CHUNK_BYTES, &tm_q, q_full + qs, c * G::CHUNK,
                         row0 + I * 128);
-          }
+        } else if (lane == 2 * G::NCHUNK) {
           bulk_load(st + 2 * G::TILE_BYTES, p.lse2 + row0 + I * 128, 512, q_full + qs);
+        } else if (lane == 2 * G::NCHUNK + 1) {
           bulk_load(st + 2 * G::TILE_BYTES + 512, p.Dvec + row0 + I * 128, 512, q_full + qs);
         }
       }
+    }
+    if (lane == 0) {
       if (kvc > 0) mbar_drain(kv_full, (kvc - 1) & 1);
       for (int s = 0; s < L::QST; ++s)
         if (qc > (uint32_t)s) mbar_drain(q_full + s, ((qc - 1 - s) / L::QST) & 1);
