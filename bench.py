@@ -29,6 +29,7 @@ from __future__ import annotations
 import argparse
 from dataclasses import replace
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -127,13 +128,19 @@ KERNEL_SOURCES = {
 }
 
 
+_COMMENT_RE = re.compile(r"//[^\n]*|/\*.*?\*/", re.S)
+
+
 def source_hash(kernel):
+    """Hash of the kernel's source files with comments and blank space
+    removed, so that a comment-only edit keeps a recorded figure valid."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dynamic_causal_attention_gb300", "csrc")
     for f in KERNEL_SOURCES.get(kernel, ()):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode())
-            h.update(fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            code = _COMMENT_RE.sub("", fh.read())
+        h.update(f.encode())
+        h.update("\n".join(ln.strip() for ln in code.splitlines() if ln.strip()).encode())
     return h.hexdigest()[:16]
 
 

@@ -19,13 +19,13 @@
 //                                                    read as an MN-major A)
 // d_h <= 64: P^T goes, as packed bf16, to spare TMEM columns (dV is a TS MMA)
 // and dS^T to one of two swizzled shared-memory tiles (dK and dQ are SS MMAs).
-// d_h = 128: TMEM has no spare columns, so P^T and dS^T are written over the
-// S^T and dP^T columns just read (dV and dK are TS MMAs) and dS^T also goes to
-// shared memory for dQ.  dQ_I is read from TMEM by a second warpgroup and
-// added into an fp32 accumulator (zeroed by the pre-pass) with one TMA tensor
-// reduce-add per 32 columns: staged in a tile of its own for d_h <= 64, in the
-// two halves of the dS^T tile (once its dQ product has read it) for
-// d_h = 128.  A post-pass scales it by 1/sqrt(d) and converts it.
+// d_h = 128: TMEM has no spare columns, so P^T and dS^T are written, packed,
+// over the S^T columns just read (dV and dK are TS MMAs), dS^T also goes to
+// shared memory for dQ, and dQ goes over the dP^T columns.  dQ_I is read from
+// TMEM by a second warpgroup and added into an fp32 accumulator (zeroed by the
+// pre-pass) with one TMA tensor reduce-add per 32 columns: staged in a tile of
+// its own for d_h <= 64, in the step's own Q_I/dO_I stage (once dV and dK have
+// read it) for d_h = 128.  A post-pass scales it by 1/sqrt(d) and converts it.
 //
 // param_grad_kernel (K5): items (h_static, J), handed out in snake order.
 // For I = J..nI-1 the batch-summed dP^T(j, i) = sum_b V_b(j) . dO_b(i) is one
