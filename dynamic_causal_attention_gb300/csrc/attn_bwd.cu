@@ -53,8 +53,8 @@ constexpr uint32_t kTmemCols = 512;
 template <int D>
 struct BwdSmem {
   using G = TileGeom<D>;
-  // d_h = 128 leaves no free TMEM columns: dQ reuses the S^T/P^T columns once
-  // the dV MMAs that read P^T have completed.
+  // d_h = 128 leaves no free TMEM columns: dQ goes over the dP^T columns once
+  // the compute has read them, and P^T and dS^T over the S^T columns.
   static constexpr bool DQ_ALIAS = (256 + 3 * D > 512);
   // d_h <= 64: P^T goes to spare TMEM columns (TS MMA for dV) and dS^T to
   // shared memory (SS MMAs for dK, dQ), so the S^T/dP^T columns are free as
@@ -379,8 +379,10 @@ __global__ void __launch_bounds__(512, 1)
           }
         }
       }
-      // d_h = 128: per step dQ (one N = 128 product into the dP^T columns the
-      // compute has read), then dV and dK.  The next step's S^T goes out once
+      // d_h = 128, per step: once the compute's first group of query columns
+      // is in TMEM, dV and dK over its k-steps; once the second is, dQ (one
+      // N = 128 product into the dP^T columns the compute has read) and the
+      // rest of dV and dK.  The next step's S^T goes out once
       // dK has completed (dV and dK read P^T and dS^T from the S^T columns;
       // this warp's products complete in issue order, so the wait only makes
       // the order explicit), its dP^T once the dQ warps have taken dQ out of
